@@ -1,0 +1,217 @@
+"""Python face of the CPU oracle — TEST INFRASTRUCTURE ONLY.
+
+The arithmetic lives in ``oracle.c`` (plain fp64 loops, see its header for the
+passages it follows). This module compiles it with gcc, loads it with ctypes
+and converts tensors to float64 numpy arrays (exact for bf16 and fp32 inputs).
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may import
+it; the CUDA library never does, and shares no code with it.
+
+Parity status: score_topk, sparse_attn and window_attn are pinned by the
+``-m "not gpu"`` tests (brute force, closed forms, special cases and an
+independent dense masked attention); none is pinned to printed values, because
+the pages print none for this path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-Wall", "-shared", "-fPIC", "-pthread",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i64, i32, f32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_double
+        lib.oracle_topk_rows.argtypes = [P, P, i64, P, i64, i64, i32, i32, i32, f32, P, P, i32]
+        lib.oracle_topk_rows.restype = i32
+        lib.oracle_attn_rows.argtypes = [P, i64, P, P, i64, i32, P, i32, f64, P, i32]
+        lib.oracle_attn_rows.restype = i64
+        lib.oracle_window_rows.argtypes = [P, P, i64, P, P, i64, i32, i32, i32, f64, P, i32]
+        lib.oracle_window_rows.restype = i32
+        _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count() or 1)
+
+
+def _f64(x) -> np.ndarray:
+    """float64 C-contiguous copy of a torch tensor or array-like."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().to("cpu", torch.float64).numpy()
+    except ImportError:
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ------------------------------------------------------------- per-head calls
+
+def topk_rows(q_rows, qpos, k_low, k: int, Tq: int, causal: bool, scale: float = 0.0,
+              nthreads: int | None = None):
+    """Top-k of one head for the given query rows.
+
+    q_rows [n, P] (query positions ``qpos`` [n]), k_low [Tk, P].
+    Returns (idx int32 [n, k], score float32 [n, k]).
+    """
+    q = _f64(q_rows)
+    kl = _f64(k_low)
+    pos = np.ascontiguousarray(np.asarray(qpos, dtype=np.int64))
+    n, P = q.shape
+    Tk = kl.shape[0]
+    assert kl.shape[1] == P and pos.shape == (n,)
+    idx = np.empty((n, k), dtype=np.int32)
+    sc = np.empty((n, k), dtype=np.float32)
+    rc = _load().oracle_topk_rows(_ptr(q), _ptr(pos), n, _ptr(kl), Tq, Tk, P, k, int(causal),
+                                  float(scale), _ptr(idx), _ptr(sc), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_topk_rows: bad arguments")
+    return idx, sc
+
+
+def attn_rows(q_rows, K, V, idx, scale: float = 0.0, nthreads: int | None = None):
+    """Attention of one head's query rows over their index lists; float64 [n, D]."""
+    q = _f64(q_rows)
+    Kd = _f64(K)
+    Vd = _f64(V)
+    ix = np.ascontiguousarray(np.asarray(idx, dtype=np.int32))
+    n, D = q.shape
+    k = ix.shape[1]
+    O = np.empty((n, D), dtype=np.float64)
+    bad = _load().oracle_attn_rows(_ptr(q), n, _ptr(Kd), _ptr(Vd), Kd.shape[0], D, _ptr(ix), k,
+                                   float(scale), _ptr(O), nthreads or default_threads())
+    if bad < 0:
+        raise ValueError("oracle_attn_rows: bad arguments")
+    return O, int(bad)
+
+
+def window_rows(q_rows, qpos, K, V, w_left: int, w_right: int, scale: float = 0.0,
+                nthreads: int | None = None):
+    """Sliding-window attention of one head's query rows; float64 [n, D]."""
+    q = _f64(q_rows)
+    Kd = _f64(K)
+    Vd = _f64(V)
+    pos = np.ascontiguousarray(np.asarray(qpos, dtype=np.int64))
+    n, D = q.shape
+    O = np.empty((n, D), dtype=np.float64)
+    rc = _load().oracle_window_rows(_ptr(q), _ptr(pos), n, _ptr(Kd), _ptr(Vd), Kd.shape[0], D,
+                                    w_left, w_right, float(scale), _ptr(O),
+                                    nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_window_rows: bad arguments")
+    return O
+
+
+# ------------------------------------------------------- whole-tensor calls
+
+def _rows_by_head(B, H, Tq, rows):
+    """Group flat row ids (b*H + h)*Tq + i by head: {(b, h): [i...]}."""
+    if rows is None:
+        return {(b, h): np.arange(Tq) for b in range(B) for h in range(H)}, None
+    rows = np.asarray(rows, dtype=np.int64)
+    out = {}
+    for r in rows:
+        bh, i = divmod(int(r), Tq)
+        b, h = divmod(bh, H)
+        out.setdefault((b, h), []).append(i)
+    return {key: np.asarray(v, dtype=np.int64) for key, v in out.items()}, rows
+
+
+def score_topk(q_low, k_low, k: int, causal: bool, scale: float = 0.0, rows=None,
+               nthreads: int | None = None):
+    """Top-k of [B,H,Tq,P] x [B,H,Tk,P] for all rows, or for flat row ids ``rows``.
+
+    Returns (idx, score): [B,H,Tq,k] for all rows, else [len(rows), k] in the
+    order of ``rows``.
+    """
+    B, H, Tq, P = q_low.shape
+    groups, flat = _rows_by_head(B, H, Tq, rows)
+    if flat is None:
+        idx = np.empty((B, H, Tq, k), np.int32)
+        sc = np.empty((B, H, Tq, k), np.float32)
+    else:
+        idx = np.empty((len(flat), k), np.int32)
+        sc = np.empty((len(flat), k), np.float32)
+        where = {int(r): n for n, r in enumerate(flat)}
+    for (b, h), qi in groups.items():
+        i_, s_ = topk_rows(q_low[b, h][qi], qi, k_low[b, h], k, Tq, causal, scale, nthreads)
+        if flat is None:
+            idx[b, h], sc[b, h] = i_, s_
+        else:
+            for t, i in enumerate(qi):
+                n = where[(b * H + h) * Tq + int(i)]
+                idx[n], sc[n] = i_[t], s_[t]
+    return idx, sc
+
+
+def sparse_attn(Q, K, V, idx, scale: float = 0.0, rows=None, nthreads: int | None = None):
+    """Sparse attention; ``idx`` is [B,H,Tq,k] (all rows) or [len(rows), k].
+
+    Returns float64 O: [B,H,Tq,D] or [len(rows), D].
+    """
+    B, H, Tq, D = Q.shape
+    groups, flat = _rows_by_head(B, H, Tq, rows)
+    idx = np.asarray(idx)
+    if flat is None:
+        O = np.empty((B, H, Tq, D), np.float64)
+    else:
+        O = np.empty((len(flat), D), np.float64)
+        where = {int(r): n for n, r in enumerate(flat)}
+    for (b, h), qi in groups.items():
+        if flat is None:
+            ix = idx[b, h][qi]
+        else:
+            ix = np.stack([idx[where[(b * H + h) * Tq + int(i)]] for i in qi])
+        o_, _ = attn_rows(Q[b, h][qi], K[b, h], V[b, h], ix, scale, nthreads)
+        if flat is None:
+            O[b, h] = o_
+        else:
+            for t, i in enumerate(qi):
+                O[where[(b * H + h) * Tq + int(i)]] = o_[t]
+    return O
+
+
+def window_attn(Q, K, V, w_left: int, w_right: int, scale: float = 0.0, rows=None,
+                nthreads: int | None = None):
+    """Sliding-window attention over [B,H,T,D]; float64 [B,H,T,D] or [len(rows), D]."""
+    B, H, T, D = Q.shape
+    groups, flat = _rows_by_head(B, H, T, rows)
+    if flat is None:
+        O = np.empty((B, H, T, D), np.float64)
+    else:
+        O = np.empty((len(flat), D), np.float64)
+        where = {int(r): n for n, r in enumerate(flat)}
+    for (b, h), qi in groups.items():
+        o_ = window_rows(Q[b, h][qi], qi, K[b, h], V[b, h], w_left, w_right, scale, nthreads)
+        if flat is None:
+            O[b, h] = o_
+        else:
+            for t, i in enumerate(qi):
+                O[where[(b * H + h) * T + int(i)]] = o_[t]
+    return O

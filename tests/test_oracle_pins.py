@@ -1,0 +1,320 @@
+"""Pins of the CPU oracle to things other than itself (CPU only).
+
+Each test checks the oracle against what the pages or the mathematics fix:
+brute-force enumeration of the rank definition, exact rational arithmetic on
+integer data, closed forms, special cases that reduce to a library routine
+(torch's scaled_dot_product_attention in float64), and the worked examples the
+pages print (tests/golden). A plausible slip in the oracle — a dropped scale,
+a flipped tie-break, an off-by-one causal edge, a transposed operand, a missing
+max-subtraction — fails at least one of them.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from workloads import WORKLOADS, make_scorer_inputs, plant_groups, plant_positions, small
+from workloads.gen import PLANT_DIMS, PLANT_GROUPS
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_int(shape, seed):
+    g = np.random.default_rng(seed)
+    return g.integers(-4, 5, size=shape).astype(np.float64)
+
+
+def _brute_topk(S, valid, k):
+    """Rank definition: key j's rank is the number of valid keys beating it
+    (higher score, or equal score and lower index). Selected iff rank < k;
+    output slot = rank. Returns idx [k] padded with -1."""
+    n = len(S)
+    out = [-1] * k
+    for j in range(n):
+        if not valid[j]:
+            continue
+        rank = 0
+        for jj in range(n):
+            if valid[jj] and (S[jj] > S[j] or (S[jj] == S[j] and jj < j)):
+                rank += 1
+        if rank < k:
+            out[rank] = j
+    return out
+
+
+@pytest.mark.parametrize("Tq,Tk,P,k,causal", [
+    (9, 9, 16, 4, False), (13, 13, 16, 5, True), (7, 20, 32, 6, True),
+    (20, 7, 16, 3, True), (16, 16, 64, 16, False), (31, 48, 16, 48, True),
+])
+def test_topk_brute_force_integer(Tq, Tk, P, k, causal):
+    """Exact: integer data, scores as Fractions, selection by the rank definition."""
+    q = _rand_int((Tq, P), 1 + Tq)
+    kl = _rand_int((Tk, P), 2 + Tk)
+    idx, sc = oracle.topk_rows(q, np.arange(Tq), kl, k, Tq, causal)
+    r = math.isqrt(P)
+    for i in range(Tq):
+        dots = [int(np.dot(q[i].astype(np.int64), kl[j].astype(np.int64))) for j in range(Tk)]
+        if r * r == P:   # scale 1/r is exact: scores are exact rationals
+            S = [Fraction(d, r) for d in dots]
+        else:            # scale rounded to fp32, product rounded to fp32
+            S = [Fraction(float(np.float32(d) * np.float32(1.0 / math.sqrt(P)))) for d in dots]
+        valid = [(not causal) or (j <= i + (Tk - Tq)) for j in range(Tk)]
+        want = _brute_topk(S, valid, k)
+        assert list(idx[i]) == want, (i, list(idx[i]), want)
+        for t, j in enumerate(want):
+            if j >= 0:
+                assert Fraction(float(sc[i, t])) == S[j]
+            else:
+                assert sc[i, t] == -np.inf
+
+
+def test_topk_brute_force_float():
+    """Continuous data: selection matches the rank definition on scores formed
+    by a library matmul (fp64), rounded to fp32 and scaled in fp32."""
+    g = np.random.default_rng(7)
+    Tq, Tk, P, k = 24, 40, 32, 10
+    q = g.standard_normal((Tq, P))
+    kl = g.standard_normal((Tk, P))
+    idx, sc = oracle.topk_rows(q, np.arange(Tq), kl, k, Tq, True)
+    S = (q @ kl.T).astype(np.float32) * np.float32(1.0 / math.sqrt(P))
+    for i in range(Tq):
+        valid = [j <= i + (Tk - Tq) for j in range(Tk)]
+        assert list(idx[i]) == _brute_topk(list(S[i]), valid, k)
+
+
+def test_topk_scale_and_order_invariants():
+    w = small("topk_f32_t1024_k32", Tq=64, Tk=300, k=40)
+    q, kl = make_scorer_inputs(w)
+    idx, sc = oracle.score_topk(q, kl, w.k, causal=False)
+    qd, kd = q.double().numpy(), kl.double().numpy()
+    for h in range(w.H):
+        for i in range(w.Tq):
+            S = (qd[0, h, i] @ kd[0, h].T) / 4.0   # P = 16: scale exactly 1/4
+            ids = idx[0, h, i]
+            assert len(set(ids.tolist())) == w.k
+            np.testing.assert_array_equal(sc[0, h, i], S[ids].astype(np.float32))
+            # sorted (score desc, index asc)
+            for a, b in zip(ids[:-1], ids[1:]):
+                assert S[a] > S[b] or (S[a] == S[b] and a < b)
+            # every unselected key is beaten by the last selected one
+            last = ids[-1]
+            rest = np.setdiff1d(np.arange(w.Tk), ids)
+            assert np.all((S[rest] < S[last]) | ((S[rest] == S[last]) & (rest > last)))
+
+
+def test_topk_all_ties_lower_index_wins():
+    Tq, Tk, k = 10, 50, 7
+    q = np.zeros((Tq, 16))
+    kl = _rand_int((Tk, 16), 3)
+    idx, sc = oracle.topk_rows(q, np.arange(Tq), kl, k, Tq, False)
+    assert (idx == np.arange(k)[None, :]).all()
+    assert (sc == 0).all()
+    idx, _ = oracle.topk_rows(q, np.arange(Tq), kl, k, Tq, True)   # causal, Tq < Tk
+    for i in range(Tq):
+        nv = min(i + (Tk - Tq) + 1, Tk)
+        want = list(range(min(k, nv))) + [-1] * max(0, k - nv)
+        assert list(idx[i]) == want
+
+
+def test_topk_k_exceeds_valid_pads():
+    Tq = Tk = 12
+    q = _rand_int((Tq, 16), 4)
+    kl = _rand_int((Tk, 16), 5)
+    k = 20
+    idx, sc = oracle.topk_rows(q, np.arange(Tq), kl, k, Tq, True)
+    for i in range(Tq):
+        sel = idx[i][idx[i] >= 0]
+        assert sorted(sel.tolist()) == list(range(i + 1))      # every valid key, nothing else
+        assert (idx[i][i + 1:] == -1).all() and np.isneginf(sc[i][i + 1:]).all()
+
+
+def test_topk_rows_with_no_valid_key():
+    """Causal with Tq > Tk: the first Tq - Tk queries see no key at all."""
+    Tq, Tk = 8, 5
+    q = _rand_int((Tq, 16), 6)
+    kl = _rand_int((Tk, 16), 7)
+    idx, _ = oracle.topk_rows(q, np.arange(Tq), kl, 3, Tq, True)
+    assert (idx[:Tq - Tk] == -1).all()
+    assert idx[Tq - Tk][0] == 0 and (idx[Tq - Tk][1:] == -1).all()
+
+
+def test_planted_keys_boost_exactly_64():
+    w = WORKLOADS["topk_causal_bf16_t128k_k512_planted"].with_(H=2, Tq=2048, Tk=2048, planted=16)
+    q, kl = make_scorer_inputs(w)
+    grp = plant_groups(w)
+    pos = plant_positions(w)
+    base = w.P - PLANT_GROUPS * PLANT_DIMS
+    qd, kd = q.double(), kl.double()
+    for h in range(w.H):
+        for i in [0, 5, 1000, 2047]:
+            g = int(grp[0, h, i])
+            full = kd[0, h] @ qd[0, h, i]
+            rand = kd[0, h, :, :base] @ qd[0, h, i, :base]
+            boost = full - rand
+            planted = set(pos[0, h, g].tolist())
+            for j in range(w.Tk):
+                assert boost[j] == (64.0 if j in planted else 0.0)
+    # integer range of every element
+    assert q.abs().max() <= 4 and kl.abs().max() <= 4
+
+
+def _sdpa(Q, K, V, mask=None, scale=None, causal=False):
+    """torch's scaled_dot_product_attention in float64 (library routine)."""
+    return F.scaled_dot_product_attention(
+        torch.as_tensor(Q, dtype=torch.float64)[None, None],
+        torch.as_tensor(K, dtype=torch.float64)[None, None],
+        torch.as_tensor(V, dtype=torch.float64)[None, None],
+        attn_mask=None if mask is None else torch.as_tensor(mask)[None, None],
+        is_causal=causal, scale=scale)[0, 0].numpy()
+
+
+def test_attn_full_selection_equals_dense_sdpa():
+    g = np.random.default_rng(11)
+    T, D = 37, 64
+    Q, K, V = (g.standard_normal((T, D)) for _ in range(3))
+    idx = np.tile(np.arange(T, dtype=np.int32), (T, 1))
+    O, bad = oracle.attn_rows(Q, K, V, idx)
+    assert bad == 0
+    np.testing.assert_allclose(O, _sdpa(Q, K, V), rtol=0, atol=1e-12)
+
+
+def test_attn_causal_full_topk_equals_causal_sdpa():
+    g = np.random.default_rng(12)
+    T, D = 29, 32
+    Q, K, V = (g.standard_normal((T, D)) for _ in range(3))
+    ql, kl = _rand_int((T, 16), 8), _rand_int((T, 16), 9)
+    idx, _ = oracle.topk_rows(ql, np.arange(T), kl, T, T, True)
+    O, _ = oracle.attn_rows(Q, K, V, idx)
+    np.testing.assert_allclose(O, _sdpa(Q, K, V, causal=True), rtol=0, atol=1e-12)
+
+
+def test_attn_equals_masked_dense():
+    """Sparse attention over idx equals dense attention under the boolean mask built from idx."""
+    g = np.random.default_rng(13)
+    Tq, Tk, D, k = 16, 64, 32, 9
+    Q = g.standard_normal((Tq, D))
+    K, V = g.standard_normal((Tk, D)), g.standard_normal((Tk, D))
+    idx = np.stack([g.choice(Tk, size=k, replace=False) for _ in range(Tq)]).astype(np.int32)
+    mask = np.zeros((Tq, Tk), dtype=bool)
+    for i in range(Tq):
+        mask[i, idx[i]] = True
+    O, _ = oracle.attn_rows(Q, K, V, idx)
+    np.testing.assert_allclose(O, _sdpa(Q, K, V, mask=mask), rtol=0, atol=1e-12)
+
+
+def test_attn_closed_forms():
+    g = np.random.default_rng(14)
+    Tk, D = 40, 16
+    Q = g.standard_normal((5, D)) * 3
+    K, V = g.standard_normal((Tk, D)), g.standard_normal((Tk, D))
+    # k = 1: the single selected value row, exactly
+    idx1 = np.array([[3], [0], [39], [17], [17]], dtype=np.int32)
+    O, _ = oracle.attn_rows(Q, K, V, idx1)
+    np.testing.assert_array_equal(O, V[idx1[:, 0]])
+    # constant V rows: output is that constant
+    Vc = np.tile(g.standard_normal(D), (Tk, 1))
+    idx = np.stack([g.choice(Tk, 8, replace=False) for _ in range(5)]).astype(np.int32)
+    O, _ = oracle.attn_rows(Q, K, Vc, idx)
+    np.testing.assert_allclose(O, np.tile(Vc[0], (5, 1)), rtol=0, atol=1e-14)
+    # identical keys: uniform weights, output is the mean of the selected values
+    Ke = np.tile(g.standard_normal(D), (Tk, 1))
+    O, _ = oracle.attn_rows(Q, Ke, V, idx)
+    np.testing.assert_allclose(O, np.stack([V[r].mean(0) for r in idx]), rtol=0, atol=1e-14)
+    # permutation of the list changes nothing beyond rounding
+    perm = idx[:, ::-1].copy()
+    O1, _ = oracle.attn_rows(Q, K, V, idx)
+    O2, _ = oracle.attn_rows(Q, K, V, perm)
+    np.testing.assert_allclose(O1, O2, rtol=0, atol=1e-13)
+
+
+def test_attn_hand_example_and_list_semantics():
+    # D = 1, scale 1: logits 0 and ln 3 -> weights 1/4 and 3/4
+    K = np.array([[0.0], [math.log(3.0)], [5.0]])
+    V = np.array([[2.0], [10.0], [-7.0]])
+    q = np.array([[1.0]])
+    O, _ = oracle.attn_rows(q, K, V, np.array([[0, 1]], np.int32), scale=1.0)
+    assert abs(O[0, 0] - (0.25 * 2.0 + 0.75 * 10.0)) < 1e-14
+    # -1 entries are skipped
+    O2, _ = oracle.attn_rows(q, K, V, np.array([[0, -1, 1, -1]], np.int32), scale=1.0)
+    assert O2[0, 0] == O[0, 0]
+    # a repeated entry counts once per occurrence: weights 1:1:3 -> (2 + 2 + 30) / 5
+    O3, _ = oracle.attn_rows(q, K, V, np.array([[0, 0, 1]], np.int32), scale=1.0)
+    assert abs(O3[0, 0] - (2.0 + 2.0 + 3.0 * 10.0) / 5.0) < 1e-14
+    # no valid entry: zeros; out-of-range entries are counted and skipped
+    O4, bad = oracle.attn_rows(q, K, V, np.array([[-1, 7]], np.int32), scale=1.0)
+    assert O4[0, 0] == 0.0 and bad == 1
+    # default scale is head_dim^-0.5: D = 4 -> 1/2
+    K4, V4 = np.array([[0.0] * 4, [1.0] * 4]), np.array([[0.0] * 4, [1.0] * 4])
+    O5, _ = oracle.attn_rows(np.array([[1.0] * 4]), K4, V4, np.array([[0, 1]], np.int32))
+    w1 = math.exp(2.0) / (1.0 + math.exp(2.0))   # logit 4 * 1/2 = 2
+    np.testing.assert_allclose(O5[0], [w1] * 4, rtol=0, atol=1e-14)
+
+
+def test_attn_large_logits_stable():
+    """Max-subtraction: logits of order 1e3 must not overflow."""
+    K = np.array([[1000.0], [999.0]])
+    V = np.array([[1.0], [0.0]])
+    O, _ = oracle.attn_rows(np.array([[1.0]]), K, V, np.array([[0, 1]], np.int32), scale=1.0)
+    assert abs(O[0, 0] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-14
+
+
+@pytest.mark.parametrize("T,w", [(50, 3), (50, 0), (20, 25), (64, 7)])
+def test_window_equals_band_masked_sdpa(T, w):
+    g = np.random.default_rng(15 + T + w)
+    D = 16
+    Q, K, V = (g.standard_normal((T, D)) for _ in range(3))
+    i = np.arange(T)[:, None]
+    j = np.arange(T)[None, :]
+    mask = np.abs(i - j) <= w
+    O = oracle.window_rows(Q, np.arange(T), K, V, w, w)
+    np.testing.assert_allclose(O, _sdpa(Q, K, V, mask=mask), rtol=0, atol=1e-12)
+    if w == 0:
+        np.testing.assert_array_equal(O, V)
+    if w >= T:
+        np.testing.assert_allclose(O, _sdpa(Q, K, V), rtol=0, atol=1e-12)
+
+
+def test_window_equals_sparse_band():
+    g = np.random.default_rng(16)
+    T, D, w = 40, 8, 4
+    Q, K, V = (g.standard_normal((T, D)) for _ in range(3))
+    Ow = oracle.window_rows(Q, np.arange(T), K, V, w, w)
+    for i in range(T):
+        band = np.arange(max(0, i - w), min(T - 1, i + w) + 1, dtype=np.int32)
+        Os, _ = oracle.attn_rows(Q[i:i + 1], K, V, band[None, :])
+        np.testing.assert_allclose(Ow[i], Os[0], rtol=0, atol=1e-14)
+
+
+def test_golden_window_radius_example():
+    """Worked example: radius 5 around token 100 covers positions 95..105."""
+    gold = json.load(open(os.path.join(GOLDEN, "window_radius.json")))
+    ex = gold["radius_example"]
+    T, w, i = 400, ex["w"], ex["i"]
+    # zero query: uniform weights; V_j = j and j^2 recover the key set's mean and second moment
+    K = np.random.default_rng(17).standard_normal((T, 2))
+    V = np.stack([np.arange(T, dtype=np.float64), np.arange(T, dtype=np.float64) ** 2], 1)
+    Q = np.zeros((T, 2))
+    O = oracle.window_rows(Q[i:i + 1], [i], K, V, w, w)
+    keys = np.arange(ex["first_key"], ex["last_key"] + 1)
+    assert len(keys) == 2 * w + 1
+    np.testing.assert_allclose(O[0], [keys.mean(), (keys ** 2).mean()], rtol=1e-15)
+    fx = gold["fraction_example"]
+    assert round(100.0 * (2 * fx["w"] + 1) / fx["n"], 1) == fx["percent_one_decimal"]
+
+
+def test_golden_selection_fraction_at_128k():
+    """k = 512 of n = 128K keys is 0.4% of the dense row: the oracle's last row selects exactly k."""
+    gold = json.load(open(os.path.join(GOLDEN, "selection_fraction.json")))
+    w = WORKLOADS["topk_causal_bf16_t128k_k512_planted"].with_(H=1)
+    assert (w.Tk, w.k) == (gold["n"], gold["k"])
+    q, kl = make_scorer_inputs(w)
+    i = w.Tq - 1
+    idx, _ = oracle.topk_rows(q[0, 0, i:i + 1], [i], kl[0, 0], w.k, w.Tq, True)
+    assert (idx >= 0).sum() == gold["k"]
+    assert round(100.0 * (idx >= 0).sum() / gold["n"], 1) == gold["percent_one_decimal"]
