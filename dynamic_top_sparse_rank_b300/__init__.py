@@ -1,0 +1,18 @@
+"""Dynamic top-k sparse attention forward on NVIDIA B300 (sm_103a).
+
+Three calls, each a hand-written CUDA kernel behind the C ABI of libssa.so
+(include/ssa.h):
+
+  ssa_score_topk   low-rank scorer fused with exact per-query top-k,
+  ssa_sparse_attn  softmax attention over the selected keys only,
+  ssa_window_attn  sliding-window attention (the fixed-index special case).
+
+The binding is marshalling only; there is no CPU fallback.
+"""
+from ._native import (EXPORTS, SSA_BF16, SSA_DEV_BAD_INDEX, SSA_DEV_OVERFLOW, SSA_DEV_WAIT_LIMIT,
+                      SSA_F32, SSAError, load, score_topk_workspace_size, ssa_score_topk,
+                      ssa_sparse_attn, ssa_window_attn, status_string)
+
+__all__ = ["EXPORTS", "SSA_BF16", "SSA_DEV_BAD_INDEX", "SSA_DEV_OVERFLOW", "SSA_DEV_WAIT_LIMIT",
+           "SSA_F32", "SSAError", "load", "score_topk_workspace_size", "ssa_score_topk",
+           "ssa_sparse_attn", "ssa_window_attn", "status_string"]

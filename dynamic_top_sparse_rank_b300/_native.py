@@ -1,0 +1,196 @@
+"""ctypes binding of libssa.so: argument marshalling only.
+
+Every step of the path runs in the CUDA kernels behind the C ABI declared in
+include/ssa.h. The functions here check tensor placement, dtype and
+contiguity, allocate outputs with torch (device memory is torch's job), pass raw
+pointers and the current CUDA stream, and turn a non-zero status into an
+exception. There is no CPU fallback: without the built library every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssa.so")
+
+SSA_OK, SSA_ERR_INVALID, SSA_ERR_UNSUPPORTED, SSA_ERR_CUDA, SSA_ERR_WORKSPACE = 0, 1, 2, 3, 4
+SSA_F32, SSA_BF16 = 0, 1
+SSA_DEV_BAD_INDEX, SSA_DEV_WAIT_LIMIT, SSA_DEV_OVERFLOW = 0x1, 0x2, 0x4
+
+EXPORTS = ("ssa_version", "ssa_status_string", "ssa_score_topk_workspace_size", "ssa_score_topk",
+           "ssa_sparse_attn", "ssa_window_attn")
+
+
+class SSAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, status_string(status), status))
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libssa.so (raises OSError when it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise OSError("libssa.so not built at %s: run __graft_entry__.build() or "
+                      "python -m dynamic_top_sparse_rank_b300.build" % p)
+    lib = ctypes.CDLL(p)
+    V, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.ssa_version.restype = I
+    lib.ssa_version.argtypes = []
+    lib.ssa_status_string.restype = ctypes.c_char_p
+    lib.ssa_status_string.argtypes = [I]
+    lib.ssa_score_topk_workspace_size.restype = Z
+    lib.ssa_score_topk_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.ssa_score_topk.restype = I
+    lib.ssa_score_topk.argtypes = [V, V, I, I, I, I, I, I, I, I, F, V, V, V, Z, V, V]
+    lib.ssa_sparse_attn.restype = I
+    lib.ssa_sparse_attn.argtypes = [V, V, V, I, I, I, I, I, I, V, I, F, V, I, V, V]
+    lib.ssa_window_attn.restype = I
+    lib.ssa_window_attn.argtypes = [V, V, V, I, I, I, I, I, I, I, F, V, I, V, V]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().ssa_status_string(status).decode()
+    except OSError:
+        return "status %d" % status
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SSA_F32
+    if t.dtype == torch.bfloat16:
+        return SSA_BF16
+    raise TypeError("unsupported dtype %s (float32 or bfloat16)" % t.dtype)
+
+
+def _dev(*ts):
+    dev = None
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("tensors on different devices")
+    return dev
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr() if t is not None else 0)
+
+
+def _stream(dev) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _check(rc: int, where: str):
+    if rc != SSA_OK:
+        raise SSAError(rc, where)
+
+
+def score_topk_workspace_size(B, H, Tq, Tk, P, k, causal) -> int:
+    return int(load().ssa_score_topk_workspace_size(B, H, Tq, Tk, P, k, int(bool(causal))))
+
+
+def ssa_score_topk(q_low: torch.Tensor, k_low: torch.Tensor, k: int, causal: bool,
+                   scale: float = 0.0, with_score: bool = False, workspace: torch.Tensor = None,
+                   idx: torch.Tensor = None, score: torch.Tensor = None,
+                   dev_status: torch.Tensor = None):
+    """Exact top-k of the low-rank scores; returns idx (and score if asked).
+
+    q_low [B,H,Tq,P], k_low [B,H,Tk,P] (float32 or bfloat16, same dtype).
+    idx int32 [B,H,Tq,k]; score float32 [B,H,Tq,k].
+    """
+    lib = load()
+    dev = _dev(q_low, k_low, workspace, idx, score, dev_status)
+    if q_low.dtype != k_low.dtype:
+        raise TypeError("q_low and k_low must share a dtype")
+    B, H, Tq, P = q_low.shape
+    Bk, Hk, Tk, Pk = k_low.shape
+    if (Bk, Hk, Pk) != (B, H, P):
+        raise ValueError("k_low shape %s does not match q_low %s" % (tuple(k_low.shape), tuple(q_low.shape)))
+    if idx is None:
+        idx = torch.empty((B, H, Tq, k), dtype=torch.int32, device=dev)
+    if with_score and score is None:
+        score = torch.empty((B, H, Tq, k), dtype=torch.float32, device=dev)
+    need = score_topk_workspace_size(B, H, Tq, Tk, P, k, causal)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = lib.ssa_score_topk(_ptr(q_low), _ptr(k_low), _dt(q_low), B, H, Tq, Tk, P, k,
+                            int(bool(causal)), float(scale), _ptr(idx), _ptr(score),
+                            _ptr(workspace), wbytes, _ptr(dev_status), _stream(dev))
+    _check(rc, "ssa_score_topk")
+    return (idx, score) if with_score else idx
+
+
+def ssa_sparse_attn(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, idx: torch.Tensor,
+                    scale: float = 0.0, out_dtype=None, out: torch.Tensor = None,
+                    dev_status: torch.Tensor = None) -> torch.Tensor:
+    """Attention of each query row over the keys its idx row lists; returns O."""
+    lib = load()
+    dev = _dev(Q, K, V, idx, out, dev_status)
+    if not (Q.dtype == K.dtype == V.dtype):
+        raise TypeError("Q, K, V must share a dtype")
+    if idx.dtype != torch.int32:
+        raise TypeError("idx must be int32")
+    B, H, Tq, D = Q.shape
+    Tk = K.shape[2]
+    if tuple(K.shape) != (B, H, Tk, D) or tuple(V.shape) != (B, H, Tk, D):
+        raise ValueError("K/V shapes do not match Q")
+    if idx.shape[:3] != (B, H, Tq):
+        raise ValueError("idx shape %s does not match Q" % (tuple(idx.shape),))
+    k = idx.shape[3]
+    odt = out_dtype or Q.dtype
+    if out is None:
+        out = torch.empty((B, H, Tq, D), dtype=odt, device=dev)
+    rc = lib.ssa_sparse_attn(_ptr(Q), _ptr(K), _ptr(V), _dt(Q), B, H, Tq, Tk, D, _ptr(idx), k,
+                             float(scale), _ptr(out), _dt(out), _ptr(dev_status), _stream(dev))
+    _check(rc, "ssa_sparse_attn")
+    return out
+
+
+def ssa_window_attn(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, w_left: int,
+                    w_right: int = None, scale: float = 0.0, out_dtype=None,
+                    out: torch.Tensor = None, dev_status: torch.Tensor = None) -> torch.Tensor:
+    """Sliding-window attention, keys i - w_left .. i + w_right clipped to [0, T)."""
+    lib = load()
+    dev = _dev(Q, K, V, out, dev_status)
+    if not (Q.dtype == K.dtype == V.dtype):
+        raise TypeError("Q, K, V must share a dtype")
+    B, H, T, D = Q.shape
+    if tuple(K.shape) != (B, H, T, D) or tuple(V.shape) != (B, H, T, D):
+        raise ValueError("K/V shapes do not match Q")
+    if w_right is None:
+        w_right = w_left
+    odt = out_dtype or Q.dtype
+    if out is None:
+        out = torch.empty((B, H, T, D), dtype=odt, device=dev)
+    rc = lib.ssa_window_attn(_ptr(Q), _ptr(K), _ptr(V), _dt(Q), B, H, T, D, int(w_left),
+                             int(w_right), float(scale), _ptr(out), _dt(out), _ptr(dev_status),
+                             _stream(dev))
+    _check(rc, "ssa_window_attn")
+    return out
+
+
+def default_scale(n: int) -> float:
+    return 1.0 / math.sqrt(n)

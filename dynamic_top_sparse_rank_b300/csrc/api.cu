@@ -1,0 +1,127 @@
+// The C ABI of libssa.so: argument checks, workspace sizing, dispatch.
+// Every call validates on the host and launches nothing on a bad argument.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace ssa {
+cudaError_t topk_rows_dispatch(const void* q_low, const void* k_low, bool bf16, int P,
+                               const int64_t* row_list, int64_t rows, int Tq, int Tk, int k,
+                               int causal, float scale, int32_t* idx, float* score, uint32_t* ws,
+                               int64_t ws_slots, int64_t ws_stride, cudaStream_t stream);
+template <bool BAND>
+cudaError_t attn_rows_dispatch(const void* Q, const void* K, const void* V, bool bf16_in, int D,
+                               const int32_t* idx, void* O, bool bf16_out, int64_t rows, int Tq,
+                               int Tk, int k, int wl, int wr, float scale, int32_t* dev_status,
+                               cudaStream_t stream);
+}  // namespace ssa
+
+namespace {
+
+constexpr int kMaxK = 2048;
+constexpr int64_t kRowSlots = 1024;   // row-wise top-k: concurrent rows with a workspace slot
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool dtype_ok(int d) { return d == SSA_F32 || d == SSA_BF16; }
+bool p_ok(int P) { return P == 16 || P == 32 || P == 64 || P == 128; }
+bool d_ok(int D) { return D == 64 || D == 128; }
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// Row-wise path: one slot of Tk 32-bit keys per concurrently processed row.
+int64_t rowwise_slots(int64_t rows) { return rows < kRowSlots ? rows : kRowSlots; }
+int64_t rowwise_stride(int Tk) { return round_up((int64_t)Tk, 64); }
+
+}  // namespace
+
+extern "C" {
+
+int ssa_version(void) { return (0 << 16) | 1; }
+
+const char* ssa_status_string(int status) {
+    switch (status) {
+        case SSA_OK: return "ok";
+        case SSA_ERR_INVALID: return "invalid argument (null or misaligned pointer, bad size or dtype)";
+        case SSA_ERR_UNSUPPORTED: return "unsupported size (P in {16,32,64,128}, D in {64,128}, k <= 2048)";
+        case SSA_ERR_CUDA: return "CUDA launch or runtime error";
+        case SSA_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+size_t ssa_score_topk_workspace_size(int B, int H, int Tq, int Tk, int P, int k, int causal) {
+    (void)causal;
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || !p_ok(P) || k < 1 || k > kMaxK) return 0;
+    const int64_t rows = (int64_t)B * H * Tq;
+    if (rows == 0 || Tk == 0) return 256;
+    return (size_t)round_up(rowwise_slots(rows) * rowwise_stride(Tk) * 4, 256);
+}
+
+ssa_status ssa_score_topk(const void* q_low, const void* k_low, int dtype, int B, int H, int Tq,
+                          int Tk, int P, int k, int causal, float scale, int32_t* idx,
+                          float* score, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, void* stream) {
+    (void)dev_status;
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || !dtype_ok(dtype) || k < 1) return SSA_ERR_INVALID;
+    if (!p_ok(P) || k > kMaxK) return SSA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)B * H * Tq;
+    if (rows == 0) return SSA_OK;
+    if (!idx || !aligned(idx, 4) || (score && !aligned(score, 4))) return SSA_ERR_INVALID;
+    if (!q_low || !aligned(q_low, 16)) return SSA_ERR_INVALID;
+    if (Tk > 0 && (!k_low || !aligned(k_low, 16))) return SSA_ERR_INVALID;
+    const size_t need = ssa_score_topk_workspace_size(B, H, Tq, Tk, P, k, causal);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return SSA_ERR_WORKSPACE;
+    const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)P));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // Tk == 0: every row is empty; the row kernel writes the padding.
+    cudaError_t e = ssa::topk_rows_dispatch(q_low, k_low, dtype == SSA_BF16, P, nullptr, rows, Tq,
+                                            Tk, k, causal, sc, idx, score,
+                                            reinterpret_cast<uint32_t*>(workspace),
+                                            rowwise_slots(rows), rowwise_stride(Tk), s);
+    return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
+}
+
+ssa_status ssa_sparse_attn(const void* Q, const void* K, const void* V, int dtype, int B, int H,
+                           int Tq, int Tk, int D, const int32_t* idx, int k, float scale, void* O,
+                           int out_dtype, int32_t* dev_status, void* stream) {
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || k < 1 || !dtype_ok(dtype) || !dtype_ok(out_dtype))
+        return SSA_ERR_INVALID;
+    if (!d_ok(D)) return SSA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)B * H * Tq;
+    if (rows == 0) return SSA_OK;
+    if (!Q || !K || !V || !idx || !O) return SSA_ERR_INVALID;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(idx, 4))
+        return SSA_ERR_INVALID;
+    if (dev_status && !aligned(dev_status, 4)) return SSA_ERR_INVALID;
+    const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)D));
+    cudaError_t e = ssa::attn_rows_dispatch<false>(Q, K, V, dtype == SSA_BF16, D, idx, O,
+                                                   out_dtype == SSA_BF16, rows, Tq, Tk, k, 0, 0,
+                                                   sc, dev_status,
+                                                   reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
+}
+
+ssa_status ssa_window_attn(const void* Q, const void* K, const void* V, int dtype, int B, int H,
+                           int T, int D, int w_left, int w_right, float scale, void* O,
+                           int out_dtype, int32_t* dev_status, void* stream) {
+    if (B < 0 || H < 0 || T < 0 || w_left < 0 || w_right < 0 || !dtype_ok(dtype) ||
+        !dtype_ok(out_dtype))
+        return SSA_ERR_INVALID;
+    if (!d_ok(D)) return SSA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)B * H * T;
+    if (rows == 0) return SSA_OK;
+    if (!Q || !K || !V || !O) return SSA_ERR_INVALID;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16))
+        return SSA_ERR_INVALID;
+    if (dev_status && !aligned(dev_status, 4)) return SSA_ERR_INVALID;
+    const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)D));
+    // a radius beyond the sequence changes nothing; clamping keeps i + w in int range
+    if (w_left > T) w_left = T;
+    if (w_right > T) w_right = T;
+    cudaError_t e = ssa::attn_rows_dispatch<true>(Q, K, V, dtype == SSA_BF16, D, nullptr, O,
+                                                  out_dtype == SSA_BF16, rows, T, T, 1, w_left,
+                                                  w_right, sc, dev_status,
+                                                  reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
+}
+
+}  // extern "C"

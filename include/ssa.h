@@ -1,0 +1,169 @@
+/*
+ * ssa.h — C ABI of the dynamic top-k sparse attention library (libssa.so).
+ *
+ * The library computes the forward pass of dynamic top-k sparse attention on
+ * one NVIDIA B300 (sm_103a), in three calls:
+ *
+ *   ssa_score_topk   low-rank scorer S = q_low . k_low^T * d_proj^-0.5 fused
+ *                    with an exact per-query top-k key selection
+ *                    (mhpq.cn/news/1098205, sections 2.2 and 3.2);
+ *   ssa_sparse_attn  softmax(q . K_sel^T / sqrt(d)) . V_sel over the selected
+ *                    keys only (same page, section 3.2; scaled dot-product
+ *                    attention as in "Attention机制优化：原理、挑战与工程实践",
+ *                    section 1.1, with the online softmax of its section 2.3.1);
+ *   ssa_window_attn  sliding-window attention, keys |i - j| <= w clipped at
+ *                    the sequence ends (nxmr.cn/news/163144, section 2.2).
+ *
+ * Conventions shared by every call
+ *  - Pointers named as device pointers must point to device memory of the
+ *    current CUDA device; the caller owns every buffer. The library allocates
+ *    no device memory in these calls: scratch space is the caller's
+ *    `workspace`.
+ *  - Layouts are dense row-major: [B, H, T, d] means element (b, h, t, e) sits
+ *    at ((b*H + h)*T + t)*d + e. Every device pointer must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *    asynchronous on that stream and return after the launch.
+ *  - Host-detectable errors (null pointers, unsupported sizes, misalignment,
+ *    a workspace that is too small) return a status synchronously and launch
+ *    nothing. A failed launch returns SSA_ERR_CUDA.
+ *  - Errors found on the device (an index out of range, a bounded wait that
+ *    ran out) never trap: the kernel ORs a bit into *dev_status (an int32 in
+ *    device memory, may be NULL) and carries on or returns. The caller clears
+ *    *dev_status and reads it back when it wants to know.
+ *  - Nothing is thrown across the ABI.
+ */
+#ifndef SSA_H_
+#define SSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes of every call. */
+typedef enum {
+    SSA_OK = 0,
+    SSA_ERR_INVALID = 1,     /* null pointer, negative size, bad enum value, misaligned pointer */
+    SSA_ERR_UNSUPPORTED = 2, /* a size outside the supported set (see each call) */
+    SSA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    SSA_ERR_WORKSPACE = 4    /* workspace NULL or smaller than the size query returned */
+} ssa_status;
+
+/* Element types of tensors at the ABI. */
+typedef enum {
+    SSA_F32 = 0,  /* IEEE binary32 */
+    SSA_BF16 = 1  /* bfloat16 (upper 16 bits of a binary32) */
+} ssa_dtype;
+
+/* Bits ORed into *dev_status by kernels. */
+#define SSA_DEV_BAD_INDEX 0x1   /* an index list entry outside [-1, Tk); the entry is skipped */
+#define SSA_DEV_WAIT_LIMIT 0x2  /* a bounded device-side wait ran out; the tile is abandoned */
+#define SSA_DEV_OVERFLOW 0x4    /* internal candidate buffer overflowed; the row was redone exactly */
+
+/* Library version, (major << 16) | minor. */
+int ssa_version(void);
+
+/* Static text for a status code (never NULL). */
+const char* ssa_status_string(int status);
+
+/*
+ * Bytes of device workspace ssa_score_topk needs for these sizes (0 if the
+ * sizes are unsupported). Depends only on the arguments.
+ */
+size_t ssa_score_topk_workspace_size(int B, int H, int Tq, int Tk, int P, int k, int causal);
+
+/*
+ * ssa_score_topk — low-rank scorer fused with exact per-query top-k.
+ *
+ * Source: mhpq.cn/news/1098205, section 2.2 (scores = q_low . k_low^T scaled by
+ * d_proj^-0.5) and section 3.2 (torch.topk over the scores; top_k =
+ * min(top_k, seq_len); masked positions get -inf before selection so they are
+ * never selected).
+ *
+ * For every query row (b, h, i), with the valid key set
+ *   valid(i) = [0, Tk)                                    if causal == 0,
+ *   valid(i) = { j : 0 <= j <= i + (Tk - Tq), j < Tk }    if causal != 0
+ *              (bottom-right alignment: the last query sees every key),
+ * the score of key j is s_j = fp32(sum_p q_low[b,h,i,p] * k_low[b,h,j,p]) *
+ * scale, products and sums in fp32 (bf16 inputs are exact in fp32; integer
+ * valued inputs give exact scores). The call writes the k_eff = min(k,
+ * |valid(i)|) valid keys with the largest scores, ordered by score
+ * descending, equal scores by key index ascending (the lower index wins a tie).
+ * Slots k_eff..k-1 hold index -1 and score -inf.
+ *
+ *   q_low     device, [B, H, Tq, P], dtype `dtype`
+ *   k_low     device, [B, H, Tk, P], dtype `dtype`
+ *   dtype     SSA_F32 or SSA_BF16
+ *   P         d_proj, one of 16, 32, 64, 128
+ *   k         1 <= k <= 2048
+ *   scale     score scale; <= 0 selects fp32(1 / sqrt(P))
+ *   idx       device, int32 [B, H, Tq, k], written
+ *   score     device, float [B, H, Tq, k], written; may be NULL
+ *   workspace device scratch of at least ssa_score_topk_workspace_size(...)
+ *             bytes (its contents on entry do not matter; it is overwritten)
+ *   dev_status device int32 or NULL (see conventions)
+ *   stream    cudaStream_t
+ *
+ * Returns SSA_OK, SSA_ERR_INVALID, SSA_ERR_UNSUPPORTED, SSA_ERR_WORKSPACE or
+ * SSA_ERR_CUDA. B*H*Tq == 0 is valid and launches nothing.
+ */
+ssa_status ssa_score_topk(const void* q_low, const void* k_low, int dtype, int B, int H, int Tq,
+                          int Tk, int P, int k, int causal, float scale, int32_t* idx,
+                          float* score, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, void* stream);
+
+/*
+ * ssa_sparse_attn — attention over the selected keys only.
+ *
+ * Source: mhpq.cn/news/1098205, section 3.2 (gather the selected K and V,
+ * logits = q . k * head_dim^-0.5, softmax, weighted sum of V); the softmax is
+ * the online (running max and sum) form of "Attention机制优化：原理、挑战与工程
+ * 实践", section 2.3.1, kept in fp32 as its section 4.2 advises.
+ *
+ * For every query row (b, h, i):
+ *   O[b,h,i,:] = sum_t softmax_t(Q[b,h,i,:] . K[b,h,idx_t,:] * scale) V[b,h,idx_t,:]
+ * over the entries idx_t = idx[b,h,i,t], t < k, with idx_t != -1. Repeated
+ * entries count once per occurrence. Entries outside [-1, Tk) set
+ * SSA_DEV_BAD_INDEX in *dev_status and are skipped. A row with no usable
+ * entry outputs zeros. Arithmetic is fp32 (inputs converted exactly).
+ *
+ *   Q         device, [B, H, Tq, D], dtype `dtype`
+ *   K, V      device, [B, H, Tk, D], dtype `dtype`
+ *   D         head_dim, 64 or 128
+ *   idx       device, int32 [B, H, Tq, k] (as written by ssa_score_topk)
+ *   k         >= 1
+ *   scale     logit scale; <= 0 selects 1 / sqrt(D)
+ *   O         device, [B, H, Tq, D], dtype `out_dtype`, written
+ *             (bf16 output is rounded to nearest even)
+ */
+ssa_status ssa_sparse_attn(const void* Q, const void* K, const void* V, int dtype, int B, int H,
+                           int Tq, int Tk, int D, const int32_t* idx, int k, float scale, void* O,
+                           int out_dtype, int32_t* dev_status, void* stream);
+
+/*
+ * ssa_window_attn — sliding-window (local band) attention.
+ *
+ * Source: nxmr.cn/news/163144, section 2.2 (each token attends the positions
+ * within radius w of itself, all others get -inf before the softmax), which
+ * is also the boolean mask of "Attention机制改进：稀疏注意力应用", section
+ * 性能收益与硬件适配. It is the fixed-index special case of ssa_sparse_attn:
+ *   O[b,h,i,:] = softmax over j in [max(0, i - w_left), min(T - 1, i + w_right)]
+ *                of Q[b,h,i,:] . K[b,h,j,:] * scale, applied to V[b,h,j,:].
+ *
+ *   Q, K, V   device, [B, H, T, D], dtype `dtype`
+ *   D         64 or 128
+ *   w_left, w_right   >= 0 (the symmetric window of radius w is w, w)
+ *   scale     <= 0 selects 1 / sqrt(D)
+ *   O         device, [B, H, T, D], dtype `out_dtype`, written
+ */
+ssa_status ssa_window_attn(const void* Q, const void* K, const void* V, int dtype, int B, int H,
+                           int T, int D, int w_left, int w_right, float scale, void* O,
+                           int out_dtype, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSA_H_ */

@@ -1,0 +1,101 @@
+"""The C ABI library: it loads, exports what include/ssa.h declares, and
+rejects bad arguments on the host without launching anything (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dynamic_top_sparse_rank_b300 as ssa
+from dynamic_top_sparse_rank_b300 import _native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b(ssa_\w+)\s*\(", src, re.M))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ssa.load()
+    names = _declared()
+    assert {"ssa_score_topk", "ssa_sparse_attn", "ssa_window_attn"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+        ctypes.cast(getattr(lib, n), ctypes.c_void_p)
+    assert set(_native.EXPORTS) <= names
+
+
+def test_version_and_status_strings():
+    lib = ssa.load()
+    assert lib.ssa_version() >= 1
+    for s in range(5):
+        assert lib.ssa_status_string(s)
+    assert b"unknown" in lib.ssa_status_string(99)
+
+
+def test_workspace_size_rules():
+    f = ssa.score_topk_workspace_size
+    assert f(1, 8, 131072, 131072, 64, 512, 1) > 0
+    assert f(1, 1, 16, 16, 48, 4, 0) == 0          # unsupported P
+    assert f(1, 1, 16, 16, 64, 4096, 0) == 0       # k too large
+    assert f(1, 1, 16, 16, 64, 0, 0) == 0          # k < 1
+    assert f(0, 1, 16, 16, 64, 4, 0) > 0           # empty problem: a token size
+
+
+V = ctypes.c_void_p
+
+
+def test_host_validation_without_gpu():
+    lib = ssa.load()
+    ok_ptr = V(4096)           # aligned, never dereferenced: validation fails first
+    bad_ptr = V(4100)
+    # score_topk: null idx, unsupported P, k too large, misaligned input, workspace too small
+    assert lib.ssa_score_topk(ok_ptr, ok_ptr, 1, 1, 1, 8, 8, 64, 4, 0, 0.0, None, None, ok_ptr,
+                              1 << 20, None, None) == _native.SSA_ERR_INVALID
+    assert lib.ssa_score_topk(ok_ptr, ok_ptr, 1, 1, 1, 8, 8, 48, 4, 0, 0.0, ok_ptr, None, ok_ptr,
+                              1 << 20, None, None) == _native.SSA_ERR_UNSUPPORTED
+    assert lib.ssa_score_topk(ok_ptr, ok_ptr, 1, 1, 1, 8, 8, 64, 4096, 0, 0.0, ok_ptr, None,
+                              ok_ptr, 1 << 20, None, None) == _native.SSA_ERR_UNSUPPORTED
+    assert lib.ssa_score_topk(bad_ptr, ok_ptr, 1, 1, 1, 8, 8, 64, 4, 0, 0.0, ok_ptr, None, ok_ptr,
+                              1 << 20, None, None) == _native.SSA_ERR_INVALID
+    assert lib.ssa_score_topk(ok_ptr, ok_ptr, 1, 1, 1, 8, 8, 64, 4, 0, 0.0, ok_ptr, None, ok_ptr,
+                              16, None, None) == _native.SSA_ERR_WORKSPACE
+    assert lib.ssa_score_topk(ok_ptr, ok_ptr, 7, 1, 1, 8, 8, 64, 4, 0, 0.0, ok_ptr, None, ok_ptr,
+                              1 << 20, None, None) == _native.SSA_ERR_INVALID
+    # empty problem: nothing to do, nothing launched
+    assert lib.ssa_score_topk(None, None, 1, 0, 1, 8, 8, 64, 4, 0, 0.0, None, None, None, 0,
+                              None, None) == _native.SSA_OK
+    # sparse_attn: unsupported D, null idx, misaligned O, bad out dtype
+    assert lib.ssa_sparse_attn(ok_ptr, ok_ptr, ok_ptr, 1, 1, 1, 8, 8, 96, ok_ptr, 4, 0.0, ok_ptr,
+                               1, None, None) == _native.SSA_ERR_UNSUPPORTED
+    assert lib.ssa_sparse_attn(ok_ptr, ok_ptr, ok_ptr, 1, 1, 1, 8, 8, 64, None, 4, 0.0, ok_ptr,
+                               1, None, None) == _native.SSA_ERR_INVALID
+    assert lib.ssa_sparse_attn(ok_ptr, ok_ptr, ok_ptr, 1, 1, 1, 8, 8, 64, ok_ptr, 4, 0.0, bad_ptr,
+                               1, None, None) == _native.SSA_ERR_INVALID
+    assert lib.ssa_sparse_attn(ok_ptr, ok_ptr, ok_ptr, 1, 1, 1, 8, 8, 64, ok_ptr, 4, 0.0, ok_ptr,
+                               5, None, None) == _native.SSA_ERR_INVALID
+    # window_attn: negative radius, unsupported D
+    assert lib.ssa_window_attn(ok_ptr, ok_ptr, ok_ptr, 1, 1, 1, 8, 64, -1, 2, 0.0, ok_ptr, 1,
+                               None, None) == _native.SSA_ERR_INVALID
+    assert lib.ssa_window_attn(ok_ptr, ok_ptr, ok_ptr, 1, 1, 1, 8, 32, 1, 2, 0.0, ok_ptr, 1,
+                               None, None) == _native.SSA_ERR_UNSUPPORTED
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ssa.ssa_score_topk(x, x, 4, False)
+    with pytest.raises(ValueError):
+        ssa.ssa_window_attn(x, x, x, 2)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(OSError):
+        _native.load(str(tmp_path / "libssa.so"))
