@@ -23,7 +23,11 @@ SSA_F32, SSA_BF16 = 0, 1
 SSA_DEV_BAD_INDEX, SSA_DEV_WAIT_LIMIT, SSA_DEV_OVERFLOW = 0x1, 0x2, 0x4
 
 EXPORTS = ("ssa_version", "ssa_status_string", "ssa_score_topk_workspace_size", "ssa_score_topk",
-           "ssa_sparse_attn", "ssa_window_attn")
+           "ssa_sparse_attn", "ssa_window_attn", "ssa_score_topk_noalloc")
+
+# Fixed scratch of ssa_score_topk_noalloc and the largest Tk it accepts.
+NOALLOC_SCRATCH_BYTES = 32 << 20
+NOALLOC_MAX_TK = NOALLOC_SCRATCH_BYTES // 4
 
 
 class SSAError(RuntimeError):
@@ -58,6 +62,8 @@ def load(path: str | None = None):
     lib.ssa_sparse_attn.argtypes = [V, V, V, I, I, I, I, I, I, V, I, F, V, I, V, V]
     lib.ssa_window_attn.restype = I
     lib.ssa_window_attn.argtypes = [V, V, V, I, I, I, I, I, I, I, F, V, I, V, V]
+    lib.ssa_score_topk_noalloc.restype = I
+    lib.ssa_score_topk_noalloc.argtypes = [V, V, I, I, I, I, I, I, I, I, F, V, V, V, V]
     if path is None:
         _lib = lib
     return lib
@@ -140,6 +146,36 @@ def ssa_score_topk(q_low: torch.Tensor, k_low: torch.Tensor, k: int, causal: boo
                             int(bool(causal)), float(scale), _ptr(idx), _ptr(score),
                             _ptr(workspace), wbytes, _ptr(dev_status), _stream(dev))
     _check(rc, "ssa_score_topk")
+    return (idx, score) if with_score else idx
+
+
+def ssa_score_topk_noalloc(q_low: torch.Tensor, k_low: torch.Tensor, k: int, causal: bool,
+                           scale: float = 0.0, with_score: bool = False, idx: torch.Tensor = None,
+                           score: torch.Tensor = None, dev_status: torch.Tensor = None):
+    """ssa_score_topk without a workspace, for callers that cannot allocate
+    device memory where they run the op: the library's fixed 32 MiB scratch
+    array is used instead (Tk <= 8,388,608). Outputs are allocated here only
+    when the caller does not pass them. Calls that overlap on the GPU race on
+    the shared scratch."""
+    lib = load()
+    dev = _dev(q_low, k_low, idx, score, dev_status)
+    if q_low.dtype != k_low.dtype:
+        raise TypeError("q_low and k_low must share a dtype")
+    B, H, Tq, P = q_low.shape
+    Tk = k_low.shape[2]
+    if tuple(k_low.shape) != (B, H, Tk, P):
+        raise ValueError("k_low shape %s does not match q_low %s" % (tuple(k_low.shape), tuple(q_low.shape)))
+    if Tk > NOALLOC_MAX_TK:
+        raise ValueError("ssa_score_topk_noalloc: Tk=%d exceeds the fixed scratch limit %d"
+                         % (Tk, NOALLOC_MAX_TK))
+    if idx is None:
+        idx = torch.empty((B, H, Tq, k), dtype=torch.int32, device=dev)
+    if with_score and score is None:
+        score = torch.empty((B, H, Tq, k), dtype=torch.float32, device=dev)
+    rc = lib.ssa_score_topk_noalloc(_ptr(q_low), _ptr(k_low), _dt(q_low), B, H, Tq, Tk, P, k,
+                                    int(bool(causal)), float(scale), _ptr(idx), _ptr(score),
+                                    _ptr(dev_status), _stream(dev))
+    _check(rc, "ssa_score_topk_noalloc")
     return (idx, score) if with_score else idx
 
 

@@ -162,6 +162,37 @@ ssa_status ssa_window_attn(const void* Q, const void* K, const void* V, int dtyp
                            int T, int D, int w_left, int w_right, float scale, void* O,
                            int out_dtype, int32_t* dev_status, void* stream);
 
+/*
+ * ssa_score_topk_noalloc — ssa_score_topk for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this call: it exists for users of this
+ * library that may not allocate device memory where they run the op — a plugin
+ * inside an inference engine that hands its ops a pre-sized memory arena and
+ * no allocator, or a latency-critical loop that must never call cudaMalloc
+ * (it can synchronize the device and its cost is unbounded). Such a caller
+ * passes inputs and outputs as for ssa_score_topk, but no workspace.
+ *
+ * It computes exactly what ssa_score_topk computes (same arguments, same
+ * results), always with the row-wise kernel, whose scratch lives in one fixed
+ * 32 MiB device array inside this library (every device that loads the
+ * library holds it until the process exits). The kernel needs
+ * round_up(Tk, 64) * 4 bytes of it per query row in flight, so Tk may be at
+ * most 8,388,608; larger Tk returns SSA_ERR_UNSUPPORTED and launches nothing.
+ * The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. All calls share the one array and it keeps the last call's
+ * contents (the kernel overwrites every scratch word before reading it, so
+ * nothing needs clearing); calls whose kernels overlap on the GPU (different
+ * streams, no ordering between them) race on it and must be serialized by
+ * the caller.
+ */
+ssa_status ssa_score_topk_noalloc(const void* q_low, const void* k_low, int dtype, int B, int H,
+                                  int Tq, int Tk, int P, int k, int causal, float scale,
+                                  int32_t* idx, float* score, int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
