@@ -174,6 +174,60 @@ int oracle_topk_rows(const double* q_rows, const int64_t* qpos, int64_t n, const
     return 0;
 }
 
+/* ------------------------------------------------------------ scores only */
+
+typedef struct {
+    const double* q_rows; /* [n, P] */
+    const int64_t* qpos;  /* [n] */
+    const double* k_low;  /* [Tk, P] */
+    int64_t Tq, Tk;
+    int P, causal;
+    float scale;
+    float* out;           /* [n, Tk] */
+} scores_ctx;
+
+static void scores_row(void* vctx, int64_t r) {
+    scores_ctx* c = (scores_ctx*)vctx;
+    const double* q = c->q_rows + r * c->P;
+    int64_t nv = valid_count(c->qpos[r], c->Tq, c->Tk, c->causal);
+    float* o = c->out + r * c->Tk;
+    for (int64_t j = 0; j < c->Tk; ++j) {
+        if (j >= nv) {
+            o[j] = -INFINITY; /* masked: never selectable */
+            continue;
+        }
+        const double* kr = c->k_low + j * c->P;
+        double acc = 0.0;
+        for (int p = 0; p < c->P; ++p) acc += q[p] * kr[p];
+        float s = (float)acc;
+        o[j] = s * c->scale;
+    }
+}
+
+/*
+ * The low-rank scorer alone (mhpq.cn/news/1098205, section 2.2):
+ * S[r, j] = fp32(q_low[r] . k_low[j]) * scale for the keys query qpos[r] may
+ * see, -inf for the masked ones (section 3.2, note 3). scale <= 0 selects
+ * d_proj^-0.5 rounded to fp32.
+ */
+int oracle_scores_rows(const double* q_rows, const int64_t* qpos, int64_t n, const double* k_low,
+                       int64_t Tq, int64_t Tk, int P, int causal, float scale, float* out,
+                       int nthreads) {
+    if (!q_rows || !qpos || !k_low || !out || n < 0 || Tk < 0 || P < 1) return 1;
+    scores_ctx c;
+    c.q_rows = q_rows;
+    c.qpos = qpos;
+    c.k_low = k_low;
+    c.Tq = Tq;
+    c.Tk = Tk;
+    c.P = P;
+    c.causal = causal;
+    c.scale = scale > 0.f ? scale : (float)(1.0 / sqrt((double)P));
+    c.out = out;
+    for_rows(scores_row, &c, n, nthreads);
+    return 0;
+}
+
 /* ---------------------------------------------------------------- attend */
 
 /* softmax(q . K_t * scale) weighted sum of V_t over the listed keys, fp64. */

@@ -48,6 +48,8 @@ def _load():
         lib.oracle_attn_rows.restype = i64
         lib.oracle_window_rows.argtypes = [P, P, i64, P, P, i64, i32, i32, i32, f64, P, i32]
         lib.oracle_window_rows.restype = i32
+        lib.oracle_scores_rows.argtypes = [P, P, i64, P, i64, i64, i32, i32, f32, P, i32]
+        lib.oracle_scores_rows.restype = i32
         _lib = lib
     return _lib
 
@@ -93,6 +95,35 @@ def topk_rows(q_rows, qpos, k_low, k: int, Tq: int, causal: bool, scale: float =
     if rc != 0:
         raise ValueError("oracle_topk_rows: bad arguments")
     return idx, sc
+
+
+def scores_rows(q_rows, qpos, k_low, Tq: int, causal: bool, scale: float = 0.0,
+                nthreads: int | None = None):
+    """Scaled low-rank scores of one head's query rows against all Tk keys,
+    float32 [n, Tk]; masked keys hold -inf."""
+    q = _f64(q_rows)
+    kl = _f64(k_low)
+    pos = np.ascontiguousarray(np.asarray(qpos, dtype=np.int64))
+    n, P = q.shape
+    Tk = kl.shape[0]
+    out = np.empty((n, Tk), dtype=np.float32)
+    rc = _load().oracle_scores_rows(_ptr(q), _ptr(pos), n, _ptr(kl), Tq, Tk, P, int(causal),
+                                    float(scale), _ptr(out), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_scores_rows: bad arguments")
+    return out
+
+
+def scores(q_low, k_low, causal: bool, scale: float = 0.0, nthreads: int | None = None):
+    """Scaled low-rank scores [B,H,Tq,Tk] (float32, -inf where masked)."""
+    B, H, Tq, P = q_low.shape
+    Tk = k_low.shape[2]
+    out = np.empty((B, H, Tq, Tk), np.float32)
+    for b in range(B):
+        for h in range(H):
+            out[b, h] = scores_rows(q_low[b, h], np.arange(Tq), k_low[b, h], Tq, causal, scale,
+                                    nthreads)
+    return out
 
 
 def attn_rows(q_rows, K, V, idx, scale: float = 0.0, nthreads: int | None = None):

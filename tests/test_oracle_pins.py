@@ -318,3 +318,40 @@ def test_golden_selection_fraction_at_128k():
     idx, _ = oracle.topk_rows(q[0, 0, i:i + 1], [i], kl[0, 0], w.k, w.Tq, True)
     assert (idx >= 0).sum() == gold["k"]
     assert round(100.0 * (idx >= 0).sum() / gold["n"], 1) == gold["percent_one_decimal"]
+
+
+# ------------------------------------------------------------ scorer alone
+
+@pytest.mark.parametrize("Tq,Tk,P,causal,scale", [
+    (9, 9, 16, False, 0.0), (7, 20, 64, True, 0.0), (20, 7, 64, True, 0.0),
+    (12, 12, 32, True, 0.5),
+])
+def test_scores_equal_exact_integer_product(Tq, Tk, P, causal, scale):
+    """Integer data: every score is an integer dot product (exact in int64)
+    times a power-of-two scale, so the oracle must reproduce it exactly; keys
+    outside the bottom-right causal band hold -inf."""
+    q = _rand_int((Tq, P), 5 + Tq)
+    kl = _rand_int((Tk, P), 6 + Tk)
+    S = oracle.scores_rows(q, np.arange(Tq), kl, Tq, causal, scale)
+    dots = q.astype(np.int64) @ kl.astype(np.int64).T
+    sc = scale if scale > 0 else 1.0 / math.isqrt(P)     # P = 16, 64: exact powers of two
+    for i in range(Tq):
+        for j in range(Tk):
+            if causal and j > i + (Tk - Tq):
+                assert S[i, j] == -np.inf
+            else:
+                assert S[i, j] == dots[i, j] * sc
+
+
+def test_scores_rank_like_the_selection():
+    """The selection is the top of each score row: sorting a row of
+    oracle.scores by (score desc, index asc) gives oracle.topk_rows."""
+    Tq, Tk, P, k = 30, 50, 16, 12
+    q = _rand_int((Tq, P), 11)
+    kl = _rand_int((Tk, P), 12)
+    S = oracle.scores_rows(q, np.arange(Tq), kl, Tq, True)
+    idx, sc = oracle.topk_rows(q, np.arange(Tq), kl, k, Tq, True)
+    for i in range(Tq):
+        order = sorted((j for j in range(Tk) if S[i, j] > -np.inf), key=lambda j: (-S[i, j], j))
+        want = (order + [-1] * k)[:k]
+        assert list(idx[i]) == want
