@@ -23,7 +23,7 @@ SSA_F32, SSA_BF16 = 0, 1
 SSA_DEV_BAD_INDEX, SSA_DEV_WAIT_LIMIT, SSA_DEV_OVERFLOW = 0x1, 0x2, 0x4
 
 EXPORTS = ("ssa_version", "ssa_status_string", "ssa_score_topk_workspace_size", "ssa_score_topk",
-           "ssa_sparse_attn", "ssa_window_attn", "ssa_score_topk_noalloc")
+           "ssa_sparse_attn", "ssa_window_attn", "ssa_score_topk_noalloc", "ssa_lowrank_scores")
 
 # Fixed scratch of ssa_score_topk_noalloc and the largest Tk it accepts.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -64,6 +64,8 @@ def load(path: str | None = None):
     lib.ssa_window_attn.argtypes = [V, V, V, I, I, I, I, I, I, I, F, V, I, V, V]
     lib.ssa_score_topk_noalloc.restype = I
     lib.ssa_score_topk_noalloc.argtypes = [V, V, I, I, I, I, I, I, I, I, F, V, V, V, V]
+    lib.ssa_lowrank_scores.restype = I
+    lib.ssa_lowrank_scores.argtypes = [V, V, I, I, I, I, I, I, I, F, V, V, V]
     if path is None:
         _lib = lib
     return lib
@@ -177,6 +179,31 @@ def ssa_score_topk_noalloc(q_low: torch.Tensor, k_low: torch.Tensor, k: int, cau
                                     _ptr(dev_status), _stream(dev))
     _check(rc, "ssa_score_topk_noalloc")
     return (idx, score) if with_score else idx
+
+
+def ssa_lowrank_scores(q_low: torch.Tensor, k_low: torch.Tensor, causal: bool,
+                       scale: float = 0.0, out: torch.Tensor = None,
+                       dev_status: torch.Tensor = None) -> torch.Tensor:
+    """The scaled low-rank scores S [B,H,Tq,Tk] (float32, -inf where masked).
+
+    Materialises the whole score matrix: meant for inspection and small
+    problems; the selection path never stores it.
+    """
+    lib = load()
+    dev = _dev(q_low, k_low, out, dev_status)
+    if q_low.dtype != k_low.dtype:
+        raise TypeError("q_low and k_low must share a dtype")
+    B, H, Tq, P = q_low.shape
+    Tk = k_low.shape[2]
+    if tuple(k_low.shape) != (B, H, Tk, P):
+        raise ValueError("k_low shape %s does not match q_low %s" % (tuple(k_low.shape), tuple(q_low.shape)))
+    if out is None:
+        out = torch.empty((B, H, Tq, Tk), dtype=torch.float32, device=dev)
+    rc = lib.ssa_lowrank_scores(_ptr(q_low), _ptr(k_low), _dt(q_low), B, H, Tq, Tk, P,
+                                int(bool(causal)), float(scale), _ptr(out), _ptr(dev_status),
+                                _stream(dev))
+    _check(rc, "ssa_lowrank_scores")
+    return out
 
 
 def ssa_sparse_attn(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, idx: torch.Tensor,

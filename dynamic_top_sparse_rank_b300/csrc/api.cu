@@ -3,12 +3,19 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "tile.h"
 
 namespace ssa {
 cudaError_t topk_rows_dispatch(const void* q_low, const void* k_low, bool bf16, int P,
-                               const int64_t* row_list, int64_t rows, int Tq, int Tk, int k,
-                               int causal, float scale, int32_t* idx, float* score, uint32_t* ws,
-                               int64_t ws_slots, int64_t ws_stride, cudaStream_t stream);
+                               const int64_t* row_list, int64_t rows, const int32_t* rows_dev,
+                               int Tq, int Tk, int k, int causal, float scale, int32_t* idx,
+                               float* score, uint32_t* ws, int64_t ws_slots, int64_t ws_stride,
+                               cudaStream_t stream);
+cudaError_t tile_select_launch(const uint16_t* gm, uint32_t* tau, int BH, int Tq, int Tk, int k,
+                               int causal, cudaStream_t stream);
+cudaError_t tile_sort_launch(const uint64_t* cand, const int32_t* cnt, int64_t rows, int Tq,
+                             int Tk, int k, int causal, int32_t* idx, float* score,
+                             int64_t* ovf_list, int32_t* ovf_count, cudaStream_t stream);
 template <bool BAND>
 cudaError_t attn_rows_dispatch(const void* Q, const void* K, const void* V, bool bf16_in, int D,
                                const int32_t* idx, void* O, bool bf16_out, int64_t rows, int Tq,
@@ -31,6 +38,13 @@ int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int64_t rowwise_slots(int64_t rows) { return rows < kRowSlots ? rows : kRowSlots; }
 int64_t rowwise_stride(int Tk) { return round_up((int64_t)Tk, 64); }
 
+// The tensor-core path serves bf16 scorer inputs with d_proj 64 or 128 and
+// k <= 512 when there are enough query rows per head to fill 128-row tiles;
+// everything else (decode, fp32, other d_proj, larger k) runs row-wise.
+bool use_tile_path(int dtype, int P, int Tq, int Tk, int k) {
+    return dtype == SSA_BF16 && (P == 64 || P == 128) && k <= 512 && Tq >= 64 && Tk > 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -48,19 +62,27 @@ const char* ssa_status_string(int status) {
     }
 }
 
+static size_t path_workspace_bytes(int dtype, int B, int H, int Tq, int Tk, int P, int k) {
+    const int64_t rows = (int64_t)B * H * Tq;
+    if (rows == 0 || Tk == 0) return 256;
+    if (use_tile_path(dtype, P, Tq, Tk, k))
+        return ssa::tile_workspace((int64_t)B * H, Tq, Tk, k).total;
+    return (size_t)round_up(rowwise_slots(rows) * rowwise_stride(Tk) * 4, 256);
+}
+
 size_t ssa_score_topk_workspace_size(int B, int H, int Tq, int Tk, int P, int k, int causal) {
     (void)causal;
     if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || !p_ok(P) || k < 1 || k > kMaxK) return 0;
-    const int64_t rows = (int64_t)B * H * Tq;
-    if (rows == 0 || Tk == 0) return 256;
-    return (size_t)round_up(rowwise_slots(rows) * rowwise_stride(Tk) * 4, 256);
+    // the larger of the two paths' needs, so the size does not depend on dtype
+    const size_t a = path_workspace_bytes(SSA_BF16, B, H, Tq, Tk, P, k);
+    const size_t b = path_workspace_bytes(SSA_F32, B, H, Tq, Tk, P, k);
+    return a > b ? a : b;
 }
 
 ssa_status ssa_score_topk(const void* q_low, const void* k_low, int dtype, int B, int H, int Tq,
                           int Tk, int P, int k, int causal, float scale, int32_t* idx,
                           float* score, void* workspace, size_t workspace_bytes,
                           int32_t* dev_status, void* stream) {
-    (void)dev_status;
     if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || !dtype_ok(dtype) || k < 1) return SSA_ERR_INVALID;
     if (!p_ok(P) || k > kMaxK) return SSA_ERR_UNSUPPORTED;
     const int64_t rows = (int64_t)B * H * Tq;
@@ -68,15 +90,81 @@ ssa_status ssa_score_topk(const void* q_low, const void* k_low, int dtype, int B
     if (!idx || !aligned(idx, 4) || (score && !aligned(score, 4))) return SSA_ERR_INVALID;
     if (!q_low || !aligned(q_low, 16)) return SSA_ERR_INVALID;
     if (Tk > 0 && (!k_low || !aligned(k_low, 16))) return SSA_ERR_INVALID;
-    const size_t need = ssa_score_topk_workspace_size(B, H, Tq, Tk, P, k, causal);
-    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return SSA_ERR_WORKSPACE;
+    if (dev_status && !aligned(dev_status, 4)) return SSA_ERR_INVALID;
+    const size_t need = path_workspace_bytes(dtype, B, H, Tq, Tk, P, k);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SSA_ERR_WORKSPACE;
     const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)P));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // Tk == 0: every row is empty; the row kernel writes the padding.
-    cudaError_t e = ssa::topk_rows_dispatch(q_low, k_low, dtype == SSA_BF16, P, nullptr, rows, Tq,
-                                            Tk, k, causal, sc, idx, score,
-                                            reinterpret_cast<uint32_t*>(workspace),
-                                            rowwise_slots(rows), rowwise_stride(Tk), s);
+    if (!use_tile_path(dtype, P, Tq, Tk, k)) {
+        // Tk == 0: every row is empty; the row kernel writes the padding.
+        cudaError_t e = ssa::topk_rows_dispatch(q_low, k_low, dtype == SSA_BF16, P, nullptr, rows,
+                                                nullptr, Tq, Tk, k, causal, sc, idx, score,
+                                                reinterpret_cast<uint32_t*>(workspace),
+                                                rowwise_slots(rows), rowwise_stride(Tk), s);
+        return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
+    }
+    // tensor-core path: group maxima -> per-row bound -> candidates -> sort,
+    // rows whose candidates overflow redone row-wise
+    const int BH = B * H;
+    const ssa::TileWorkspace w = ssa::tile_workspace(BH, Tq, Tk, k);
+    char* ws = reinterpret_cast<char*>(workspace);
+    int32_t* ovf_count = reinterpret_cast<int32_t*>(ws + w.ovf_count);
+    uint32_t* tau = reinterpret_cast<uint32_t*>(ws + w.tau);
+    int32_t* cnt = reinterpret_cast<int32_t*>(ws + w.cnt);
+    int64_t* ovf_list = reinterpret_cast<int64_t*>(ws + w.ovf_list);
+    uint16_t* gm = reinterpret_cast<uint16_t*>(ws + w.gm);
+    uint64_t* cand = reinterpret_cast<uint64_t*>(ws + w.cand);
+    ssa::TileParams p = {};
+    p.BH = BH;
+    p.Tq = Tq;
+    p.Tk = Tk;
+    p.k = k;
+    p.causal = causal ? 1 : 0;
+    p.scale = sc;
+    p.gm = gm;
+    p.G_stride = ssa::tile_group_stride(k);
+    p.tau = tau;
+    p.cand = cand;
+    p.cnt = cnt;
+    p.cap = ssa::tile_cand_cap(k);
+    p.dev_status = dev_status;
+    cudaError_t e = cudaMemsetAsync(ovf_count, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = ssa::tile_scores_launch(q_low, k_low, P, ssa::MODE_GROUPMAX, p, s);
+    if (e == cudaSuccess) e = ssa::tile_select_launch(gm, tau, BH, Tq, Tk, k, p.causal, s);
+    if (e == cudaSuccess) e = ssa::tile_scores_launch(q_low, k_low, P, ssa::MODE_COLLECT, p, s);
+    if (e == cudaSuccess)
+        e = ssa::tile_sort_launch(cand, cnt, rows, Tq, Tk, k, p.causal, idx, score, ovf_list,
+                                  ovf_count, s);
+    if (e == cudaSuccess)
+        e = ssa::topk_rows_dispatch(q_low, k_low, true, P, ovf_list, rows, ovf_count, Tq, Tk, k,
+                                    p.causal, sc, idx, score,
+                                    reinterpret_cast<uint32_t*>(ws + w.rowwise), w.rowwise_slots,
+                                    w.rowwise_stride, s);
+    return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
+}
+
+ssa_status ssa_lowrank_scores(const void* q_low, const void* k_low, int dtype, int B, int H,
+                              int Tq, int Tk, int P, int causal, float scale, float* S,
+                              int32_t* dev_status, void* stream) {
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || !dtype_ok(dtype)) return SSA_ERR_INVALID;
+    if (!p_ok(P)) return SSA_ERR_UNSUPPORTED;
+    if (dtype != SSA_BF16 || !(P == 64 || P == 128)) return SSA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)B * H * Tq;
+    if (rows == 0 || Tk == 0) return SSA_OK;
+    if (!S || !aligned(S, 4) || !q_low || !k_low || !aligned(q_low, 16) || !aligned(k_low, 16))
+        return SSA_ERR_INVALID;
+    if (dev_status && !aligned(dev_status, 4)) return SSA_ERR_INVALID;
+    ssa::TileParams p = {};
+    p.BH = B * H;
+    p.Tq = Tq;
+    p.Tk = Tk;
+    p.k = 1;
+    p.causal = causal ? 1 : 0;
+    p.scale = scale > 0.f ? scale : (float)(1.0 / sqrt((double)P));
+    p.S = S;
+    p.dev_status = dev_status;
+    cudaError_t e = ssa::tile_scores_launch(q_low, k_low, P, ssa::MODE_RAW, p,
+                                            reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
 }
 

@@ -14,9 +14,10 @@
 
 namespace ssa {
 cudaError_t topk_rows_dispatch(const void* q_low, const void* k_low, bool bf16, int P,
-                               const int64_t* row_list, int64_t rows, int Tq, int Tk, int k,
-                               int causal, float scale, int32_t* idx, float* score, uint32_t* ws,
-                               int64_t ws_slots, int64_t ws_stride, cudaStream_t stream);
+                               const int64_t* row_list, int64_t rows, const int32_t* rows_dev,
+                               int Tq, int Tk, int k, int causal, float scale, int32_t* idx,
+                               float* score, uint32_t* ws, int64_t ws_slots, int64_t ws_stride,
+                               cudaStream_t stream);
 }  // namespace ssa
 
 namespace {
@@ -78,8 +79,8 @@ extern "C" ssa_status ssa_score_topk_noalloc(const void* q_low, const void* k_lo
     void* scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess) return SSA_ERR_CUDA;
     const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)P));
-    cudaError_t e = ssa::topk_rows_dispatch(q_low, k_low, dtype == SSA_BF16, P, nullptr, rows, Tq,
-                                            Tk, k, causal, sc, idx, score,
+    cudaError_t e = ssa::topk_rows_dispatch(q_low, k_low, dtype == SSA_BF16, P, nullptr, rows,
+                                            nullptr, Tq, Tk, k, causal, sc, idx, score,
                                             reinterpret_cast<uint32_t*>(scratch), slots, stride,
                                             reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;

@@ -1,0 +1,97 @@
+// Definitions shared by the tensor-core score+top-k path (host and device):
+// tile sizes, the per-row valid key count, the group size rule, the launch
+// parameters of the tile kernel and the workspace layout of the whole path.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssa {
+
+constexpr int kTileM = 128;   // query rows per unit (TMEM lanes)
+constexpr int kTileN = 128;   // keys per MMA tile (TMEM columns per buffer)
+
+enum TileMode { MODE_RAW = 0, MODE_GROUPMAX = 1, MODE_COLLECT = 2 };
+
+// Number of keys query i may select: all Tk, or under the bottom-right causal
+// mask the keys j <= i + (Tk - Tq).
+__host__ __device__ __forceinline__ int tile_valid_count(int i, int Tq, int Tk, int causal) {
+    if (!causal) return Tk;
+    const int64_t last = static_cast<int64_t>(i) + (Tk - Tq);
+    if (last < 0) return 0;
+    return last + 1 < Tk ? static_cast<int>(last + 1) : Tk;
+}
+
+// Group size g of a unit whose rows have between n_lo and n_hi valid keys.
+// Every row with more than k valid keys must be split into at least 2k
+// groups (so that the k-th largest group maximum is a tight lower bound on
+// the k-th largest score), and g is a power of two. 0 when no row of the unit
+// has more than k valid keys (every valid key is then selected).
+__host__ __device__ __forceinline__ int tile_group_size(int n_lo, int n_hi, int k) {
+    if (n_hi <= k) return 0;
+    const int n_ref = n_lo > k + 1 ? n_lo : k + 1;
+    const int q = n_ref / (2 * k);
+    int g = 1;
+    while (g * 2 <= q) g *= 2;
+    return g;
+}
+
+// Groups per row and unit that the group-maximum array reserves: a row has at
+// most ceil(n_hi / g) groups, which stays below 4k + 128 for every unit.
+__host__ __device__ __forceinline__ int tile_group_stride(int k) { return 4 * k + 128; }
+
+// Candidate capacity per row: twice the next power of two >= k. The bound
+// from the group maxima leaves about 1.25 k candidates; a row with more
+// (heavy ties at its k-th score) is recomputed by the row-wise kernel.
+__host__ __device__ __forceinline__ int tile_cand_cap(int k) {
+    int c = 32;
+    while (c < k) c *= 2;
+    return 2 * c;
+}
+
+struct TileParams {
+    int BH, Tq, Tk, k, causal;
+    float scale;
+    int units_per_head, num_units;   // filled by the launcher
+    float* S;                        // MODE_RAW: [BH, Tq, Tk]
+    uint16_t* gm;                    // MODE_GROUPMAX: [units, G_stride, 128]
+    int G_stride;
+    const uint32_t* tau;             // MODE_COLLECT: [BH*Tq] order-key thresholds
+    uint64_t* cand;                  // MODE_COLLECT: [BH*Tq, cap] composite keys
+    int32_t* cnt;                    // MODE_COLLECT: [BH*Tq] candidates found
+    int cap;
+    int32_t* dev_status;
+    uint64_t wait_limit_ns;          // 0: one second
+};
+
+cudaError_t tile_scores_launch(const void* q_low, const void* k_low, int P, int mode,
+                               TileParams p, cudaStream_t stream);
+int tile_sm_count();
+
+// Workspace of the tile path, carved from the caller's buffer (offsets in
+// bytes, each 256-byte aligned).
+struct TileWorkspace {
+    size_t ovf_count, tau, cnt, ovf_list, gm, cand, rowwise, total;
+    int64_t rowwise_slots, rowwise_stride;
+};
+
+inline TileWorkspace tile_workspace(int64_t BH, int Tq, int Tk, int k) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    TileWorkspace w;
+    const int64_t rows = BH * Tq;
+    const int64_t units = BH * ((Tq + kTileM - 1) / kTileM);
+    size_t o = 0;
+    w.ovf_count = o; o += 256;
+    w.tau = o; o += up(rows * 4);
+    w.cnt = o; o += up(rows * 4);
+    w.ovf_list = o; o += up(rows * 8);
+    w.gm = o; o += up(static_cast<size_t>(units) * tile_group_stride(k) * kTileM * 2);
+    w.cand = o; o += up(static_cast<size_t>(rows) * tile_cand_cap(k) * 8);
+    w.rowwise_slots = rows < 256 ? rows : 256;
+    w.rowwise_stride = (static_cast<int64_t>(Tk) + 63) / 64 * 64;
+    w.rowwise = o; o += up(static_cast<size_t>(w.rowwise_slots) * w.rowwise_stride * 4);
+    w.total = o;
+    return w;
+}
+
+}  // namespace ssa

@@ -114,8 +114,9 @@ struct ScoreGeom {
 template <bool BF16, int P>
 __global__ void __launch_bounds__(TOPK_THREADS) topk_rows_kernel(
     const void* __restrict__ q_low, const void* __restrict__ k_low, const int64_t* __restrict__ row_list,
-    int64_t rows, int Tq, int Tk, int k, int causal, float scale, int32_t* __restrict__ idx_out,
-    float* __restrict__ score_out, uint32_t* __restrict__ ws, int64_t ws_stride) {
+    int64_t rows, const int32_t* __restrict__ rows_dev, int Tq, int Tk, int k, int causal,
+    float scale, int32_t* __restrict__ idx_out, float* __restrict__ score_out,
+    uint32_t* __restrict__ ws, int64_t ws_stride) {
     using Gm = ScoreGeom<BF16, P>;
     constexpr int L = Gm::L, G = Gm::G, E = Gm::E, R = Gm::R;
     __shared__ uint32_t hist[256];
@@ -128,6 +129,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_rows_kernel(
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane / L, s = lane % L;
     uint32_t* wrow = ws + (int64_t)blockIdx.x * ws_stride;
+    if (rows_dev) rows = *rows_dev;   // row count known only on the device
 
     for (int64_t rr = blockIdx.x; rr < rows; rr += gridDim.x) {
         const int64_t row = row_list ? row_list[rr] : rr;
@@ -292,16 +294,20 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_rows_kernel(
     }
 }
 
+// rows_dev != NULL: the number of rows of row_list is read on the device
+// (at most `rows`), so a list built by an earlier kernel needs no host sync.
 cudaError_t topk_rows_dispatch(const void* q_low, const void* k_low, bool bf16, int P,
-                               const int64_t* row_list, int64_t rows, int Tq, int Tk, int k,
-                               int causal, float scale, int32_t* idx, float* score, uint32_t* ws,
-                               int64_t ws_slots, int64_t ws_stride, cudaStream_t stream) {
+                               const int64_t* row_list, int64_t rows, const int32_t* rows_dev,
+                               int Tq, int Tk, int k, int causal, float scale, int32_t* idx,
+                               float* score, uint32_t* ws, int64_t ws_slots, int64_t ws_stride,
+                               cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
     const int64_t grid = rows < ws_slots ? rows : ws_slots;
 #define SSA_TOPK_CASE(BF, PP)                                                                \
     if (bf16 == BF && P == PP) {                                                             \
         topk_rows_kernel<BF, PP><<<(unsigned)grid, TOPK_THREADS, 0, stream>>>(              \
-            q_low, k_low, row_list, rows, Tq, Tk, k, causal, scale, idx, score, ws, ws_stride); \
+            q_low, k_low, row_list, rows, rows_dev, Tq, Tk, k, causal, scale, idx, score, ws,  \
+            ws_stride);                                                                      \
         return cudaGetLastError();                                                           \
     }
     SSA_TOPK_CASE(true, 16)

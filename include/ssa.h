@@ -115,6 +115,33 @@ ssa_status ssa_score_topk(const void* q_low, const void* k_low, int dtype, int B
                           int32_t* dev_status, void* stream);
 
 /*
+ * ssa_lowrank_scores — the low-rank scorer alone, materialised.
+ *
+ * Source: mhpq.cn/news/1098205, section 2.2 (scores = q_low . k_low^T scaled
+ * by d_proj^-0.5, a [b, h, n, n] tensor) with the masking of section 3.2,
+ * note 3 (masked positions hold -inf).
+ *
+ * S[b,h,i,j] = fp32(sum_p q_low[b,h,i,p] * k_low[b,h,j,p]) * scale for j in
+ * valid(i) (as defined for ssa_score_topk), -inf otherwise. The contraction
+ * runs on the tensor cores with fp32 accumulation; it is the same contraction
+ * ssa_score_topk uses, so for bf16 inputs S holds exactly the scores that call
+ * ranks (integer-valued inputs give exact scores).
+ *
+ *   q_low     device, [B, H, Tq, P], bf16
+ *   k_low     device, [B, H, Tk, P], bf16
+ *   P         64 or 128 (other d_proj or fp32 inputs: SSA_ERR_UNSUPPORTED)
+ *   scale     <= 0 selects fp32(1 / sqrt(P))
+ *   S         device, float [B, H, Tq, Tk], written (B*H*Tq*Tk*4 bytes:
+ *             meant for inspection and small problems)
+ *   dev_status device int32 or NULL
+ *
+ * Returns SSA_OK, SSA_ERR_INVALID, SSA_ERR_UNSUPPORTED or SSA_ERR_CUDA.
+ */
+ssa_status ssa_lowrank_scores(const void* q_low, const void* k_low, int dtype, int B, int H,
+                              int Tq, int Tk, int P, int causal, float scale, float* S,
+                              int32_t* dev_status, void* stream);
+
+/*
  * ssa_sparse_attn — attention over the selected keys only.
  *
  * Source: mhpq.cn/news/1098205, section 3.2 (gather the selected K and V,

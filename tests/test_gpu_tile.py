@@ -1,0 +1,112 @@
+"""The tensor-core score path against the oracle (needs a B300).
+
+ssa_lowrank_scores runs the tcgen05 contraction alone and must reproduce the
+oracle's scores bit for bit on integer data. ssa_score_topk on bf16 inputs
+with d_proj 64 or 128, k <= 512 and at least 64 query rows runs the
+tensor-core selection (group maxima -> per-row bound -> candidates -> sort,
+rows that overflow their candidate list redone row-wise); these cases cover
+every group size, several 128-row tiles with ragged tails, Tq != Tk, and rows
+whose candidates overflow.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dynamic_top_sparse_rank_b300 as ssa
+import oracle
+from workloads import fill
+
+pytestmark = pytest.mark.gpu
+
+
+def _int_inputs(B, H, Tq, Tk, P, seed, lo=-4, hi=4):
+    q = fill((B, H, Tq, P), "int", seed, 1, torch.bfloat16, "cpu")
+    k = fill((B, H, Tk, P), "int", seed, 2, torch.bfloat16, "cpu")
+    if (lo, hi) != (-4, 4):
+        q, k = torch.clamp(q, lo, hi), torch.clamp(k, lo, hi)
+    return q, k
+
+
+@pytest.mark.parametrize("B,H,Tq,Tk,P,causal", [
+    (1, 2, 300, 500, 64, True),      # ragged query and key tiles, bottom-right causal
+    (2, 1, 129, 1000, 128, False),   # two K atoms per row
+    (1, 1, 256, 256, 64, True),      # exact tiles
+    (1, 1, 500, 200, 64, True),      # Tq > Tk: leading rows see no key
+])
+def test_lowrank_scores_exact(cuda_dev, B, H, Tq, Tk, P, causal):
+    q, kl = _int_inputs(B, H, Tq, Tk, P, seed=30 + Tq)
+    S = ssa.ssa_lowrank_scores(q.to(cuda_dev), kl.to(cuda_dev), causal)
+    torch.cuda.synchronize()
+    ref = oracle.scores(q, kl, causal)
+    np.testing.assert_array_equal(S.cpu().numpy(), ref)
+
+
+TILE_CASES = [
+    # B, H, Tq, Tk, P, k, causal
+    (1, 1, 2048, 2048, 64, 64, True),     # group sizes 1..16 across the tiles
+    (1, 2, 4096, 4096, 64, 512, True),    # k = 512, groups of 1..2
+    (1, 1, 8192, 8192, 64, 32, False),    # group size 128, every row full
+    (1, 1, 1000, 3000, 128, 100, True),   # d_proj 128, Tq < Tk
+    (1, 1, 3000, 1000, 64, 50, True),     # Tq > Tk: 2000 empty rows
+    (2, 3, 333, 777, 64, 17, False),      # ragged everything, small k
+    (1, 1, 640, 640, 64, 512, False),     # k close to Tk
+    (1, 1, 96, 96, 64, 1, True),          # k = 1
+]
+
+
+@pytest.mark.parametrize("B,H,Tq,Tk,P,k,causal", TILE_CASES)
+def test_tile_topk_matches_oracle(cuda_dev, B, H, Tq, Tk, P, k, causal):
+    q, kl = _int_inputs(B, H, Tq, Tk, P, seed=40 + Tq + k)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    idx, sc = ssa.ssa_score_topk(q.to(cuda_dev), kl.to(cuda_dev), k, causal, with_score=True,
+                                 dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref_idx, ref_sc = oracle.score_topk(q, kl, k, causal)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    np.testing.assert_array_equal(sc.cpu().numpy(), ref_sc)
+
+
+def test_tile_topk_heavy_ties_overflow(cuda_dev):
+    """Values in {-1, 0, 1}: few distinct scores, so many rows hold more tied
+    candidates than their list and are redone row-wise; others are not."""
+    B, H, Tq, Tk, P, k = 1, 2, 700, 2500, 64, 64
+    q, kl = _int_inputs(B, H, Tq, Tk, P, seed=77, lo=-1, hi=1)
+    idx, sc = ssa.ssa_score_topk(q.to(cuda_dev), kl.to(cuda_dev), k, True, with_score=True)
+    ref_idx, ref_sc = oracle.score_topk(q, kl, k, True)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    np.testing.assert_array_equal(sc.cpu().numpy(), ref_sc)
+
+
+def test_tile_topk_two_calls_one_workspace(cuda_dev):
+    """Back-to-back calls on one workspace (stale bounds, counts and
+    candidates from the first call must not leak into the second)."""
+    B, H, Tq, Tk, P, k = 1, 2, 1500, 1500, 64, 128
+    q1, k1 = _int_inputs(B, H, Tq, Tk, P, seed=91)
+    q2, k2 = _int_inputs(B, H, Tq, Tk, P, seed=92)
+    ws = torch.full((ssa.score_topk_workspace_size(B, H, Tq, Tk, P, k, 1),), 0x5A,
+                    dtype=torch.uint8, device=cuda_dev)
+    a = ssa.ssa_score_topk(q1.to(cuda_dev), k1.to(cuda_dev), k, True, workspace=ws).cpu()
+    b = ssa.ssa_score_topk(q2.to(cuda_dev), k2.to(cuda_dev), k, True, workspace=ws).cpu()
+    np.testing.assert_array_equal(a.numpy(), oracle.score_topk(q1, k1, k, True)[0])
+    np.testing.assert_array_equal(b.numpy(), oracle.score_topk(q2, k2, k, True)[0])
+
+
+def test_tile_topk_continuous_scores_are_consistent(cuda_dev):
+    """Non-integer bf16 inputs: the selection must be exactly the top of the
+    scores the same contraction produces (ssa_lowrank_scores), under the
+    (score desc, index asc) order."""
+    B, H, Tq, Tk, P, k = 1, 1, 384, 900, 64, 40
+    q = fill((B, H, Tq, P), "normal", 5, 1, torch.bfloat16, "cpu")
+    kl = fill((B, H, Tk, P), "normal", 5, 2, torch.bfloat16, "cpu")
+    qd, kd = q.to(cuda_dev), kl.to(cuda_dev)
+    idx, sc = ssa.ssa_score_topk(qd, kd, k, True, with_score=True)
+    S = ssa.ssa_lowrank_scores(qd, kd, True).cpu().numpy()
+    idx, sc = idx.cpu().numpy(), sc.cpu().numpy()
+    for i in range(Tq):
+        row = S[0, 0, i]
+        order = sorted((j for j in range(Tk) if row[j] > -np.inf), key=lambda j: (-row[j], j))
+        want = (order + [-1] * k)[:k]
+        assert list(idx[0, 0, i]) == want
+        got = sc[0, 0, i][: min(k, len(order))]
+        np.testing.assert_array_equal(got, row[want[: len(got)]])
