@@ -23,7 +23,8 @@ SSA_F32, SSA_BF16 = 0, 1
 SSA_DEV_BAD_INDEX, SSA_DEV_WAIT_LIMIT, SSA_DEV_OVERFLOW = 0x1, 0x2, 0x4
 
 EXPORTS = ("ssa_version", "ssa_status_string", "ssa_score_topk_workspace_size", "ssa_score_topk",
-           "ssa_sparse_attn", "ssa_window_attn", "ssa_score_topk_noalloc", "ssa_lowrank_scores")
+           "ssa_sparse_attn", "ssa_window_attn", "ssa_score_topk_noalloc", "ssa_lowrank_scores",
+           "ssa_trace_begin", "ssa_trace_end")
 
 # Fixed scratch of ssa_score_topk_noalloc and the largest Tk it accepts.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -64,6 +65,10 @@ def load(path: str | None = None):
     lib.ssa_window_attn.argtypes = [V, V, V, I, I, I, I, I, I, I, F, V, I, V, V]
     lib.ssa_score_topk_noalloc.restype = I
     lib.ssa_score_topk_noalloc.argtypes = [V, V, I, I, I, I, I, I, I, I, F, V, V, V, V]
+    lib.ssa_trace_begin.restype = I
+    lib.ssa_trace_begin.argtypes = []
+    lib.ssa_trace_end.restype = I
+    lib.ssa_trace_end.argtypes = [V, I]
     lib.ssa_lowrank_scores.restype = I
     lib.ssa_lowrank_scores.argtypes = [V, V, I, I, I, I, I, I, I, F, V, V, V]
     if path is None:
@@ -253,6 +258,25 @@ def ssa_window_attn(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, w_left: i
                              _stream(dev))
     _check(rc, "ssa_window_attn")
     return out
+
+
+class _TraceRecord(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 56), ("ms", ctypes.c_float)]
+
+
+def trace_begin():
+    """Start timing every kernel the library launches (CUDA events on the
+    launching stream)."""
+    load().ssa_trace_begin()
+
+
+def trace_end(max_records: int = 4096):
+    """Stop tracing; returns [(kernel name, ms), ...] in launch order."""
+    buf = (_TraceRecord * max_records)()
+    n = load().ssa_trace_end(ctypes.cast(buf, ctypes.c_void_p), max_records)
+    if n < 0:
+        raise SSAError(SSA_ERR_CUDA, "ssa_trace_end")
+    return [(buf[i].name.decode(), float(buf[i].ms)) for i in range(min(n, max_records))]
 
 
 def default_scale(n: int) -> float:

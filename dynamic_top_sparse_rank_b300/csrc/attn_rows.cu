@@ -23,6 +23,7 @@
 // Padding entries (-1) and the tail of the last chunk are masked with a -inf
 // logit (their loads read row 0 of the head, which is always valid memory).
 #include "common.cuh"
+#include "trace.h"
 
 namespace ssa {
 
@@ -210,6 +211,7 @@ static cudaError_t launch_attn_rows(const void* Q, const void* K, const void* V,
     constexpr int WARPS = 8;
     const int64_t blocks = (rows + WARPS - 1) / WARPS;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    TraceLaunch tr(BAND ? "attn_rows.window" : "attn_rows.sparse", stream);
     attn_rows_kernel<BF16_IN, D, BF16_OUT, BAND><<<(unsigned)blocks, WARPS * 32, 0, stream>>>(
         Q, K, V, idx, O, rows, Tq, Tk, k, wl, wr, scale * kLog2e, dev_status);
     return cudaGetLastError();

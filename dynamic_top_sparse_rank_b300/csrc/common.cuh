@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ssa.h"
+#include "ssa.h"
 
 #define SSA_DEVINL __device__ __forceinline__
 

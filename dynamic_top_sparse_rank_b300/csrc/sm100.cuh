@@ -47,6 +47,21 @@ SSA_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` inside the
+// instruction waiting for the phase (it wakes as soon as the phase
+// completes), so a waiting warp does not take issue slots from the others.
+SSA_DEVINL bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 SSA_DEVINL uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -62,15 +77,13 @@ SSA_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* 
                                   int32_t* dev_status, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 255u) == 0) {
-            if (abort && *abort) return false;
-            if (globaltimer_ns() - t0 > limit_ns) {
-                if (abort) *abort = 1;
-                report(dev_status, SSA_DEV_WAIT_LIMIT);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (abort && *abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            if (abort) *abort = 1;
+            report(dev_status, SSA_DEV_WAIT_LIMIT);
+            return false;
         }
     }
 }

@@ -8,8 +8,9 @@
 
 namespace ssa {
 
-constexpr int kTileM = 128;   // query rows per unit (TMEM lanes)
-constexpr int kTileN = 128;   // keys per MMA tile (TMEM columns per buffer)
+constexpr int kTileM = 128;   // query rows per accumulator (TMEM lanes)
+constexpr int kUnitM = 256;   // query rows per unit: two accumulators share every key tile
+constexpr int kTileN = 128;   // keys per MMA tile (TMEM columns per accumulator)
 
 enum TileMode { MODE_RAW = 0, MODE_GROUPMAX = 1, MODE_COLLECT = 2 };
 
@@ -36,13 +37,42 @@ __host__ __device__ __forceinline__ int tile_group_size(int n_lo, int n_hi, int 
     return g;
 }
 
-// Groups per row and unit that the group-maximum array reserves: a row has at
-// most ceil(n_hi / g) groups, which stays below 4k + 128 for every unit.
-__host__ __device__ __forceinline__ int tile_group_stride(int k) { return 4 * k + 128; }
+// Layout of the groups of a row (both the score kernel and the selection use
+// it). g < 32: group grp holds the consecutive keys [grp*g, grp*g + g).
+// g >= 32 (m = g/32): the key tiles of a unit alternate between kTileGroups
+// TMEM buffers, each drained by its own epilogue warps (tile t by buffer
+// t % 2); group grp = 4*(2*T + b) + c holds the 32-key chunk c of the m tiles
+// T*m .. T*m + m - 1 among those of buffer b, i.e. of tiles 2*(T*m + i) + b,
+// i < m. Every warp then forms its groups alone. Groups need not be
+// contiguous: any partition of the valid keys into G >= k groups gives a
+// valid bound.
+constexpr int kTileGroups = 2;
 
-// Candidate capacity per row: twice the next power of two >= k. The bound
-// from the group maxima leaves about 1.25 k candidates; a row with more
-// (heavy ties at its k-th score) is recomputed by the row-wise kernel.
+__host__ __device__ __forceinline__ int tile_group_first_key(int grp, int g) {
+    if (g < 32) return grp * g;
+    const int m = g / 32;
+    const int T = grp / (4 * kTileGroups), b = (grp / 4) % kTileGroups, c = grp % 4;
+    return (T * m * kTileGroups + b) * 128 + c * 32;
+}
+
+// Number of group indices a unit uses (rows have up to n_hi valid keys).
+__host__ __device__ __forceinline__ int tile_groups_in_unit(int n_hi, int g) {
+    if (g < 32) return (n_hi + g - 1) / g;
+    const int m = g / 32;
+    const int tiles = (n_hi + 127) / 128;
+    const int per_buffer = (tiles + kTileGroups - 1) / kTileGroups;   // tiles of buffer 0
+    return 4 * kTileGroups * ((per_buffer + m - 1) / m);
+}
+
+// Groups per unit that the group-maximum array reserves: a unit's rows have
+// n_hi <= n_ref + 255 valid keys and g > n_ref / (4k), so a unit uses fewer
+// than 4k + 256 / g + 28 indices.
+__host__ __device__ __forceinline__ int tile_group_stride(int k) { return 4 * k + 288; }
+
+// Candidate capacity per row: twice the next power of two >= k, split in two
+// equal lists (one per TMEM tile buffer and its epilogue warps). The bound from the
+// group maxima leaves about 1.25 k candidates; a row that fills one of its
+// lists (heavy ties at its k-th score) is recomputed by the row-wise kernel.
 __host__ __device__ __forceinline__ int tile_cand_cap(int k) {
     int c = 32;
     while (c < k) c *= 2;
@@ -54,12 +84,12 @@ struct TileParams {
     float scale;
     int units_per_head, num_units;   // filled by the launcher
     float* S;                        // MODE_RAW: [BH, Tq, Tk]
-    uint16_t* gm;                    // MODE_GROUPMAX: [units, G_stride, 128]
+    uint16_t* gm;                    // MODE_GROUPMAX: [units, G_stride, 256]
     int G_stride;
     const uint32_t* tau;             // MODE_COLLECT: [BH*Tq] order-key thresholds
-    uint64_t* cand;                  // MODE_COLLECT: [BH*Tq, cap] composite keys
-    int32_t* cnt;                    // MODE_COLLECT: [BH*Tq] candidates found
-    int cap;
+    uint64_t* cand;                  // MODE_COLLECT: [BH*Tq, 2, cap/2] composite keys
+    int32_t* cnt;                    // MODE_COLLECT: [BH*Tq, 2] candidates found
+    int cap;                         // per row; half per TMEM tile buffer
     int32_t* dev_status;
     uint64_t wait_limit_ns;          // 0: one second
 };
@@ -79,13 +109,13 @@ inline TileWorkspace tile_workspace(int64_t BH, int Tq, int Tk, int k) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     TileWorkspace w;
     const int64_t rows = BH * Tq;
-    const int64_t units = BH * ((Tq + kTileM - 1) / kTileM);
+    const int64_t units = BH * ((Tq + kUnitM - 1) / kUnitM);
     size_t o = 0;
     w.ovf_count = o; o += 256;
     w.tau = o; o += up(rows * 4);
-    w.cnt = o; o += up(rows * 4);
+    w.cnt = o; o += up(rows * 8);
     w.ovf_list = o; o += up(rows * 8);
-    w.gm = o; o += up(static_cast<size_t>(units) * tile_group_stride(k) * kTileM * 2);
+    w.gm = o; o += up(static_cast<size_t>(units) * tile_group_stride(k) * kUnitM * 2);
     w.cand = o; o += up(static_cast<size_t>(rows) * tile_cand_cap(k) * 8);
     w.rowwise_slots = rows < 256 ? rows : 256;
     w.rowwise_stride = (static_cast<int64_t>(Tk) + 63) / 64 * 64;

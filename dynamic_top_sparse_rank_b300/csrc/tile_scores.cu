@@ -1,35 +1,44 @@
-// Tensor-core scorer: S = q_low . k_low^T * scale on tcgen05, one 128-query
-// tile of a head against all its valid keys, 128 keys at a time. The score
-// tile lives in TMEM only; an epilogue warpgroup reduces it on the fly, so the
-// n x n score matrix never reaches HBM (the low-rank scorer of
-// mhpq.cn/news/1098205, section 2.2; the selection of its section 3.2).
+// Tensor-core scorer: S = q_low . k_low^T * scale on tcgen05, one 256-query
+// unit of a head against all its valid keys, 128 keys at a time. The scores
+// live in TMEM only; the epilogue warps reduce them on the fly, so the n x n
+// score matrix never reaches HBM (the low-rank scorer of mhpq.cn/news/1098205,
+// section 2.2; the selection of its section 3.2).
 //
 // The same kernel runs in three modes (the epilogue differs, the contraction
 // does not, and it is deterministic, so every mode sees bit-identical scores):
 //   MODE_RAW       writes the scaled scores, -inf where the key is masked
 //                  (the scorer output as its own call);
-//   MODE_GROUPMAX  splits each query row's valid keys into consecutive groups
-//                  of g keys and writes the 16 high bits of the order key of
-//                  every group's maximum score;
+//   MODE_GROUPMAX  splits each query row's valid keys into groups of g keys
+//                  (layout in tile.h) and writes the 16 high bits of the order
+//                  key of every group's maximum score;
 //   MODE_COLLECT   appends every valid key whose score reaches the row's
-//                  threshold to the row's candidate list.
+//                  threshold to the row's candidate lists.
 // The exact top-k of a row is then found from these (tile_select.cu).
 //
-// Block layout (192 threads): warp 0 issues TMA loads (the query tile once per
-// unit, key tiles through a ring of shared-memory stages), warp 1 allocates
-// TMEM and issues the MMAs (M=128 queries, N=128 keys, K=16 per instruction,
-// bf16 operands K-major with the 128-byte swizzle, fp32 accumulators in one of
-// two TMEM buffers), warps 2..5 are the epilogue: thread r of the warpgroup
-// owns TMEM lane r, i.e. query row r of the tile, and reads its 128 scores of
-// a key tile as four 32-column tcgen05.ld. Every wait on an mbarrier is
-// bounded in time; a wait that runs out sets SSA_DEV_WAIT_LIMIT, stops every
-// role of the block, lets copies and MMAs in flight finish and frees TMEM.
+// Block layout (576 threads, one block per SM): warp 0 issues TMA loads (the
+// two 128-row query tiles of a unit, key tiles through a ring of shared-memory
+// stages), warp 1 allocates all 512 TMEM columns and issues the MMAs: every
+// 128-key tile is multiplied with both query tiles (M=128, N=128, K=16 per
+// instruction, bf16 operands K-major with the 128-byte swizzle, fp32
+// accumulators), so one 16 KB key tile feeds 512 tensor-core cycles and the
+// load ring hides the full latency of freeing and refilling a stage. Tile t of
+// a unit goes to TMEM buffer t % 2, which holds one accumulator per query
+// tile. Warps 2..17 are the epilogue, four groups of four warps, one per
+// (buffer, query tile): warp w of a group reads TMEM lane quarter w%4 (one
+// query row per thread), all 128 columns as four 32-column tcgen05.ld, frees
+// the buffer and works on the scores in registers. Every wait on an mbarrier
+// is bounded in time; a wait that runs out sets SSA_DEV_WAIT_LIMIT, stops
+// every role of the block, lets copies and MMAs in flight finish and frees
+// TMEM.
 //
-// Work is a list of units (head, 128-query tile) in head-major order, the
-// query tiles of a head from the last (most keys under a causal mask) to the
+// Work is a list of units (head, 256-query block) in head-major order, the
+// query blocks of a head from the last (most keys under a causal mask) to the
 // first; a persistent grid takes units round-robin.
+#include <float.h>
+
 #include "sm100.cuh"
 #include "tile.h"
+#include "trace.h"
 
 namespace ssa {
 
@@ -37,18 +46,23 @@ using namespace sm100;
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kTBuf = 2;                      // TMEM accumulator buffers
-constexpr uint32_t kTmemCols = kTBuf * kTileN;
+constexpr int kEpiWarps = 16;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kTBuf = kTileGroups;            // TMEM tile buffers (two accumulators each)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
 template <int P>
 struct TileCfg {
     static constexpr int KA = P / 64;                       // 128-byte K atoms per row
-    static constexpr int STAGES = (P == 64) ? 4 : 2;        // key-tile ring depth
-    static constexpr uint32_t QBYTES = KA * kTileM * 128;
+    static constexpr int STAGES = (P == 64) ? 8 : 4;        // key-tile ring depth
+    static constexpr int QSLOTS = (P == 64) ? 2 : 1;        // query-unit slots
+    static constexpr uint32_t QHALF = KA * kTileM * 128;    // one 128-row query tile
+    static constexpr uint32_t QBYTES = 2 * QHALF;           // a unit's two query tiles
     static constexpr uint32_t KBYTES = KA * kTileN * 128;
-    static constexpr uint32_t BAR_OFF = QBYTES + STAGES * KBYTES;
-    static constexpr uint32_t SMEM = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+    static constexpr uint32_t K_OFF = QSLOTS * QBYTES;
+    static constexpr uint32_t BAR_OFF = K_OFF + STAGES * KBYTES;
+    static constexpr uint32_t SMEM = BAR_OFF + 512 + 1024;  // + barriers + alignment slack
 };
 
 struct Unit {
@@ -59,12 +73,16 @@ SSA_DEVINL Unit unit_at(const TileParams& p, int u) {
     Unit U;
     U.bh = u / p.units_per_head;
     const int qb = p.units_per_head - 1 - (u - U.bh * p.units_per_head);
-    U.i0 = qb * kTileM;
-    U.rows = min(kTileM, p.Tq - U.i0);
+    U.i0 = qb * kUnitM;
+    U.rows = min(kUnitM, p.Tq - U.i0);
     U.n_lo = tile_valid_count(U.i0, p.Tq, p.Tk, p.causal);
     U.n_hi = tile_valid_count(U.i0 + U.rows - 1, p.Tq, p.Tk, p.causal);
     U.ntiles = (U.n_hi + kTileN - 1) / kTileN;
     return U;
+}
+
+SSA_DEVINL float max8(const float* v) {
+    return fmaxf(fmax3(v[0], v[1], v[2]), fmax3(v[3], v[4], fmaxf(v[5], fmaxf(v[6], v[7]))));
 }
 
 SSA_DEVINL float max32(const float (&v)[32]) {
@@ -79,10 +97,33 @@ SSA_DEVINL float max32(const float (&v)[32]) {
     return fmaxf(fmax3(b0, b1, b2), b3);
 }
 
+// v[e] for a runtime e in 0..7 (a select tree keeps v in registers).
+SSA_DEVINL float pick8(const float* v, int e) {
+    const float a0 = (e & 1) ? v[1] : v[0];
+    const float a1 = (e & 1) ? v[3] : v[2];
+    const float a2 = (e & 1) ? v[5] : v[4];
+    const float a3 = (e & 1) ? v[7] : v[6];
+    const float b0 = (e & 2) ? a1 : a0;
+    const float b1 = (e & 2) ? a3 : a2;
+    return (e & 4) ? b1 : b0;
+}
+
+// Smallest float x with fl(x * scale) >= t (scale > 0): fl(x * scale) is
+// non-decreasing in x, so `raw >= x` decides `fl(raw * scale) >= t` exactly
+// without a multiply per score.
+SSA_DEVINL float raw_threshold(float t, float scale) {
+    if (t == -INFINITY) return -FLT_MAX;   // every finite score qualifies, -inf (masked) does not
+    float x = t / scale;
+    for (int it = 0; it < 8 && x * scale < t; ++it) x = nextafterf(x, INFINITY);
+    for (int it = 0; it < 8 && nextafterf(x, -INFINITY) * scale >= t; ++it)
+        x = nextafterf(x, -INFINITY);
+    return x;
+}
+
 }  // namespace
 
 template <int P, int MODE>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     tile_scores_kernel(const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ CUtensorMap kmap, const TileParams p) {
     using C = TileCfg<P>;
@@ -92,29 +133,31 @@ __global__ void __launch_bounds__(kThreads, 2)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sq = smem;
-    uint8_t* sk = smem + C::QBYTES;
+    uint8_t* sq = smem;                                   // query-unit slots
+    uint8_t* sk = smem + C::K_OFF;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-    uint64_t* q_full = bars;
-    uint64_t* q_empty = bars + 1;
-    uint64_t* k_full = bars + 2;
-    uint64_t* k_empty = k_full + S;
-    uint64_t* t_full = k_empty + S;
-    uint64_t* t_empty = t_full + kTBuf;
+    uint64_t* q_full = bars;                              // [QSLOTS]
+    uint64_t* q_empty = bars + 2;                         // [QSLOTS]
+    uint64_t* k_full = bars + 4;                          // [S]
+    uint64_t* k_empty = k_full + S;                       // [S]
+    uint64_t* t_full = k_empty + S;                       // [kTBuf]
+    uint64_t* t_empty = t_full + kTBuf;                   // [kTBuf]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(t_empty + kTBuf);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
+        for (int i = 0; i < C::QSLOTS; ++i) {
+            mbar_init(q_full + i, 1);
+            mbar_init(q_empty + i, 1);
+        }
         for (int s = 0; s < S; ++s) {
             mbar_init(k_full + s, 1);
             mbar_init(k_empty + s, 1);
         }
         for (int b = 0; b < kTBuf; ++b) {
             mbar_init(t_full + b, 1);
-            mbar_init(t_empty + b, 128);
+            mbar_init(t_empty + b, kEpiWarps / kTBuf);   // one arrive per epilogue warp
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -128,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint64_t lim = p.wait_limit_ns;
+    const uint64_t lim = p.wait_limit_ns ? p.wait_limit_ns : kDefaultWaitNs;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -138,14 +181,19 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
                 const Unit U = unit_at(p, u);
                 if (U.ntiles == 0) continue;
-                if (!mbar_wait_bounded(q_empty, (qc & 1) ^ 1, abort_flag, p.dev_status, lim)) {
+                const uint32_t qs = qc % C::QSLOTS, quse = qc / C::QSLOTS;
+                if (!mbar_wait_bounded(q_empty + qs, (quse & 1) ^ 1, abort_flag, p.dev_status,
+                                       lim)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(q_full, C::QBYTES);
+                mbar_arrive_expect_tx(q_full + qs, C::QBYTES);
 #pragma unroll
-                for (int a = 0; a < C::KA; ++a)
-                    tma_load_2d(sq + a * 16384, &qmap, a * 64, U.bh * p.Tq + U.i0, q_full);
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int a = 0; a < C::KA; ++a)
+                        tma_load_2d(sq + qs * C::QBYTES + h * C::QHALF + a * 16384, &qmap, a * 64,
+                                    U.bh * p.Tq + U.i0 + h * kTileM, q_full + qs);
                 ++qc;
                 for (int t = 0; t < U.ntiles; ++t) {
                     const uint32_t s = kc % S;
@@ -166,63 +214,82 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint32_t first = kc > (uint32_t)S ? kc - S : 0;
             for (uint32_t m = first; m < kc; ++m)
                 mbar_wait_bounded(k_full + (m % S), (m / S) & 1, nullptr, p.dev_status, lim);
-            if (qc > 0) mbar_wait_bounded(q_full, (qc - 1) & 1, nullptr, p.dev_status, lim);
+            const uint32_t qfirst = qc > (uint32_t)C::QSLOTS ? qc - C::QSLOTS : 0;
+            for (uint32_t m = qfirst; m < qc; ++m)
+                mbar_wait_bounded(q_full + (m % C::QSLOTS), (m / C::QSLOTS) & 1, nullptr,
+                                  p.dev_status, lim);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t kc = 0, tc = 0, qc = 0;
+            uint32_t kc = 0, qc = 0;
+            uint32_t tpar = 0;                 // bit b: phase parity of TMEM buffer b
+            int last_b = -1;
             bool ok = true;
+            // descriptors of the first K slice of stage 0 and of query slot 0;
+            // other stages, slots and K slices only move the start address
+            const uint64_t bdesc0 = smem_desc_k_sw128(smem_u32(sk));
+            const uint64_t adesc0 = smem_desc_k_sw128(smem_u32(sq));
             for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
                 const Unit U = unit_at(p, u);
                 if (U.ntiles == 0) continue;
-                if (!mbar_wait_bounded(q_full, qc & 1, abort_flag, p.dev_status, lim)) {
+                const uint32_t qs = qc % C::QSLOTS, quse = qc / C::QSLOTS;
+                if (!mbar_wait_bounded(q_full + qs, quse & 1, abort_flag, p.dev_status, lim)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sq_addr = smem_u32(sq);
+                const uint64_t adesc = adesc0 + ((qs * C::QBYTES) >> 4);
                 for (int t = 0; t < U.ntiles; ++t) {
-                    const uint32_t s = kc % S, b = tc % kTBuf;
+                    const uint32_t s = kc % S, b = t & (kTBuf - 1);
+                    const uint32_t par = (tpar >> b) & 1;
                     if (!mbar_wait_bounded(k_full + s, (kc / S) & 1, abort_flag, p.dev_status,
                                            lim) ||
-                        !mbar_wait_bounded(t_empty + b, ((tc / kTBuf) & 1) ^ 1, abort_flag,
-                                           p.dev_status, lim)) {
+                        !mbar_wait_bounded(t_empty + b, par ^ 1, abort_flag, p.dev_status, lim)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + b * kTileN;
-                    const uint32_t sk_addr = smem_u32(sk + s * C::KBYTES);
+                    const uint64_t bdesc = bdesc0 + ((s * C::KBYTES) >> 4);
 #pragma unroll
-                    for (int a = 0; a < C::KA; ++a) {
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t d_tmem = tmem_base + (2 * b + h) * kTileN;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = smem_desc_k_sw128(sq_addr + a * 16384 + kk * 32);
-                            const uint64_t bd = smem_desc_k_sw128(sk_addr + a * 16384 + kk * 32);
-                            mma_bf16(d_tmem, ad, bd, IDESC, (a | kk) != 0);
+                        for (int a = 0; a < C::KA; ++a) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t off = (a * 16384 + kk * 32) >> 4;
+                                mma_bf16(d_tmem, adesc + ((h * C::QHALF) >> 4) + off, bdesc + off,
+                                         IDESC, (a | kk) != 0);
+                            }
                         }
                     }
                     mma_commit(k_empty + s);
                     mma_commit(t_full + b);
+                    tpar ^= 1u << b;
+                    last_b = static_cast<int>(b);
                     ++kc;
-                    ++tc;
                 }
                 if (!ok) break;
-                mma_commit(q_empty);
+                mma_commit(q_empty + qs);
                 ++qc;
             }
             // MMAs in flight finish by themselves; wait for the last one
-            if (tc > 0)
-                mbar_wait_bounded(t_full + (tc - 1) % kTBuf, ((tc - 1) / kTBuf) & 1, nullptr,
+            if (last_b >= 0)
+                mbar_wait_bounded(t_full + last_b, ((tpar >> last_b) & 1) ^ 1, nullptr,
                                   p.dev_status, lim);
         }
     } else {
         // ------------------------------------------------ epilogue
-        const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;
-        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-        uint32_t tc = 0;
+        const int quarter = warp & 3;          // TMEM lane quarter of this warp
+        const int grp4 = (warp - 2) >> 2;      // epilogue warp group
+        const int tb = grp4 >> 1;              // TMEM tile buffer = tile % 2
+        const int half = grp4 & 1;             // query tile (accumulator) of the unit
+        const int r = half * kTileM + quarter * 32 + lane;   // query row within the unit
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                static_cast<uint32_t>((2 * tb + half) * kTileN);
+        const int capc = p.cap / kTBuf;        // this buffer's candidate list of the row
+        uint32_t tpar = 0;                     // phase parity of TMEM buffer tb
         bool ok = true;
         for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
             const Unit U = unit_at(p, u);
@@ -231,33 +298,44 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int n_i = row_ok ? tile_valid_count(i, p.Tq, p.Tk, p.causal) : 0;
             const int64_t row = static_cast<int64_t>(U.bh) * p.Tq + i;
             // mode state
-            int g = 0;
-            bool emit = false;
-            float gacc = -INFINITY;
-            float tau_f = -INFINITY;
+            int g = 0, m_shift = 0, g_shift = 0;   // g and m = g/32 are powers of two
+            float gacc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            float t_raw = -FLT_MAX;            // raw-score bound of this thread's row
             int cnt = 0;
+            uint16_t* gcol = nullptr;
+            uint64_t* clist = nullptr;
             if constexpr (MODE == MODE_GROUPMAX) {
                 g = tile_group_size(U.n_lo, U.n_hi, p.k);
-                emit = n_i > p.k;
+                g_shift = g > 0 ? __ffs(g) - 1 : 0;
+                m_shift = g >= 32 ? g_shift - 5 : 0;
+                if (n_i <= p.k) g = 0;   // this row selects all its keys: no groups
+                gcol = p.gm + static_cast<int64_t>(u) * p.G_stride * kUnitM + r;
             }
             if constexpr (MODE == MODE_COLLECT) {
                 if (row_ok) {
                     const uint32_t t32 = p.tau[row];
-                    tau_f = t32 == 0 ? -INFINITY : order_key_f32(t32);
+                    t_raw = raw_threshold(t32 == 0 ? -INFINITY : order_key_f32(t32), p.scale);
                 }
             }
-            for (int t = 0; t < U.ntiles; ++t) {
-                const uint32_t b = tc % kTBuf;
+            if constexpr (MODE == MODE_COLLECT)
+                clist = p.cand + (row * kTBuf + tb) * static_cast<int64_t>(capc);
+            for (int t = tb; t < U.ntiles; t += kTBuf) {
                 // warp-uniform outcome: tcgen05.ld below needs the whole warp
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(t_full + b, (tc / kTBuf) & 1,
-                                                              abort_flag, p.dev_status, lim));
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(t_full + tb, tpar, abort_flag,
+                                                              p.dev_status, lim));
                 if (!ok) break;
+                tpar ^= 1;
                 tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < kTileN / 32; ++c) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
                     uint32_t raw[32];
-                    tmem_ld32(t_lane + b * kTileN + c * 32, raw);
+                    tmem_ld32(t_lane + c * 32, raw);
                     tmem_ld_wait();
+                    if (c == 3) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(t_empty + tb);   // the buffer is free again
+                    }
                     const int j0 = t * kTileN + c * 32;
                     float v[32];
 #pragma unroll
@@ -271,81 +349,90 @@ __global__ void __launch_bounds__(kThreads, 2)
                                 if (j < p.Tk) out[j] = j < n_i ? v[e] * p.scale : -INFINITY;
                             }
                         }
-                    } else if (j0 < n_i) {
-                        if (j0 + 32 > n_i) {
+                    } else {
+                        const bool live = j0 < n_i;   // this row has keys in the chunk
+                        if (live && j0 + 32 > n_i) {
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
                                 if (j0 + e >= n_i) v[e] = -INFINITY;
                         }
                         if constexpr (MODE == MODE_GROUPMAX) {
-                            if (emit) {
-                                uint16_t* gcol = p.gm + static_cast<int64_t>(u) * p.G_stride *
-                                                            kTileM + r;
-                                if (g >= 32) {
-                                    gacc = fmaxf(gacc, max32(v));
-                                    const int jend = j0 + 32;
-                                    if ((jend & (g - 1)) == 0 || jend >= n_i) {
-                                        gcol[static_cast<int64_t>(j0 / g) * kTileM] =
-                                            static_cast<uint16_t>(f32_order_key(gacc * p.scale) >> 16);
-                                        gacc = -INFINITY;
-                                    }
-                                } else {
-                                    // in-place max tree: v[m*g] ends as the max of group m
-                                    if (g >= 2) {
+                            if (live && g >= 32) {
+                                gacc[c] = fmaxf(gacc[c], max32(v));
+                                // last tile of the group, or the row has no key in this
+                                // chunk of this buffer's next tile
+                                const int lt = t / kTBuf;
+                                if (((lt + 1) & ((1 << m_shift) - 1)) == 0 ||
+                                    (t + kTBuf) * kTileN + c * 32 >= n_i) {
+                                    const int grp = ((lt >> m_shift) * kTBuf + tb) * 4 + c;
+                                    gcol[static_cast<int64_t>(grp) * kUnitM] =
+                                        static_cast<uint16_t>(f32_order_key(gacc[c] * p.scale) >> 16);
+                                    gacc[c] = -INFINITY;
+                                }
+                            } else if (live && g > 0) {
+                                // in-place max tree: v[m*g] ends as the max of group m
+                                if (g >= 2) {
 #pragma unroll
-                                        for (int e = 0; e < 32; e += 2) v[e] = fmaxf(v[e], v[e + 1]);
-                                    }
-                                    if (g >= 4) {
+                                    for (int e = 0; e < 32; e += 2) v[e] = fmaxf(v[e], v[e + 1]);
+                                }
+                                if (g >= 4) {
 #pragma unroll
-                                        for (int e = 0; e < 32; e += 4) v[e] = fmaxf(v[e], v[e + 2]);
-                                    }
-                                    if (g >= 8) {
+                                    for (int e = 0; e < 32; e += 4) v[e] = fmaxf(v[e], v[e + 2]);
+                                }
+                                if (g >= 8) {
 #pragma unroll
-                                        for (int e = 0; e < 32; e += 8) v[e] = fmaxf(v[e], v[e + 4]);
-                                    }
-                                    if (g >= 16) {
+                                    for (int e = 0; e < 32; e += 8) v[e] = fmaxf(v[e], v[e + 4]);
+                                }
+                                if (g >= 16) {
 #pragma unroll
-                                        for (int e = 0; e < 32; e += 16) v[e] = fmaxf(v[e], v[e + 8]);
-                                    }
+                                    for (int e = 0; e < 32; e += 16) v[e] = fmaxf(v[e], v[e + 8]);
+                                }
 #pragma unroll
-                                    for (int e = 0; e < 32; ++e) {
-                                        if ((e & (g - 1)) == 0 && j0 + e < n_i)
-                                            gcol[static_cast<int64_t>((j0 + e) / g) * kTileM] =
-                                                static_cast<uint16_t>(f32_order_key(v[e] * p.scale) >> 16);
-                                    }
+                                for (int e = 0; e < 32; ++e) {
+                                    if ((e & (g - 1)) == 0 && j0 + e < n_i)
+                                        gcol[static_cast<int64_t>((j0 + e) >> g_shift) * kUnitM] =
+                                            static_cast<uint16_t>(f32_order_key(v[e] * p.scale) >> 16);
                                 }
                             }
                         }
                         if constexpr (MODE == MODE_COLLECT) {
-                            if (max32(v) * p.scale >= tau_f) {
-                                uint64_t* crow = p.cand + row * static_cast<int64_t>(p.cap);
+                            // every score >= the row's bound is a candidate; 8-key
+                            // sub-chunk maxima skip the sub-chunks without one
+                            if (live) {
 #pragma unroll
-                                for (int e = 0; e < 32; ++e) {
-                                    const float s = v[e] * p.scale;
-                                    if (j0 + e < n_i && s >= tau_f) {
-                                        if (cnt < p.cap)
-                                            crow[cnt] = sel_key(f32_order_key(s),
-                                                                static_cast<uint32_t>(j0 + e));
-                                        ++cnt;
+                                for (int s8 = 0; s8 < 4; ++s8) {
+                                    const float* w = v + 8 * s8;
+                                    if (max8(w) >= t_raw) {
+                                        uint32_t bits = 0;
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e)
+                                            bits |= (w[e] >= t_raw ? 1u : 0u) << e;
+                                        while (bits) {
+                                            const int e = __ffs(bits) - 1;
+                                            bits &= bits - 1;
+                                            const float sc = pick8(w, e) * p.scale;
+                                            if (cnt < capc)
+                                                clist[cnt] = sel_key(
+                                                    f32_order_key(sc),
+                                                    static_cast<uint32_t>(j0 + 8 * s8 + e));
+                                            ++cnt;
+                                        }
                                     }
                                 }
                             }
                         }
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(t_empty + b);
-                ++tc;
             }
             if (!ok) break;
             if constexpr (MODE == MODE_COLLECT) {
-                if (row_ok) p.cnt[row] = cnt;
+                if (row_ok) p.cnt[row * kTBuf + tb] = cnt;
             }
             if constexpr (MODE == MODE_RAW) {
                 // columns past the unit's last key tile are masked for every row
                 if (row_ok) {
                     float* out = p.S + row * static_cast<int64_t>(p.Tk);
-                    for (int j = U.ntiles * kTileN; j < p.Tk; ++j) out[j] = -INFINITY;
+                    for (int j = U.ntiles * kTileN + tb; j < p.Tk; j += kTBuf) out[j] = -INFINITY;
                 }
             }
         }
@@ -403,6 +490,9 @@ cudaError_t launch_mode(const CUtensorMap& qm, const CUtensorMap& km, const Tile
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
+    TraceLaunch tr(MODE == MODE_RAW ? "tile_scores.raw"
+                   : MODE == MODE_GROUPMAX ? "tile_scores.groupmax" : "tile_scores.collect",
+                   stream);
     kern<<<grid, kThreads, C::SMEM, stream>>>(qm, km, p);
     return cudaGetLastError();
 }
@@ -422,13 +512,12 @@ cudaError_t tile_scores_launch(const void* q_low, const void* k_low, int P, int 
     if (!make_map(&qm, q_low, static_cast<int64_t>(p.BH) * p.Tq, P) ||
         !make_map(&km, k_low, static_cast<int64_t>(p.BH) * p.Tk, P))
         return cudaErrorInvalidValue;
-    p.units_per_head = (p.Tq + kTileM - 1) / kTileM;
+    p.units_per_head = (p.Tq + kUnitM - 1) / kUnitM;
     p.num_units = p.BH * p.units_per_head;
     if (p.num_units == 0) return cudaSuccess;
-    if (p.wait_limit_ns == 0) p.wait_limit_ns = 1000000000ull;   // 1 s
     const int sms = tile_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const int grid = p.num_units < 2 * sms ? p.num_units : 2 * sms;
+    const int grid = p.num_units < sms ? p.num_units : sms;
 #define SSA_TILE_CASE(PP, MM) \
     if (P == PP && mode == MM) return launch_mode<PP, MM>(qm, km, p, grid, stream);
     SSA_TILE_CASE(64, MODE_RAW)

@@ -19,99 +19,130 @@
 // score) is put on an overflow list and redone by the row-wise kernel.
 #include "common.cuh"
 #include "tile.h"
+#include "trace.h"
 
 namespace ssa {
 
 // ---------------------------------------------------------------- tau
 //
-// One block per unit (128 query rows). Histograms live in shared memory as
-// [bin][row pair] words holding two 16-bit counters (a row has < 65536 groups).
+// One block per 128-row half of a unit. Histograms live in shared memory as
+// [bin][row pair] words holding two 16-bit counters (a row has < 65536
+// groups). Thread t reads row t % 128 of group after group (a warp reads 64
+// contiguous bytes per load), eight loads in flight per thread.
 constexpr int kSelThreads = 256;
+constexpr int kSelUnroll = 8;
 
 __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
     const uint16_t* __restrict__ gm, uint32_t* __restrict__ tau, int BH, int Tq, int Tk, int k,
     int causal, int G_stride) {
     extern __shared__ uint32_t hist[];   // 256 * (kTileM / 2) words
+    __shared__ int n_row[kTileM];
     __shared__ uint32_t sel_hi[kTileM], need[kTileM];
-    const int units_per_head = (Tq + kTileM - 1) / kTileM;
-    const int num_units = BH * units_per_head;
+    const int units_per_head = (Tq + kUnitM - 1) / kUnitM;
+    const int num_items = BH * units_per_head * 2;   // (unit, 128-row half)
     const int tid = threadIdx.x;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+    const int r = tid % kTileM;
+    const int gstep = kSelThreads / kTileM;
+    for (int w = blockIdx.x; w < num_items; w += gridDim.x) {
+        const int u = w >> 1, h = w & 1;
         const int bh = u / units_per_head;
         const int qb = units_per_head - 1 - (u - bh * units_per_head);
-        const int i0 = qb * kTileM;
-        const int rows = min(kTileM, Tq - i0);
-        const int n_lo = tile_valid_count(i0, Tq, Tk, causal);
-        const int n_hi = tile_valid_count(i0 + rows - 1, Tq, Tk, causal);
+        const int i0u = qb * kUnitM;
+        const int rows_u = min(kUnitM, Tq - i0u);
+        const int rows = min(kTileM, rows_u - h * kTileM);
+        if (rows <= 0) continue;
+        // the group size and layout belong to the whole 256-row unit
+        const int n_lo = tile_valid_count(i0u, Tq, Tk, causal);
+        const int n_hi = tile_valid_count(i0u + rows_u - 1, Tq, Tk, causal);
         const int g = tile_group_size(n_lo, n_hi, k);
+        const int i0 = i0u + h * kTileM;
         uint32_t* tau_u = tau + static_cast<int64_t>(bh) * Tq + i0;
         if (g == 0) {   // no row has more than k valid keys: select everything
             if (tid < rows) tau_u[tid] = 0;
             continue;
         }
-        const int G_u = (n_hi + g - 1) / g;
-        const uint16_t* gu = gm + static_cast<int64_t>(u) * G_stride * kTileM;
-
+        const int G_u = tile_groups_in_unit(n_hi, g);
+        const uint16_t* gu = gm + static_cast<int64_t>(u) * G_stride * kUnitM + h * kTileM;
+        if (tid < kTileM) n_row[tid] = tid < rows ? tile_valid_count(i0 + tid, Tq, Tk, causal) : 0;
         for (int x = tid; x < 256 * (kTileM / 2); x += kSelThreads) hist[x] = 0;
         __syncthreads();
-        for (int x = tid; x < G_u * kTileM; x += kSelThreads) {
-            const int grp = x / kTileM, r = x % kTileM;
-            const int n_r = r < rows ? tile_valid_count(i0 + r, Tq, Tk, causal) : 0;
-            if (n_r > k && grp * g < n_r) {
-                const uint32_t v = gu[x];
-                atomicAdd(&hist[(v >> 8) * (kTileM / 2) + (r >> 1)], 1u << ((r & 1) * 16));
+        const int n_r = n_row[r];
+        const bool active = n_r > k;
+        const int word = r >> 1;
+        const uint32_t one = 1u << ((r & 1) * 16);
+        // pass 1: high byte of every group maximum of the row
+        if (active) {
+            for (int g0 = tid / kTileM; g0 < G_u; g0 += gstep * kSelUnroll) {
+                uint32_t v[kSelUnroll];
+#pragma unroll
+                for (int q = 0; q < kSelUnroll; ++q) {
+                    const int grp = g0 + q * gstep;
+                    v[q] = (grp < G_u && tile_group_first_key(grp, g) < n_r)
+                               ? static_cast<uint32_t>(gu[static_cast<int64_t>(grp) * kUnitM + r])
+                               : 0x10000u;
+                }
+#pragma unroll
+                for (int q = 0; q < kSelUnroll; ++q)
+                    if (v[q] < 0x10000u) atomicAdd(&hist[(v[q] >> 8) * (kTileM / 2) + word], one);
             }
         }
         __syncthreads();
         if (tid < kTileM) {
-            const int r = tid;
-            const int n_r = r < rows ? tile_valid_count(i0 + r, Tq, Tk, causal) : 0;
             uint32_t hi = 0, nd = 0;
-            if (n_r > k) {
+            if (n_row[tid] > k) {
                 uint32_t cum = 0;
                 for (int b = 255; b >= 0; --b) {
-                    const uint32_t c = (hist[b * (kTileM / 2) + (r >> 1)] >> ((r & 1) * 16)) & 0xFFFFu;
-                    if (cum + c >= static_cast<uint32_t>(k)) {
+                    const uint32_t cb =
+                        (hist[b * (kTileM / 2) + (tid >> 1)] >> ((tid & 1) * 16)) & 0xFFFFu;
+                    if (cum + cb >= static_cast<uint32_t>(k)) {
                         hi = b;
                         nd = k - cum;
                         break;
                     }
-                    cum += c;
+                    cum += cb;
                 }
             }
-            sel_hi[r] = hi;
-            need[r] = nd;
+            sel_hi[tid] = hi;
+            need[tid] = nd;
         }
         __syncthreads();
         for (int x = tid; x < 256 * (kTileM / 2); x += kSelThreads) hist[x] = 0;
         __syncthreads();
-        for (int x = tid; x < G_u * kTileM; x += kSelThreads) {
-            const int grp = x / kTileM, r = x % kTileM;
-            const int n_r = r < rows ? tile_valid_count(i0 + r, Tq, Tk, causal) : 0;
-            if (n_r > k && grp * g < n_r) {
-                const uint32_t v = gu[x];
-                if ((v >> 8) == sel_hi[r])
-                    atomicAdd(&hist[(v & 0xFFu) * (kTileM / 2) + (r >> 1)], 1u << ((r & 1) * 16));
+        // pass 2: low byte of the group maxima in the selected high-byte bin
+        if (active) {
+            const uint32_t hsel = sel_hi[r];
+            for (int g0 = tid / kTileM; g0 < G_u; g0 += gstep * kSelUnroll) {
+                uint32_t v[kSelUnroll];
+#pragma unroll
+                for (int q = 0; q < kSelUnroll; ++q) {
+                    const int grp = g0 + q * gstep;
+                    v[q] = (grp < G_u && tile_group_first_key(grp, g) < n_r)
+                               ? static_cast<uint32_t>(gu[static_cast<int64_t>(grp) * kUnitM + r])
+                               : 0x10000u;
+                }
+#pragma unroll
+                for (int q = 0; q < kSelUnroll; ++q)
+                    if ((v[q] >> 8) == hsel)
+                        atomicAdd(&hist[(v[q] & 0xFFu) * (kTileM / 2) + word], one);
             }
         }
         __syncthreads();
         if (tid < rows) {
-            const int r = tid;
-            const int n_r = tile_valid_count(i0 + r, Tq, Tk, causal);
             uint32_t t32 = 0;
-            if (n_r > k) {
+            if (n_row[tid] > k) {
                 uint32_t cum = 0, lo = 0;
                 for (int b = 255; b >= 0; --b) {
-                    const uint32_t c = (hist[b * (kTileM / 2) + (r >> 1)] >> ((r & 1) * 16)) & 0xFFFFu;
-                    if (cum + c >= need[r]) {
+                    const uint32_t cb =
+                        (hist[b * (kTileM / 2) + (tid >> 1)] >> ((tid & 1) * 16)) & 0xFFFFu;
+                    if (cum + cb >= need[tid]) {
                         lo = b;
                         break;
                     }
-                    cum += c;
+                    cum += cb;
                 }
-                t32 = ((sel_hi[r] << 8) | lo) << 16;
+                t32 = ((sel_hi[tid] << 8) | lo) << 16;
             }
-            tau_u[r] = t32;
+            tau_u[tid] = t32;
         }
         __syncthreads();
     }
@@ -165,29 +196,33 @@ __global__ void __launch_bounds__(256) cand_sort_kernel(
     const uint64_t* __restrict__ cand, const int32_t* __restrict__ cnt, int64_t rows, int Tq,
     int Tk, int k, int causal, int32_t* __restrict__ idx_out, float* __restrict__ score_out,
     int64_t* __restrict__ ovf_list, int32_t* __restrict__ ovf_count) {
-    constexpr int CAP = 32 * E;
+    constexpr int CAP = 32 * E;       // two lists of CAP/2 = 16E; lane l reads list l/16
+    constexpr int CAPC = CAP / 2;
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (row >= rows) return;
     const int i = static_cast<int>(row % Tq);
     const int n = tile_valid_count(i, Tq, Tk, causal);
     const int keff = min(k, n);
-    const int c = n > 0 ? cnt[row] : 0;
-    if (c > CAP) {
+    int c_list = 0;
+    if (n > 0 && lane < 2) c_list = cnt[row * 2 + lane];
+    const bool overflow = __any_sync(0xffffffffu, c_list > CAPC);
+    if (overflow) {
         if (lane == 0) ovf_list[atomicAdd(ovf_count, 1)] = row;
         return;
     }
+    const int my_cnt = __shfl_sync(0xffffffffu, c_list, lane >> 4);
+    const int off = (lane & 15) * E;   // offset of this lane's elements in its list
     uint64_t x[E];
-    const uint64_t* src = cand + row * CAP + lane * E;
+    const uint64_t* src = cand + row * CAP + (lane >> 4) * CAPC + off;
 #pragma unroll
     for (int r = 0; r < E; r += 2) {
-        const int e = lane * E + r;
-        if (e + 1 < c) {
+        if (off + r + 1 < my_cnt) {
             const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(src + r);
             x[r] = v.x;
             x[r + 1] = v.y;
         } else {
-            x[r] = e < c ? src[r] : 0ull;
+            x[r] = off + r < my_cnt ? src[r] : 0ull;
             x[r + 1] = 0ull;
         }
     }
@@ -211,14 +246,15 @@ __global__ void __launch_bounds__(256) cand_sort_kernel(
 
 cudaError_t tile_select_launch(const uint16_t* gm, uint32_t* tau, int BH, int Tq, int Tk, int k,
                                int causal, cudaStream_t stream) {
-    const int units = BH * ((Tq + kTileM - 1) / kTileM);
-    if (units == 0) return cudaSuccess;
+    const int items = 2 * BH * ((Tq + kUnitM - 1) / kUnitM);
+    if (items == 0) return cudaSuccess;
     const int sms = tile_sm_count();
-    const int grid = units < 3 * sms ? units : 3 * sms;
+    const int grid = items < 3 * sms ? items : 3 * sms;
     constexpr int kHistBytes = 256 * (kTileM / 2) * 4;
     cudaError_t e = cudaFuncSetAttribute(group_select_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kHistBytes);
     if (e != cudaSuccess) return e;
+    TraceLaunch tr("group_select", stream);
     group_select_kernel<<<grid, kSelThreads, kHistBytes, stream>>>(gm, tau, BH, Tq, Tk, k, causal,
                                                                    tile_group_stride(k));
     return cudaGetLastError();
@@ -231,6 +267,7 @@ cudaError_t tile_sort_launch(const uint64_t* cand, const int32_t* cnt, int64_t r
     const int64_t blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int cap = tile_cand_cap(k);
+    TraceLaunch tr("cand_sort", stream);
 #define SSA_SORT_CASE(EE)                                                                      \
     if (cap == 32 * EE) {                                                                      \
         cand_sort_kernel<EE><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(               \

@@ -15,6 +15,7 @@
 // lanes share one 16-byte-sliced key row, a transpose-reduction leaves one
 // score per lane.
 #include "common.cuh"
+#include "trace.h"
 
 namespace ssa {
 
@@ -303,6 +304,7 @@ cudaError_t topk_rows_dispatch(const void* q_low, const void* k_low, bool bf16, 
                                cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
     const int64_t grid = rows < ws_slots ? rows : ws_slots;
+    TraceLaunch tr("topk_rows", stream);
 #define SSA_TOPK_CASE(BF, PP)                                                                \
     if (bf16 == BF && P == PP) {                                                             \
         topk_rows_kernel<BF, PP><<<(unsigned)grid, TOPK_THREADS, 0, stream>>>(              \

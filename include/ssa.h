@@ -220,6 +220,24 @@ ssa_status ssa_score_topk_noalloc(const void* q_low, const void* k_low, int dtyp
                                   int Tq, int Tk, int P, int k, int causal, float scale,
                                   int32_t* idx, float* score, int32_t* dev_status, void* stream);
 
+/*
+ * Launch tracing. Between ssa_trace_begin() and ssa_trace_end(), every kernel
+ * this library launches is bracketed by two CUDA events recorded on the
+ * launching stream (the tracing itself launches nothing and allocates no
+ * device memory). ssa_trace_end() waits for the recorded events, copies up to
+ * max_records (kernel name, milliseconds) pairs in launch order into `out`
+ * (may be NULL), stops tracing and returns the number of launches recorded,
+ * or -1 if a CUDA event call failed. Meant for profiling: tracing adds two
+ * event records per launch.
+ */
+typedef struct {
+    char name[56];
+    float ms;
+} ssa_trace_record;
+
+int ssa_trace_begin(void);
+int ssa_trace_end(ssa_trace_record* out, int max_records);
+
 #ifdef __cplusplus
 }
 #endif
