@@ -88,7 +88,11 @@ size_t ssa_score_topk_workspace_size(int B, int H, int Tq, int Tk, int P, int k,
  *              (bottom-right alignment: the last query sees every key),
  * the score of key j is s_j = fp32(sum_p q_low[b,h,i,p] * k_low[b,h,j,p]) *
  * scale, products and sums in fp32 (bf16 inputs are exact in fp32; integer
- * valued inputs give exact scores). The call writes the k_eff = min(k,
+ * valued inputs give exact scores). For bf16 inputs with P in {64, 128},
+ * k <= 512 and Tq >= 64 the sum runs on the tensor cores with fp32
+ * accumulation in the hardware's order (the scores ssa_lowrank_scores
+ * returns); otherwise as a sequential fp32 sum. The selection is exact for
+ * the scores so computed. The call writes the k_eff = min(k,
  * |valid(i)|) valid keys with the largest scores, ordered by score
  * descending, equal scores by key index ascending (the lower index wins a tie).
  * Slots k_eff..k-1 hold index -1 and score -inf.
@@ -102,7 +106,8 @@ size_t ssa_score_topk_workspace_size(int B, int H, int Tq, int Tk, int P, int k,
  *   idx       device, int32 [B, H, Tq, k], written
  *   score     device, float [B, H, Tq, k], written; may be NULL
  *   workspace device scratch of at least ssa_score_topk_workspace_size(...)
- *             bytes (its contents on entry do not matter; it is overwritten)
+ *             bytes, 256-byte aligned (its contents on entry do not matter;
+ *             it is overwritten)
  *   dev_status device int32 or NULL (see conventions)
  *   stream    cudaStream_t
  *
