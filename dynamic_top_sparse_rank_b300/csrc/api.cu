@@ -14,7 +14,7 @@ cudaError_t topk_rows_dispatch(const void* q_low, const void* k_low, bool bf16, 
 cudaError_t tile_select_launch(const uint16_t* gm, uint32_t* tau, int BH, int Tq, int Tk, int k,
                                int causal, cudaStream_t stream);
 cudaError_t tile_sort_launch(const uint64_t* cand, const int32_t* cnt, int64_t rows, int Tq,
-                             int Tk, int k, int causal, int32_t* idx, float* score,
+                             int Tk, int k, int causal, float scale, int32_t* idx, float* score,
                              int64_t* ovf_list, int32_t* ovf_count, cudaStream_t stream);
 template <bool BAND>
 cudaError_t attn_rows_dispatch(const void* Q, const void* K, const void* V, bool bf16_in, int D,
@@ -133,8 +133,8 @@ ssa_status ssa_score_topk(const void* q_low, const void* k_low, int dtype, int B
     if (e == cudaSuccess) e = ssa::tile_select_launch(gm, tau, BH, Tq, Tk, k, p.causal, s);
     if (e == cudaSuccess) e = ssa::tile_scores_launch(q_low, k_low, P, ssa::MODE_COLLECT, p, s);
     if (e == cudaSuccess)
-        e = ssa::tile_sort_launch(cand, cnt, rows, Tq, Tk, k, p.causal, idx, score, ovf_list,
-                                  ovf_count, s);
+        e = ssa::tile_sort_launch(cand, cnt, rows, Tq, Tk, k, p.causal, sc, idx, score,
+                                  ovf_list, ovf_count, s);
     if (e == cudaSuccess)
         e = ssa::topk_rows_dispatch(q_low, k_low, true, P, ovf_list, rows, ovf_count, Tq, Tk, k,
                                     p.causal, sc, idx, score,

@@ -87,7 +87,7 @@ struct TileParams {
     uint16_t* gm;                    // MODE_GROUPMAX: [units, G_stride, 256]
     int G_stride;
     const uint32_t* tau;             // MODE_COLLECT: [BH*Tq] order-key thresholds
-    uint64_t* cand;                  // MODE_COLLECT: [BH*Tq, 2, cap/2] composite keys
+    uint64_t* cand;                  // MODE_COLLECT: [BH*Tq, 2, cap/2] (raw score bits << 32) | index
     int32_t* cnt;                    // MODE_COLLECT: [BH*Tq, 2] candidates found
     int cap;                         // per row; half per TMEM tile buffer
     int32_t* dev_status;

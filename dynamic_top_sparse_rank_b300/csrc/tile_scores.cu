@@ -12,7 +12,8 @@
 //                  (layout in tile.h) and writes the 16 high bits of the order
 //                  key of every group's maximum score;
 //   MODE_COLLECT   appends every valid key whose score reaches the row's
-//                  threshold to the row's candidate lists.
+//                  threshold to the row's candidate lists, as (raw score
+//                  bits, key index) pairs.
 // The exact top-k of a row is then found from these (tile_select.cu).
 //
 // Block layout (576 threads, one block per SM): warp 0 issues TMA loads (the
@@ -52,17 +53,27 @@ constexpr int kTBuf = kTileGroups;            // TMEM tile buffers (two accumula
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
-template <int P>
+// Candidate queue of one epilogue warp (MODE_COLLECT): each entry is an 8-key
+// sub-chunk holding at least one candidate (its 8 raw scores, its first key,
+// the lane = row that owns it); the warp drains 32 entries at a time, one per
+// lane, so the per-candidate work runs on full warps.
+constexpr int kQueue = 64;                                   // entries, power of two
+constexpr uint32_t kQueueWarpBytes = kQueue * 32 + kQueue * 4 + 32 * 4;
+
+template <int P, int MODE>
 struct TileCfg {
     static constexpr int KA = P / 64;                       // 128-byte K atoms per row
-    static constexpr int STAGES = (P == 64) ? 8 : 4;        // key-tile ring depth
+    static constexpr bool QUEUE = MODE == MODE_COLLECT;
+    static constexpr int STAGES = (P == 64) ? (QUEUE ? 7 : 8) : (QUEUE ? 3 : 4);   // key ring
     static constexpr int QSLOTS = (P == 64) ? 2 : 1;        // query-unit slots
     static constexpr uint32_t QHALF = KA * kTileM * 128;    // one 128-row query tile
     static constexpr uint32_t QBYTES = 2 * QHALF;           // a unit's two query tiles
     static constexpr uint32_t KBYTES = KA * kTileN * 128;
     static constexpr uint32_t K_OFF = QSLOTS * QBYTES;
     static constexpr uint32_t BAR_OFF = K_OFF + STAGES * KBYTES;
-    static constexpr uint32_t SMEM = BAR_OFF + 512 + 1024;  // + barriers + alignment slack
+    static constexpr uint32_t QUEUE_OFF = BAR_OFF + 512;
+    static constexpr uint32_t SMEM =
+        QUEUE_OFF + (QUEUE ? kEpiWarps * kQueueWarpBytes : 0) + 1024;   // + alignment slack
 };
 
 struct Unit {
@@ -97,15 +108,17 @@ SSA_DEVINL float max32(const float (&v)[32]) {
     return fmaxf(fmax3(b0, b1, b2), b3);
 }
 
-// v[e] for a runtime e in 0..7 (a select tree keeps v in registers).
-SSA_DEVINL float pick8(const float* v, int e) {
-    const float a0 = (e & 1) ? v[1] : v[0];
-    const float a1 = (e & 1) ? v[3] : v[2];
-    const float a2 = (e & 1) ? v[5] : v[4];
-    const float a3 = (e & 1) ? v[7] : v[6];
-    const float b0 = (e & 2) ? a1 : a0;
-    const float b1 = (e & 2) ? a3 : a2;
-    return (e & 4) ? b1 : b0;
+// Bit e of the result is set iff v[e] >= t (e < 8): one set + one funnel
+// shift per element, no branches.
+SSA_DEVINL uint32_t ge_mask8(const float* v, float t) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int e = 7; e >= 0; --e) {
+        uint32_t d;
+        asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(d) : "f"(v[e]), "f"(t));
+        m = __funnelshift_l(d, m, 1);   // (m << 1) | (d >> 31)
+    }
+    return m;
 }
 
 // Smallest float x with fl(x * scale) >= t (scale > 0): fl(x * scale) is
@@ -126,7 +139,7 @@ template <int P, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     tile_scores_kernel(const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ CUtensorMap kmap, const TileParams p) {
-    using C = TileCfg<P>;
+    using C = TileCfg<P, MODE>;
     constexpr int S = C::STAGES;
     constexpr uint32_t IDESC = idesc_bf16_f32(kTileM, kTileN);
 
@@ -291,6 +304,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int capc = p.cap / kTBuf;        // this buffer's candidate list of the row
         uint32_t tpar = 0;                     // phase parity of TMEM buffer tb
         bool ok = true;
+        // MODE_COLLECT queue of this warp and the candidate count of each row
+        float* qv = nullptr;                   // [kQueue][8] raw scores
+        uint32_t* qm = nullptr;                // [kQueue] (first key / 8) << 5 | owning lane
+        int* qcnt = nullptr;                   // [32] candidates appended per row
+        int q_tail = 0;                        // warp-uniform: entries in the queue
+        int64_t row0 = 0;                      // global row of lane 0
+        float t_raw = -FLT_MAX;                // raw-score bound of this thread's row
+        if constexpr (MODE == MODE_COLLECT) {
+            uint8_t* qb = smem + C::QUEUE_OFF + (warp - 2) * kQueueWarpBytes;
+            qv = reinterpret_cast<float*>(qb);
+            qm = reinterpret_cast<uint32_t*>(qb + kQueue * 32);
+            qcnt = reinterpret_cast<int*>(qb + kQueue * 36);
+            qcnt[lane] = 0;
+            __syncwarp();
+        }
+        // Drain the first `n` (<= 32) queue entries, entry l by lane l: its
+        // candidates (scores >= the owning row's bound) are appended to that
+        // row's list; a shared-memory count per row hands out the slots.
+        auto drain = [&](int n) {
+            const bool act = lane < n;
+            const uint32_t meta = act ? qm[lane] : 0u;
+            const int owner = static_cast<int>(meta & 31u);
+            const float t_own = __shfl_sync(0xffffffffu, t_raw, owner);
+            uint32_t bits = 0;
+            if (act) {
+                const float4 a = reinterpret_cast<const float4*>(qv + lane * 8)[0];
+                const float4 b = reinterpret_cast<const float4*>(qv + lane * 8)[1];
+                const float w8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                bits = ge_mask8(w8, t_own);
+            }
+            if (bits) {
+                int slot = atomicAdd(qcnt + owner, __popc(bits));
+                uint64_t* dst = p.cand + ((row0 + owner) * kTBuf + tb) * static_cast<int64_t>(capc);
+                const uint32_t jb = (meta >> 5) << 3;
+                while (bits) {
+                    const int e = __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    if (slot < capc)
+                        dst[slot] = (static_cast<uint64_t>(__float_as_uint(qv[lane * 8 + e])) << 32) |
+                                    (jb + static_cast<uint32_t>(e));
+                    ++slot;
+                }
+            }
+            __syncwarp();
+        };
         for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
             const Unit U = unit_at(p, u);
             const bool row_ok = r < U.rows;
@@ -300,10 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // mode state
             int g = 0, m_shift = 0, g_shift = 0;   // g and m = g/32 are powers of two
             float gacc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            float t_raw = -FLT_MAX;            // raw-score bound of this thread's row
-            int cnt = 0;
+            t_raw = -FLT_MAX;
             uint16_t* gcol = nullptr;
-            uint64_t* clist = nullptr;
             if constexpr (MODE == MODE_GROUPMAX) {
                 g = tile_group_size(U.n_lo, U.n_hi, p.k);
                 g_shift = g > 0 ? __ffs(g) - 1 : 0;
@@ -317,8 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     t_raw = raw_threshold(t32 == 0 ? -INFINITY : order_key_f32(t32), p.scale);
                 }
             }
-            if constexpr (MODE == MODE_COLLECT)
-                clist = p.cand + (row * kTBuf + tb) * static_cast<int64_t>(capc);
+            row0 = row - lane;
             for (int t = tb; t < U.ntiles; t += kTBuf) {
                 // warp-uniform outcome: tcgen05.ld below needs the whole warp
                 ok = __all_sync(0xffffffffu, mbar_wait_bounded(t_full + tb, tpar, abort_flag,
@@ -397,25 +452,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         if constexpr (MODE == MODE_COLLECT) {
                             // every score >= the row's bound is a candidate; 8-key
-                            // sub-chunk maxima skip the sub-chunks without one
-                            if (live) {
+                            // sub-chunk maxima pick the sub-chunks holding one, which
+                            // are queued and drained 32 at a time
 #pragma unroll
-                                for (int s8 = 0; s8 < 4; ++s8) {
-                                    const float* w = v + 8 * s8;
-                                    if (max8(w) >= t_raw) {
-                                        uint32_t bits = 0;
-#pragma unroll
-                                        for (int e = 0; e < 8; ++e)
-                                            bits |= (w[e] >= t_raw ? 1u : 0u) << e;
-                                        while (bits) {
-                                            const int e = __ffs(bits) - 1;
-                                            bits &= bits - 1;
-                                            const float sc = pick8(w, e) * p.scale;
-                                            if (cnt < capc)
-                                                clist[cnt] = sel_key(
-                                                    f32_order_key(sc),
-                                                    static_cast<uint32_t>(j0 + 8 * s8 + e));
-                                            ++cnt;
+                            for (int s8 = 0; s8 < 4; ++s8) {
+                                const float* w = v + 8 * s8;
+                                const bool hot = live && max8(w) >= t_raw;
+                                const uint32_t B = __ballot_sync(0xffffffffu, hot);
+                                if (B) {
+                                    if (hot) {
+                                        const int q = q_tail + __popc(B & ((1u << lane) - 1));
+                                        float4* dst = reinterpret_cast<float4*>(qv + q * 8);
+                                        dst[0] = make_float4(w[0], w[1], w[2], w[3]);
+                                        dst[1] = make_float4(w[4], w[5], w[6], w[7]);
+                                        qm[q] = (static_cast<uint32_t>((j0 + 8 * s8) >> 3) << 5) |
+                                                static_cast<uint32_t>(lane);
+                                    }
+                                    q_tail += __popc(B);
+                                    __syncwarp();
+                                    if (q_tail >= 32) {
+                                        drain(32);
+                                        q_tail -= 32;
+                                        if (q_tail > 0) {   // move the rest to the front
+                                            if (lane < q_tail) {
+                                                const float4* from = reinterpret_cast<const float4*>(qv + (32 + lane) * 8);
+                                                float4* to = reinterpret_cast<float4*>(qv + lane * 8);
+                                                // entry 32+l moves to l: sources and targets
+                                                // never overlap (fewer than 32 remain)
+                                                const float4 a = from[0], b2 = from[1];
+                                                const uint32_t mm = qm[32 + lane];
+                                                to[0] = a;
+                                                to[1] = b2;
+                                                qm[lane] = mm;
+                                            }
+                                            __syncwarp();
                                         }
                                     }
                                 }
@@ -426,7 +496,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             if constexpr (MODE == MODE_COLLECT) {
-                if (row_ok) p.cnt[row * kTBuf + tb] = cnt;
+                if (q_tail > 0) drain(q_tail);
+                q_tail = 0;
+                if (row_ok) p.cnt[row * kTBuf + tb] = qcnt[lane];
+                qcnt[lane] = 0;
+                __syncwarp();
             }
             if constexpr (MODE == MODE_RAW) {
                 // columns past the unit's last key tile are masked for every row
@@ -485,7 +559,7 @@ bool make_map(CUtensorMap* m, const void* base, int64_t nrows, int P) {
 template <int P, int MODE>
 cudaError_t launch_mode(const CUtensorMap& qm, const CUtensorMap& km, const TileParams& p,
                         int grid, cudaStream_t stream) {
-    using C = TileCfg<P>;
+    using C = TileCfg<P, MODE>;
     auto kern = tile_scores_kernel<P, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::SMEM));

@@ -12,8 +12,8 @@
 //   pass 1 (tile kernel, MODE_GROUPMAX) writes the rounded group maxima;
 //   group_select_kernel finds tau per row (a 2 x 8-bit radix select);
 //   pass 2 (tile kernel, MODE_COLLECT) keeps every valid key with score >= tau;
-//   cand_sort_kernel sorts a row's candidates by (score desc, index asc) and
-//   writes the first k_eff.
+//   cand_sort_kernel selects the k_eff largest candidates (radix select) and
+//   sorts them by (score desc, index asc).
 // With G between 2k and 4k, about k + k^2/(2G) <= 1.25k keys pass the bound.
 // A row with more candidates than its list holds (heavy ties at the k-th
 // score) is put on an overflow list and redone by the row-wise kernel.
@@ -150,10 +150,21 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
 
 // ---------------------------------------------------------------- sort
 //
-// One warp per row: the row's candidates (composite keys, see sel_key) are
-// loaded lane-major (lane l holds elements l*E .. l*E+E-1), sorted descending
-// by a bitonic network (strides below E inside a lane, the others across
-// lanes by shuffles), and the first k_eff written out.
+// One warp per row. The candidate pass stores (raw score bits, index) pairs;
+// here they become composite keys x = (order key of raw * scale << 32) |
+// ~index, all distinct, so the row's answer is its k_eff largest keys in
+// descending order (score descending, index ascending).
+//  1. Radix select (MSB first, 8-bit digits) finds the k_eff-th largest key:
+//     a digit all candidates share is skipped without a histogram (found from
+//     the OR and AND of all keys), and the search stops as soon as the
+//     remaining rank fills a whole bin.
+//  2. The keys >= that key (exactly k_eff of them) are compacted into shared
+//     memory and sorted descending by a bitonic network in registers (strides
+//     below E inside a lane, the others across lanes by shuffles).
+// Keys live in registers batch-major: register b of lane l holds element
+// 32*b + l.
+constexpr int kSortWarps = 8;
+
 template <int E>
 SSA_DEVINL void warp_bitonic_desc(uint64_t (&x)[E], int lane) {
     constexpr int N = 32 * E;
@@ -191,42 +202,138 @@ SSA_DEVINL void warp_bitonic_desc(uint64_t (&x)[E], int lane) {
     }
 }
 
-template <int E>
-__global__ void __launch_bounds__(256) cand_sort_kernel(
+template <int NB, int E>   // NB batches of 32 candidates; E = winners per lane (32E >= k)
+__global__ void __launch_bounds__(kSortWarps * 32) cand_sort_kernel(
     const uint64_t* __restrict__ cand, const int32_t* __restrict__ cnt, int64_t rows, int Tq,
-    int Tk, int k, int causal, int32_t* __restrict__ idx_out, float* __restrict__ score_out,
-    int64_t* __restrict__ ovf_list, int32_t* __restrict__ ovf_count) {
-    constexpr int CAP = 32 * E;       // two lists of CAP/2 = 16E; lane l reads list l/16
+    int Tk, int k, int causal, float scale, int32_t* __restrict__ idx_out,
+    float* __restrict__ score_out, int64_t* __restrict__ ovf_list,
+    int32_t* __restrict__ ovf_count) {
+    constexpr int CAP = 32 * NB;      // two lists of CAP/2
     constexpr int CAPC = CAP / 2;
-    const int lane = threadIdx.x & 31;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    constexpr int W = 32 * E;         // sorted winners
+    __shared__ uint32_t bins_all[kSortWarps][256];
+    __shared__ uint64_t win_all[kSortWarps][W];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    uint32_t* bins = bins_all[wid];
+    uint64_t* win = win_all[wid];
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kSortWarps + wid;
     if (row >= rows) return;
     const int i = static_cast<int>(row % Tq);
     const int n = tile_valid_count(i, Tq, Tk, causal);
     const int keff = min(k, n);
-    int c_list = 0;
-    if (n > 0 && lane < 2) c_list = cnt[row * 2 + lane];
-    const bool overflow = __any_sync(0xffffffffu, c_list > CAPC);
-    if (overflow) {
+    const int c0 = n > 0 ? cnt[row * 2] : 0, c1 = n > 0 ? cnt[row * 2 + 1] : 0;
+    if (c0 > CAPC || c1 > CAPC) {
         if (lane == 0) ovf_list[atomicAdd(ovf_count, 1)] = row;
         return;
     }
-    const int my_cnt = __shfl_sync(0xffffffffu, c_list, lane >> 4);
-    const int off = (lane & 15) * E;   // offset of this lane's elements in its list
-    uint64_t x[E];
-    const uint64_t* src = cand + row * CAP + (lane >> 4) * CAPC + off;
+    const int c = c0 + c1;
+    const uint64_t* src = cand + row * CAP;
+    uint64_t x[NB];
+    uint64_t kor = 0, kand = ~0ull;
 #pragma unroll
-    for (int r = 0; r < E; r += 2) {
-        if (off + r + 1 < my_cnt) {
-            const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(src + r);
-            x[r] = v.x;
-            x[r + 1] = v.y;
-        } else {
-            x[r] = off + r < my_cnt ? src[r] : 0ull;
-            x[r + 1] = 0ull;
+    for (int b = 0; b < NB; ++b) {
+        const int e = 32 * b + lane;
+        const uint64_t raw = e < c0 ? src[e] : (e < c ? src[CAPC + e - c0] : 0ull);
+        x[b] = e < c ? sel_key(f32_order_key(__uint_as_float(static_cast<uint32_t>(raw >> 32)) * scale),
+                               static_cast<uint32_t>(raw))
+                     : 0ull;   // 0 sorts last
+        if (e < c) {
+            kor |= x[b];
+            kand &= x[b];
         }
     }
-    warp_bitonic_desc<E>(x, lane);
+    // 1. radix select of the keff-th largest key
+    uint64_t thr = 0;   // keys >= thr are the winners
+    if (keff > 0 && keff < c) {
+        const uint32_t or_lo = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(kor));
+        const uint32_t or_hi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(kor >> 32));
+        const uint32_t and_lo = __reduce_and_sync(0xffffffffu, static_cast<uint32_t>(kand));
+        const uint32_t and_hi = __reduce_and_sync(0xffffffffu, static_cast<uint32_t>(kand >> 32));
+        const uint64_t vary = ((static_cast<uint64_t>(or_hi ^ and_hi)) << 32) | (or_lo ^ and_lo);
+        const uint64_t same = (static_cast<uint64_t>(and_hi) << 32) | and_lo;
+        uint64_t prefix = 0, pmask = 0;
+        uint32_t need = static_cast<uint32_t>(keff);
+        for (int d = 7; d >= 0; --d) {
+            const int sh = 8 * d;
+            const uint64_t dm = 0xFFull << sh;
+            if ((vary & dm) == 0) {   // every candidate has this digit
+                prefix |= same & dm;
+                pmask |= dm;
+                continue;
+            }
+            for (int t = lane; t < 256; t += 32) bins[t] = 0;
+            __syncwarp();
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                if (32 * b >= c) break;
+                if (32 * b + lane < c && (x[b] & pmask) == prefix)
+                    atomicAdd(&bins[static_cast<uint32_t>(x[b] >> sh) & 0xFFu], 1u);
+            }
+            __syncwarp();
+            // bin holding the need-th largest: lane l owns bins 255-8l .. 248-8l
+            uint32_t cb[8], tot = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                cb[q] = bins[255 - 8 * lane - q];
+                tot += cb[q];
+            }
+            uint32_t incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const uint32_t excl = incl - tot;
+            uint32_t sel = 0, above = 0, inbin = 0;
+            const bool mine = excl < need && need <= incl;
+            if (mine) {
+                uint32_t a = excl;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (a + cb[q] >= need) {
+                        sel = 255 - 8 * lane - q;
+                        above = a;
+                        inbin = cb[q];
+                        break;
+                    }
+                    a += cb[q];
+                }
+            }
+            const unsigned who = __ballot_sync(0xffffffffu, mine);
+            const int src_lane = __ffs(who) - 1;
+            sel = __shfl_sync(0xffffffffu, sel, src_lane);
+            above = __shfl_sync(0xffffffffu, above, src_lane);
+            inbin = __shfl_sync(0xffffffffu, inbin, src_lane);
+            __syncwarp();
+            prefix |= static_cast<uint64_t>(sel) << sh;
+            pmask |= dm;
+            need -= above;
+            if (inbin == need) break;   // the whole bin is selected: thr = its lowest key
+        }
+        thr = prefix;   // digits below the last fixed one are zero
+    }
+    // 2. compact the winners (keys >= thr, exactly keff of them) and sort them
+    int base = 0;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        if (32 * b >= c) break;
+        const bool w = 32 * b + lane < c && x[b] >= thr;
+        const unsigned m = __ballot_sync(0xffffffffu, w);
+        if (w) {
+            const int pos = base + __popc(m & ((1u << lane) - 1));
+            const int pl = pos / E, pr = pos % E;   // its lane and register in the sort
+            if (pos < W) win[pl * E + (pr ^ (pl % E))] = x[b];
+        }
+        base += __popc(m);
+    }
+    __syncwarp();
+    uint64_t y[E];
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+        const int e = lane * E + r;
+        y[r] = e < keff ? win[lane * E + (r ^ (lane % E))] : 0ull;   // swizzled: no bank conflicts
+    }
+    warp_bitonic_desc<E>(y, lane);
     int32_t* io = idx_out + row * k;
     float* so = score_out ? score_out + row * k : nullptr;
 #pragma unroll
@@ -234,8 +341,8 @@ __global__ void __launch_bounds__(256) cand_sort_kernel(
         const int e = lane * E + r;
         if (e < k) {
             if (e < keff) {
-                io[e] = static_cast<int32_t>(sel_key_index(x[r]));
-                if (so) so[e] = order_key_f32(sel_key_okey(x[r]));
+                io[e] = static_cast<int32_t>(sel_key_index(y[r]));
+                if (so) so[e] = order_key_f32(sel_key_okey(y[r]));
             } else {
                 io[e] = -1;
                 if (so) so[e] = -INFINITY;
@@ -261,17 +368,18 @@ cudaError_t tile_select_launch(const uint16_t* gm, uint32_t* tau, int BH, int Tq
 }
 
 cudaError_t tile_sort_launch(const uint64_t* cand, const int32_t* cnt, int64_t rows, int Tq,
-                             int Tk, int k, int causal, int32_t* idx, float* score,
+                             int Tk, int k, int causal, float scale, int32_t* idx, float* score,
                              int64_t* ovf_list, int32_t* ovf_count, cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
-    const int64_t blocks = (rows + 7) / 8;
+    const int64_t blocks = (rows + kSortWarps - 1) / kSortWarps;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const int cap = tile_cand_cap(k);
+    const int cap = tile_cand_cap(k);   // 2 * pow2ceil(k), at least 64
     TraceLaunch tr("cand_sort", stream);
-#define SSA_SORT_CASE(EE)                                                                      \
-    if (cap == 32 * EE) {                                                                      \
-        cand_sort_kernel<EE><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(               \
-            cand, cnt, rows, Tq, Tk, k, causal, idx, score, ovf_list, ovf_count);              \
+#define SSA_SORT_CASE(NB)                                                                      \
+    if (cap == 32 * NB) {                                                                      \
+        cand_sort_kernel<NB, NB / 2><<<static_cast<unsigned>(blocks), kSortWarps * 32, 0,      \
+                                       stream>>>(cand, cnt, rows, Tq, Tk, k, causal, scale,    \
+                                                 idx, score, ovf_list, ovf_count);             \
         return cudaGetLastError();                                                             \
     }
     SSA_SORT_CASE(2)
