@@ -66,6 +66,24 @@ SSA_DEVINL float warp_sum(float v) {
     return v;
 }
 
+// acc + sum of the products of the 8 bf16 pairs of two 16-byte slices, each
+// product and sum in fp32 (fma.rn.f32.bf16: the bf16 operands need no
+// conversion instruction).
+SSA_DEVINL float dot8_bf16(const uint4& a, const uint4& b, float acc) {
+    asm("{\n\t.reg .b16 a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3, b4, b5, b6, b7;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\t mov.b32 {a2, a3}, %2;\n\t"
+        "mov.b32 {a4, a5}, %3;\n\t mov.b32 {a6, a7}, %4;\n\t"
+        "mov.b32 {b0, b1}, %5;\n\t mov.b32 {b2, b3}, %6;\n\t"
+        "mov.b32 {b4, b5}, %7;\n\t mov.b32 {b6, b7}, %8;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\t fma.rn.f32.bf16 %0, a1, b1, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a2, b2, %0;\n\t fma.rn.f32.bf16 %0, a3, b3, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a4, b4, %0;\n\t fma.rn.f32.bf16 %0, a5, b5, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a6, b6, %0;\n\t fma.rn.f32.bf16 %0, a7, b7, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w));
+    return acc;
+}
+
 template <bool BF16_OUT, int E>
 SSA_DEVINL void store_out(void* O, int64_t elem_off, const float* v) {
     if constexpr (BF16_OUT) {
@@ -98,7 +116,7 @@ SSA_DEVINL void store_out(void* O, int64_t elem_off, const float* v) {
 // BAND == false: keys from idx[row, 0..k).  BAND == true: keys
 // max(0, i - wl) .. min(Tk - 1, i + wr) (window attention, Tq == Tk).
 template <bool BF16_IN, int D, bool BF16_OUT, bool BAND>
-__global__ void __launch_bounds__(256) attn_rows_kernel(
+__global__ void __launch_bounds__(256, 3) attn_rows_kernel(
     const void* __restrict__ Q, const void* __restrict__ K, const void* __restrict__ V,
     const int32_t* __restrict__ idx, void* __restrict__ O, int64_t rows, int Tq, int Tk, int k,
     int wl, int wr, float scale_log2, int32_t* dev_status) {
@@ -113,8 +131,11 @@ __global__ void __launch_bounds__(256) attn_rows_kernel(
     const char* Kb = reinterpret_cast<const char*>(K) + bh * (int64_t)Tk * R + s * 16;
     const char* Vb = reinterpret_cast<const char*>(V) + bh * (int64_t)Tk * R + s * 16;
 
+    // bf16 inputs: q stays packed and the scale goes onto the dot product;
+    // f32 inputs: q is pre-scaled
+    const uint4 q16 = ldg16(reinterpret_cast<const char*>(Q) + row * R + s * 16);
     float q[E];
-    Vec16<BF16_IN>::to_f32(ldg16(reinterpret_cast<const char*>(Q) + row * R + s * 16), q);
+    Vec16<BF16_IN>::to_f32(q16, q);
 #pragma unroll
     for (int e = 0; e < E; ++e) q[e] *= scale_log2;
 
@@ -155,12 +176,16 @@ __global__ void __launch_bounds__(256) attn_rows_kernel(
             }
 #pragma unroll
             for (int r = 0; r < L; ++r) {
-                float kf[E];
-                Vec16<BF16_IN>::to_f32(kv[r], kf);
-                float a = 0.f;
+                if constexpr (BF16_IN) {
+                    part[r] = dot8_bf16(q16, kv[r], 0.f);
+                } else {
+                    float kf[E];
+                    Vec16<BF16_IN>::to_f32(kv[r], kf);
+                    float a = 0.f;
 #pragma unroll
-                for (int e = 0; e < E; ++e) a = fmaf(q[e], kf[e], a);
-                part[r] = a;
+                    for (int e = 0; e < E; ++e) a = fmaf(q[e], kf[e], a);
+                    part[r] = a;
+                }
             }
         }
         uint4 vv[L];
@@ -169,7 +194,8 @@ __global__ void __launch_bounds__(256) attn_rows_kernel(
             const int jc = __shfl_sync(0xffffffffu, jj, r * G + g);
             vv[r] = ldg16(Vb + (int64_t)jc * R);
         }
-        const float dot = transpose_reduce<L>(part, lane);
+        float dot = transpose_reduce<L>(part, lane);
+        if constexpr (BF16_IN) dot *= scale_log2;
         const bool ok_mine = __shfl_sync(0xffffffffu, ok, s * G + g);
         const float lg = ok_mine ? dot : -INFINITY;
         const float mn = fmaxf(m, warp_max(lg));
