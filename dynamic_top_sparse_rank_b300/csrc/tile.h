@@ -55,6 +55,26 @@ __host__ __device__ __forceinline__ int tile_group_first_key(int grp, int g) {
     return (T * m * kTileGroups + b) * 128 + c * 32;
 }
 
+// Number of groups of a row with n valid keys among the first `limit` group
+// indices: the first keys increase with the index, so the groups holding a
+// valid key are exactly 0 .. count-1 (binary search for g >= 32).
+__host__ __device__ __forceinline__ int tile_groups_of_row(int n, int g, int limit) {
+    if (n <= 0) return 0;
+    if (g < 32) {
+        const int c = (n + g - 1) / g;
+        return c < limit ? c : limit;
+    }
+    int lo = 0, hi = limit;   // first index in [lo, hi] whose first key is >= n
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (tile_group_first_key(mid, g) < n)
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
 // Number of group indices a unit uses (rows have up to n_hi valid keys).
 __host__ __device__ __forceinline__ int tile_groups_in_unit(int n_hi, int g) {
     if (g < 32) return (n_hi + g - 1) / g;

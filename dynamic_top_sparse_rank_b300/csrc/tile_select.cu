@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
     const uint16_t* __restrict__ gm, uint32_t* __restrict__ tau, int BH, int Tq, int Tk, int k,
     int causal, int G_stride) {
     extern __shared__ uint32_t hist[];   // 256 * (kTileM / 2) words
-    __shared__ int n_row[kTileM];
+    __shared__ int n_row[kTileM], g_row[kTileM];   // valid keys, groups with a valid key
     __shared__ uint32_t sel_hi[kTileM], need[kTileM];
     const int units_per_head = (Tq + kUnitM - 1) / kUnitM;
     const int num_items = BH * units_per_head * 2;   // (unit, 128-row half)
@@ -63,23 +63,26 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
         }
         const int G_u = tile_groups_in_unit(n_hi, g);
         const uint16_t* gu = gm + static_cast<int64_t>(u) * G_stride * kUnitM + h * kTileM;
-        if (tid < kTileM) n_row[tid] = tid < rows ? tile_valid_count(i0 + tid, Tq, Tk, causal) : 0;
+        if (tid < kTileM) {
+            const int nr = tid < rows ? tile_valid_count(i0 + tid, Tq, Tk, causal) : 0;
+            n_row[tid] = nr;
+            g_row[tid] = nr > k ? tile_groups_of_row(nr, g, G_u) : 0;
+        }
         for (int x = tid; x < 256 * (kTileM / 2); x += kSelThreads) hist[x] = 0;
         __syncthreads();
-        const int n_r = n_row[r];
-        const bool active = n_r > k;
+        const int G_r = g_row[r];   // groups 0 .. G_r-1 of row r hold a valid key
+        const bool active = G_r > 0;
         const int word = r >> 1;
         const uint32_t one = 1u << ((r & 1) * 16);
         // pass 1: high byte of every group maximum of the row
         if (active) {
-            for (int g0 = tid / kTileM; g0 < G_u; g0 += gstep * kSelUnroll) {
+            for (int g0 = tid / kTileM; g0 < G_r; g0 += gstep * kSelUnroll) {
                 uint32_t v[kSelUnroll];
 #pragma unroll
                 for (int q = 0; q < kSelUnroll; ++q) {
                     const int grp = g0 + q * gstep;
-                    v[q] = (grp < G_u && tile_group_first_key(grp, g) < n_r)
-                               ? static_cast<uint32_t>(gu[static_cast<int64_t>(grp) * kUnitM + r])
-                               : 0x10000u;
+                    v[q] = grp < G_r ? static_cast<uint32_t>(gu[static_cast<int64_t>(grp) * kUnitM + r])
+                                     : 0x10000u;
                 }
 #pragma unroll
                 for (int q = 0; q < kSelUnroll; ++q)
@@ -111,14 +114,13 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
         // pass 2: low byte of the group maxima in the selected high-byte bin
         if (active) {
             const uint32_t hsel = sel_hi[r];
-            for (int g0 = tid / kTileM; g0 < G_u; g0 += gstep * kSelUnroll) {
+            for (int g0 = tid / kTileM; g0 < G_r; g0 += gstep * kSelUnroll) {
                 uint32_t v[kSelUnroll];
 #pragma unroll
                 for (int q = 0; q < kSelUnroll; ++q) {
                     const int grp = g0 + q * gstep;
-                    v[q] = (grp < G_u && tile_group_first_key(grp, g) < n_r)
-                               ? static_cast<uint32_t>(gu[static_cast<int64_t>(grp) * kUnitM + r])
-                               : 0x10000u;
+                    v[q] = grp < G_r ? static_cast<uint32_t>(gu[static_cast<int64_t>(grp) * kUnitM + r])
+                                     : 0x10000u;
                 }
 #pragma unroll
                 for (int q = 0; q < kSelUnroll; ++q)
