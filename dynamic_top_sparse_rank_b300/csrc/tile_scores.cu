@@ -53,18 +53,19 @@ constexpr int kTBuf = kTileGroups;            // TMEM tile buffers (two accumula
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
-// Candidate queue of one epilogue warp (MODE_COLLECT): each entry is an 8-key
-// sub-chunk holding at least one candidate (its 8 raw scores, its first key,
+// Candidate queue of one epilogue warp (MODE_COLLECT): each entry is a 16-key
+// half-chunk holding at least one candidate (its 16 raw scores, its first key,
 // the lane = row that owns it); the warp drains 32 entries at a time, one per
 // lane, so the per-candidate work runs on full warps.
 constexpr int kQueue = 64;                                   // entries, power of two
-constexpr uint32_t kQueueWarpBytes = kQueue * 32 + kQueue * 4 + 32 * 4;
+constexpr int kSub = 16;                                     // keys per entry
+constexpr uint32_t kQueueWarpBytes = kQueue * kSub * 4 + kQueue * 4 + 32 * 4;
 
 template <int P, int MODE>
 struct TileCfg {
     static constexpr int KA = P / 64;                       // 128-byte K atoms per row
     static constexpr bool QUEUE = MODE == MODE_COLLECT;
-    static constexpr int STAGES = (P == 64) ? (QUEUE ? 7 : 8) : (QUEUE ? 3 : 4);   // key ring
+    static constexpr int STAGES = (P == 64) ? (QUEUE ? 5 : 8) : (QUEUE ? 2 : 4);   // key ring
     static constexpr int QSLOTS = (P == 64) ? 2 : 1;        // query-unit slots
     static constexpr uint32_t QHALF = KA * kTileM * 128;    // one 128-row query tile
     static constexpr uint32_t QBYTES = 2 * QHALF;           // a unit's two query tiles
@@ -305,8 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tpar = 0;                     // phase parity of TMEM buffer tb
         bool ok = true;
         // MODE_COLLECT queue of this warp and the candidate count of each row
-        float* qv = nullptr;                   // [kQueue][8] raw scores
-        uint32_t* qm = nullptr;                // [kQueue] (first key / 8) << 5 | owning lane
+        float* qv = nullptr;                   // [kQueue][kSub] raw scores
+        uint32_t* qm = nullptr;                // [kQueue] (first key / kSub) << 5 | owning lane
         int* qcnt = nullptr;                   // [32] candidates appended per row
         int q_tail = 0;                        // warp-uniform: entries in the queue
         int64_t row0 = 0;                      // global row of lane 0
@@ -314,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (MODE == MODE_COLLECT) {
             uint8_t* qb = smem + C::QUEUE_OFF + (warp - 2) * kQueueWarpBytes;
             qv = reinterpret_cast<float*>(qb);
-            qm = reinterpret_cast<uint32_t*>(qb + kQueue * 32);
-            qcnt = reinterpret_cast<int*>(qb + kQueue * 36);
+            qm = reinterpret_cast<uint32_t*>(qb + kQueue * kSub * 4);
+            qcnt = reinterpret_cast<int*>(qb + kQueue * (kSub * 4 + 4));
             qcnt[lane] = 0;
             __syncwarp();
         }
@@ -329,20 +330,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float t_own = __shfl_sync(0xffffffffu, t_raw, owner);
             uint32_t bits = 0;
             if (act) {
-                const float4 a = reinterpret_cast<const float4*>(qv + lane * 8)[0];
-                const float4 b = reinterpret_cast<const float4*>(qv + lane * 8)[1];
-                const float w8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                bits = ge_mask8(w8, t_own);
+                const float4* src4 = reinterpret_cast<const float4*>(qv + lane * kSub);
+                const float4 a = src4[0], b = src4[1], c4 = src4[2], d4 = src4[3];
+                const float w0[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                const float w1[8] = {c4.x, c4.y, c4.z, c4.w, d4.x, d4.y, d4.z, d4.w};
+                bits = ge_mask8(w0, t_own) | (ge_mask8(w1, t_own) << 8);
             }
             if (bits) {
                 int slot = atomicAdd(qcnt + owner, __popc(bits));
                 uint64_t* dst = p.cand + ((row0 + owner) * kTBuf + tb) * static_cast<int64_t>(capc);
-                const uint32_t jb = (meta >> 5) << 3;
+                const uint32_t jb = (meta >> 5) * kSub;
                 while (bits) {
                     const int e = __ffs(bits) - 1;
                     bits &= bits - 1;
                     if (slot < capc)
-                        dst[slot] = (static_cast<uint64_t>(__float_as_uint(qv[lane * 8 + e])) << 32) |
+                        dst[slot] = (static_cast<uint64_t>(__float_as_uint(qv[lane * kSub + e])) << 32) |
                                     (jb + static_cast<uint32_t>(e));
                     ++slot;
                 }
@@ -451,21 +453,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                         if constexpr (MODE == MODE_COLLECT) {
-                            // every score >= the row's bound is a candidate; 8-key
-                            // sub-chunk maxima pick the sub-chunks holding one, which
+                            // every score >= the row's bound is a candidate; 16-key
+                            // half-chunk maxima pick the half-chunks holding one, which
                             // are queued and drained 32 at a time
 #pragma unroll
-                            for (int s8 = 0; s8 < 4; ++s8) {
-                                const float* w = v + 8 * s8;
-                                const bool hot = live && max8(w) >= t_raw;
+                            for (int h16 = 0; h16 < 2; ++h16) {
+                                const float* w = v + kSub * h16;
+                                const bool hot = live && fmaxf(max8(w), max8(w + 8)) >= t_raw;
                                 const uint32_t B = __ballot_sync(0xffffffffu, hot);
                                 if (B) {
                                     if (hot) {
                                         const int q = q_tail + __popc(B & ((1u << lane) - 1));
-                                        float4* dst = reinterpret_cast<float4*>(qv + q * 8);
+                                        float4* dst = reinterpret_cast<float4*>(qv + q * kSub);
                                         dst[0] = make_float4(w[0], w[1], w[2], w[3]);
                                         dst[1] = make_float4(w[4], w[5], w[6], w[7]);
-                                        qm[q] = (static_cast<uint32_t>((j0 + 8 * s8) >> 3) << 5) |
+                                        dst[2] = make_float4(w[8], w[9], w[10], w[11]);
+                                        dst[3] = make_float4(w[12], w[13], w[14], w[15]);
+                                        qm[q] = (static_cast<uint32_t>((j0 + kSub * h16) / kSub) << 5) |
                                                 static_cast<uint32_t>(lane);
                                     }
                                     q_tail += __popc(B);
@@ -475,14 +479,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         q_tail -= 32;
                                         if (q_tail > 0) {   // move the rest to the front
                                             if (lane < q_tail) {
-                                                const float4* from = reinterpret_cast<const float4*>(qv + (32 + lane) * 8);
-                                                float4* to = reinterpret_cast<float4*>(qv + lane * 8);
                                                 // entry 32+l moves to l: sources and targets
                                                 // never overlap (fewer than 32 remain)
-                                                const float4 a = from[0], b2 = from[1];
+                                                const float4* from = reinterpret_cast<const float4*>(qv + (32 + lane) * kSub);
+                                                float4* to = reinterpret_cast<float4*>(qv + lane * kSub);
+                                                const float4 a = from[0], b2 = from[1], c2 = from[2], d2 = from[3];
                                                 const uint32_t mm = qm[32 + lane];
                                                 to[0] = a;
                                                 to[1] = b2;
+                                                to[2] = c2;
+                                                to[3] = d2;
                                                 qm[lane] = mm;
                                             }
                                             __syncwarp();
