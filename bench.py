@@ -63,8 +63,22 @@ def valid_pairs(w):
     return int(nv.sum()) * bh, int(keff.sum()) * bh
 
 
+def band_pairs(w):
+    """(query, key) pairs of the sliding window |i - j| <= w, clipped at both ends."""
+    i = np.arange(w.Tq, dtype=np.int64)
+    lo = np.maximum(0, i - w.window)
+    hi = np.minimum(w.Tk - 1, i + w.window)
+    return int((hi - lo + 1).sum()) * w.B * w.H
+
+
 def algorithmic(w):
     esize = 4 if w.dtype == "f32" else 2
+    if w.P == 0:   # the sliding-window workload: no scorer
+        sel = band_pairs(w)
+        return {"score_flops": 0.0, "attn_flops": 4.0 * w.D * sel,
+                "gather_bytes": 2.0 * sel * w.D * esize, "selected_pairs": sel,
+                "scored_pairs": 0,
+                "window_bytes": float(esize * w.D * w.B * w.H * (w.Tq * 2 + w.Tk * 2))}
     pairs, sel = valid_pairs(w)
     return {
         "score_flops": 2.0 * w.P * pairs,
@@ -93,7 +107,10 @@ def roofline_for(name, ms, w, alg, pk, pk_kind):
                 "traffic": None, "peak_kind": pk_kind + " bf16 burst (clocks at max during the run)",
                 "algorithmic": "2 * d_proj FLOP per valid (query, key) pair, %.4g per launch"
                 % alg["score_flops"]}
-    if name.startswith("attn_rows"):
+    if name == "attn_rows.window":
+        by = alg["window_bytes"]
+        what = "unique Q, K, V and O bytes of the window workload"
+    elif name.startswith("attn_rows"):
         by = alg["gather_bytes"]
         what = "selected K+V rows: k_eff * D * esize * 2 per query row"
     elif name == "cand_sort":
@@ -102,9 +119,9 @@ def roofline_for(name, ms, w, alg, pk, pk_kind):
     elif name == "group_select":
         by = rows * 3 * w.k * 2 * 2
         what = "group maxima read twice (about 3k x 2 B per row)"
-    else:
-        by = alg["scored_pairs"] * 4
-        what = "one 32-bit key per valid (query, key) pair"
+    else:   # the row-wise top-k: every valid key's k_low row, once per query row
+        by = alg["scored_pairs"] * w.P * (4 if w.dtype == "f32" else 2)
+        what = "k_low rows scored: d_proj * esize per valid (query, key) pair"
     achieved = by / sec / 1e9
     return {"kernel": name, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
             "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
@@ -164,6 +181,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ ranks
+
+def rank_workload(w, rank: int):
+    """The batch rank `rank` processes: the same workload with its own seed
+    (weak scaling: independent batches, no data exchanged between ranks)."""
+    return w.with_(seed_base=w.seed_base + 1000 * rank)
+
+
+def max_over_ranks(vals, world: int, device):
+    """Element-wise maximum of `vals` over all ranks (the slowest rank's times)."""
+    t = torch.tensor(list(vals), dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
 # ------------------------------------------------------------------ ours
 
 def run_ours(args, rank, world, local_rank):
@@ -172,28 +205,41 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     w = WORKLOADS[args.workload]
-    # each rank: its own batch of the workload (independent seed per rank)
-    w = w.with_(seed_base=w.seed_base + 1000 * rank)
-    q_low, k_low = make_scorer_inputs(w, dev)
+    w = rank_workload(w, rank)   # each rank: its own batch of the workload
+    window = w.P == 0
     Q, K, V = make_attn_inputs(w, dev)
+    if window:
+        q_low = k_low = ws = idx = None
+    else:
+        q_low, k_low = make_scorer_inputs(w, dev)
+        ws = torch.empty(ssa.score_topk_workspace_size(w.B, w.H, w.Tq, w.Tk, w.P, w.k, w.causal),
+                         dtype=torch.uint8, device=dev)
+        idx = torch.empty((w.B, w.H, w.Tq, w.k), dtype=torch.int32, device=dev)
     torch.cuda.synchronize()
-    ws = torch.empty(ssa.score_topk_workspace_size(w.B, w.H, w.Tq, w.Tk, w.P, w.k, w.causal),
-                     dtype=torch.uint8, device=dev)
-    idx = torch.empty((w.B, w.H, w.Tq, w.k), dtype=torch.int32, device=dev)
     O = torch.empty((w.B, w.H, w.Tq, w.D), dtype=w.torch_dtype, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    # the phases of one step: (name, call)
+    if window:
+        phase_list = [("window_attn", lambda: ssa.ssa_window_attn(Q, K, V, w.window, out=O))]
+    else:
+        phase_list = [("score_topk", lambda: ssa.ssa_score_topk(q_low, k_low, w.k, w.causal,
+                                                                workspace=ws, idx=idx)),
+                      ("sparse_attn", lambda: ssa.ssa_sparse_attn(Q, K, V, idx, out=O))]
+
     def step():
-        ssa.ssa_score_topk(q_low, k_low, w.k, w.causal, workspace=ws, idx=idx)
-        ssa.ssa_sparse_attn(Q, K, V, idx, out=O)
+        for _, fn in phase_list:
+            fn()
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
 
-    # device-resident timing: per step three events on the launching stream
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # device-resident timing: per step one event before and after each phase,
+    # on the launching stream
+    nph = len(phase_list)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(args.steps)]
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
                           else local_rank)
     if world > 1:
@@ -204,17 +250,16 @@ def run_ours(args, rank, world, local_rank):
     for s in range(args.steps):
         flush.fill_(s & 0xFF)                       # L2 flush, outside the events
         ev[s][0].record(stream)
-        ssa.ssa_score_topk(q_low, k_low, w.k, w.causal, workspace=ws, idx=idx)
-        ev[s][1].record(stream)
-        ssa.ssa_sparse_attn(Q, K, V, idx, out=O)
-        ev[s][2].record(stream)
+        for ph, (_, fn) in enumerate(phase_list):
+            fn()
+            ev[s][ph + 1].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
-    t_score = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
-    t_attn = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
-    ms_step = float(np.mean([a + b for a, b in zip(t_score, t_attn)]))
+    t_phase = [[ev[s][ph].elapsed_time(ev[s][ph + 1]) for s in range(args.steps)]
+               for ph in range(nph)]
+    ms_step = float(np.mean([sum(t_phase[ph][s] for ph in range(nph)) for s in range(args.steps)]))
 
     # per-kernel times: the same steps again with the library's launch tracing
     # (CUDA events recorded on the launching stream around every kernel)
@@ -232,17 +277,21 @@ def run_ours(args, rank, world, local_rank):
                for n, v in per_kernel.items()}
 
     # end to end through the public calls: pinned host in, O back to host
-    host_in = [t.cpu().pin_memory() for t in (q_low, k_low, Q, K, V)]
+    dev_src = [Q, K, V] if window else [q_low, k_low, Q, K, V]
+    host_in = [t.cpu().pin_memory() for t in dev_src]
     host_out = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
-    dev_in = [torch.empty_like(t) for t in (q_low, k_low, Q, K, V)]
+    dev_in = [torch.empty_like(t) for t in dev_src]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = host_out.numel() * host_out.element_size()
 
     def e2e_step():
         for d, h in zip(dev_in, host_in):
             d.copy_(h, non_blocking=True)
-        ssa.ssa_score_topk(dev_in[0], dev_in[1], w.k, w.causal, workspace=ws, idx=idx)
-        ssa.ssa_sparse_attn(dev_in[2], dev_in[3], dev_in[4], idx, out=O)
+        if window:
+            ssa.ssa_window_attn(dev_in[0], dev_in[1], dev_in[2], w.window, out=O)
+        else:
+            ssa.ssa_score_topk(dev_in[0], dev_in[1], w.k, w.causal, workspace=ws, idx=idx)
+            ssa.ssa_sparse_attn(dev_in[2], dev_in[3], dev_in[4], idx, out=O)
         host_out.copy_(O, non_blocking=True)
 
     e2e_step()
@@ -259,11 +308,8 @@ def run_ours(args, rank, world, local_rank):
     ms_e2e = e0.elapsed_time(e1) / args.steps
 
     # max over ranks
-    t = torch.tensor([ms_step, ms_e2e, float(np.mean(t_score)), float(np.mean(t_attn))],
-                     dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_step, ms_e2e, ms_score, ms_attn = t.tolist()
+    vals = max_over_ranks([ms_step, ms_e2e] + [float(np.mean(tp)) for tp in t_phase], world, dev)
+    ms_step, ms_e2e, ms_phase = vals[0], vals[1], vals[2:]
 
     if rank != 0:
         return None
@@ -283,19 +329,26 @@ def run_ours(args, rank, world, local_rank):
         r = roofline_for(n, kinfo["ms"] / max(1, kinfo["launches_per_step"]), w, alg, pk, pk_kind)
         kinfo.update({"bound": r["bound"], "achieved": r["achieved"], "unit": r["unit"],
                       "frac": r["frac"]})
-    phases = {
-        "score_topk": {"ms": ms_score, "tflops": alg["score_flops"] / (ms_score * 1e-3) / 1e12,
-                       "frac_bf16_peak": alg["score_flops"] / (ms_score * 1e-3) / 1e12 / pk["bf16_tflops"]},
-        "sparse_attn": {"ms": ms_attn, "gbs": alg["gather_bytes"] / (ms_attn * 1e-3) / 1e9,
-                        "frac_hbm": alg["gather_bytes"] / (ms_attn * 1e-3) / 1e9 / pk["hbm_gbs"]},
-    }
+    phases = {}
+    for (name, _), ms in zip(phase_list, ms_phase):
+        ph = {"ms": ms}
+        if name == "score_topk":
+            ph["tflops"] = alg["score_flops"] / (ms * 1e-3) / 1e12
+            ph["frac_bf16_peak"] = ph["tflops"] / pk["bf16_tflops"]
+        elif name == "sparse_attn":
+            ph["gbs"] = alg["gather_bytes"] / (ms * 1e-3) / 1e9
+            ph["frac_hbm"] = ph["gbs"] / pk["hbm_gbs"]
+        else:
+            ph["gbs"] = alg["window_bytes"] / (ms * 1e-3) / 1e9
+            ph["frac_hbm"] = ph["gbs"] / pk["hbm_gbs"]
+        phases[name] = ph
     line = {
         "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64; integer q_low/k_low in [-4,4] with planted keys, Q/K/V ~ N(0,1))",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Tq": w.Tq, "Tk": w.Tk, "D": w.D,
-                   "d_proj": w.P, "k": w.k, "causal": w.causal,
+                   "d_proj": w.P, "k": w.k, "causal": w.causal, "window": w.window,
                    "l2": "flushed between timed steps (512 MB write) and inputs > L2",
                    "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
         "effective_tflops": eff_tflops,
@@ -314,39 +367,59 @@ def run_ours(args, rank, world, local_rank):
 # ------------------------------------------------------------ CPU oracle
 
 def cpu_baseline(w, n_rows: int, seed: int = 0):
-    """The oracle (plain fp64 C, all host cores) on n_rows sampled query rows of
-    the workload: score + top-k and attention. Returns (queries/s, cores, sample)."""
+    """The oracle (plain fp64 C, all host cores) on a bounded sample of the
+    workload's query rows, the whole path for each (score + top-k + attention,
+    or window attention). Returns (queries/s, cores, sample description)."""
     import oracle
     g = np.random.default_rng(seed)
-    qi = np.sort(g.choice(w.Tq, size=n_rows, replace=False)).astype(np.int64)
-    # head (0, 0) of the workload: the same elements as the one-head workload
-    wl = w.with_(B=1, H=1)
+    cores = oracle.default_threads()
+    if w.P == 0:   # sliding window: rows of head (0, 0)
+        n = min(n_rows, w.Tq)
+        qi = np.sort(g.choice(w.Tq, size=n, replace=False)).astype(np.int64)
+        Q, K, V = make_attn_inputs(w.with_(B=1, H=1))
+        t0 = time.perf_counter()
+        oracle.window_rows(Q[0, 0][qi], qi, K[0, 0], V[0, 0], w.window, w.window, nthreads=cores)
+        dt = time.perf_counter() - t0
+        return n / dt, cores, "%d random query rows of head 0 of %s (window attention)" % (n, w.name), n
+    if w.Tq >= n_rows:   # long sequences: random rows of head (0, 0)
+        qi = np.sort(g.choice(w.Tq, size=n_rows, replace=False)).astype(np.int64)
+        wl = w.with_(B=1, H=1)   # the same elements as head (0, 0) of the workload
+        q_low, k_low = make_scorer_inputs(wl)
+        Q, K, V = make_attn_inputs(wl)
+        t0 = time.perf_counter()
+        idx, _ = oracle.topk_rows(q_low[0, 0][qi], qi, k_low[0, 0], w.k, w.Tq, w.causal,
+                                  nthreads=cores)
+        oracle.attn_rows(Q[0, 0][qi], K[0, 0], V[0, 0], idx, nthreads=cores)
+        dt = time.perf_counter() - t0
+        return n_rows / dt, cores, ("%d random query rows of head 0 of %s (score + top-k + "
+                                    "attention)" % (n_rows, w.name)), n_rows
+    # few query rows per head (decode): every row of the first heads
+    heads = max(1, min(16, n_rows // max(1, w.Tq)))
+    wl = w.with_(B=1, H=heads)
     q_low, k_low = make_scorer_inputs(wl)
     Q, K, V = make_attn_inputs(wl)
-    cores = oracle.default_threads()
-    qd = q_low[0, 0][qi]
     t0 = time.perf_counter()
-    idx, _ = oracle.topk_rows(qd, qi, k_low[0, 0], w.k, w.Tq, w.causal, nthreads=cores)
-    oracle.attn_rows(Q[0, 0][qi], K[0, 0], V[0, 0], idx, nthreads=cores)
+    idx, _ = oracle.score_topk(q_low, k_low, w.k, w.causal, nthreads=cores)
+    oracle.sparse_attn(Q, K, V, idx, nthreads=cores)
     dt = time.perf_counter() - t0
-    return n_rows / dt, cores, ("%d random query rows of head 0 of %s (score + top-k + attention)"
-                                % (n_rows, w.name))
+    n = heads * w.Tq
+    return n / dt, cores, ("all %d query rows of the first %d heads of %s (score + top-k + "
+                           "attention)" % (n, heads, w.name)), n
 
 
 def run_reference(args):
     w = WORKLOADS[args.workload]
     vals = []
-    cores = 1
-    sample = ""
+    cores, sample, n = 1, "", 1
     for s in range(args.warmup + args.steps):
-        v, cores, sample = cpu_baseline(w, args.cpu_rows, seed=s)
+        v, cores, sample, n = cpu_baseline(w, args.cpu_rows, seed=s)
         if s >= args.warmup:
             vals.append(v)
     value = float(np.mean(vals))
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * args.cpu_rows / value, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": 1e3 * n / value, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "sample": sample},
         "cpu_baseline": {"value": value, "unit": "queries/s", "cores": cores, "kind": "oracle",
@@ -384,7 +457,7 @@ def main():
     line = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
-            v, cores, sample = cpu_baseline(WORKLOADS[args.workload], args.cpu_rows)
+            v, cores, sample, _ = cpu_baseline(WORKLOADS[args.workload], args.cpu_rows)
             line["cpu_baseline"] = {"value": v, "unit": "queries/s", "cores": cores,
                                     "kind": "oracle", "sample": sample}
         print(json.dumps(line), flush=True)
