@@ -122,6 +122,23 @@ SSA_DEVINL void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 SSA_DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 SSA_DEVINL void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// ---- named barriers -----------------------------------------------------------
+
+// Hardware named barrier `id` over `nthreads` threads (whole, converged warps)
+// that also ORs one predicate across them. Unlike an mbarrier poll it reads no
+// shared memory, so a thread that issues tcgen05.mma can sync through it
+// without waiting behind the operand reads of its MMAs in flight.
+SSA_DEVINL bool bar_red_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred q, p;\n setp.ne.u32 q, %1, 0;\n"
+        " bar.red.or.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // ---- tcgen05.mma ------------------------------------------------------------
 
 // Shared-memory matrix descriptor of a K-major operand tile stored with the
@@ -186,6 +203,14 @@ SSA_DEVINL void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 SSA_DEVINL void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Ties the registers of a TMEM load to the tcgen05.wait::ld before this call:
+// the compiler may not move a use of them above it.
+template <int N>
+SSA_DEVINL void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
 
 // Three-input maximum (sm_100 family).
 SSA_DEVINL float fmax3(float a, float b, float c) {

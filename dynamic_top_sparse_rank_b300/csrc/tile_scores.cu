@@ -16,7 +16,7 @@
 //                  bits, key index) pairs.
 // The exact top-k of a row is then found from these (tile_select.cu).
 //
-// Block layout (576 threads, one block per SM): warp 0 issues TMA loads (the
+// Block layout (608 threads, one block per SM): warp 0 issues TMA loads (the
 // two 128-row query tiles of a unit, key tiles through a ring of shared-memory
 // stages), warp 1 allocates all 512 TMEM columns and issues the MMAs: every
 // 128-key tile is multiplied with both query tiles (M=128, N=128, K=16 per
@@ -27,8 +27,13 @@
 // tile. Warps 2..17 are the epilogue, four groups of four warps, one per
 // (buffer, query tile): warp w of a group reads TMEM lane quarter w%4 (one
 // query row per thread), all 128 columns as four 32-column tcgen05.ld, frees
-// the buffer and works on the scores in registers. Every wait on an mbarrier
-// is bounded in time; a wait that runs out sets SSA_DEV_WAIT_LIMIT, stops
+// the buffer and works on the scores in registers. Warp 18 waits, for every
+// tile, until its key stage has landed and its TMEM buffer is free, and hands
+// the tile to the MMA warp through a named barrier: a thread that issues MMAs
+// and then polls an mbarrier itself waits behind the shared-memory operand
+// reads of its MMAs in flight, which leaves the tensor pipe idle for several
+// hundred cycles per poll, while a named barrier costs a few tens. Every wait
+// on an mbarrier is bounded in time; a wait that runs out sets SSA_DEV_WAIT_LIMIT, stops
 // every role of the block, lets copies and MMAs in flight finish and frees
 // TMEM.
 //
@@ -48,7 +53,9 @@ using namespace sm100;
 namespace {
 
 constexpr int kEpiWarps = 16;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kWaiterWarp = 2 + kEpiWarps;
+constexpr int kThreads = 32 * (kWaiterWarp + 1);
+constexpr uint32_t kHandoffBar = 1;          // named barrier: waiter warp + MMA warp
 constexpr int kTBuf = kTileGroups;            // TMEM tile buffers (two accumulators each)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
@@ -107,6 +114,29 @@ SSA_DEVINL float max32(const float (&v)[32]) {
     const float b2 = fmax3(a[6], a[7], a[8]);
     const float b3 = fmaxf(a[9], a[10]);
     return fmaxf(fmax3(b0, b1, b2), b3);
+}
+
+// Maximum of the G consecutive scores at w (G a power of two <= 16).
+template <int G>
+SSA_DEVINL float max_of(const float* w) {
+    if constexpr (G == 1) return w[0];
+    else if constexpr (G == 2) return fmaxf(w[0], w[1]);
+    else if constexpr (G == 4) return fmax3(w[0], w[1], fmaxf(w[2], w[3]));
+    else if constexpr (G == 8) return max8(w);
+    else return fmaxf(max8(w), max8(w + 8));
+}
+
+// Group maxima of a 32-key chunk starting at key j0 (a multiple of 32) for a
+// group size G < 32: the chunk holds 32/G whole groups, group (j0+e)/G for
+// e = 0, G, 2G, ...; each group with a valid key writes the 16 high bits of
+// the order key of its scaled maximum (masked keys were set to -inf).
+template <int G>
+SSA_DEVINL void small_groups(const float (&v)[32], int j0, int n_i, uint16_t* gcol, float scale) {
+#pragma unroll
+    for (int e = 0; e < 32; e += G)
+        if (j0 + e < n_i)
+            gcol[static_cast<int64_t>((j0 + e) / G) * kUnitM] =
+                static_cast<uint16_t>(f32_order_key(max_of<G>(v + e) * scale) >> 16);
 }
 
 // Bit e of the result is set iff v[e] >= t (e < 8): one set + one funnel
@@ -235,35 +265,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t kc = 0, qc = 0;
-            uint32_t tpar = 0;                 // bit b: phase parity of TMEM buffer b
-            int last_b = -1;
-            bool ok = true;
-            // descriptors of the first K slice of stage 0 and of query slot 0;
-            // other stages, slots and K slices only move the start address
-            const uint64_t bdesc0 = smem_desc_k_sw128(smem_u32(sk));
-            const uint64_t adesc0 = smem_desc_k_sw128(smem_u32(sq));
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                const Unit U = unit_at(p, u);
-                if (U.ntiles == 0) continue;
-                const uint32_t qs = qc % C::QSLOTS, quse = qc / C::QSLOTS;
-                if (!mbar_wait_bounded(q_full + qs, quse & 1, abort_flag, p.dev_status, lim)) {
+        // The whole warp runs the loop (the handoff barrier counts whole
+        // warps); lane 0 issues. The waiter warp has checked every barrier
+        // the tile needs before the handoff; its OR carries "stop".
+        uint32_t kc = 0, qc = 0;
+        uint32_t tpar = 0;                     // bit b: phase parity of TMEM buffer b
+        int last_b = -1;
+        bool ok = true;
+        // descriptors of the first K slice of stage 0 and of query slot 0;
+        // other stages, slots and K slices only move the start address
+        const uint64_t bdesc0 = smem_desc_k_sw128(smem_u32(sk));
+        const uint64_t adesc0 = smem_desc_k_sw128(smem_u32(sq));
+        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            const Unit U = unit_at(p, u);
+            if (U.ntiles == 0) continue;
+            const uint32_t qs = qc % C::QSLOTS;
+            const uint64_t adesc = adesc0 + ((qs * C::QBYTES) >> 4);
+            for (int t = 0; t < U.ntiles; ++t) {
+                const uint32_t s = kc % S, b = t & (kTBuf - 1);
+                if (bar_red_or(kHandoffBar, 64, false)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t adesc = adesc0 + ((qs * C::QBYTES) >> 4);
-                for (int t = 0; t < U.ntiles; ++t) {
-                    const uint32_t s = kc % S, b = t & (kTBuf - 1);
-                    const uint32_t par = (tpar >> b) & 1;
-                    if (!mbar_wait_bounded(k_full + s, (kc / S) & 1, abort_flag, p.dev_status,
-                                           lim) ||
-                        !mbar_wait_bounded(t_empty + b, par ^ 1, abort_flag, p.dev_status, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                if (lane == 0) {
                     const uint64_t bdesc = bdesc0 + ((s * C::KBYTES) >> 4);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -280,18 +305,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mma_commit(k_empty + s);
                     mma_commit(t_full + b);
-                    tpar ^= 1u << b;
-                    last_b = static_cast<int>(b);
-                    ++kc;
                 }
-                if (!ok) break;
-                mma_commit(q_empty + qs);
-                ++qc;
+                __syncwarp();
+                tpar ^= 1u << b;
+                last_b = static_cast<int>(b);
+                ++kc;
             }
-            // MMAs in flight finish by themselves; wait for the last one
-            if (last_b >= 0)
-                mbar_wait_bounded(t_full + last_b, ((tpar >> last_b) & 1) ^ 1, nullptr,
-                                  p.dev_status, lim);
+            if (!ok) break;
+            if (lane == 0) mma_commit(q_empty + qs);
+            __syncwarp();
+            ++qc;
+        }
+        // MMAs in flight finish by themselves; wait for the last one
+        if (lane == 0 && last_b >= 0)
+            mbar_wait_bounded(t_full + last_b, ((tpar >> last_b) & 1) ^ 1, nullptr, p.dev_status,
+                              lim);
+        __syncwarp();
+    } else if (warp == kWaiterWarp) {
+        // ------------------------------------------------ MMA handoff
+        // Same unit and tile sequence as the MMA warp, one handoff per tile:
+        // lane 0 waits for the unit's query tiles (first tile of a unit), the
+        // tile's key stage and its TMEM buffer. A failed wait (time limit or
+        // abort) is handed over as "stop" and both warps leave their loops.
+        uint32_t kc = 0, qc = 0;
+        uint32_t tpar = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            const Unit U = unit_at(p, u);
+            if (U.ntiles == 0) continue;
+            const uint32_t qs = qc % C::QSLOTS, quse = qc / C::QSLOTS;
+            bool good = true;
+            if (lane == 0) good = mbar_wait_bounded(q_full + qs, quse & 1, abort_flag, p.dev_status, lim);
+            for (int t = 0; t < U.ntiles; ++t) {
+                const uint32_t s = kc % S, b = t & (kTBuf - 1);
+                const uint32_t par = (tpar >> b) & 1;
+                if (lane == 0)
+                    good = good &&
+                           mbar_wait_bounded(k_full + s, (kc / S) & 1, abort_flag, p.dev_status, lim) &&
+                           mbar_wait_bounded(t_empty + b, par ^ 1, abort_flag, p.dev_status, lim);
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (bar_red_or(kHandoffBar, 64, !good)) {
+                    ok = false;
+                    break;
+                }
+                tpar ^= 1u << b;
+                ++kc;
+            }
+            if (!ok) break;
+            ++qc;
         }
     } else {
         // ------------------------------------------------ epilogue
@@ -383,20 +444,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tpar ^= 1;
                 tc_fence_after();
+                // two 32-column loads in flight per wait: half the load round
+                // trips that hold the buffer
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t raw[32];
-                    tmem_ld32(t_lane + c * 32, raw);
-                    tmem_ld_wait();
-                    if (c == 3) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(t_empty + tb);   // the buffer is free again
-                    }
+                for (int c2 = 0; c2 < 2; ++c2) {
+                  uint32_t raw2[2][32];
+                  tmem_ld32(t_lane + c2 * 64, raw2[0]);
+                  tmem_ld32(t_lane + c2 * 64 + 32, raw2[1]);
+                  tmem_ld_wait();
+                  reg_fence(raw2[0]);
+                  reg_fence(raw2[1]);
+                  if (c2 == 1) {
+                      tc_fence_before();
+                      __syncwarp();
+                      if (lane == 0) mbar_arrive(t_empty + tb);   // the buffer is free again
+                  }
+#pragma unroll
+                  for (int c1 = 0; c1 < 2; ++c1) {
+                    const int c = 2 * c2 + c1;
                     const int j0 = t * kTileN + c * 32;
                     float v[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(raw[e]);
+                    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(raw2[c1][e]);
                     if constexpr (MODE == MODE_RAW) {
                         if (row_ok) {
                             float* out = p.S + row * static_cast<int64_t>(p.Tk);
@@ -427,28 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     gacc[c] = -INFINITY;
                                 }
                             } else if (live && g > 0) {
-                                // in-place max tree: v[m*g] ends as the max of group m
-                                if (g >= 2) {
-#pragma unroll
-                                    for (int e = 0; e < 32; e += 2) v[e] = fmaxf(v[e], v[e + 1]);
-                                }
-                                if (g >= 4) {
-#pragma unroll
-                                    for (int e = 0; e < 32; e += 4) v[e] = fmaxf(v[e], v[e + 2]);
-                                }
-                                if (g >= 8) {
-#pragma unroll
-                                    for (int e = 0; e < 32; e += 8) v[e] = fmaxf(v[e], v[e + 4]);
-                                }
-                                if (g >= 16) {
-#pragma unroll
-                                    for (int e = 0; e < 32; e += 16) v[e] = fmaxf(v[e], v[e + 8]);
-                                }
-#pragma unroll
-                                for (int e = 0; e < 32; ++e) {
-                                    if ((e & (g - 1)) == 0 && j0 + e < n_i)
-                                        gcol[static_cast<int64_t>((j0 + e) >> g_shift) * kUnitM] =
-                                            static_cast<uint16_t>(f32_order_key(v[e] * p.scale) >> 16);
+                                switch (g) {
+                                    case 16: small_groups<16>(v, j0, n_i, gcol, p.scale); break;
+                                    case 8: small_groups<8>(v, j0, n_i, gcol, p.scale); break;
+                                    case 4: small_groups<4>(v, j0, n_i, gcol, p.scale); break;
+                                    case 2: small_groups<2>(v, j0, n_i, gcol, p.scale); break;
+                                    default: small_groups<1>(v, j0, n_i, gcol, p.scale); break;
                                 }
                             }
                         }
@@ -498,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
+                  }
                 }
             }
             if (!ok) break;
