@@ -63,7 +63,9 @@ constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 // Candidate queue of one epilogue warp (MODE_COLLECT): each entry is a 16-key
 // half-chunk holding at least one candidate (its 16 raw scores, its first key,
 // the lane = row that owns it); the warp drains 32 entries at a time, one per
-// lane, so the per-candidate work runs on full warps.
+// lane, so the per-candidate work runs on full warps. The scores are stored
+// slot-major, float4 slot i of entry q at [i][q], so that lanes touching
+// consecutive entries touch consecutive 16-byte words (no bank conflicts).
 constexpr int kQueue = 64;                                   // entries, power of two
 constexpr int kSub = 16;                                     // keys per entry
 constexpr uint32_t kQueueWarpBytes = kQueue * kSub * 4 + kQueue * 4 + 32 * 4;
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tpar = 0;                     // phase parity of TMEM buffer tb
         bool ok = true;
         // MODE_COLLECT queue of this warp and the candidate count of each row
-        float* qv = nullptr;                   // [kQueue][kSub] raw scores
+        float4* qv = nullptr;                  // [kSub/4][kQueue] raw scores
         uint32_t* qm = nullptr;                // [kQueue] (first key / kSub) << 5 | owning lane
         int* qcnt = nullptr;                   // [32] candidates appended per row
         int q_tail = 0;                        // warp-uniform: entries in the queue
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float t_raw = -FLT_MAX;                // raw-score bound of this thread's row
         if constexpr (MODE == MODE_COLLECT) {
             uint8_t* qb = smem + C::QUEUE_OFF + (warp - 2) * kQueueWarpBytes;
-            qv = reinterpret_cast<float*>(qb);
+            qv = reinterpret_cast<float4*>(qb);
             qm = reinterpret_cast<uint32_t*>(qb + kQueue * kSub * 4);
             qcnt = reinterpret_cast<int*>(qb + kQueue * (kSub * 4 + 4));
             qcnt[lane] = 0;
@@ -391,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float t_own = __shfl_sync(0xffffffffu, t_raw, owner);
             uint32_t bits = 0;
             if (act) {
-                const float4* src4 = reinterpret_cast<const float4*>(qv + lane * kSub);
-                const float4 a = src4[0], b = src4[1], c4 = src4[2], d4 = src4[3];
+                const float4 a = qv[lane], b = qv[kQueue + lane], c4 = qv[2 * kQueue + lane],
+                             d4 = qv[3 * kQueue + lane];
                 const float w0[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
                 const float w1[8] = {c4.x, c4.y, c4.z, c4.w, d4.x, d4.y, d4.z, d4.w};
                 bits = ge_mask8(w0, t_own) | (ge_mask8(w1, t_own) << 8);
@@ -405,7 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int e = __ffs(bits) - 1;
                     bits &= bits - 1;
                     if (slot < capc)
-                        dst[slot] = (static_cast<uint64_t>(__float_as_uint(qv[lane * kSub + e])) << 32) |
+                        dst[slot] = (static_cast<uint64_t>(__float_as_uint(
+                                         reinterpret_cast<const float*>(qv + (e >> 2) * kQueue + lane)[e & 3]))
+                                     << 32) |
                                     (jb + static_cast<uint32_t>(e));
                     ++slot;
                 }
@@ -517,11 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (B) {
                                     if (hot) {
                                         const int q = q_tail + __popc(B & ((1u << lane) - 1));
-                                        float4* dst = reinterpret_cast<float4*>(qv + q * kSub);
-                                        dst[0] = make_float4(w[0], w[1], w[2], w[3]);
-                                        dst[1] = make_float4(w[4], w[5], w[6], w[7]);
-                                        dst[2] = make_float4(w[8], w[9], w[10], w[11]);
-                                        dst[3] = make_float4(w[12], w[13], w[14], w[15]);
+                                        qv[q] = make_float4(w[0], w[1], w[2], w[3]);
+                                        qv[kQueue + q] = make_float4(w[4], w[5], w[6], w[7]);
+                                        qv[2 * kQueue + q] = make_float4(w[8], w[9], w[10], w[11]);
+                                        qv[3 * kQueue + q] = make_float4(w[12], w[13], w[14], w[15]);
                                         qm[q] = (static_cast<uint32_t>((j0 + kSub * h16) / kSub) << 5) |
                                                 static_cast<uint32_t>(lane);
                                     }
@@ -534,14 +537,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             if (lane < q_tail) {
                                                 // entry 32+l moves to l: sources and targets
                                                 // never overlap (fewer than 32 remain)
-                                                const float4* from = reinterpret_cast<const float4*>(qv + (32 + lane) * kSub);
-                                                float4* to = reinterpret_cast<float4*>(qv + lane * kSub);
-                                                const float4 a = from[0], b2 = from[1], c2 = from[2], d2 = from[3];
+                                                const float4 a = qv[32 + lane], b2 = qv[kQueue + 32 + lane],
+                                                             c2 = qv[2 * kQueue + 32 + lane],
+                                                             d2 = qv[3 * kQueue + 32 + lane];
                                                 const uint32_t mm = qm[32 + lane];
-                                                to[0] = a;
-                                                to[1] = b2;
-                                                to[2] = c2;
-                                                to[3] = d2;
+                                                qv[lane] = a;
+                                                qv[kQueue + lane] = b2;
+                                                qv[2 * kQueue + lane] = c2;
+                                                qv[3 * kQueue + lane] = d2;
                                                 qm[lane] = mm;
                                             }
                                             __syncwarp();
