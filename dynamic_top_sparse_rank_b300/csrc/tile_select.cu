@@ -167,40 +167,74 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
 // 32*b + l.
 constexpr int kSortWarps = 8;
 
+// One bitonic stage: compare-exchange at distance `stride` (< E, inside the
+// lane) within merges of `size` elements; element e = lane*E + r.
+template <int E, int STRIDE>
+SSA_DEVINL void bitonic_stage_in_lane(uint64_t (&x)[E], int lane, int size) {
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+        if ((r & STRIDE) == 0) {
+            const int e = lane * E + r;
+            const bool desc = (e & size) == 0;
+            const uint64_t a = x[r], b = x[r + STRIDE];
+            if ((a < b) == desc) {
+                x[r] = b;
+                x[r + STRIDE] = a;
+            }
+        }
+    }
+}
+
+// All in-lane stages of a merge of `size` elements (strides E/2 .. 1).
+template <int E>
+SSA_DEVINL void bitonic_in_lane_tail(uint64_t (&x)[E], int lane, int size) {
+    if constexpr (E >= 16) bitonic_stage_in_lane<E, 8>(x, lane, size);
+    if constexpr (E >= 8) bitonic_stage_in_lane<E, 4>(x, lane, size);
+    if constexpr (E >= 4) bitonic_stage_in_lane<E, 2>(x, lane, size);
+    if constexpr (E >= 2) bitonic_stage_in_lane<E, 1>(x, lane, size);
+}
+
+// Sorts the 32*E keys of a warp in descending order (bitonic network).
+// Merges up to E elements run inside each lane (unrolled); for larger merges
+// the cross-lane strides (>= E, by shuffles) run as a loop and the in-lane
+// tail is shared, which keeps the code small enough for the instruction cache.
 template <int E>
 SSA_DEVINL void warp_bitonic_desc(uint64_t (&x)[E], int lane) {
     constexpr int N = 32 * E;
+    if constexpr (E >= 2) {
+        bitonic_stage_in_lane<E, 1>(x, lane, 2);
+    }
+    if constexpr (E >= 4) {
+        bitonic_stage_in_lane<E, 2>(x, lane, 4);
+        bitonic_stage_in_lane<E, 1>(x, lane, 4);
+    }
+    if constexpr (E >= 8) {
+        bitonic_stage_in_lane<E, 4>(x, lane, 8);
+        bitonic_stage_in_lane<E, 2>(x, lane, 8);
+        bitonic_stage_in_lane<E, 1>(x, lane, 8);
+    }
+    if constexpr (E >= 16) {
+        bitonic_stage_in_lane<E, 8>(x, lane, 16);
+        bitonic_stage_in_lane<E, 4>(x, lane, 16);
+        bitonic_stage_in_lane<E, 2>(x, lane, 16);
+        bitonic_stage_in_lane<E, 1>(x, lane, 16);
+    }
+#pragma unroll 1
+    for (int size = 2 * E; size <= N; size <<= 1) {
+#pragma unroll 1
+        for (int stride = size >> 1; stride >= E; stride >>= 1) {
+            const int lx = stride / E;
+            const bool lower = (lane & lx) == 0;
+            const bool desc = ((lane * E) & size) == 0;   // the same for all r of the lane
+            const bool take_max = lower == desc;
 #pragma unroll
-    for (int size = 2; size <= N; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            if (stride >= E) {
-                const int lx = stride / E;
-#pragma unroll
-                for (int r = 0; r < E; ++r) {
-                    const int e = lane * E + r;
-                    const uint64_t y = __shfl_xor_sync(0xffffffffu, x[r], lx);
-                    const bool lower = (e & stride) == 0;
-                    const bool desc = (e & size) == 0;
-                    const bool take_max = lower == desc;
-                    const bool y_big = y > x[r];
-                    x[r] = (take_max == y_big) ? y : x[r];
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < E; ++r) {
-                    if ((r & stride) == 0) {
-                        const int e = lane * E + r;
-                        const bool desc = (e & size) == 0;
-                        const uint64_t a = x[r], b = x[r + stride];
-                        if ((a < b) == desc) {
-                            x[r] = b;
-                            x[r + stride] = a;
-                        }
-                    }
-                }
+            for (int r = 0; r < E; ++r) {
+                const uint64_t y = __shfl_xor_sync(0xffffffffu, x[r], lx);
+                const bool y_big = y > x[r];
+                x[r] = (take_max == y_big) ? y : x[r];
             }
         }
+        bitonic_in_lane_tail<E>(x, lane, size);
     }
 }
 
