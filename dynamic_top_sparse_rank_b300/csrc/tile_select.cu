@@ -153,22 +153,25 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
 // ---------------------------------------------------------------- sort
 //
 // One warp per row. The candidate pass stores (raw score bits, index) pairs;
-// here they become composite keys x = (order key of raw * scale << 32) |
-// ~index, all distinct, so the row's answer is its k_eff largest keys in
-// descending order (score descending, index ascending).
-//  1. Radix select (MSB first, 8-bit digits) finds the k_eff-th largest key:
-//     a digit all candidates share is skipped without a histogram (found from
-//     the OR and AND of all keys), and the search stops as soon as the
-//     remaining rank fills a whole bin.
-//  2. The keys >= that key (exactly k_eff of them) are compacted into shared
-//     memory and sorted descending by a bitonic network in registers (strides
-//     below E inside a lane, the others across lanes by shuffles).
+// the row's answer is its k_eff largest composite keys (order key of
+// raw * scale, then the smaller index) in descending order.
+//  1. Radix select (MSB first, 8-bit digits) over the 32-bit score order keys
+//     held in registers finds the k_eff-th largest score T: a digit all
+//     candidates share is skipped without a histogram (found from the OR and
+//     AND of all keys), and the search stops as soon as the remaining rank
+//     fills a whole bin.
+//  2. The candidates above T, and of those equal to T the ones with the
+//     smallest indices (rank by index among the ties, which sit in a short
+//     shared-memory list), are compacted into shared memory as composite keys
+//     (the index is read back from the candidate list) and sorted descending
+//     by a bitonic network in registers (strides below E inside a lane, the
+//     others across lanes by shuffles). A row with more ties at T than the
+//     list holds goes to the row-wise kernel.
 // Keys live in registers batch-major: register b of lane l holds element
 // 32*b + l.
 constexpr int kSortWarps = 8;
+constexpr int kMaxTies = 256;
 
-// One bitonic stage: compare-exchange at distance `stride` (< E, inside the
-// lane) within merges of `size` elements; element e = lane*E + r.
 template <int E, int STRIDE>
 SSA_DEVINL void bitonic_stage_in_lane(uint64_t (&x)[E], int lane, int size) {
 #pragma unroll
@@ -247,9 +250,10 @@ __global__ void __launch_bounds__(kSortWarps * 32) cand_sort_kernel(
     constexpr int CAP = 32 * NB;      // two lists of CAP/2
     constexpr int CAPC = CAP / 2;
     constexpr int W = 32 * E;         // sorted winners
-    __shared__ uint32_t bins_all[kSortWarps][256];
+    __shared__ uint32_t bins_all[kSortWarps][256];   // histogram, then the list of ties
     __shared__ uint64_t win_all[kSortWarps][W];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const uint32_t below = (1u << lane) - 1;
     uint32_t* bins = bins_all[wid];
     uint64_t* win = win_all[wid];
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kSortWarps + wid;
@@ -264,34 +268,32 @@ __global__ void __launch_bounds__(kSortWarps * 32) cand_sort_kernel(
     }
     const int c = c0 + c1;
     const uint64_t* src = cand + row * CAP;
-    uint64_t x[NB];
-    uint64_t kor = 0, kand = ~0ull;
+    // element e of the row: list 0 holds e < c0, list 1 the rest
+    auto elem = [&](int e) -> uint64_t { return e < c0 ? src[e] : src[CAPC + e - c0]; };
+    uint32_t ok[NB];   // score order keys; 0 (below every real key) for no element
+    uint32_t kor = 0, kand = ~0u;
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
         const int e = 32 * b + lane;
-        const uint64_t raw = e < c0 ? src[e] : (e < c ? src[CAPC + e - c0] : 0ull);
-        x[b] = e < c ? sel_key(f32_order_key(__uint_as_float(static_cast<uint32_t>(raw >> 32)) * scale),
-                               static_cast<uint32_t>(raw))
-                     : 0ull;   // 0 sorts last
+        ok[b] = 0;
         if (e < c) {
-            kor |= x[b];
-            kand &= x[b];
+            ok[b] = f32_order_key(__uint_as_float(static_cast<uint32_t>(elem(e) >> 32)) * scale);
+            kor |= ok[b];
+            kand &= ok[b];
         }
     }
-    // 1. radix select of the keff-th largest key
-    uint64_t thr = 0;   // keys >= thr are the winners
+    // 1. radix select of the keff-th largest score key T
+    uint32_t thr = 0;        // winners: keys >= thr (all of them) ...
+    bool partial = false;    // ... or keys > thr plus `need` of the keys == thr
+    uint32_t need = static_cast<uint32_t>(keff);
     if (keff > 0 && keff < c) {
-        const uint32_t or_lo = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(kor));
-        const uint32_t or_hi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(kor >> 32));
-        const uint32_t and_lo = __reduce_and_sync(0xffffffffu, static_cast<uint32_t>(kand));
-        const uint32_t and_hi = __reduce_and_sync(0xffffffffu, static_cast<uint32_t>(kand >> 32));
-        const uint64_t vary = ((static_cast<uint64_t>(or_hi ^ and_hi)) << 32) | (or_lo ^ and_lo);
-        const uint64_t same = (static_cast<uint64_t>(and_hi) << 32) | and_lo;
-        uint64_t prefix = 0, pmask = 0;
-        uint32_t need = static_cast<uint32_t>(keff);
-        for (int d = 7; d >= 0; --d) {
+        const uint32_t vary = __reduce_or_sync(0xffffffffu, kor) ^ __reduce_and_sync(0xffffffffu, kand);
+        const uint32_t same = __reduce_and_sync(0xffffffffu, kand);
+        uint32_t prefix = 0, pmask = 0, inbin = static_cast<uint32_t>(c);
+        bool whole = false;
+        for (int d = 3; d >= 0; --d) {
             const int sh = 8 * d;
-            const uint64_t dm = 0xFFull << sh;
+            const uint32_t dm = 0xFFu << sh;
             if ((vary & dm) == 0) {   // every candidate has this digit
                 prefix |= same & dm;
                 pmask |= dm;
@@ -302,8 +304,7 @@ __global__ void __launch_bounds__(kSortWarps * 32) cand_sort_kernel(
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 if (32 * b >= c) break;
-                if (32 * b + lane < c && (x[b] & pmask) == prefix)
-                    atomicAdd(&bins[static_cast<uint32_t>(x[b] >> sh) & 0xFFu], 1u);
+                if (32 * b + lane < c && (ok[b] & pmask) == prefix) atomicAdd(&bins[(ok[b] >> sh) & 0xFFu], 1u);
             }
             __syncwarp();
             // bin holding the need-th largest: lane l owns bins 255-8l .. 248-8l
@@ -320,7 +321,7 @@ __global__ void __launch_bounds__(kSortWarps * 32) cand_sort_kernel(
                 if (lane >= o) incl += y;
             }
             const uint32_t excl = incl - tot;
-            uint32_t sel = 0, above = 0, inbin = 0;
+            uint32_t sel = 0, above = 0, cnt_sel = 0;
             const bool mine = excl < need && need <= incl;
             if (mine) {
                 uint32_t a = excl;
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(kSortWarps * 32) cand_sort_kernel(
                     if (a + cb[q] >= need) {
                         sel = 255 - 8 * lane - q;
                         above = a;
-                        inbin = cb[q];
+                        cnt_sel = cb[q];
                         break;
                     }
                     a += cb[q];
@@ -339,28 +340,73 @@ __global__ void __launch_bounds__(kSortWarps * 32) cand_sort_kernel(
             const int src_lane = __ffs(who) - 1;
             sel = __shfl_sync(0xffffffffu, sel, src_lane);
             above = __shfl_sync(0xffffffffu, above, src_lane);
-            inbin = __shfl_sync(0xffffffffu, inbin, src_lane);
+            inbin = __shfl_sync(0xffffffffu, cnt_sel, src_lane);
             __syncwarp();
-            prefix |= static_cast<uint64_t>(sel) << sh;
+            prefix |= sel << sh;
             pmask |= dm;
             need -= above;
-            if (inbin == need) break;   // the whole bin is selected: thr = its lowest key
+            if (inbin == need) {   // the whole bin is selected: keys >= its lowest key
+                whole = true;
+                break;
+            }
         }
         thr = prefix;   // digits below the last fixed one are zero
+        // every digit fixed and only part of the keys equal to T selected
+        partial = !whole && need < inbin;
     }
-    // 2. compact the winners (keys >= thr, exactly keff of them) and sort them
-    int base = 0;
+    // 2. compact the winners into shared memory (swizzled: the sort's lane
+    //    pl reads its register pr at pl*E + (pr ^ (pl % E)), free of bank
+    //    conflicts); the ties at T go to a list first
+    int base = 0, nties = 0;
+    uint32_t* ties = bins;
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
         if (32 * b >= c) break;
-        const bool w = 32 * b + lane < c && x[b] >= thr;
-        const unsigned m = __ballot_sync(0xffffffffu, w);
-        if (w) {
-            const int pos = base + __popc(m & ((1u << lane) - 1));
-            const int pl = pos / E, pr = pos % E;   // its lane and register in the sort
-            if (pos < W) win[pl * E + (pr ^ (pl % E))] = x[b];
+        const int e = 32 * b + lane;
+        const bool valid = e < c;
+        const bool up = valid && (partial ? ok[b] > thr : ok[b] >= thr);
+        const bool tie = partial && valid && ok[b] == thr;
+        const unsigned mu = __ballot_sync(0xffffffffu, up);
+        const unsigned mt = __ballot_sync(0xffffffffu, tie);
+        if (up || tie) {
+            const uint32_t j = static_cast<uint32_t>(elem(e));
+            if (up) {
+                const int pos = base + __popc(mu & below);
+                const int pl = pos / E, pr = pos % E;
+                if (pos < W) win[pl * E + (pr ^ (pl % E))] = sel_key(ok[b], j);
+            } else {
+                const int tp = nties + __popc(mt & below);
+                if (tp < kMaxTies) ties[tp] = j;
+            }
         }
-        base += __popc(m);
+        base += __popc(mu);
+        nties += __popc(mt);
+    }
+    if (partial) {
+        if (nties > kMaxTies) {   // too many equal scores at T for the list
+            if (lane == 0) ovf_list[atomicAdd(ovf_count, 1)] = row;
+            return;
+        }
+        __syncwarp();
+        // a tie wins iff fewer than `need` ties have a smaller index
+        for (int q0 = 0; q0 < nties; q0 += 32) {
+            const int q = q0 + lane;
+            bool w = false;
+            uint32_t j = 0;
+            if (q < nties) {
+                j = ties[q];
+                uint32_t rank = 0;
+                for (int r = 0; r < nties; ++r) rank += ties[r] < j;
+                w = rank < need;
+            }
+            const unsigned mw = __ballot_sync(0xffffffffu, w);
+            if (w) {
+                const int pos = base + __popc(mw & below);
+                const int pl = pos / E, pr = pos % E;
+                if (pos < W) win[pl * E + (pr ^ (pl % E))] = sel_key(thr, j);
+            }
+            base += __popc(mw);
+        }
     }
     __syncwarp();
     uint64_t y[E];
