@@ -141,6 +141,20 @@ SSA_DEVINL void small_groups(const float (&v)[32], int j0, int n_i, uint16_t* gc
                 static_cast<uint16_t>(f32_order_key(max_of<G>(v + e) * scale) >> 16);
 }
 
+// As small_groups for any group size g in {1, 2, 4} (rows of fewer than 8k
+// keys only): one running maximum, written at the last key of each group.
+SSA_DEVINL void tiny_groups(const float (&v)[32], int j0, int n_i, uint16_t* gcol, float scale,
+                            int g) {
+    float run = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        run = (e & (g - 1)) == 0 ? v[e] : fmaxf(run, v[e]);
+        if ((e & (g - 1)) == g - 1 && j0 + e - (g - 1) < n_i)
+            gcol[static_cast<int64_t>((j0 + e) / g) * kUnitM] =
+                static_cast<uint16_t>(f32_order_key(run * scale) >> 16);
+    }
+}
+
 // Bit e of the result is set iff v[e] >= t (e < 8): one set + one funnel
 // shift per element, no branches.
 SSA_DEVINL uint32_t ge_mask8(const float* v, float t) {
@@ -500,13 +514,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     gacc[c] = -INFINITY;
                                 }
                             } else if (live && g > 0) {
-                                switch (g) {
-                                    case 16: small_groups<16>(v, j0, n_i, gcol, p.scale); break;
-                                    case 8: small_groups<8>(v, j0, n_i, gcol, p.scale); break;
-                                    case 4: small_groups<4>(v, j0, n_i, gcol, p.scale); break;
-                                    case 2: small_groups<2>(v, j0, n_i, gcol, p.scale); break;
-                                    default: small_groups<1>(v, j0, n_i, gcol, p.scale); break;
-                                }
+                                if (g == 16)
+                                    small_groups<16>(v, j0, n_i, gcol, p.scale);
+                                else if (g == 8)
+                                    small_groups<8>(v, j0, n_i, gcol, p.scale);
+                                else
+                                    tiny_groups(v, j0, n_i, gcol, p.scale, g);
                             }
                         }
                         if constexpr (MODE == MODE_COLLECT) {
