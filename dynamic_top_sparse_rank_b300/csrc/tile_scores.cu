@@ -477,6 +477,70 @@ __global__ void __launch_bounds__(kThreads, 1)
                       __syncwarp();
                       if (lane == 0) mbar_arrive(t_empty + tb);   // the buffer is free again
                   }
+                  if constexpr (MODE == MODE_COLLECT) {
+                      // every score >= the row's bound is a candidate: the 16-key
+                      // half-chunks holding one are queued and drained 32 at a
+                      // time. The four tests of the two chunks come first (they
+                      // are independent), then the appends.
+                      const int jp = t * kTileN + c2 * 64;   // first key of the pair
+                      float v[64];
+#pragma unroll
+                      for (int e = 0; e < 32; ++e) {
+                          v[e] = __uint_as_float(raw2[0][e]);
+                          v[32 + e] = __uint_as_float(raw2[1][e]);
+                      }
+                      if (jp < n_i && jp + 64 > n_i) {
+#pragma unroll
+                          for (int e = 0; e < 64; ++e)
+                              if (jp + e >= n_i) v[e] = -INFINITY;
+                      }
+                      uint32_t B[4];
+                      bool hot[4];
+#pragma unroll
+                      for (int hs = 0; hs < 4; ++hs) {
+                          const float* w = v + 16 * hs;
+                          hot[hs] = jp + 16 * hs < n_i && fmaxf(max8(w), max8(w + 8)) >= t_raw;
+                      }
+#pragma unroll
+                      for (int hs = 0; hs < 4; ++hs) B[hs] = __ballot_sync(0xffffffffu, hot[hs]);
+#pragma unroll
+                      for (int hs = 0; hs < 4; ++hs) {
+                          if (B[hs]) {
+                              const float* w = v + 16 * hs;
+                              if (hot[hs]) {
+                                  const int q = q_tail + __popc(B[hs] & ((1u << lane) - 1));
+                                  qv[q] = make_float4(w[0], w[1], w[2], w[3]);
+                                  qv[kQueue + q] = make_float4(w[4], w[5], w[6], w[7]);
+                                  qv[2 * kQueue + q] = make_float4(w[8], w[9], w[10], w[11]);
+                                  qv[3 * kQueue + q] = make_float4(w[12], w[13], w[14], w[15]);
+                                  qm[q] = (static_cast<uint32_t>((jp + 16 * hs) / kSub) << 5) |
+                                          static_cast<uint32_t>(lane);
+                              }
+                              q_tail += __popc(B[hs]);
+                              if (q_tail >= 32) {
+                                  __syncwarp();   // the queued entries are visible to every lane
+                                  drain(32);
+                                  q_tail -= 32;
+                                  if (q_tail > 0) {   // move the rest to the front
+                                      if (lane < q_tail) {
+                                          // entry 32+l moves to l: sources and targets
+                                          // never overlap (fewer than 32 remain)
+                                          const float4 a = qv[32 + lane], b2 = qv[kQueue + 32 + lane],
+                                                       c2v = qv[2 * kQueue + 32 + lane],
+                                                       d2 = qv[3 * kQueue + 32 + lane];
+                                          const uint32_t mm = qm[32 + lane];
+                                          qv[lane] = a;
+                                          qv[kQueue + lane] = b2;
+                                          qv[2 * kQueue + lane] = c2v;
+                                          qv[3 * kQueue + lane] = d2;
+                                          qm[lane] = mm;
+                                      }
+                                      __syncwarp();
+                                  }
+                              }
+                          }
+                      }
+                  } else {
 #pragma unroll
                   for (int c1 = 0; c1 < 2; ++c1) {
                     const int c = 2 * c2 + c1;
@@ -522,56 +586,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     tiny_groups(v, j0, n_i, gcol, p.scale, g);
                             }
                         }
-                        if constexpr (MODE == MODE_COLLECT) {
-                            // every score >= the row's bound is a candidate; 16-key
-                            // half-chunk maxima pick the half-chunks holding one, which
-                            // are queued and drained 32 at a time
-#pragma unroll
-                            for (int h16 = 0; h16 < 2; ++h16) {
-                                const float* w = v + kSub * h16;
-                                const bool hot = live && fmaxf(max8(w), max8(w + 8)) >= t_raw;
-                                const uint32_t B = __ballot_sync(0xffffffffu, hot);
-                                if (B) {
-                                    if (hot) {
-                                        const int q = q_tail + __popc(B & ((1u << lane) - 1));
-                                        qv[q] = make_float4(w[0], w[1], w[2], w[3]);
-                                        qv[kQueue + q] = make_float4(w[4], w[5], w[6], w[7]);
-                                        qv[2 * kQueue + q] = make_float4(w[8], w[9], w[10], w[11]);
-                                        qv[3 * kQueue + q] = make_float4(w[12], w[13], w[14], w[15]);
-                                        qm[q] = (static_cast<uint32_t>((j0 + kSub * h16) / kSub) << 5) |
-                                                static_cast<uint32_t>(lane);
-                                    }
-                                    q_tail += __popc(B);
-                                    __syncwarp();
-                                    if (q_tail >= 32) {
-                                        drain(32);
-                                        q_tail -= 32;
-                                        if (q_tail > 0) {   // move the rest to the front
-                                            if (lane < q_tail) {
-                                                // entry 32+l moves to l: sources and targets
-                                                // never overlap (fewer than 32 remain)
-                                                const float4 a = qv[32 + lane], b2 = qv[kQueue + 32 + lane],
-                                                             c2 = qv[2 * kQueue + 32 + lane],
-                                                             d2 = qv[3 * kQueue + 32 + lane];
-                                                const uint32_t mm = qm[32 + lane];
-                                                qv[lane] = a;
-                                                qv[kQueue + lane] = b2;
-                                                qv[2 * kQueue + lane] = c2;
-                                                qv[3 * kQueue + lane] = d2;
-                                                qm[lane] = mm;
-                                            }
-                                            __syncwarp();
-                                        }
-                                    }
-                                }
-                            }
-                        }
                     }
+                  }
                   }
                 }
             }
             if (!ok) break;
             if constexpr (MODE == MODE_COLLECT) {
+                __syncwarp();
                 if (q_tail > 0) drain(q_tail);
                 q_tail = 0;
                 if (row_ok) p.cnt[row * kTBuf + tb] = qcnt[lane];
