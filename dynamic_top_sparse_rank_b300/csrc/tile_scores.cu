@@ -106,6 +106,14 @@ SSA_DEVINL float max8(const float* v) {
     return fmaxf(fmax3(v[0], v[1], v[2]), fmax3(v[3], v[4], fmaxf(v[5], fmaxf(v[6], v[7]))));
 }
 
+// Maximum of 16 scores: an fmax3 tree (8 instructions).
+SSA_DEVINL float max16(const float* v) {
+    const float a = fmax3(v[0], v[1], v[2]), b = fmax3(v[3], v[4], v[5]);
+    const float c = fmax3(v[6], v[7], v[8]), d = fmax3(v[9], v[10], v[11]);
+    const float e = fmax3(v[12], v[13], v[14]);
+    return fmaxf(fmax3(a, b, c), fmax3(d, e, v[15]));
+}
+
 SSA_DEVINL float max32(const float (&v)[32]) {
     float a[11];
 #pragma unroll
@@ -489,7 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                           v[e] = __uint_as_float(raw2[0][e]);
                           v[32 + e] = __uint_as_float(raw2[1][e]);
                       }
-                      if (jp < n_i && jp + 64 > n_i) {
+                      // mask the keys past the row's last one: only in the tile
+                      // where a row of this warp ends (a warp-uniform branch)
+                      if (__any_sync(0xffffffffu, jp < n_i && jp + 64 > n_i)) {
 #pragma unroll
                           for (int e = 0; e < 64; ++e)
                               if (jp + e >= n_i) v[e] = -INFINITY;
@@ -499,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                       for (int hs = 0; hs < 4; ++hs) {
                           const float* w = v + 16 * hs;
-                          hot[hs] = jp + 16 * hs < n_i && fmaxf(max8(w), max8(w + 8)) >= t_raw;
+                          hot[hs] = jp + 16 * hs < n_i && max16(w) >= t_raw;
                       }
 #pragma unroll
                       for (int hs = 0; hs < 4; ++hs) B[hs] = __ballot_sync(0xffffffffu, hot[hs]);
