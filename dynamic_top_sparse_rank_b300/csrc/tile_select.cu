@@ -242,7 +242,7 @@ SSA_DEVINL void warp_bitonic_desc(uint64_t (&x)[E], int lane) {
 }
 
 template <int NB, int E>   // NB batches of 32 candidates; E = winners per lane (32E >= k)
-__global__ void __launch_bounds__(kSortWarps * 32) cand_sort_kernel(
+__global__ void __launch_bounds__(kSortWarps * 32, 4) cand_sort_kernel(
     const uint64_t* __restrict__ cand, const int32_t* __restrict__ cnt, int64_t rows, int Tq,
     int Tk, int k, int causal, float scale, int32_t* __restrict__ idx_out,
     float* __restrict__ score_out, int64_t* __restrict__ ovf_list,
