@@ -27,22 +27,24 @@ namespace ssa {
 //
 // One block per 128-row half of a unit. Histograms live in shared memory as
 // [bin][row pair] words holding two 16-bit counters (a row has < 65536
-// groups). Thread t reads row t % 128 of group after group (a warp reads 64
-// contiguous bytes per load), eight loads in flight per thread.
+// groups). Thread t works on row pair t % 64 and reads both rows' maxima of
+// one group in a 32-bit load (a warp reads 128 contiguous bytes per load),
+// groups t / 64, t / 64 + 4, ...; eight loads in flight per thread.
 constexpr int kSelThreads = 256;
 constexpr int kSelUnroll = 8;
+constexpr int kSelPairs = kTileM / 2;
+constexpr int kSelGStep = kSelThreads / kSelPairs;
 
 __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
     const uint16_t* __restrict__ gm, uint32_t* __restrict__ tau, int BH, int Tq, int Tk, int k,
     int causal, int G_stride) {
-    extern __shared__ uint32_t hist[];   // 256 * (kTileM / 2) words
+    extern __shared__ uint32_t hist[];   // 256 * kSelPairs words
     __shared__ int n_row[kTileM], g_row[kTileM];   // valid keys, groups with a valid key
     __shared__ uint32_t sel_hi[kTileM], need[kTileM];
     const int units_per_head = (Tq + kUnitM - 1) / kUnitM;
     const int num_items = BH * units_per_head * 2;   // (unit, 128-row half)
     const int tid = threadIdx.x;
-    const int r = tid % kTileM;
-    const int gstep = kSelThreads / kTileM;
+    const int pr = tid % kSelPairs;                  // row pair: rows 2pr, 2pr+1
     for (int w = blockIdx.x; w < num_items; w += gridDim.x) {
         const int u = w >> 1, h = w & 1;
         const int bh = u / units_per_head;
@@ -62,31 +64,31 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
             continue;
         }
         const int G_u = tile_groups_in_unit(n_hi, g);
-        const uint16_t* gu = gm + static_cast<int64_t>(u) * G_stride * kUnitM + h * kTileM;
+        // row pair pr of this half: 32-bit words of the [group][256 rows] array
+        const uint32_t* gu = reinterpret_cast<const uint32_t*>(
+                                 gm + static_cast<int64_t>(u) * G_stride * kUnitM + h * kTileM) + pr;
         if (tid < kTileM) {
             const int nr = tid < rows ? tile_valid_count(i0 + tid, Tq, Tk, causal) : 0;
             n_row[tid] = nr;
             g_row[tid] = nr > k ? tile_groups_of_row(nr, g, G_u) : 0;
         }
-        for (int x = tid; x < 256 * (kTileM / 2); x += kSelThreads) hist[x] = 0;
+        for (int x = tid; x < 256 * kSelPairs; x += kSelThreads) hist[x] = 0;
         __syncthreads();
-        const int G_r = g_row[r];   // groups 0 .. G_r-1 of row r hold a valid key
-        const bool active = G_r > 0;
-        const int word = r >> 1;
-        const uint32_t one = 1u << ((r & 1) * 16);
-        // pass 1: high byte of every group maximum of the row
-        if (active) {
-            for (int g0 = tid / kTileM; g0 < G_r; g0 += gstep * kSelUnroll) {
-                uint32_t v[kSelUnroll];
+        const int G0 = g_row[2 * pr], G1 = g_row[2 * pr + 1];   // groups 0 .. G-1 hold a valid key
+        const int Gm = max(G0, G1);
+        // pass 1: high byte of every group maximum of the rows
+        for (int g0 = tid / kSelPairs; g0 < Gm; g0 += kSelGStep * kSelUnroll) {
+            uint32_t v[kSelUnroll];
 #pragma unroll
-                for (int q = 0; q < kSelUnroll; ++q) {
-                    const int grp = g0 + q * gstep;
-                    v[q] = grp < G_r ? static_cast<uint32_t>(gu[static_cast<int64_t>(grp) * kUnitM + r])
-                                     : 0x10000u;
-                }
+            for (int q = 0; q < kSelUnroll; ++q) {
+                const int grp = g0 + q * kSelGStep;
+                v[q] = grp < Gm ? gu[static_cast<int64_t>(grp) * (kUnitM / 2)] : 0u;
+            }
 #pragma unroll
-                for (int q = 0; q < kSelUnroll; ++q)
-                    if (v[q] < 0x10000u) atomicAdd(&hist[(v[q] >> 8) * (kTileM / 2) + word], one);
+            for (int q = 0; q < kSelUnroll; ++q) {
+                const int grp = g0 + q * kSelGStep;
+                if (grp < G0) atomicAdd(&hist[((v[q] & 0xFFFFu) >> 8) * kSelPairs + pr], 1u);
+                if (grp < G1) atomicAdd(&hist[(v[q] >> 24) * kSelPairs + pr], 0x10000u);
             }
         }
         __syncthreads();
@@ -95,8 +97,7 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
             if (n_row[tid] > k) {
                 uint32_t cum = 0;
                 for (int b = 255; b >= 0; --b) {
-                    const uint32_t cb =
-                        (hist[b * (kTileM / 2) + (tid >> 1)] >> ((tid & 1) * 16)) & 0xFFFFu;
+                    const uint32_t cb = (hist[b * kSelPairs + (tid >> 1)] >> ((tid & 1) * 16)) & 0xFFFFu;
                     if (cum + cb >= static_cast<uint32_t>(k)) {
                         hi = b;
                         nd = k - cum;
@@ -109,23 +110,26 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
             need[tid] = nd;
         }
         __syncthreads();
-        for (int x = tid; x < 256 * (kTileM / 2); x += kSelThreads) hist[x] = 0;
+        for (int x = tid; x < 256 * kSelPairs; x += kSelThreads) hist[x] = 0;
         __syncthreads();
         // pass 2: low byte of the group maxima in the selected high-byte bin
-        if (active) {
-            const uint32_t hsel = sel_hi[r];
-            for (int g0 = tid / kTileM; g0 < G_r; g0 += gstep * kSelUnroll) {
+        {
+            const uint32_t hs0 = sel_hi[2 * pr], hs1 = sel_hi[2 * pr + 1];
+            for (int g0 = tid / kSelPairs; g0 < Gm; g0 += kSelGStep * kSelUnroll) {
                 uint32_t v[kSelUnroll];
 #pragma unroll
                 for (int q = 0; q < kSelUnroll; ++q) {
-                    const int grp = g0 + q * gstep;
-                    v[q] = grp < G_r ? static_cast<uint32_t>(gu[static_cast<int64_t>(grp) * kUnitM + r])
-                                     : 0x10000u;
+                    const int grp = g0 + q * kSelGStep;
+                    v[q] = grp < Gm ? gu[static_cast<int64_t>(grp) * (kUnitM / 2)] : 0u;
                 }
 #pragma unroll
-                for (int q = 0; q < kSelUnroll; ++q)
-                    if ((v[q] >> 8) == hsel)
-                        atomicAdd(&hist[(v[q] & 0xFFu) * (kTileM / 2) + word], one);
+                for (int q = 0; q < kSelUnroll; ++q) {
+                    const int grp = g0 + q * kSelGStep;
+                    if (grp < G0 && ((v[q] & 0xFFFFu) >> 8) == hs0)
+                        atomicAdd(&hist[(v[q] & 0xFFu) * kSelPairs + pr], 1u);
+                    if (grp < G1 && (v[q] >> 24) == hs1)
+                        atomicAdd(&hist[((v[q] >> 16) & 0xFFu) * kSelPairs + pr], 0x10000u);
+                }
             }
         }
         __syncthreads();
@@ -134,8 +138,7 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
             if (n_row[tid] > k) {
                 uint32_t cum = 0, lo = 0;
                 for (int b = 255; b >= 0; --b) {
-                    const uint32_t cb =
-                        (hist[b * (kTileM / 2) + (tid >> 1)] >> ((tid & 1) * 16)) & 0xFFFFu;
+                    const uint32_t cb = (hist[b * kSelPairs + (tid >> 1)] >> ((tid & 1) * 16)) & 0xFFFFu;
                     if (cum + cb >= need[tid]) {
                         lo = b;
                         break;
@@ -439,7 +442,7 @@ cudaError_t tile_select_launch(const uint16_t* gm, uint32_t* tau, int BH, int Tq
     if (items == 0) return cudaSuccess;
     const int sms = tile_sm_count();
     const int grid = items < 3 * sms ? items : 3 * sms;
-    constexpr int kHistBytes = 256 * (kTileM / 2) * 4;
+    constexpr int kHistBytes = 256 * kSelPairs * 4;
     cudaError_t e = cudaFuncSetAttribute(group_select_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kHistBytes);
     if (e != cudaSuccess) return e;
