@@ -27,13 +27,15 @@ namespace ssa {
 //
 // One block per 128-row half of a unit. Histograms live in shared memory as
 // [bin][row pair] words holding two 16-bit counters (a row has < 65536
-// groups). Thread t works on row pair t % 64 and reads both rows' maxima of
-// one group in a 32-bit load (a warp reads 128 contiguous bytes per load),
-// groups t / 64, t / 64 + 4, ...; eight loads in flight per thread.
+// groups). Thread t works on rows 4(t % 32) .. 4(t % 32) + 3 and reads the
+// four rows' maxima of one group in a 64-bit load (a warp reads 256
+// contiguous bytes per load), groups t / 32, t / 32 + 8, ...; eight loads in
+// flight per thread.
 constexpr int kSelThreads = 256;
 constexpr int kSelUnroll = 8;
 constexpr int kSelPairs = kTileM / 2;
-constexpr int kSelGStep = kSelThreads / kSelPairs;
+constexpr int kSelQuads = kTileM / 4;
+constexpr int kSelGStep = kSelThreads / kSelQuads;
 
 __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
     const uint16_t* __restrict__ gm, uint32_t* __restrict__ tau, int BH, int Tq, int Tk, int k,
@@ -44,7 +46,7 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
     const int units_per_head = (Tq + kUnitM - 1) / kUnitM;
     const int num_items = BH * units_per_head * 2;   // (unit, 128-row half)
     const int tid = threadIdx.x;
-    const int pr = tid % kSelPairs;                  // row pair: rows 2pr, 2pr+1
+    const int qd = tid % kSelQuads;                  // rows 4qd .. 4qd+3
     for (int w = blockIdx.x; w < num_items; w += gridDim.x) {
         const int u = w >> 1, h = w & 1;
         const int bh = u / units_per_head;
@@ -65,8 +67,8 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
         }
         const int G_u = tile_groups_in_unit(n_hi, g);
         // row pair pr of this half: 32-bit words of the [group][256 rows] array
-        const uint32_t* gu = reinterpret_cast<const uint32_t*>(
-                                 gm + static_cast<int64_t>(u) * G_stride * kUnitM + h * kTileM) + pr;
+        const uint64_t* gu = reinterpret_cast<const uint64_t*>(
+                                 gm + static_cast<int64_t>(u) * G_stride * kUnitM + h * kTileM) + qd;
         if (tid < kTileM) {
             const int nr = tid < rows ? tile_valid_count(i0 + tid, Tq, Tk, causal) : 0;
             n_row[tid] = nr;
@@ -74,21 +76,26 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
         }
         for (int x = tid; x < 256 * kSelPairs; x += kSelThreads) hist[x] = 0;
         __syncthreads();
-        const int G0 = g_row[2 * pr], G1 = g_row[2 * pr + 1];   // groups 0 .. G-1 hold a valid key
-        const int Gm = max(G0, G1);
+        int Gr[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) Gr[r] = g_row[4 * qd + r];
+        const int Gm = max(max(Gr[0], Gr[1]), max(Gr[2], Gr[3]));
         // pass 1: high byte of every group maximum of the rows
-        for (int g0 = tid / kSelPairs; g0 < Gm; g0 += kSelGStep * kSelUnroll) {
-            uint32_t v[kSelUnroll];
+        for (int g0 = tid / kSelQuads; g0 < Gm; g0 += kSelGStep * kSelUnroll) {
+            uint64_t v[kSelUnroll];
 #pragma unroll
             for (int q = 0; q < kSelUnroll; ++q) {
                 const int grp = g0 + q * kSelGStep;
-                v[q] = grp < Gm ? gu[static_cast<int64_t>(grp) * (kUnitM / 2)] : 0u;
+                v[q] = grp < Gm ? gu[static_cast<int64_t>(grp) * (kUnitM / 4)] : 0ull;
             }
 #pragma unroll
             for (int q = 0; q < kSelUnroll; ++q) {
                 const int grp = g0 + q * kSelGStep;
-                if (grp < G0) atomicAdd(&hist[((v[q] & 0xFFFFu) >> 8) * kSelPairs + pr], 1u);
-                if (grp < G1) atomicAdd(&hist[(v[q] >> 24) * kSelPairs + pr], 0x10000u);
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    if (grp < Gr[r])
+                        atomicAdd(&hist[((v[q] >> (16 * r + 8)) & 0xFFu) * kSelPairs + 2 * qd + (r >> 1)],
+                                  1u << (16 * (r & 1)));
             }
         }
         __syncthreads();
@@ -114,21 +121,25 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
         __syncthreads();
         // pass 2: low byte of the group maxima in the selected high-byte bin
         {
-            const uint32_t hs0 = sel_hi[2 * pr], hs1 = sel_hi[2 * pr + 1];
-            for (int g0 = tid / kSelPairs; g0 < Gm; g0 += kSelGStep * kSelUnroll) {
-                uint32_t v[kSelUnroll];
+            uint32_t hsr[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) hsr[r] = sel_hi[4 * qd + r];
+            for (int g0 = tid / kSelQuads; g0 < Gm; g0 += kSelGStep * kSelUnroll) {
+                uint64_t v[kSelUnroll];
 #pragma unroll
                 for (int q = 0; q < kSelUnroll; ++q) {
                     const int grp = g0 + q * kSelGStep;
-                    v[q] = grp < Gm ? gu[static_cast<int64_t>(grp) * (kUnitM / 2)] : 0u;
+                    v[q] = grp < Gm ? gu[static_cast<int64_t>(grp) * (kUnitM / 4)] : 0ull;
                 }
 #pragma unroll
                 for (int q = 0; q < kSelUnroll; ++q) {
                     const int grp = g0 + q * kSelGStep;
-                    if (grp < G0 && ((v[q] & 0xFFFFu) >> 8) == hs0)
-                        atomicAdd(&hist[(v[q] & 0xFFu) * kSelPairs + pr], 1u);
-                    if (grp < G1 && (v[q] >> 24) == hs1)
-                        atomicAdd(&hist[((v[q] >> 16) & 0xFFu) * kSelPairs + pr], 0x10000u);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const uint32_t x = static_cast<uint32_t>(v[q] >> (16 * r)) & 0xFFFFu;
+                        if (grp < Gr[r] && (x >> 8) == hsr[r])
+                            atomicAdd(&hist[(x & 0xFFu) * kSelPairs + 2 * qd + (r >> 1)], 1u << (16 * (r & 1)));
+                    }
                 }
             }
         }
@@ -421,16 +432,37 @@ __global__ void __launch_bounds__(kSortWarps * 32, 4) cand_sort_kernel(
     warp_bitonic_desc<E>(y, lane);
     int32_t* io = idx_out + row * k;
     float* so = score_out ? score_out + row * k : nullptr;
+    const int e0 = lane * E;   // this lane's E consecutive outputs
+    bool vec = false;
+    if constexpr (E % 4 == 0)
+        vec = e0 + E <= k && (reinterpret_cast<uintptr_t>(io + e0) & 15) == 0 &&
+              (so == nullptr || (reinterpret_cast<uintptr_t>(so + e0) & 15) == 0);
+    if (vec) {   // 16-byte stores: a quarter of the store requests
 #pragma unroll
-    for (int r = 0; r < E; ++r) {
-        const int e = lane * E + r;
-        if (e < k) {
-            if (e < keff) {
-                io[e] = static_cast<int32_t>(sel_key_index(y[r]));
-                if (so) so[e] = order_key_f32(sel_key_okey(y[r]));
-            } else {
-                io[e] = -1;
-                if (so) so[e] = -INFINITY;
+        for (int r4 = 0; r4 < E; r4 += 4) {
+            int32_t iv[4];
+            float sv[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const bool in = e0 + r4 + t < keff;
+                iv[t] = in ? static_cast<int32_t>(sel_key_index(y[r4 + t])) : -1;
+                sv[t] = in ? order_key_f32(sel_key_okey(y[r4 + t])) : -INFINITY;
+            }
+            *reinterpret_cast<int4*>(io + e0 + r4) = make_int4(iv[0], iv[1], iv[2], iv[3]);
+            if (so) *reinterpret_cast<float4*>(so + e0 + r4) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < E; ++r) {
+            const int e = e0 + r;
+            if (e < k) {
+                if (e < keff) {
+                    io[e] = static_cast<int32_t>(sel_key_index(y[r]));
+                    if (so) so[e] = order_key_f32(sel_key_okey(y[r]));
+                } else {
+                    io[e] = -1;
+                    if (so) so[e] = -INFINITY;
+                }
             }
         }
     }
