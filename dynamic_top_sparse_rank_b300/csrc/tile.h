@@ -103,6 +103,7 @@ struct TileParams {
     int BH, Tq, Tk, k, causal;
     float scale;
     int units_per_head, num_units;   // filled by the launcher
+    int pair_units;                  // launcher: work items are unit pairs (see tile_scores.cu)
     float* S;                        // MODE_RAW: [BH, Tq, Tk]
     uint16_t* gm;                    // MODE_GROUPMAX: [units, G_stride, 256]
     int G_stride;

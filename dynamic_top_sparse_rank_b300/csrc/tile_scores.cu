@@ -90,6 +90,29 @@ struct Unit {
     int bh, i0, rows, n_lo, n_hi, ntiles;
 };
 
+// The k-th unit of this CTA (kNoUnit past the last, -2 for an empty slot).
+// Causal units shrink from the last query block to the first, so with enough
+// units each work item pairs the unit qb of a head with the unit
+// units_per_head-1-qb of the same head (every pair then holds about the same
+// number of key tiles) and the pairs go round-robin over the persistent grid:
+// the slowest CTA has about 1% more work than the mean instead of 8-15%, and
+// the CTAs still work on one or two heads at a time (their k_low stays in
+// L2). With fewer than two units per CTA, units go round-robin one by one.
+constexpr int kNoUnit = -1;
+SSA_DEVINL int cta_unit(const TileParams& p, int k) {
+    if (!p.pair_units) {
+        const int u = blockIdx.x + k * gridDim.x;
+        return u < p.num_units ? u : kNoUnit;
+    }
+    const int P = (p.units_per_head + 1) >> 1;   // pairs per head
+    const int pi = blockIdx.x + (k >> 1) * gridDim.x;
+    if (pi >= p.BH * P) return kNoUnit;
+    const int bh = pi / P, j = pi - (pi / P) * P;
+    const int l = (k & 1) ? p.units_per_head - 1 - j : j;
+    if ((k & 1) && l == j) return -2;
+    return bh * p.units_per_head + l;
+}
+
 SSA_DEVINL Unit unit_at(const TileParams& p, int u) {
     Unit U;
     U.bh = u / p.units_per_head;
@@ -246,7 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t kc = 0, qc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            for (int wk = 0; ok; ++wk) {
+                const int u = cta_unit(p, wk);
+                if (u == kNoUnit) break;
+                if (u < 0) continue;   // the second half of an unpaired middle unit
                 const Unit U = unit_at(p, u);
                 if (U.ntiles == 0) continue;
                 const uint32_t qs = qc % C::QSLOTS, quse = qc / C::QSLOTS;
@@ -300,7 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // other stages, slots and K slices only move the start address
         const uint64_t bdesc0 = smem_desc_k_sw128(smem_u32(sk));
         const uint64_t adesc0 = smem_desc_k_sw128(smem_u32(sq));
-        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        for (int wk = 0; ok; ++wk) {
+            const int u = cta_unit(p, wk);
+            if (u == kNoUnit) break;
+            if (u < 0) continue;   // the second half of an unpaired middle unit
             const Unit U = unit_at(p, u);
             if (U.ntiles == 0) continue;
             const uint32_t qs = qc % C::QSLOTS;
@@ -354,7 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t kc = 0, qc = 0;
         uint32_t tpar = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        for (int wk = 0; ok; ++wk) {
+            const int u = cta_unit(p, wk);
+            if (u == kNoUnit) break;
+            if (u < 0) continue;   // the second half of an unpaired middle unit
             const Unit U = unit_at(p, u);
             if (U.ntiles == 0) continue;
             const uint32_t qs = qc % C::QSLOTS, quse = qc / C::QSLOTS;
@@ -438,7 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         };
-        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        for (int wk = 0; ok; ++wk) {
+            const int u = cta_unit(p, wk);
+            if (u == kNoUnit) break;
+            if (u < 0) continue;   // the second half of an unpaired middle unit
             const Unit U = unit_at(p, u);
             const bool row_ok = r < U.rows;
             const int i = U.i0 + r;
@@ -699,7 +734,9 @@ cudaError_t tile_scores_launch(const void* q_low, const void* k_low, int P, int 
     if (p.num_units == 0) return cudaSuccess;
     const int sms = tile_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const int grid = p.num_units < sms ? p.num_units : sms;
+    p.pair_units = p.num_units >= 2 * sms;
+    const int items = p.pair_units ? p.BH * ((p.units_per_head + 1) / 2) : p.num_units;
+    const int grid = items < sms ? items : sms;
 #define SSA_TILE_CASE(PP, MM) \
     if (P == PP && mode == MM) return launch_mode<PP, MM>(qm, km, p, grid, stream);
     SSA_TILE_CASE(64, MODE_RAW)
