@@ -107,7 +107,7 @@ def roofline_for(name, ms, w, alg, pk, pk_kind):
                 "traffic": None, "peak_kind": pk_kind + " bf16 burst (clocks at max during the run)",
                 "algorithmic": "2 * d_proj FLOP per valid (query, key) pair, %.4g per launch"
                 % alg["score_flops"]}
-    if name == "attn_rows.window":
+    if name in ("attn_rows.window", "window_tc"):
         by = alg["window_bytes"]
         what = "unique Q, K, V and O bytes of the window workload"
     elif name.startswith("attn_rows"):

@@ -16,6 +16,10 @@ cudaError_t tile_select_launch(const uint16_t* gm, uint32_t* tau, int BH, int Tq
 cudaError_t tile_sort_launch(const uint64_t* cand, const int32_t* cnt, int64_t rows, int Tq,
                              int Tk, int k, int causal, float scale, int32_t* idx, float* score,
                              int64_t* ovf_list, int32_t* ovf_count, cudaStream_t stream);
+bool window_tc_supported(bool bf16_in, int D, int T, int wl, int wr);
+cudaError_t window_tc_launch(const void* Q, const void* K, const void* V, void* O, bool bf16_out,
+                             int BH, int T, int wl, int wr, float scale, int32_t* dev_status,
+                             cudaStream_t stream);
 template <bool BAND>
 cudaError_t attn_rows_dispatch(const void* Q, const void* K, const void* V, bool bf16_in, int D,
                                const int32_t* idx, void* O, bool bf16_out, int64_t rows, int Tq,
@@ -205,10 +209,16 @@ ssa_status ssa_window_attn(const void* Q, const void* K, const void* V, int dtyp
     // a radius beyond the sequence changes nothing; clamping keeps i + w in int range
     if (w_left > T) w_left = T;
     if (w_right > T) w_right = T;
-    cudaError_t e = ssa::attn_rows_dispatch<true>(Q, K, V, dtype == SSA_BF16, D, nullptr, O,
-                                                  out_dtype == SSA_BF16, rows, T, T, 1, w_left,
-                                                  w_right, sc, dev_status,
-                                                  reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e;
+    if (ssa::window_tc_supported(dtype == SSA_BF16, D, T, w_left, w_right)) {
+        // dense band tiles on the tensor cores
+        e = ssa::window_tc_launch(Q, K, V, O, out_dtype == SSA_BF16, B * H, T, w_left, w_right, sc,
+                                  dev_status, reinterpret_cast<cudaStream_t>(stream));
+    } else {
+        e = ssa::attn_rows_dispatch<true>(Q, K, V, dtype == SSA_BF16, D, nullptr, O,
+                                          out_dtype == SSA_BF16, rows, T, T, 1, w_left, w_right,
+                                          sc, dev_status, reinterpret_cast<cudaStream_t>(stream));
+    }
     return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
 }
 

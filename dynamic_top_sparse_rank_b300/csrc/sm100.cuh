@@ -98,6 +98,21 @@ SSA_DEVINL void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y
         : "memory");
 }
 
+SSA_DEVINL void tma_load_3d(void* smem_dst, const CUtensorMap* map, int x, int y, int z,
+                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Makes this thread's generic-proxy writes to shared memory visible to the
+// async proxy (operands that tcgen05.mma reads after a thread sync).
+SSA_DEVINL void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 SSA_DEVINL void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -153,6 +168,29 @@ SSA_DEVINL uint64_t smem_desc_k_sw128(uint32_t addr) {
     d |= static_cast<uint64_t>(1) << 46;                         // descriptor version
     d |= static_cast<uint64_t>(2) << 61;                         // 128-byte swizzle
     return d;
+}
+
+// Descriptor of an MN-major operand stored with the 128-byte swizzle: rows of
+// 128 bytes hold 64 consecutive MN elements, consecutive rows are consecutive
+// K, 8-row atoms of 1024 bytes (stride byte offset); `mn_block_bytes` is the
+// distance between 64-element MN blocks (leading byte offset, unused for an
+// operand 64 elements wide). This is the layout a TMA box of 64 elements x R
+// rows with the 128-byte swizzle writes, read with K along the rows.
+SSA_DEVINL uint64_t smem_desc_mn_sw128(uint32_t addr, uint32_t mn_block_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_block_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A (K-major) and B (MN-major when
+// b_mn), fp32 D.
+constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.

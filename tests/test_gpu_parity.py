@@ -196,6 +196,41 @@ def test_window_edges(cuda_dev, T, D, wl, wr, dtype):
         assert torch.equal(O.cpu(), V.float())
 
 
+@pytest.mark.parametrize("T,wl,wr", [
+    (1, 0, 0), (2, 1, 1), (128, 128, 0), (129, 64, 64), (300, 100, 20), (385, 0, 128),
+    (1000, 128, 128), (2048, 3, 117),
+])
+def test_window_tensor_core_tiles(cuda_dev, T, wl, wr):
+    """bf16, head size 64 and a band of at most three 128-key tiles per
+    128-query tile run as dense tensor-core tiles (the launch is window_tc);
+    every row is compared with the oracle."""
+    Q, K, V = _normal_inputs(2, 3, T, T, 64, torch.bfloat16, seed=7 * T + wl + 3 * wr)
+    ref = oracle.window_attn(Q, K, V, wl, wr)
+    dq, dk, dv = (t.to(cuda_dev) for t in (Q, K, V))
+    ssa.trace_begin()
+    O = ssa.ssa_window_attn(dq, dk, dv, wl, wr, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert [n for n, _ in ssa.trace_end()] == ["window_tc"]
+    assert_out_close(O.cpu().numpy(), ref, TOL_BF16, False)
+    Ob = ssa.ssa_window_attn(dq, dk, dv, wl, wr)
+    assert_out_close(Ob.float().cpu().numpy(), ref, TOL_BF16, True)
+    if wl == 0 and wr == 0:
+        assert torch.equal(O.cpu(), V.float())
+
+
+def test_window_wide_band_uses_gather(cuda_dev):
+    """A band wider than three key tiles per query tile goes to the gather kernel."""
+    T, wl, wr = 1000, 300, 300
+    Q, K, V = _normal_inputs(1, 2, T, T, 64, torch.bfloat16, seed=99)
+    ref = oracle.window_attn(Q, K, V, wl, wr)
+    ssa.trace_begin()
+    O = ssa.ssa_window_attn(Q.to(cuda_dev), K.to(cuda_dev), V.to(cuda_dev), wl, wr,
+                            out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert [n for n, _ in ssa.trace_end()] == ["attn_rows.window"]
+    assert_out_close(O.cpu().numpy(), ref, TOL_BF16, False)
+
+
 # ------------------------------------------------- full-size sampled parity
 
 FULL = ["topk_causal_bf16_t32k_k256", "topk_causal_bf16_t128k_k512_planted",
