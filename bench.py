@@ -37,7 +37,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import WORKLOADS, make_attn_inputs, make_scorer_inputs  # noqa: E402
+from workloads import WORKLOADS, fill, make_attn_inputs, make_scorer_inputs  # noqa: E402
 
 DEFAULT_WORKLOAD = "topk_causal_bf16_t128k_k512_planted"
 METRIC = "queries/s and effective TFLOP/s at T=128K, k=512; % of phase roofline"
@@ -441,13 +441,126 @@ def run_reference(args):
     }
 
 
+# ------------------------------------------------------------ projection
+
+# The scorer's projections q_low = q_proj(query), k_low = k_proj(key) at the
+# 32K shape of the pages' scorer: 8 heads x 32768 rows, d_model 4096 -> d_proj
+# 64 (x is 2.1 GB, above L2). One step = one call (the query side).
+PROJECT_WORKLOAD = "project_bf16_h8_t32k_d4096_p64"
+PROJ_SHAPE = (1, 8, 32768, 4096, 64)   # B, H, T, d_model, d_proj
+
+
+def run_project(args, rank, world, local_rank):
+    import dynamic_top_sparse_rank_b300 as ssa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    B, H, T, DM, P = PROJ_SHAPE
+    rows = B * H * T
+    x = fill((B, H, T, DM), "normal", 1234 + 1000 * rank, 31, torch.bfloat16, dev)
+    W = fill((P, DM), "normal", 1234, 32, torch.bfloat16, dev)
+    out = torch.empty((B, H, T, P), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: ssa.ssa_lowrank_project(x, W, out=out)   # noqa: E731
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for s_ in range(args.steps):
+        flush.fill_(s_ & 0xFF)
+        ev[s_][0].record(stream)
+        step()
+        ev[s_][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    ssa.trace_begin()
+    for s_ in range(args.steps):
+        flush.fill_(s_ & 0xFF)
+        step()
+    recs = ssa.trace_end()
+    torch.cuda.synchronize()
+    k_ms = float(np.mean([t for n, t in recs if n == "lowrank_project"]))
+    # end to end: x from pinned host memory, out back to the host
+    hx = x.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dx = torch.empty_like(x)
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        ssa.ssa_lowrank_project(dx, W, out=out)
+        hout.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    ms, ms_e2e, k_ms = max_over_ranks([ms, ms_e2e, k_ms], world, dev)
+    if rank != 0:
+        return None
+    pk, pk_kind = peaks()
+    traffic = 2.0 * rows * DM + 2.0 * P * DM + 2.0 * rows * P   # x, W, out
+    achieved = traffic / (k_ms * 1e-3) / 1e9
+    flops = 2.0 * rows * DM * P
+    return {
+        "metric": METRIC, "value": rows * world / (ms * 1e-3), "unit": "queries/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64; x, W ~ N(0,1))",
+        "config": {"workload": PROJECT_WORKLOAD, "B": B, "H": H, "T": T, "d_model": DM,
+                   "d_proj": P, "l2": "flushed between timed steps (512 MB write) and inputs > L2",
+                   "parallelism": "replicas"},
+        "effective_tflops": flops / (ms * 1e-3) / 1e12,
+        "kernels": {"lowrank_project": {"launches_per_step": 1, "ms": k_ms, "bound": "hbm",
+                                        "achieved": achieved, "unit": "GB/s",
+                                        "frac": achieved / pk["hbm_gbs"]}},
+        "roofline": {"kernel": "lowrank_project", "bound": "hbm", "achieved": achieved,
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                     "traffic": None, "peak_kind": pk_kind + " HBM copy",
+                     "algorithmic": "x, W and out bytes, %.4g per launch (%.4g FLOP)" % (traffic, flops)},
+        "e2e": {"value": rows * world / (ms_e2e * 1e-3), "unit": "queries/s", "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": hout.numel() * 2},
+        "gpu_launches": 1,
+        "clocks": clk,
+    }
+
+
+def cpu_baseline_project(n_rows: int = 256):
+    """The oracle's projection of a bounded sample of rows of the projection
+    workload on this host's cores; rows per second."""
+    import oracle
+    B, H, T, DM, P = PROJ_SHAPE
+    x = fill((n_rows, DM), "normal", 1234, 31, torch.bfloat16, "cpu")
+    W = fill((P, DM), "normal", 1234, 32, torch.bfloat16, "cpu")
+    cores = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.lowrank_project(x, W, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return n_rows / dt, cores, "%d rows of %s" % (n_rows, PROJECT_WORKLOAD)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(WORKLOADS) + [PROJECT_WORKLOAD])
     ap.add_argument("--cpu-rows", type=int, default=2048,
                     help="query rows the CPU oracle times (bounded sample)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -458,6 +571,34 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.workload == PROJECT_WORKLOAD:
+        if args.impl == "reference":
+            if rank == 0:
+                v, cores, sample = cpu_baseline_project()
+                print(json.dumps({"impl": "reference", "metric": METRIC, "value": v,
+                                  "unit": "queries/s", "n_gpus": args.gpus, "steps": 1,
+                                  "warmup": args.warmup, "ms_per_step": 1e3 * 256 / v,
+                                  "higher_is_better": True, "scaling": "weak",
+                                  "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                                  "config": {"workload": PROJECT_WORKLOAD, "sample": sample},
+                                  "cpu_baseline": {"value": v, "unit": "queries/s", "cores": cores,
+                                                   "kind": "oracle", "sample": sample},
+                                  "e2e": {"value": v, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                                          "d2h_bytes_per_step": 0}}), flush=True)
+            return
+        if world > 1:
+            torch.distributed.init_process_group("nccl")
+        line = run_project(args, rank, world, local_rank)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                v, cores, sample = cpu_baseline_project()
+                line["cpu_baseline"] = {"value": v, "unit": "queries/s", "cores": cores,
+                                        "kind": "oracle", "sample": sample}
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
 
     if args.impl == "reference":
         if rank == 0:

@@ -24,7 +24,7 @@ SSA_DEV_BAD_INDEX, SSA_DEV_WAIT_LIMIT, SSA_DEV_OVERFLOW = 0x1, 0x2, 0x4
 
 EXPORTS = ("ssa_version", "ssa_status_string", "ssa_score_topk_workspace_size", "ssa_score_topk",
            "ssa_sparse_attn", "ssa_window_attn", "ssa_score_topk_noalloc", "ssa_lowrank_scores",
-           "ssa_trace_begin", "ssa_trace_end")
+           "ssa_lowrank_project", "ssa_trace_begin", "ssa_trace_end")
 
 # Fixed scratch of ssa_score_topk_noalloc and the largest Tk it accepts.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -71,6 +71,8 @@ def load(path: str | None = None):
     lib.ssa_trace_end.argtypes = [V, I]
     lib.ssa_lowrank_scores.restype = I
     lib.ssa_lowrank_scores.argtypes = [V, V, I, I, I, I, I, I, I, F, V, V, V]
+    lib.ssa_lowrank_project.restype = I
+    lib.ssa_lowrank_project.argtypes = [V, V, I, ctypes.c_int64, I, I, V, V, V]
     if path is None:
         _lib = lib
     return lib
@@ -208,6 +210,27 @@ def ssa_lowrank_scores(q_low: torch.Tensor, k_low: torch.Tensor, causal: bool,
                                 int(bool(causal)), float(scale), _ptr(out), _ptr(dev_status),
                                 _stream(dev))
     _check(rc, "ssa_lowrank_scores")
+    return out
+
+
+def ssa_lowrank_project(x: torch.Tensor, W: torch.Tensor, out: torch.Tensor = None,
+                        dev_status: torch.Tensor = None) -> torch.Tensor:
+    """The scorer's low-rank projection out = x W^T (bf16 in, fp32 sums, bf16
+    out): x [..., d_model] (e.g. [B, H, T, d_model]), W [P, d_model] (a linear
+    layer's weight); returns [..., P]."""
+    lib = load()
+    dev = _dev(x, W, out, dev_status)
+    if x.dtype != W.dtype:
+        raise TypeError("x and W must share a dtype")
+    P, d_model = W.shape
+    if x.shape[-1] != d_model:
+        raise ValueError("x has %d columns, W %d" % (x.shape[-1], d_model))
+    rows = x.numel() // d_model if d_model else 0
+    if out is None:
+        out = torch.empty(tuple(x.shape[:-1]) + (P,), dtype=x.dtype, device=dev)
+    rc = lib.ssa_lowrank_project(_ptr(x), _ptr(W), _dt(x), rows, d_model, P, _ptr(out),
+                                 _ptr(dev_status), _stream(dev))
+    _check(rc, "ssa_lowrank_project")
     return out
 
 

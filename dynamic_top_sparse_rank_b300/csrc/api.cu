@@ -16,6 +16,8 @@ cudaError_t tile_select_launch(const uint16_t* gm, uint32_t* tau, int BH, int Tq
 cudaError_t tile_sort_launch(const uint64_t* cand, const int32_t* cnt, int64_t rows, int Tq,
                              int Tk, int k, int causal, float scale, int32_t* idx, float* score,
                              int64_t* ovf_list, int32_t* ovf_count, cudaStream_t stream);
+cudaError_t lowrank_project_launch(const void* x, const void* W, int64_t rows, int d_model, int P,
+                                   void* out, int32_t* dev_status, cudaStream_t stream);
 bool window_tc_supported(bool bf16_in, int D, int T, int wl, int wr);
 cudaError_t window_tc_launch(const void* Q, const void* K, const void* V, void* O, bool bf16_out,
                              int BH, int T, int wl, int wr, float scale, int32_t* dev_status,
@@ -169,6 +171,19 @@ ssa_status ssa_lowrank_scores(const void* q_low, const void* k_low, int dtype, i
     p.dev_status = dev_status;
     cudaError_t e = ssa::tile_scores_launch(q_low, k_low, P, ssa::MODE_RAW, p,
                                             reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
+}
+
+ssa_status ssa_lowrank_project(const void* x, const void* W, int dtype, int64_t rows, int d_model,
+                               int P, void* out, int32_t* dev_status, void* stream) {
+    if (rows < 0 || d_model <= 0 || !dtype_ok(dtype)) return SSA_ERR_INVALID;
+    if (dtype != SSA_BF16 || !(P == 64 || P == 128) || d_model % 64 != 0) return SSA_ERR_UNSUPPORTED;
+    if (rows == 0) return SSA_OK;
+    if (!x || !W || !out || !aligned(x, 16) || !aligned(W, 16) || !aligned(out, 16))
+        return SSA_ERR_INVALID;
+    if (dev_status && !aligned(dev_status, 4)) return SSA_ERR_INVALID;
+    cudaError_t e = ssa::lowrank_project_launch(x, W, rows, d_model, P, out, dev_status,
+                                                reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
 }
 

@@ -44,6 +44,7 @@
 
 #include "sm100.cuh"
 #include "tile.h"
+#include "tmap.h"
 #include "trace.h"
 
 namespace ssa {
@@ -667,36 +668,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return static_cast<EncodeTiledFn>(nullptr);
-        return reinterpret_cast<EncodeTiledFn>(f);
-    }();
-    return fn;
-}
-
 // 2-D map over rows of P bf16 elements: box = 64 elements x 128 rows, 128-byte
 // swizzle (the shared-memory layout the MMA descriptors describe).
 bool make_map(CUtensorMap* m, const void* base, int64_t nrows, int P) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(nrows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(P) * 2};
-    cuuint32_t box[2] = {64, 128};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const uint64_t dims[2] = {static_cast<uint64_t>(P), static_cast<uint64_t>(nrows)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(P) * 2};
+    const uint32_t box[2] = {64, 128};
+    return tmap_bf16_sw128(m, base, 2, dims, strides, box);
 }
 
 template <int P, int MODE>
@@ -704,8 +682,7 @@ cudaError_t launch_mode(const CUtensorMap& qm, const CUtensorMap& km, const Tile
                         int grid, cudaStream_t stream) {
     using C = TileCfg<P, MODE>;
     auto kern = tile_scores_kernel<P, MODE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(C::SMEM));
+    cudaError_t e = set_max_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
     TraceLaunch tr(MODE == MODE_RAW ? "tile_scores.raw"
                    : MODE == MODE_GROUPMAX ? "tile_scores.groupmax" : "tile_scores.collect",

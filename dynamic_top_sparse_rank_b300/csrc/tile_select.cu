@@ -19,6 +19,7 @@
 // score) is put on an overflow list and redone by the row-wise kernel.
 #include "common.cuh"
 #include "tile.h"
+#include "tmap.h"
 #include "trace.h"
 
 namespace ssa {
@@ -475,8 +476,7 @@ cudaError_t tile_select_launch(const uint16_t* gm, uint32_t* tau, int BH, int Tq
     const int sms = tile_sm_count();
     const int grid = items < 3 * sms ? items : 3 * sms;
     constexpr int kHistBytes = 256 * kSelPairs * 4;
-    cudaError_t e = cudaFuncSetAttribute(group_select_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kHistBytes);
+    cudaError_t e = set_max_dyn_smem(reinterpret_cast<const void*>(group_select_kernel), kHistBytes);
     if (e != cudaSuccess) return e;
     TraceLaunch tr("group_select", stream);
     group_select_kernel<<<grid, kSelThreads, kHistBytes, stream>>>(gm, tau, BH, Tq, Tk, k, causal,

@@ -30,6 +30,7 @@
 #include <float.h>
 
 #include "sm100.cuh"
+#include "tmap.h"
 #include "trace.h"
 
 namespace ssa {
@@ -334,38 +335,15 @@ __global__ void __launch_bounds__(kWThreads, 1)
 
 namespace {
 
-using EncodeTiledFn3 = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn3 encode_fn3() {
-    static EncodeTiledFn3 fn = [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return static_cast<EncodeTiledFn3>(nullptr);
-        return reinterpret_cast<EncodeTiledFn3>(f);
-    }();
-    return fn;
-}
-
 // [BH][T][64] bf16, box 64 x 128 rows x 1 head, 128-byte swizzle; rows outside
 // [0, T) of a head read as zeros.
 bool make_map_3d(CUtensorMap* m, const void* base, int BH, int T) {
-    EncodeTiledFn3 fn = encode_fn3();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kWD), static_cast<cuuint64_t>(T),
-                          static_cast<cuuint64_t>(BH)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kWD) * 2,
-                             static_cast<cuuint64_t>(kWD) * 2 * static_cast<cuuint64_t>(T)};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(kWD), static_cast<cuuint32_t>(kWN), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const uint64_t dims[3] = {static_cast<uint64_t>(kWD), static_cast<uint64_t>(T),
+                              static_cast<uint64_t>(BH)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(kWD) * 2,
+                                 static_cast<uint64_t>(kWD) * 2 * static_cast<uint64_t>(T)};
+    const uint32_t box[3] = {static_cast<uint32_t>(kWD), static_cast<uint32_t>(kWN), 1};
+    return tmap_bf16_sw128(m, base, 3, dims, strides, box);
 }
 
 }  // namespace
@@ -402,8 +380,8 @@ cudaError_t window_tc_launch(const void* Q, const void* K, const void* V, void* 
     const int64_t blocks = static_cast<int64_t>(BH) * ((T + kWM - 1) / kWM);
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    cudaError_t e = cudaFuncSetAttribute(window_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kWSmem));
+    cudaError_t e = set_max_dyn_smem(reinterpret_cast<const void*>(window_tc_kernel),
+                                     static_cast<int>(kWSmem));
     if (e != cudaSuccess) return e;
     TraceLaunch tr("window_tc", stream);
     window_tc_kernel<<<static_cast<unsigned>(blocks), kWThreads, kWSmem, stream>>>(qm, km, vm, p);

@@ -147,6 +147,38 @@ ssa_status ssa_lowrank_scores(const void* q_low, const void* k_low, int dtype, i
                               int32_t* dev_status, void* stream);
 
 /*
+ * ssa_lowrank_project — the scorer's low-rank projection on the tensor cores.
+ *
+ * Source: mhpq.cn/news/1098205, section 2.2: the lightweight scorer maps the
+ * query and the key of every head from d_model to d_proj with bias-free
+ * linear layers, q_low = q_proj(query), k_low = k_proj(key); this call is one
+ * such map, run once for the queries and once for the keys.
+ *
+ *   out[r, p] = bf16( sum_c x[r, c] * W[p, c] )   for r < rows, p < P,
+ *
+ * products and sums in fp32 on the tensor cores (the hardware's summation
+ * order), rounded once to bf16 (round to nearest even). Integer-valued inputs
+ * whose sums stay below 2^24 in magnitude give the exact sum.
+ *
+ *   x        device, bf16 [rows, d_model] (for a [B, H, T, d_model] input,
+ *            rows = B*H*T), 16-byte aligned
+ *   W        device, bf16 [P, d_model] (a linear layer's weight), 16-byte aligned
+ *   dtype    SSA_BF16 (SSA_F32 returns SSA_ERR_UNSUPPORTED)
+ *   rows     >= 0
+ *   d_model  a positive multiple of 64
+ *   P        64 or 128
+ *   out      device, bf16 [rows, P], written, 16-byte aligned (feeds
+ *            ssa_score_topk as q_low or k_low)
+ *   dev_status device int32 or NULL (see conventions)
+ *   stream   cudaStream_t
+ *
+ * Returns SSA_OK, SSA_ERR_INVALID, SSA_ERR_UNSUPPORTED or SSA_ERR_CUDA.
+ * rows == 0 is valid and launches nothing.
+ */
+ssa_status ssa_lowrank_project(const void* x, const void* W, int dtype, int64_t rows, int d_model,
+                               int P, void* out, int32_t* dev_status, void* stream);
+
+/*
  * ssa_sparse_attn — attention over the selected keys only.
  *
  * Source: mhpq.cn/news/1098205, section 3.2 (gather the selected K and V,

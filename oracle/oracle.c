@@ -16,6 +16,10 @@
  *    weighted sum of V.
  *  - "Attention机制优化：原理、挑战与工程实践" (bjdmk.com.cn), section 1.1:
  *    scaled dot-product attention softmax(Q K^T / sqrt(d_k)) V.
+ *  - mhpq.cn/news/1098205, section 2.2 (the scorer class): q_low and k_low
+ *    come from bias-free linear layers d_model -> d_proj applied to each
+ *    head's query and key, q_low = q_proj(query), i.e. x . W^T with W in a
+ *    linear layer's [d_proj][d_model] layout.
  *  - nxmr.cn/news/163144 (global vs local attention), section 2.2: a local
  *    window is a radius w around the query, i.e. keys |i - j| <= w, clipped at
  *    the sequence ends; "Attention机制改进：稀疏注意力应用" (yongjin360.com),
@@ -365,5 +369,42 @@ int oracle_window_rows(const double* q_rows, const int64_t* qpos, int64_t n, con
     c.scale = scale > 0.0 ? scale : 1.0 / sqrt((double)D);
     c.O = O;
     for_rows(win_row, &c, n, nthreads);
+    return 0;
+}
+
+/*
+ * Low-rank projection of the scorer: out[r][p] = sum_c x[r][c] * W[p][c] in
+ * fp64, for rows r < n, p < P (W is a linear layer's weight, [P][d_model];
+ * no bias). Rounding to the output precision is the caller's.
+ */
+typedef struct {
+    const double* x;
+    const double* W;
+    int64_t dm;
+    int P;
+    double* out;
+} proj_ctx;
+
+static void proj_row(void* vctx, int64_t r) {
+    proj_ctx* c = (proj_ctx*)vctx;
+    const double* xr = c->x + r * c->dm;
+    for (int p = 0; p < c->P; ++p) {
+        const double* wp = c->W + (int64_t)p * c->dm;
+        double acc = 0.0;
+        for (int64_t cc = 0; cc < c->dm; ++cc) acc += xr[cc] * wp[cc];
+        c->out[r * c->P + p] = acc;
+    }
+}
+
+int oracle_project_rows(const double* x, const double* W, int64_t n, int64_t dm, int P,
+                        double* out, int nthreads) {
+    if (!x || !W || !out || n < 0 || dm < 1 || P < 1) return 1;
+    proj_ctx c;
+    c.x = x;
+    c.W = W;
+    c.dm = dm;
+    c.P = P;
+    c.out = out;
+    for_rows(proj_row, &c, n, nthreads);
     return 0;
 }

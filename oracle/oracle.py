@@ -6,7 +6,8 @@ and converts tensors to float64 numpy arrays (exact for bf16 and fp32 inputs).
 Only the tests, the smoke check and the benchmark's CPU-baseline leg may import
 it; the CUDA library never does, and shares no code with it.
 
-Parity status: score_topk, sparse_attn and window_attn are pinned by the
+Parity status: score_topk, sparse_attn, window_attn and lowrank_project are
+pinned by the
 ``-m "not gpu"`` tests (brute force, closed forms, special cases and an
 independent dense masked attention); none is pinned to printed values, because
 the pages print none for this path.
@@ -49,6 +50,7 @@ def _load():
         lib.oracle_window_rows.argtypes = [P, P, i64, P, P, i64, i32, i32, i32, f64, P, i32]
         lib.oracle_window_rows.restype = i32
         lib.oracle_scores_rows.argtypes = [P, P, i64, P, i64, i64, i32, i32, f32, P, i32]
+        lib.oracle_project_rows.argtypes = [P, P, i64, i64, i32, P, i32]
         lib.oracle_scores_rows.restype = i32
         _lib = lib
     return _lib
@@ -157,6 +159,32 @@ def window_rows(q_rows, qpos, K, V, w_left: int, w_right: int, scale: float = 0.
     if rc != 0:
         raise ValueError("oracle_window_rows: bad arguments")
     return O
+
+
+def lowrank_project(x, W, nthreads: int | None = None):
+    """The scorer's projection x W^T in fp64: x [..., d_model], W [P, d_model];
+    returns float64 [..., P] (unrounded)."""
+    Wd = _f64(W)
+    P, dm = Wd.shape
+    xd = _f64(x)
+    lead = xd.shape[:-1]
+    xr = np.ascontiguousarray(xd.reshape(-1, dm))
+    out = np.empty((xr.shape[0], P), dtype=np.float64)
+    rc = _load().oracle_project_rows(_ptr(xr), _ptr(Wd), xr.shape[0], dm, P, _ptr(out),
+                                     nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_project_rows: bad arguments")
+    return out.reshape(lead + (P,))
+
+
+def round_bf16(v) -> np.ndarray:
+    """float64 -> the nearest bf16 value (ties to even), returned as float64.
+    bf16 keeps 8 significant bits: a value m * 2^e with m in [0.5, 1) becomes
+    rint(m * 256) / 256 * 2^e (numpy's rint rounds half to even). Normal range
+    only (the values of these tests)."""
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)
 
 
 # ------------------------------------------------------- whole-tensor calls

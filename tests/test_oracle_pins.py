@@ -355,3 +355,66 @@ def test_scores_rank_like_the_selection():
         order = sorted((j for j in range(Tk) if S[i, j] > -np.inf), key=lambda j: (-S[i, j], j))
         want = (order + [-1] * k)[:k]
         assert list(idx[i]) == want
+
+
+# ------------------------------------------------------ scorer projection
+# The scorer's q_low / k_low come from bias-free linear layers d_model ->
+# d_proj (mhpq.cn/news/1098205, section 2.2): out = x W^T with W in a linear
+# layer's [d_proj][d_model] layout.
+
+def test_project_selects_and_scales_columns():
+    """Rows of W that are unit vectors (times a power of two) copy one column
+    of x exactly; a transposed W or a wrong index would pick other columns."""
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((7, 64))
+    perm = rng.permutation(64)[:40]
+    W = np.zeros((40, 64))
+    for p, c in enumerate(perm):
+        W[p, c] = 2.0 ** (p % 5 - 2)
+    out = oracle.lowrank_project(x, W)
+    for p, c in enumerate(perm):
+        assert np.array_equal(out[:, p], x[:, c] * 2.0 ** (p % 5 - 2))
+
+
+def test_project_is_linear_in_the_weight_exactly():
+    """Integer-valued inputs: every product and sum is exact in fp64, so
+    x (W1 + W2)^T equals x W1^T + x W2^T to the last bit."""
+    rng = np.random.default_rng(12)
+    x = rng.integers(-4, 5, (9, 128)).astype(np.float64)
+    W1 = rng.integers(-4, 5, (64, 128)).astype(np.float64)
+    W2 = rng.integers(-4, 5, (64, 128)).astype(np.float64)
+    assert np.array_equal(oracle.lowrank_project(x, W1 + W2),
+                          oracle.lowrank_project(x, W1) + oracle.lowrank_project(x, W2))
+
+
+def test_project_feeds_the_scorer_reassociated():
+    """(x Wq^T)(x Wk^T)^T equals x (Wq^T Wk) x^T, computed in the other
+    association by numpy on exact integers: pins the projection's layout
+    (rows of W are output features) against an independent product, and its
+    output against the scorer oracle that consumes it."""
+    rng = np.random.default_rng(13)
+    T, dm, P = 40, 64, 16
+    x = rng.integers(-2, 3, (T, dm)).astype(np.float64)
+    Wq = rng.integers(-2, 3, (P, dm)).astype(np.float64)
+    Wk = rng.integers(-2, 3, (P, dm)).astype(np.float64)
+    ql = oracle.lowrank_project(x, Wq)
+    kl = oracle.lowrank_project(x, Wk)
+    S_other = x @ (Wq.T @ Wk) @ x.T
+    assert np.array_equal(ql @ kl.T, S_other)
+    # the scorer oracle on these projections: fp64 dot rounded to fp32, times 1
+    S = oracle.scores(torch.from_numpy(ql)[None, None], torch.from_numpy(kl)[None, None],
+                      causal=False, scale=1.0)
+    assert np.array_equal(np.asarray(S)[0, 0], S_other.astype(np.float32).astype(np.float64))
+
+
+def test_round_bf16_nearest_even():
+    """bf16 keeps 8 significant bits; ties go to the even significand."""
+    v = [1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 0.75 * 2 ** -7, 257.0, 259.0, -3.0 - 2 ** -7,
+         2 ** -100, 65504.0]
+    want = [1.0, 1.0, 1.0 + 2 ** -6, 1.0 + 2 ** -7, 256.0, 260.0, -3.0, 2 ** -100, 65536.0]
+    assert np.array_equal(oracle.round_bf16(v), np.array(want))
+    # agrees with torch's own float64 -> bfloat16 conversion
+    rng = np.random.default_rng(14)
+    r = rng.standard_normal(4096) * 10.0 ** rng.integers(-6, 6, 4096)
+    ref = torch.from_numpy(r).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.round_bf16(r), ref)
