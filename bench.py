@@ -205,22 +205,41 @@ def max_over_ranks(vals, world: int, device):
 
 # ------------------------------------------------------------------ ours
 
+# The 128K workload in the pages' shared-scorer layout (mhpq.cn/news/1098205,
+# section 3.2): one q_low/k_low per position, scored once, its index list
+# broadcast to the 8 query heads, which read 2 key/value heads (grouped-query
+# attention). Its inputs are those of the 128K workload's first head (scorer)
+# and first two heads (K, V).
+SHARED_WORKLOAD = "topk_causal_bf16_t128k_k512_shared_scorer_kv2"
+SHARED_BASE, SHARED_KV = "topk_causal_bf16_t128k_k512_planted", 2
+
+
 def run_ours(args, rank, world, local_rank):
     import dynamic_top_sparse_rank_b300 as ssa
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = WORKLOADS[args.workload]
+    shared = args.workload == SHARED_WORKLOAD
+    w = WORKLOADS[SHARED_BASE if shared else args.workload]
     w = rank_workload(w, rank)   # each rank: its own batch of the workload
     window = w.P == 0
-    Q, K, V = make_attn_inputs(w, dev)
+    if shared:
+        Q = make_attn_inputs(w, dev)[0]
+        _, K, V = make_attn_inputs(w.with_(H=SHARED_KV), dev)
+        torch.cuda.empty_cache()
+        ws_sc = w.with_(H=1)   # the scorer runs once per position
+    else:
+        Q, K, V = make_attn_inputs(w, dev)
+        ws_sc = w
     if window:
         q_low = k_low = ws = idx = None
     else:
-        q_low, k_low = make_scorer_inputs(w, dev)
-        ws = torch.empty(ssa.score_topk_workspace_size(w.B, w.H, w.Tq, w.Tk, w.P, w.k, w.causal),
+        q_low, k_low = make_scorer_inputs(ws_sc, dev)
+        ws = torch.empty(ssa.score_topk_workspace_size(ws_sc.B, ws_sc.H, w.Tq, w.Tk, w.P, w.k,
+                                                       w.causal),
                          dtype=torch.uint8, device=dev)
-        idx = torch.empty((w.B, w.H, w.Tq, w.k), dtype=torch.int32, device=dev)
+        idx = torch.empty((w.B, ws_sc.H, w.Tq, w.k), dtype=torch.int32, device=dev)
+    attn = ssa.ssa_sparse_attn_grouped if shared else ssa.ssa_sparse_attn
     torch.cuda.synchronize()
     O = torch.empty((w.B, w.H, w.Tq, w.D), dtype=w.torch_dtype, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -232,7 +251,7 @@ def run_ours(args, rank, world, local_rank):
     else:
         phase_list = [("score_topk", lambda: ssa.ssa_score_topk(q_low, k_low, w.k, w.causal,
                                                                 workspace=ws, idx=idx)),
-                      ("sparse_attn", lambda: ssa.ssa_sparse_attn(Q, K, V, idx, out=O))]
+                      ("sparse_attn", lambda: attn(Q, K, V, idx, out=O))]
 
     def step():
         for _, fn in phase_list:
@@ -309,7 +328,7 @@ def run_ours(args, rank, world, local_rank):
                     d.copy_(h, non_blocking=True)
             ssa.ssa_score_topk(dev_in[0], dev_in[1], w.k, w.causal, workspace=ws, idx=idx)
             stream.wait_stream(copy_stream)
-            ssa.ssa_sparse_attn(dev_in[2], dev_in[3], dev_in[4], idx, out=O)
+            attn(dev_in[2], dev_in[3], dev_in[4], idx, out=O)
         host_out.copy_(O, non_blocking=True)
 
     e2e_step()
@@ -332,6 +351,9 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     alg = algorithmic(w)
+    if shared:   # one scorer for all heads
+        alg["score_flops"] /= w.H
+        alg["scored_pairs"] //= w.H
     pk, pk_kind = peaks()
     nq = w.n_queries * world
     value = nq / (ms_step * 1e-3)
@@ -365,7 +387,9 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64; integer q_low/k_low in [-4,4] with planted keys, Q/K/V ~ N(0,1))",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Tq": w.Tq, "Tk": w.Tk, "D": w.D,
+        "config": {"workload": SHARED_WORKLOAD if shared else w.name, "B": w.B, "H": w.H,
+                   "scorer_heads": ws_sc.H, "kv_heads": SHARED_KV if shared else w.H,
+                   "Tq": w.Tq, "Tk": w.Tk, "D": w.D,
                    "d_proj": w.P, "k": w.k, "causal": w.causal, "window": w.window,
                    "l2": "flushed between timed steps (512 MB write) and inputs > L2",
                    "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
@@ -426,7 +450,7 @@ def cpu_baseline(w, n_rows: int, seed: int = 0):
 
 
 def run_reference(args):
-    w = WORKLOADS[args.workload]
+    w = WORKLOADS[SHARED_BASE if args.workload == SHARED_WORKLOAD else args.workload]
     vals = []
     cores, sample, n = 1, "", 1
     for s in range(args.warmup + args.steps):
@@ -567,7 +591,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(WORKLOADS) + [PROJECT_WORKLOAD])
+                    choices=sorted(WORKLOADS) + [PROJECT_WORKLOAD, SHARED_WORKLOAD])
     ap.add_argument("--cpu-rows", type=int, default=2048,
                     help="query rows the CPU oracle times (bounded sample)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -617,7 +641,8 @@ def main():
     line = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
-            v, cores, sample, _ = cpu_baseline(WORKLOADS[args.workload], args.cpu_rows)
+            base = SHARED_BASE if args.workload == SHARED_WORKLOAD else args.workload
+            v, cores, sample, _ = cpu_baseline(WORKLOADS[base], args.cpu_rows)
             line["cpu_baseline"] = {"value": v, "unit": "queries/s", "cores": cores,
                                     "kind": "oracle", "sample": sample}
         print(json.dumps(line), flush=True)

@@ -24,7 +24,7 @@ SSA_DEV_BAD_INDEX, SSA_DEV_WAIT_LIMIT, SSA_DEV_OVERFLOW = 0x1, 0x2, 0x4
 
 EXPORTS = ("ssa_version", "ssa_status_string", "ssa_score_topk_workspace_size", "ssa_score_topk",
            "ssa_sparse_attn", "ssa_window_attn", "ssa_score_topk_noalloc", "ssa_lowrank_scores",
-           "ssa_lowrank_project", "ssa_trace_begin", "ssa_trace_end")
+           "ssa_lowrank_project", "ssa_sparse_attn_grouped", "ssa_trace_begin", "ssa_trace_end")
 
 # Fixed scratch of ssa_score_topk_noalloc and the largest Tk it accepts.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -71,6 +71,8 @@ def load(path: str | None = None):
     lib.ssa_trace_end.argtypes = [V, I]
     lib.ssa_lowrank_scores.restype = I
     lib.ssa_lowrank_scores.argtypes = [V, V, I, I, I, I, I, I, I, F, V, V, V]
+    lib.ssa_sparse_attn_grouped.restype = I
+    lib.ssa_sparse_attn_grouped.argtypes = [V, V, V, I, I, I, I, I, I, I, V, I, I, F, V, I, V, V]
     lib.ssa_lowrank_project.restype = I
     lib.ssa_lowrank_project.argtypes = [V, V, I, ctypes.c_int64, I, I, V, V, V]
     if path is None:
@@ -257,6 +259,35 @@ def ssa_sparse_attn(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, idx: torc
     rc = lib.ssa_sparse_attn(_ptr(Q), _ptr(K), _ptr(V), _dt(Q), B, H, Tq, Tk, D, _ptr(idx), k,
                              float(scale), _ptr(out), _dt(out), _ptr(dev_status), _stream(dev))
     _check(rc, "ssa_sparse_attn")
+    return out
+
+
+def ssa_sparse_attn_grouped(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, idx: torch.Tensor,
+                            scale: float = 0.0, out_dtype=None, out: torch.Tensor = None,
+                            dev_status: torch.Tensor = None) -> torch.Tensor:
+    """Attention with shared key/value heads and/or shared index lists:
+    Q [B,H,Tq,D], K/V [B,H_kv,Tk,D], idx [B,H_idx,Tq,k] (H_kv, H_idx divide H);
+    head h reads K/V head h // (H // H_kv) and index list h // (H // H_idx)."""
+    lib = load()
+    dev = _dev(Q, K, V, idx, out, dev_status)
+    if not (Q.dtype == K.dtype == V.dtype):
+        raise TypeError("Q, K, V must share a dtype")
+    if idx.dtype != torch.int32:
+        raise TypeError("idx must be int32")
+    B, H, Tq, D = Q.shape
+    H_kv, Tk = K.shape[1], K.shape[2]
+    if tuple(K.shape) != (B, H_kv, Tk, D) or tuple(V.shape) != (B, H_kv, Tk, D):
+        raise ValueError("K/V shapes do not match Q")
+    H_idx, k = idx.shape[1], idx.shape[3]
+    if tuple(idx.shape) != (B, H_idx, Tq, k):
+        raise ValueError("idx shape %s does not match Q" % (tuple(idx.shape),))
+    odt = out_dtype or Q.dtype
+    if out is None:
+        out = torch.empty((B, H, Tq, D), dtype=odt, device=dev)
+    rc = lib.ssa_sparse_attn_grouped(_ptr(Q), _ptr(K), _ptr(V), _dt(Q), B, H, H_kv, Tq, Tk, D,
+                                     _ptr(idx), H_idx, k, float(scale), _ptr(out), _dt(out),
+                                     _ptr(dev_status), _stream(dev))
+    _check(rc, "ssa_sparse_attn_grouped")
     return out
 
 

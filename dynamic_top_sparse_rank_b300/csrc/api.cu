@@ -26,7 +26,7 @@ template <bool BAND>
 cudaError_t attn_rows_dispatch(const void* Q, const void* K, const void* V, bool bf16_in, int D,
                                const int32_t* idx, void* O, bool bf16_out, int64_t rows, int Tq,
                                int Tk, int k, int wl, int wr, float scale, int32_t* dev_status,
-                               cudaStream_t stream);
+                               const HeadMap& hm, cudaStream_t stream);
 }  // namespace ssa
 
 namespace {
@@ -202,7 +202,30 @@ ssa_status ssa_sparse_attn(const void* Q, const void* K, const void* V, int dtyp
     const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)D));
     cudaError_t e = ssa::attn_rows_dispatch<false>(Q, K, V, dtype == SSA_BF16, D, idx, O,
                                                    out_dtype == SSA_BF16, rows, Tq, Tk, k, 0, 0,
-                                                   sc, dev_status,
+                                                   sc, dev_status, ssa::HeadMap{1, 1, 1, 0, 0},
+                                                   reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
+}
+
+ssa_status ssa_sparse_attn_grouped(const void* Q, const void* K, const void* V, int dtype, int B,
+                                   int H, int H_kv, int Tq, int Tk, int D, const int32_t* idx,
+                                   int H_idx, int k, float scale, void* O, int out_dtype,
+                                   int32_t* dev_status, void* stream) {
+    if (B < 0 || H < 1 || H_kv < 1 || H_idx < 1 || Tq < 0 || Tk < 0 || k < 1 || !dtype_ok(dtype) ||
+        !dtype_ok(out_dtype) || H % H_kv != 0 || H % H_idx != 0)
+        return SSA_ERR_INVALID;
+    if (!d_ok(D)) return SSA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)B * H * Tq;
+    if (rows == 0) return SSA_OK;
+    if (!Q || !K || !V || !idx || !O) return SSA_ERR_INVALID;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(idx, 4))
+        return SSA_ERR_INVALID;
+    if (dev_status && !aligned(dev_status, 4)) return SSA_ERR_INVALID;
+    const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)D));
+    ssa::HeadMap hm{H, H_kv, H_idx, 1, (H_kv < H || H_idx < H) ? 1 : 0};
+    cudaError_t e = ssa::attn_rows_dispatch<false>(Q, K, V, dtype == SSA_BF16, D, idx, O,
+                                                   out_dtype == SSA_BF16, rows, Tq, Tk, k, 0, 0,
+                                                   sc, dev_status, hm,
                                                    reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
 }
@@ -232,7 +255,8 @@ ssa_status ssa_window_attn(const void* Q, const void* K, const void* V, int dtyp
     } else {
         e = ssa::attn_rows_dispatch<true>(Q, K, V, dtype == SSA_BF16, D, nullptr, O,
                                           out_dtype == SSA_BF16, rows, T, T, 1, w_left, w_right,
-                                          sc, dev_status, reinterpret_cast<cudaStream_t>(stream));
+                                          sc, dev_status, ssa::HeadMap{1, 1, 1, 0, 0},
+                                          reinterpret_cast<cudaStream_t>(stream));
     }
     return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
 }

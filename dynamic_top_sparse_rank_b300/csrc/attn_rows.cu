@@ -115,19 +115,48 @@ SSA_DEVINL void store_out(void* O, int64_t elem_off, const float* v) {
 
 // BAND == false: keys from idx[row, 0..k).  BAND == true: keys
 // max(0, i - wl) .. min(Tk - 1, i + wr) (window attention, Tq == Tk).
+//
+// Grouped heads (hm.grouped): query head h of H reads key/value head
+// h / (H / H_kv) and index list h / (H / H_idx) (grouped-query and
+// multi-query attention, and a scorer shared by all heads whose index list is
+// broadcast, the layout of mhpq.cn/news/1098205, section 3.2). With
+// hm.head_inner the warps walk rows in (batch, query, head) order, so the
+// heads that share an index list gather the same key rows side by side and
+// hit in L1 and L2 instead of each streaming them.
 template <bool BF16_IN, int D, bool BF16_OUT, bool BAND>
 __global__ void __launch_bounds__(256, 3) attn_rows_kernel(
     const void* __restrict__ Q, const void* __restrict__ K, const void* __restrict__ V,
     const int32_t* __restrict__ idx, void* __restrict__ O, int64_t rows, int Tq, int Tk, int k,
-    int wl, int wr, float scale_log2, int32_t* dev_status) {
+    int wl, int wr, float scale_log2, int32_t* dev_status, const HeadMap hm) {
     using Gm = RowGeom<BF16_IN, D>;
     constexpr int L = Gm::L, G = Gm::G, E = Gm::E, R = Gm::R;
     const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (row >= rows) return;
+    const int64_t wrow = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (wrow >= rows) return;
     const int g = lane / L, s = lane % L;
-    const int64_t bh = row / Tq;
-    const int i = (int)(row - bh * Tq);
+    int64_t row, bh, irow_id;   // query/output row, key/value head, index row
+    int i;
+    if (hm.grouped) {
+        const int64_t per_b = (int64_t)Tq * hm.H;
+        const int64_t b = wrow / per_b;
+        const int64_t rem = wrow - b * per_b;
+        int h;
+        if (hm.head_inner) {
+            i = (int)(rem / hm.H);
+            h = (int)(rem - (int64_t)i * hm.H);
+        } else {
+            h = (int)(rem / Tq);
+            i = (int)(rem - (int64_t)h * Tq);
+        }
+        row = (b * hm.H + h) * Tq + i;
+        bh = b * hm.H_kv + h / (hm.H / hm.H_kv);
+        irow_id = (b * hm.H_idx + h / (hm.H / hm.H_idx)) * Tq + i;
+    } else {
+        row = wrow;
+        bh = row / Tq;
+        i = (int)(row - bh * Tq);
+        irow_id = row;
+    }
     const char* Kb = reinterpret_cast<const char*>(K) + bh * (int64_t)Tk * R + s * 16;
     const char* Vb = reinterpret_cast<const char*>(V) + bh * (int64_t)Tk * R + s * 16;
 
@@ -152,7 +181,7 @@ __global__ void __launch_bounds__(256, 3) attn_rows_kernel(
     } else {
         n_entries = Tk > 0 ? k : 0;   // no key at all: every row outputs zeros
     }
-    const int32_t* irow = BAND ? nullptr : idx + row * (int64_t)k;
+    const int32_t* irow = BAND ? nullptr : idx + irow_id * (int64_t)k;
 
     for (int t0 = 0; t0 < n_entries; t0 += 32) {
         const int t = t0 + lane;
@@ -233,13 +262,14 @@ __global__ void __launch_bounds__(256, 3) attn_rows_kernel(
 template <bool BF16_IN, int D, bool BF16_OUT, bool BAND>
 static cudaError_t launch_attn_rows(const void* Q, const void* K, const void* V, const int32_t* idx,
                                     void* O, int64_t rows, int Tq, int Tk, int k, int wl, int wr,
-                                    float scale, int32_t* dev_status, cudaStream_t stream) {
+                                    float scale, int32_t* dev_status, const HeadMap& hm,
+                                    cudaStream_t stream) {
     constexpr int WARPS = 8;
     const int64_t blocks = (rows + WARPS - 1) / WARPS;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     TraceLaunch tr(BAND ? "attn_rows.window" : "attn_rows.sparse", stream);
     attn_rows_kernel<BF16_IN, D, BF16_OUT, BAND><<<(unsigned)blocks, WARPS * 32, 0, stream>>>(
-        Q, K, V, idx, O, rows, Tq, Tk, k, wl, wr, scale * kLog2e, dev_status);
+        Q, K, V, idx, O, rows, Tq, Tk, k, wl, wr, scale * kLog2e, dev_status, hm);
     return cudaGetLastError();
 }
 
@@ -247,11 +277,11 @@ template <bool BAND>
 cudaError_t attn_rows_dispatch(const void* Q, const void* K, const void* V, bool bf16_in, int D,
                                const int32_t* idx, void* O, bool bf16_out, int64_t rows, int Tq,
                                int Tk, int k, int wl, int wr, float scale, int32_t* dev_status,
-                               cudaStream_t stream) {
+                               const HeadMap& hm, cudaStream_t stream) {
 #define SSA_ATTN_CASE(BI, DD, BO)                                                               \
     if (bf16_in == BI && D == DD && bf16_out == BO)                                             \
         return launch_attn_rows<BI, DD, BO, BAND>(Q, K, V, idx, O, rows, Tq, Tk, k, wl, wr, scale, \
-                                                  dev_status, stream);
+                                                  dev_status, hm, stream);
     SSA_ATTN_CASE(true, 64, true)
     SSA_ATTN_CASE(true, 64, false)
     SSA_ATTN_CASE(true, 128, true)
@@ -266,9 +296,11 @@ cudaError_t attn_rows_dispatch(const void* Q, const void* K, const void* V, bool
 
 template cudaError_t attn_rows_dispatch<false>(const void*, const void*, const void*, bool, int,
                                                const int32_t*, void*, bool, int64_t, int, int, int,
-                                               int, int, float, int32_t*, cudaStream_t);
+                                               int, int, float, int32_t*, const HeadMap&,
+                                               cudaStream_t);
 template cudaError_t attn_rows_dispatch<true>(const void*, const void*, const void*, bool, int,
                                               const int32_t*, void*, bool, int64_t, int, int, int,
-                                              int, int, float, int32_t*, cudaStream_t);
+                                              int, int, float, int32_t*, const HeadMap&,
+                                              cudaStream_t);
 
 }  // namespace ssa

@@ -74,6 +74,14 @@ SSA_DEVINL float order_key_f32(uint32_t k) {
     return __uint_as_float(u);
 }
 
+// Head mapping of the gather attention: H query heads, H_kv key/value heads
+// and H_idx index lists (both dividing H); grouped == 0 is the plain layout
+// (one of each per head).
+struct HeadMap {
+    int H, H_kv, H_idx;
+    int grouped, head_inner;
+};
+
 // Composite selection key: larger score first, then smaller index first.
 SSA_DEVINL uint64_t sel_key(uint32_t okey, uint32_t j) {
     return (static_cast<uint64_t>(okey) << 32) | static_cast<uint64_t>(~j);

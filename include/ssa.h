@@ -207,6 +207,33 @@ ssa_status ssa_sparse_attn(const void* Q, const void* K, const void* V, int dtyp
                            int out_dtype, int32_t* dev_status, void* stream);
 
 /*
+ * ssa_sparse_attn_grouped — ssa_sparse_attn with heads that share keys,
+ * values or index lists.
+ *
+ * Source: mhpq.cn/news/1098205, section 3.2: the scorer may be shared by all
+ * heads ([batch, seq_len, d_proj]) and its index list broadcast to every head;
+ * "Attention机制优化：原理、挑战与工程实践" (bjdmk.com.cn), sections 3.1-3.2:
+ * grouped-query and multi-query attention, where groups of query heads read
+ * one key/value head.
+ *
+ * Query head h (of H) attends, for its row i, the keys listed in index row
+ * (b, h / (H / H_idx), i) using key/value head h / (H / H_kv); otherwise the
+ * arithmetic is that of ssa_sparse_attn (same scale, padding and error rules).
+ *
+ *   Q, O     [B, H, Tq, D]; K, V [B, H_kv, Tk, D]; idx int32 [B, H_idx, Tq, k]
+ *   H_kv, H_idx  >= 1, each dividing H (H_kv = H_idx = H gives ssa_sparse_attn)
+ *
+ * When heads share index lists or key/value heads, rows run in (batch,
+ * query, head) order so that the heads reading the same key rows do so side
+ * by side. Returns as ssa_sparse_attn; H % H_kv or H % H_idx != 0 is
+ * SSA_ERR_INVALID.
+ */
+ssa_status ssa_sparse_attn_grouped(const void* Q, const void* K, const void* V, int dtype, int B,
+                                   int H, int H_kv, int Tq, int Tk, int D, const int32_t* idx,
+                                   int H_idx, int k, float scale, void* O, int out_dtype,
+                                   int32_t* dev_status, void* stream);
+
+/*
  * ssa_window_attn — sliding-window (local band) attention.
  *
  * Source: nxmr.cn/news/163144, section 2.2 (each token attends the positions

@@ -146,6 +146,64 @@ def test_sparse_attn_matches_oracle(cuda_dev, B, H, Tq, Tk, D, k, dtype):
         assert_out_close(Ob.float().cpu().numpy(), ref, TOL_BF16, True)
 
 
+@pytest.mark.parametrize("H,H_kv,H_idx,dtype", [
+    (4, 1, 1, torch.bfloat16), (4, 2, 2, torch.bfloat16), (4, 4, 1, torch.bfloat16),
+    (4, 2, 1, torch.bfloat16), (4, 1, 4, torch.bfloat16), (4, 4, 4, torch.bfloat16),
+    (6, 3, 2, torch.float32),
+])
+def test_sparse_attn_grouped_heads(cuda_dev, H, H_kv, H_idx, dtype):
+    """Shared key/value heads (grouped- and multi-query attention) and shared
+    index lists: head h reads K/V head h // (H // H_kv) and index list
+    h // (H // H_idx). The reference expands the shared heads and runs the
+    plain per-head oracle."""
+    B, Tq, Tk, D, k = 2, 150, 500, 128 if dtype == torch.bfloat16 else 64, 48
+    Q = fill((B, H, Tq, D), "normal", 300 + H_kv, 3, dtype, "cpu")
+    K = fill((B, H_kv, Tk, D), "normal", 300 + H_kv, 4, dtype, "cpu")
+    V = fill((B, H_kv, Tk, D), "normal", 300 + H_kv, 5, dtype, "cpu")
+    g = np.random.default_rng(H * 100 + H_kv * 10 + H_idx)
+    idx = g.integers(0, Tk, size=(B, H_idx, Tq, k)).astype(np.int32)
+    idx[..., -1] = -1
+    idx_t = torch.from_numpy(idx)
+    ref = oracle.sparse_attn(Q, K.repeat_interleave(H // H_kv, dim=1),
+                             V.repeat_interleave(H // H_kv, dim=1),
+                             idx_t.repeat_interleave(H // H_idx, dim=1).numpy())
+    dq, dk, dv, di = (t.to(cuda_dev) for t in (Q, K, V, idx_t))
+    O = ssa.ssa_sparse_attn_grouped(dq, dk, dv, di, out_dtype=torch.float32)
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert_out_close(O.cpu().numpy(), ref, tol, False)
+    if H_kv == H and H_idx == H:   # the plain layout: the same arithmetic as ssa_sparse_attn
+        assert torch.equal(O, ssa.ssa_sparse_attn(dq, dk, dv, di, out_dtype=torch.float32))
+
+
+def test_head_shared_scorer_feeds_grouped_attention(cuda_dev):
+    """The page's shared-scorer layout: one q_low/k_low per position scored
+    once ([B, 1, T, d_proj]), the index list broadcast to 8 query heads that
+    read 2 key/value heads."""
+    B, H, H_kv, T, P, D, k = 1, 8, 2, 600, 64, 128, 64
+    q = fill((B, 1, T, P), "int", 41, 1, torch.bfloat16, "cpu")
+    kl = fill((B, 1, T, P), "int", 41, 2, torch.bfloat16, "cpu")
+    Q = fill((B, H, T, D), "normal", 41, 3, torch.bfloat16, "cpu")
+    K = fill((B, H_kv, T, D), "normal", 41, 4, torch.bfloat16, "cpu")
+    V = fill((B, H_kv, T, D), "normal", 41, 5, torch.bfloat16, "cpu")
+    idx = ssa.ssa_score_topk(q.to(cuda_dev), kl.to(cuda_dev), k, True)
+    ref_idx, _ = oracle.score_topk(q, kl, k, True)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    O = ssa.ssa_sparse_attn_grouped(Q.to(cuda_dev), K.to(cuda_dev), V.to(cuda_dev), idx,
+                                    out_dtype=torch.float32)
+    ref = oracle.sparse_attn(Q, K.repeat_interleave(H // H_kv, dim=1),
+                             V.repeat_interleave(H // H_kv, dim=1),
+                             np.repeat(ref_idx, H, axis=1))
+    assert_out_close(O.cpu().numpy(), ref, TOL_BF16, False)
+
+
+def test_sparse_attn_grouped_rejects_bad_groups(cuda_dev):
+    Q = torch.zeros((1, 4, 8, 64), dtype=torch.bfloat16, device=cuda_dev)
+    K = torch.zeros((1, 3, 8, 64), dtype=torch.bfloat16, device=cuda_dev)
+    idx = torch.zeros((1, 1, 8, 4), dtype=torch.int32, device=cuda_dev)
+    with pytest.raises(ssa.SSAError):
+        ssa.ssa_sparse_attn_grouped(Q, K, K, idx)   # 3 does not divide 4
+
+
 def test_sparse_attn_k1_is_exact_value_row(cuda_dev):
     Q, K, V = _normal_inputs(1, 2, 64, 500, 128, torch.bfloat16, 9)
     idx = torch.randint(0, 500, (1, 2, 64, 1), dtype=torch.int32, generator=torch.Generator().manual_seed(1))
