@@ -222,7 +222,7 @@ ssa_status ssa_sparse_attn_grouped(const void* Q, const void* K, const void* V, 
         return SSA_ERR_INVALID;
     if (dev_status && !aligned(dev_status, 4)) return SSA_ERR_INVALID;
     const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)D));
-    ssa::HeadMap hm{H, H_kv, H_idx, 1, (H_kv < H || H_idx < H) ? 1 : 0};
+    ssa::HeadMap hm{H, H_kv, H_idx, 1, H_kv < H ? 1 : 0};
     cudaError_t e = ssa::attn_rows_dispatch<false>(Q, K, V, dtype == SSA_BF16, D, idx, O,
                                                    out_dtype == SSA_BF16, rows, Tq, Tk, k, 0, 0,
                                                    sc, dev_status, hm,

@@ -120,9 +120,11 @@ SSA_DEVINL void store_out(void* O, int64_t elem_off, const float* v) {
 // h / (H / H_kv) and index list h / (H / H_idx) (grouped-query and
 // multi-query attention, and a scorer shared by all heads whose index list is
 // broadcast, the layout of mhpq.cn/news/1098205, section 3.2). With
-// hm.head_inner the warps walk rows in (batch, query, head) order, so the
-// heads that share an index list gather the same key rows side by side and
-// hit in L1 and L2 instead of each streaming them.
+// hm.head_inner (key/value heads shared by groups of query heads) the warps
+// walk rows in (batch, key/value head, query, head of the group) order: one
+// key/value head at a time, so its K and V stay in L2 (at 128K, one head's K
+// and V are 64 MB, two are more than L2), and the heads of a group, which
+// share the index list when H_idx <= H_kv, gather the same rows side by side.
 template <bool BF16_IN, int D, bool BF16_OUT, bool BAND>
 __global__ void __launch_bounds__(256, 3) attn_rows_kernel(
     const void* __restrict__ Q, const void* __restrict__ K, const void* __restrict__ V,
@@ -142,8 +144,12 @@ __global__ void __launch_bounds__(256, 3) attn_rows_kernel(
         const int64_t rem = wrow - b * per_b;
         int h;
         if (hm.head_inner) {
-            i = (int)(rem / hm.H);
-            h = (int)(rem - (int64_t)i * hm.H);
+            const int gsz = hm.H / hm.H_kv;                  // query heads per key/value head
+            const int64_t per_kv = (int64_t)Tq * gsz;
+            const int kvh = (int)(rem / per_kv);
+            const int64_t rem2 = rem - kvh * per_kv;
+            i = (int)(rem2 / gsz);
+            h = kvh * gsz + (int)(rem2 - (int64_t)i * gsz);
         } else {
             h = (int)(rem / Tq);
             i = (int)(rem - (int64_t)h * Tq);

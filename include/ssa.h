@@ -223,9 +223,9 @@ ssa_status ssa_sparse_attn(const void* Q, const void* K, const void* V, int dtyp
  *   Q, O     [B, H, Tq, D]; K, V [B, H_kv, Tk, D]; idx int32 [B, H_idx, Tq, k]
  *   H_kv, H_idx  >= 1, each dividing H (H_kv = H_idx = H gives ssa_sparse_attn)
  *
- * When heads share index lists or key/value heads, rows run in (batch,
- * query, head) order so that the heads reading the same key rows do so side
- * by side. Returns as ssa_sparse_attn; H % H_kv or H % H_idx != 0 is
+ * When groups of query heads share a key/value head, rows run one key/value
+ * head at a time (its K and V stay in L2), query by query, with the heads of
+ * the group side by side. Returns as ssa_sparse_attn; H % H_kv or H % H_idx != 0 is
  * SSA_ERR_INVALID.
  */
 ssa_status ssa_sparse_attn_grouped(const void* Q, const void* K, const void* V, int dtype, int B,
