@@ -212,6 +212,12 @@ def max_over_ranks(vals, world: int, device):
 # and first two heads (K, V).
 SHARED_WORKLOAD = "topk_causal_bf16_t128k_k512_shared_scorer_kv2"
 SHARED_BASE, SHARED_KV = "topk_causal_bf16_t128k_k512_planted", 2
+# The 128K workload with the boundary smoothing of mhpq.cn/news/1098205,
+# section 4.2: k = 511 (the k + 1 selection stays on the tensor-core path),
+# threshold 0.5 on the scaled scores (q_low . k_low / 8: integer dot products
+# within 4 of each other); the index lists have k + 1 = 512 slots.
+SMOOTH_WORKLOAD = "topk_causal_bf16_t128k_k511_smooth_delta0.5"
+SMOOTH_K, SMOOTH_DELTA = 511, 0.5
 
 
 def run_ours(args, rank, world, local_rank):
@@ -220,7 +226,10 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     shared = args.workload == SHARED_WORKLOAD
-    w = WORKLOADS[SHARED_BASE if shared else args.workload]
+    smooth = args.workload == SMOOTH_WORKLOAD
+    w = WORKLOADS[SHARED_BASE if (shared or smooth) else args.workload]
+    if smooth:
+        w = w.with_(k=SMOOTH_K)
     w = rank_workload(w, rank)   # each rank: its own batch of the workload
     window = w.P == 0
     if shared:
@@ -235,10 +244,17 @@ def run_ours(args, rank, world, local_rank):
         q_low = k_low = ws = idx = None
     else:
         q_low, k_low = make_scorer_inputs(ws_sc, dev)
-        ws = torch.empty(ssa.score_topk_workspace_size(ws_sc.B, ws_sc.H, w.Tq, w.Tk, w.P, w.k,
-                                                       w.causal),
+        wsize = (ssa.score_topk_smooth_workspace_size if smooth else ssa.score_topk_workspace_size)
+        ws = torch.empty(wsize(ws_sc.B, ws_sc.H, w.Tq, w.Tk, w.P, w.k, w.causal),
                          dtype=torch.uint8, device=dev)
-        idx = torch.empty((w.B, ws_sc.H, w.Tq, w.k), dtype=torch.int32, device=dev)
+        idx = torch.empty((w.B, ws_sc.H, w.Tq, w.k + (1 if smooth else 0)), dtype=torch.int32,
+                          device=dev)
+    if smooth:
+        topk = lambda ql, kl: ssa.ssa_score_topk_smooth(ql, kl, w.k, w.causal,   # noqa: E731
+                                                        SMOOTH_DELTA, workspace=ws, idx=idx)
+    else:
+        topk = lambda ql, kl: ssa.ssa_score_topk(ql, kl, w.k, w.causal,   # noqa: E731
+                                                 workspace=ws, idx=idx)
     attn = ssa.ssa_sparse_attn_grouped if shared else ssa.ssa_sparse_attn
     torch.cuda.synchronize()
     O = torch.empty((w.B, w.H, w.Tq, w.D), dtype=w.torch_dtype, device=dev)
@@ -249,8 +265,7 @@ def run_ours(args, rank, world, local_rank):
     if window:
         phase_list = [("window_attn", lambda: ssa.ssa_window_attn(Q, K, V, w.window, out=O))]
     else:
-        phase_list = [("score_topk", lambda: ssa.ssa_score_topk(q_low, k_low, w.k, w.causal,
-                                                                workspace=ws, idx=idx)),
+        phase_list = [("score_topk", lambda: topk(q_low, k_low)),
                       ("sparse_attn", lambda: attn(Q, K, V, idx, out=O))]
 
     def step():
@@ -326,7 +341,7 @@ def run_ours(args, rank, world, local_rank):
             with torch.cuda.stream(copy_stream):
                 for d, h in zip(dev_in[2:], host_in[2:]):
                     d.copy_(h, non_blocking=True)
-            ssa.ssa_score_topk(dev_in[0], dev_in[1], w.k, w.causal, workspace=ws, idx=idx)
+            topk(dev_in[0], dev_in[1])
             stream.wait_stream(copy_stream)
             attn(dev_in[2], dev_in[3], dev_in[4], idx, out=O)
         host_out.copy_(O, non_blocking=True)
@@ -351,6 +366,9 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     alg = algorithmic(w)
+    if smooth:   # the gather runs over k + 1 slots per row
+        alg_g = algorithmic(w.with_(k=w.k + 1))
+        alg["gather_bytes"], alg["attn_flops"] = alg_g["gather_bytes"], alg_g["attn_flops"]
     if shared:   # one scorer for all heads
         alg["score_flops"] /= w.H
         alg["scored_pairs"] //= w.H
@@ -387,10 +405,12 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64; integer q_low/k_low in [-4,4] with planted keys, Q/K/V ~ N(0,1))",
-        "config": {"workload": SHARED_WORKLOAD if shared else w.name, "B": w.B, "H": w.H,
+        "config": {"workload": (SHARED_WORKLOAD if shared else SMOOTH_WORKLOAD if smooth
+                                else w.name), "B": w.B, "H": w.H,
                    "scorer_heads": ws_sc.H, "kv_heads": SHARED_KV if shared else w.H,
                    "Tq": w.Tq, "Tk": w.Tk, "D": w.D,
                    "d_proj": w.P, "k": w.k, "causal": w.causal, "window": w.window,
+                   "boundary_delta": SMOOTH_DELTA if smooth else None,
                    "l2": "flushed between timed steps (512 MB write) and inputs > L2",
                    "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
         "effective_tflops": eff_tflops,
@@ -450,7 +470,8 @@ def cpu_baseline(w, n_rows: int, seed: int = 0):
 
 
 def run_reference(args):
-    w = WORKLOADS[SHARED_BASE if args.workload == SHARED_WORKLOAD else args.workload]
+    w = WORKLOADS[SHARED_BASE if args.workload in (SHARED_WORKLOAD, SMOOTH_WORKLOAD)
+                  else args.workload]
     vals = []
     cores, sample, n = 1, "", 1
     for s in range(args.warmup + args.steps):
@@ -591,7 +612,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(WORKLOADS) + [PROJECT_WORKLOAD, SHARED_WORKLOAD])
+                    choices=sorted(WORKLOADS) + [PROJECT_WORKLOAD, SHARED_WORKLOAD,
+                                                 SMOOTH_WORKLOAD])
     ap.add_argument("--cpu-rows", type=int, default=2048,
                     help="query rows the CPU oracle times (bounded sample)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -641,7 +663,8 @@ def main():
     line = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
-            base = SHARED_BASE if args.workload == SHARED_WORKLOAD else args.workload
+            base = (SHARED_BASE if args.workload in (SHARED_WORKLOAD, SMOOTH_WORKLOAD)
+                    else args.workload)
             v, cores, sample, _ = cpu_baseline(WORKLOADS[base], args.cpu_rows)
             line["cpu_baseline"] = {"value": v, "unit": "queries/s", "cores": cores,
                                     "kind": "oracle", "sample": sample}

@@ -24,7 +24,8 @@ SSA_DEV_BAD_INDEX, SSA_DEV_WAIT_LIMIT, SSA_DEV_OVERFLOW = 0x1, 0x2, 0x4
 
 EXPORTS = ("ssa_version", "ssa_status_string", "ssa_score_topk_workspace_size", "ssa_score_topk",
            "ssa_sparse_attn", "ssa_window_attn", "ssa_score_topk_noalloc", "ssa_lowrank_scores",
-           "ssa_lowrank_project", "ssa_sparse_attn_grouped", "ssa_trace_begin", "ssa_trace_end")
+           "ssa_lowrank_project", "ssa_sparse_attn_grouped", "ssa_score_topk_smooth",
+           "ssa_score_topk_smooth_workspace_size", "ssa_trace_begin", "ssa_trace_end")
 
 # Fixed scratch of ssa_score_topk_noalloc and the largest Tk it accepts.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -73,6 +74,10 @@ def load(path: str | None = None):
     lib.ssa_lowrank_scores.argtypes = [V, V, I, I, I, I, I, I, I, F, V, V, V]
     lib.ssa_sparse_attn_grouped.restype = I
     lib.ssa_sparse_attn_grouped.argtypes = [V, V, V, I, I, I, I, I, I, I, V, I, I, F, V, I, V, V]
+    lib.ssa_score_topk_smooth_workspace_size.restype = Z
+    lib.ssa_score_topk_smooth_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.ssa_score_topk_smooth.restype = I
+    lib.ssa_score_topk_smooth.argtypes = [V, V, I, I, I, I, I, I, I, I, F, F, V, V, V, Z, V, V]
     lib.ssa_lowrank_project.restype = I
     lib.ssa_lowrank_project.argtypes = [V, V, I, ctypes.c_int64, I, I, V, V, V]
     if path is None:
@@ -157,6 +162,40 @@ def ssa_score_topk(q_low: torch.Tensor, k_low: torch.Tensor, k: int, causal: boo
                             int(bool(causal)), float(scale), _ptr(idx), _ptr(score),
                             _ptr(workspace), wbytes, _ptr(dev_status), _stream(dev))
     _check(rc, "ssa_score_topk")
+    return (idx, score) if with_score else idx
+
+
+def score_topk_smooth_workspace_size(B, H, Tq, Tk, P, k, causal) -> int:
+    return int(load().ssa_score_topk_smooth_workspace_size(B, H, Tq, Tk, P, k, int(bool(causal))))
+
+
+def ssa_score_topk_smooth(q_low: torch.Tensor, k_low: torch.Tensor, k: int, causal: bool,
+                          delta: float, scale: float = 0.0, with_score: bool = False,
+                          workspace: torch.Tensor = None, idx: torch.Tensor = None,
+                          score: torch.Tensor = None, dev_status: torch.Tensor = None):
+    """Top-k with boundary smoothing: k + 1 slots per row, the last one kept
+    only when its score is within delta of the k-th (else -1 / -inf)."""
+    lib = load()
+    dev = _dev(q_low, k_low, workspace, idx, score, dev_status)
+    if q_low.dtype != k_low.dtype:
+        raise TypeError("q_low and k_low must share a dtype")
+    B, H, Tq, P = q_low.shape
+    Tk = k_low.shape[2]
+    if tuple(k_low.shape) != (B, H, Tk, P):
+        raise ValueError("k_low shape %s does not match q_low %s" % (tuple(k_low.shape), tuple(q_low.shape)))
+    if idx is None:
+        idx = torch.empty((B, H, Tq, k + 1), dtype=torch.int32, device=dev)
+    if with_score and score is None:
+        score = torch.empty((B, H, Tq, k + 1), dtype=torch.float32, device=dev)
+    need = score_topk_smooth_workspace_size(B, H, Tq, Tk, P, k, causal)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = lib.ssa_score_topk_smooth(_ptr(q_low), _ptr(k_low), _dt(q_low), B, H, Tq, Tk, P, k,
+                                   int(bool(causal)), float(scale), float(delta), _ptr(idx),
+                                   _ptr(score), _ptr(workspace), wbytes, _ptr(dev_status),
+                                   _stream(dev))
+    _check(rc, "ssa_score_topk_smooth")
     return (idx, score) if with_score else idx
 
 

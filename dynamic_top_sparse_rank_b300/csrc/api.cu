@@ -19,6 +19,8 @@ cudaError_t tile_sort_launch(const uint64_t* cand, const int32_t* cnt, int64_t r
 cudaError_t lowrank_project_launch(const void* x, const void* W, int64_t rows, int d_model, int P,
                                    void* out, int32_t* dev_status, cudaStream_t stream);
 bool window_tc_supported(bool bf16_in, int D, int T, int wl, int wr);
+cudaError_t smooth_boundary_launch(int32_t* idx, float* score, int64_t rows, int k, float delta,
+                                   cudaStream_t stream);
 cudaError_t window_tc_launch(const void* Q, const void* K, const void* V, void* O, bool bf16_out,
                              int BH, int T, int wl, int wr, float scale, int32_t* dev_status,
                              cudaStream_t stream);
@@ -171,6 +173,38 @@ ssa_status ssa_lowrank_scores(const void* q_low, const void* k_low, int dtype, i
     p.dev_status = dev_status;
     cudaError_t e = ssa::tile_scores_launch(q_low, k_low, P, ssa::MODE_RAW, p,
                                             reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
+}
+
+size_t ssa_score_topk_smooth_workspace_size(int B, int H, int Tq, int Tk, int P, int k,
+                                            int causal) {
+    if (k < 1 || k + 1 > kMaxK) return 0;
+    const size_t a = ssa_score_topk_workspace_size(B, H, Tq, Tk, P, k + 1, causal);
+    if (a == 0) return 0;
+    const int64_t rows = (int64_t)B * H * Tq;
+    return (size_t)round_up((int64_t)a, 256) + (size_t)round_up(rows * (k + 1) * 4, 256);
+}
+
+ssa_status ssa_score_topk_smooth(const void* q_low, const void* k_low, int dtype, int B, int H,
+                                 int Tq, int Tk, int P, int k, int causal, float scale,
+                                 float delta, int32_t* idx, float* score, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || !dtype_ok(dtype) || k < 1) return SSA_ERR_INVALID;
+    if (!p_ok(P) || k + 1 > kMaxK) return SSA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)B * H * Tq;
+    if (rows == 0) return SSA_OK;
+    const size_t a = ssa_score_topk_workspace_size(B, H, Tq, Tk, P, k + 1, causal);
+    const size_t need = ssa_score_topk_smooth_workspace_size(B, H, Tq, Tk, P, k, causal);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return SSA_ERR_WORKSPACE;
+    // scores of the k+1 selection: the caller's, else scratch after the selection's workspace
+    float* sc = score ? score
+                      : reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                 round_up((int64_t)a, 256));
+    const ssa_status st = ssa_score_topk(q_low, k_low, dtype, B, H, Tq, Tk, P, k + 1, causal,
+                                         scale, idx, sc, workspace, a, dev_status, stream);
+    if (st != SSA_OK) return st;
+    cudaError_t e = ssa::smooth_boundary_launch(idx, sc, rows, k, delta,
+                                                reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
 }
 

@@ -120,6 +120,36 @@ ssa_status ssa_score_topk(const void* q_low, const void* k_low, int dtype, int B
                           int32_t* dev_status, void* stream);
 
 /*
+ * ssa_score_topk_smooth — the top-k with boundary smoothing.
+ *
+ * Source: mhpq.cn/news/1098205, section 4.2: when the k-th and the (k+1)-th
+ * scores differ by less than a threshold, both are selected, so that k varies
+ * a little and near-ties at the boundary do not flip between runs. (The
+ * temperature of the same section, scores / T, is the `scale` argument:
+ * scale = d_proj^-0.5 / T; a positive factor leaves the ordering unchanged.)
+ *
+ * Runs the exact selection of ssa_score_topk with k + 1 (same scores, order
+ * and tie rule; the tensor-core path while k + 1 <= 512), then keeps slot k
+ * (the (k+1)-th key) only if it holds a key and fp32(score[k-1] - score[k]) <
+ * delta; otherwise slot k becomes index -1 / score -inf. delta <= 0 gives the
+ * plain top-k in the first k slots.
+ *
+ *   idx       device, int32 [B, H, Tq, k + 1], written
+ *   score     device, float [B, H, Tq, k + 1], written; may be NULL
+ *   workspace at least ssa_score_topk_smooth_workspace_size(...) bytes,
+ *             256-byte aligned
+ *   other arguments as ssa_score_topk; 1 <= k <= 2047.
+ *
+ * The index lists feed ssa_sparse_attn with k + 1 entries per row (-1
+ * entries are skipped).
+ */
+size_t ssa_score_topk_smooth_workspace_size(int B, int H, int Tq, int Tk, int P, int k, int causal);
+ssa_status ssa_score_topk_smooth(const void* q_low, const void* k_low, int dtype, int B, int H,
+                                 int Tq, int Tk, int P, int k, int causal, float scale,
+                                 float delta, int32_t* idx, float* score, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
  * ssa_lowrank_scores — the low-rank scorer alone, materialised.
  *
  * Source: mhpq.cn/news/1098205, section 2.2 (scores = q_low . k_low^T scaled

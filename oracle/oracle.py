@@ -229,6 +229,23 @@ def score_topk(q_low, k_low, k: int, causal: bool, scale: float = 0.0, rows=None
     return idx, sc
 
 
+def smooth_boundary(idx, score, k: int, delta: float):
+    """Boundary smoothing of a top-(k+1) selection (mhpq.cn/news/1098205,
+    section 4.2: when the k-th and the (k+1)-th scores differ by less than a
+    threshold, both are selected, so k varies a little). ``idx``/``score`` are
+    the sorted top-(k+1) lists [..., k+1]; slot k (the (k+1)-th key) is kept
+    iff it holds a key and fp32(score[k-1] - score[k]) < delta, otherwise it
+    becomes index -1 / score -inf. The gap is an fp32 subtraction of the two
+    fp32 scores (the selection's own precision)."""
+    idx = np.array(idx, dtype=np.int32, copy=True)
+    score = np.array(score, dtype=np.float32, copy=True)
+    gap = (score[..., k - 1] - score[..., k]).astype(np.float32)
+    keep = (idx[..., k] >= 0) & (gap < np.float32(delta))
+    idx[..., k] = np.where(keep, idx[..., k], -1)
+    score[..., k] = np.where(keep, score[..., k], np.float32(-np.inf))
+    return idx, score
+
+
 def sparse_attn(Q, K, V, idx, scale: float = 0.0, rows=None, nthreads: int | None = None):
     """Sparse attention; ``idx`` is [B,H,Tq,k] (all rows) or [len(rows), k].
 

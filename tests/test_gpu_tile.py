@@ -110,3 +110,27 @@ def test_tile_topk_continuous_scores_are_consistent(cuda_dev):
         assert list(idx[0, 0, i]) == want
         got = sc[0, 0, i][: min(k, len(order))]
         np.testing.assert_array_equal(got, row[want[: len(got)]])
+
+
+# ------------------------------------------------ boundary smoothing
+# mhpq.cn/news/1098205, section 4.2: the (k+1)-th key joins when its score is
+# within a threshold of the k-th.
+
+@pytest.mark.parametrize("Tq,Tk,k,causal,delta,dtype,P", [
+    (300, 300, 20, True, 3.0, torch.bfloat16, 64),
+    (1000, 1000, 64, True, 0.5, torch.bfloat16, 64),
+    (129, 700, 31, False, 1e-6, torch.bfloat16, 64),   # only exact ties join
+    (1000, 1000, 64, False, 0.0, torch.bfloat16, 64),  # the plain top-k
+    (200, 500, 32, True, 1.0, torch.float32, 16),      # the row-wise path
+])
+def test_score_topk_smooth_matches_oracle(cuda_dev, Tq, Tk, k, causal, delta, dtype, P):
+    q = fill((1, 2, Tq, P), "int", Tq + k, 1, dtype, "cpu")
+    kl = fill((1, 2, Tk, P), "int", Tq + k, 2, dtype, "cpu")
+    idx, sc = ssa.ssa_score_topk_smooth(q.to(cuda_dev), kl.to(cuda_dev), k, causal, delta,
+                                        with_score=True)
+    ri, rs = oracle.score_topk(q, kl, k + 1, causal)
+    ri, rs = oracle.smooth_boundary(ri, rs, k, delta)
+    assert np.array_equal(idx.cpu().numpy(), ri)
+    assert np.array_equal(sc.cpu().numpy(), rs)
+    if delta <= 0:
+        assert (idx[..., k] == -1).all()

@@ -418,3 +418,58 @@ def test_round_bf16_nearest_even():
     r = rng.standard_normal(4096) * 10.0 ** rng.integers(-6, 6, 4096)
     ref = torch.from_numpy(r).to(torch.bfloat16).to(torch.float64).numpy()
     assert np.array_equal(oracle.round_bf16(r), ref)
+
+
+# ------------------------------------------------- selection variants
+# mhpq.cn/news/1098205, section 4.2: a temperature divides the scores before
+# the selection; boundary smoothing also selects the (k+1)-th key when it is
+# within a threshold of the k-th.
+
+def test_temperature_is_a_scale_and_keeps_the_selection():
+    """scores / T with T > 0 is the scorer's scale times 1/T: on exact
+    (integer) scores the selection is unchanged and the scores scale."""
+    q = torch.from_numpy(_rand_int((1, 2, 64, 16), 77))
+    kl = torch.from_numpy(_rand_int((1, 2, 300, 16), 78))
+    i1, s1 = oracle.score_topk(q, kl, 24, True, scale=0.25)
+    i2, s2 = oracle.score_topk(q, kl, 24, True, scale=2.5)   # the same with temperature 0.1
+    assert np.array_equal(i1, i2)
+    fin = np.isfinite(s1)
+    assert np.array_equal(s2[fin], (s1[fin] * np.float32(10.0)).astype(np.float32))
+
+
+def test_boundary_smoothing_hand_example():
+    """Scores 5, 4, 3.95, 1 with k = 2: the third key joins when the gap
+    0.05 is below the threshold, and not otherwise; equal scores always join
+    for a positive threshold; a missing (k+1)-th key stays missing."""
+    idx = np.array([[7, 3, 9, 1]], np.int32)[:, :3]
+    sc = np.array([[5.0, 4.0, 3.95, 1.0]], np.float32)[:, :3]
+    i, s = oracle.smooth_boundary(idx, sc, 2, 0.1)
+    assert i.tolist() == [[7, 3, 9]] and s[0, 2] == np.float32(3.95)
+    i, s = oracle.smooth_boundary(idx, sc, 2, 0.01)
+    assert i.tolist() == [[7, 3, -1]] and s[0, 2] == -np.inf
+    i, _ = oracle.smooth_boundary(np.array([[1, 2, 3]], np.int32),
+                                  np.array([[2.0, 1.5, 1.5]], np.float32), 2, 1e-30)
+    assert i.tolist() == [[1, 2, 3]]
+    i, _ = oracle.smooth_boundary(np.array([[1, 2, -1]], np.int32),
+                                  np.array([[2.0, 1.5, -np.inf]], np.float32), 2, 10.0)
+    assert i.tolist() == [[1, 2, -1]]
+    i, _ = oracle.smooth_boundary(idx, sc, 2, 0.0)   # threshold 0: the plain top-k
+    assert i.tolist() == [[7, 3, -1]]
+
+
+def test_boundary_smoothing_against_brute_force():
+    """On exact integer scores the smoothed selection equals a direct
+    enumeration: the top k by (score desc, index asc), plus the next key when
+    its score is within delta of the k-th."""
+    q = torch.from_numpy(_rand_int((1, 1, 20, 8), 79))
+    kl = torch.from_numpy(_rand_int((1, 1, 60, 8), 80))
+    k, delta = 5, 2.5
+    i, s = oracle.score_topk(q, kl, k + 1, False, scale=1.0)
+    i, s = oracle.smooth_boundary(i, s, k, delta)
+    qn, kn = q.numpy()[0, 0], kl.numpy()[0, 0]
+    for r in range(20):
+        sc = qn[r] @ kn.T
+        order = sorted(range(60), key=lambda j: (-sc[j], j))
+        want = order[:k] + ([order[k]] if sc[order[k - 1]] - sc[order[k]] < delta else [])
+        got = [int(j) for j in i[0, 0, r] if j >= 0]
+        assert got == want
