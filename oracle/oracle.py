@@ -239,7 +239,8 @@ def smooth_boundary(idx, score, k: int, delta: float):
     fp32 scores (the selection's own precision)."""
     idx = np.array(idx, dtype=np.int32, copy=True)
     score = np.array(score, dtype=np.float32, copy=True)
-    gap = (score[..., k - 1] - score[..., k]).astype(np.float32)
+    with np.errstate(invalid="ignore"):   # -inf - -inf (padded rows) is NaN: not kept
+        gap = (score[..., k - 1] - score[..., k]).astype(np.float32)
     keep = (idx[..., k] >= 0) & (gap < np.float32(delta))
     idx[..., k] = np.where(keep, idx[..., k], -1)
     score[..., k] = np.where(keep, score[..., k], np.float32(-np.inf))
