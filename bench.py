@@ -12,7 +12,9 @@ Prints one JSON line (rank 0). ``value`` is queries/s (query rows B*H*Tq per
 second over the whole job) with inputs resident in HBM; ``e2e`` is the same
 metric through the public calls with pinned host buffers, the host<->device
 copies inside the timed region (the copies of Q, K and V, which only the
-attention call reads, run on a second stream while the scorer computes). Under torchrun (N > 1) every rank runs its own
+attention call reads, run on a second stream while the scorer computes; with
+B = 1 the step runs in two halves of the heads so that copies of one half
+overlap the other half's kernels). Under torchrun (N > 1) every rank runs its own
 independent batch (weak scaling, no collective on the data path); the timed
 region is bracketed by barriers and the slowest rank's time is used.
 
@@ -250,11 +252,11 @@ def run_ours(args, rank, world, local_rank):
         idx = torch.empty((w.B, ws_sc.H, w.Tq, w.k + (1 if smooth else 0)), dtype=torch.int32,
                           device=dev)
     if smooth:
-        topk = lambda ql, kl: ssa.ssa_score_topk_smooth(ql, kl, w.k, w.causal,   # noqa: E731
-                                                        SMOOTH_DELTA, workspace=ws, idx=idx)
+        topk = lambda ql, kl, ix=idx: ssa.ssa_score_topk_smooth(   # noqa: E731
+            ql, kl, w.k, w.causal, SMOOTH_DELTA, workspace=ws, idx=ix)
     else:
-        topk = lambda ql, kl: ssa.ssa_score_topk(ql, kl, w.k, w.causal,   # noqa: E731
-                                                 workspace=ws, idx=idx)
+        topk = lambda ql, kl, ix=idx: ssa.ssa_score_topk(   # noqa: E731
+            ql, kl, w.k, w.causal, workspace=ws, idx=ix)
     attn = ssa.ssa_sparse_attn_grouped if shared else ssa.ssa_sparse_attn
     torch.cuda.synchronize()
     O = torch.empty((w.B, w.H, w.Tq, w.D), dtype=w.torch_dtype, device=dev)
@@ -326,8 +328,46 @@ def run_ours(args, rank, world, local_rank):
     d2h = host_out.numel() * host_out.element_size()
 
     copy_stream = torch.cuda.Stream(dev)
+    d2h_stream = torch.cuda.Stream(dev)
+    # one batch of heads split in two halves (contiguous head slices): the
+    # second half's inputs arrive while the first half computes, and the first
+    # half's output returns while the second half's attention runs
+    split = not window and not shared and not smooth and w.B == 1 and w.H >= 2
+    halves = [(0, w.H // 2), (w.H // 2, w.H)]
+
+    def e2e_step_split():
+        copy_stream.wait_stream(stream)   # the previous step is done with the buffers
+        ev_in = []
+        with torch.cuda.stream(copy_stream):
+            for h0, h1 in halves:           # q_low, k_low of each half, then Q, K, V of each
+                for d, h in zip(dev_in[:2], host_in[:2]):
+                    d[:, h0:h1].copy_(h[:, h0:h1], non_blocking=True)
+                ev_in.append(torch.cuda.Event())
+                ev_in[-1].record(copy_stream)
+            for h0, h1 in halves:
+                for d, h in zip(dev_in[2:], host_in[2:]):
+                    d[:, h0:h1].copy_(h[:, h0:h1], non_blocking=True)
+                ev_in.append(torch.cuda.Event())
+                ev_in[-1].record(copy_stream)
+        for n, (h0, h1) in enumerate(halves):
+            stream.wait_event(ev_in[n])
+            topk(dev_in[0][:, h0:h1], dev_in[1][:, h0:h1], idx[:, h0:h1])
+        d2h_stream.wait_stream(stream)
+        for n, (h0, h1) in enumerate(halves):
+            stream.wait_event(ev_in[2 + n])
+            attn(dev_in[2][:, h0:h1], dev_in[3][:, h0:h1], dev_in[4][:, h0:h1], idx[:, h0:h1],
+                 out=O[:, h0:h1])
+            ev_o = torch.cuda.Event()
+            ev_o.record(stream)
+            d2h_stream.wait_event(ev_o)
+            with torch.cuda.stream(d2h_stream):
+                host_out[:, h0:h1].copy_(O[:, h0:h1], non_blocking=True)
+        stream.wait_stream(d2h_stream)
 
     def e2e_step():
+        if split:
+            e2e_step_split()
+            return
         if window:
             for d, h in zip(dev_in, host_in):
                 d.copy_(h, non_blocking=True)
