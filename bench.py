@@ -97,6 +97,18 @@ def algorithmic(w):
     }
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of these kernels on these workloads (the profile
+# traffic_tile_scores_topk_causal_bf16_t128k_k512.md); to be re-measured, or
+# dropped, when the kernels change.
+MEASURED_TRAFFIC = {
+    ("topk_causal_bf16_t128k_k512_planted", "tile_scores.groupmax"): 3.580e9,
+    ("topk_causal_bf16_t128k_k512_planted", "tile_scores.collect"): 7.363e9,
+    ("topk_causal_bf16_t32k_k256", "tile_scores.groupmax"): 0.892e9,
+    ("topk_causal_bf16_t32k_k256", "tile_scores.collect"): 1.831e9,
+}
+
+
 def roofline_for(name, ms, w, alg, pk, pk_kind):
     """Roofline of one kernel launch: algorithmic work per launch / its time.
 
@@ -112,7 +124,8 @@ def roofline_for(name, ms, w, alg, pk, pk_kind):
         achieved = alg["score_flops"] / sec / 1e12
         return {"kernel": name, "bound": "tensor", "achieved": achieved,
                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                "traffic": None, "peak_kind": pk_kind + " bf16 burst (clocks at max during the run)",
+                "traffic": MEASURED_TRAFFIC.get((w.name, name)),
+                "peak_kind": pk_kind + " bf16 burst (clocks at max during the run)",
                 "algorithmic": "2 * d_proj FLOP per valid (query, key) pair, %.4g per launch"
                 % alg["score_flops"]}
     if name in ("attn_rows.window", "window_tc"):
