@@ -15,8 +15,9 @@
 //   cand_sort_kernel selects the k_eff largest candidates (radix select) and
 //   sorts them by (score desc, index asc).
 // With G between 2k and 4k, about k + k^2/(2G) <= 1.25k keys pass the bound.
-// A row with more candidates than its list holds (heavy ties at the k-th
-// score) is put on an overflow list and redone by the row-wise kernel.
+// A row with more candidates than its list holds, or with more than 256
+// candidates tied at its k-th score (heavy ties), is put on an overflow list
+// and redone by the row-wise kernel.
 #include "common.cuh"
 #include "tile.h"
 #include "tmap.h"
