@@ -61,12 +61,15 @@ constexpr int kTBuf = kTileGroups;            // TMEM tile buffers (two accumula
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
-// Candidate queue of one epilogue warp (MODE_COLLECT): each entry is a 16-key
-// half-chunk holding at least one candidate (its 16 raw scores, its first key,
-// the lane = row that owns it); the warp drains 32 entries at a time, one per
-// lane, so the per-candidate work runs on full warps. The scores are stored
-// slot-major, float4 slot i of entry q at [i][q], so that lanes touching
-// consecutive entries touch consecutive 16-byte words (no bank conflicts).
+// Candidate queue of one epilogue warp (MODE_COLLECT), a ring of 64 entries:
+// each entry is a 16-key half-chunk holding at least one candidate (its 16 raw
+// scores, its first key, the lane = row that owns it); the warp drains 32
+// entries at a time, one per lane, so the per-candidate work runs on full
+// warps. Fewer than 32 entries wait before a step and a step adds at most 32,
+// so the ring never holds more than 63 and a drain never moves entries. The
+// scores are stored slot-major, float4 slot i of entry q at [i][q], so that
+// lanes touching consecutive entries touch consecutive 16-byte words (no bank
+// conflicts).
 constexpr int kQueue = 64;                                   // entries, power of two
 constexpr int kSub = 16;                                     // keys per entry
 constexpr uint32_t kQueueWarpBytes = kQueue * kSub * 4 + kQueue * 4 + 32 * 4;
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float4* qv = nullptr;                  // [kSub/4][kQueue] raw scores
         uint32_t* qm = nullptr;                // [kQueue] (first key / kSub) << 5 | owning lane
         int* qcnt = nullptr;                   // [32] candidates appended per row
-        int q_tail = 0;                        // warp-uniform: entries in the queue
+        int q_head = 0, q_tail = 0;            // warp-uniform ring positions (unwrapped)
         int64_t row0 = 0;                      // global row of lane 0
         float t_raw = -FLT_MAX;                // raw-score bound of this thread's row
         if constexpr (MODE == MODE_COLLECT) {
@@ -438,18 +441,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             qcnt[lane] = 0;
             __syncwarp();
         }
-        // Drain the first `n` (<= 32) queue entries, entry l by lane l: its
+        // Drain the `n` (<= 32) ring entries from q_head on, entry l by lane l: its
         // candidates (scores >= the owning row's bound) are appended to that
         // row's list; a shared-memory count per row hands out the slots.
         auto drain = [&](int n) {
             const bool act = lane < n;
-            const uint32_t meta = act ? qm[lane] : 0u;
+            const int qi = (q_head + lane) & (kQueue - 1);
+            const uint32_t meta = act ? qm[qi] : 0u;
             const int owner = static_cast<int>(meta & 31u);
             const float t_own = __shfl_sync(0xffffffffu, t_raw, owner);
             uint32_t bits = 0;
             if (act) {
-                const float4 a = qv[lane], b = qv[kQueue + lane], c4 = qv[2 * kQueue + lane],
-                             d4 = qv[3 * kQueue + lane];
+                const float4 a = qv[qi], b = qv[kQueue + qi], c4 = qv[2 * kQueue + qi],
+                             d4 = qv[3 * kQueue + qi];
                 const float w0[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
                 const float w1[8] = {c4.x, c4.y, c4.z, c4.w, d4.x, d4.y, d4.z, d4.w};
                 bits = ge_mask8(w0, t_own) | (ge_mask8(w1, t_own) << 8);
@@ -463,12 +467,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bits &= bits - 1;
                     if (slot < capc)
                         dst[slot] = (static_cast<uint64_t>(__float_as_uint(
-                                         reinterpret_cast<const float*>(qv + (e >> 2) * kQueue + lane)[e & 3]))
+                                         reinterpret_cast<const float*>(qv + (e >> 2) * kQueue + qi)[e & 3]))
                                      << 32) |
                                     (jb + static_cast<uint32_t>(e));
                     ++slot;
                 }
             }
+            q_head += n;
             __syncwarp();
         };
         for (int wk = 0; ok; ++wk) {
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           if (B[hs]) {
                               const float* w = v + 16 * hs;
                               if (hot[hs]) {
-                                  const int q = q_tail + __popc(B[hs] & ((1u << lane) - 1));
+                                  const int q = (q_tail + __popc(B[hs] & ((1u << lane) - 1))) & (kQueue - 1);
                                   qv[q] = make_float4(w[0], w[1], w[2], w[3]);
                                   qv[kQueue + q] = make_float4(w[4], w[5], w[6], w[7]);
                                   qv[2 * kQueue + q] = make_float4(w[8], w[9], w[10], w[11]);
@@ -563,26 +568,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           static_cast<uint32_t>(lane);
                               }
                               q_tail += __popc(B[hs]);
-                              if (q_tail >= 32) {
+                              if (q_tail - q_head >= 32) {
                                   __syncwarp();   // the queued entries are visible to every lane
                                   drain(32);
-                                  q_tail -= 32;
-                                  if (q_tail > 0) {   // move the rest to the front
-                                      if (lane < q_tail) {
-                                          // entry 32+l moves to l: sources and targets
-                                          // never overlap (fewer than 32 remain)
-                                          const float4 a = qv[32 + lane], b2 = qv[kQueue + 32 + lane],
-                                                       c2v = qv[2 * kQueue + 32 + lane],
-                                                       d2 = qv[3 * kQueue + 32 + lane];
-                                          const uint32_t mm = qm[32 + lane];
-                                          qv[lane] = a;
-                                          qv[kQueue + lane] = b2;
-                                          qv[2 * kQueue + lane] = c2v;
-                                          qv[3 * kQueue + lane] = d2;
-                                          qm[lane] = mm;
-                                      }
-                                      __syncwarp();
-                                  }
                               }
                           }
                       }
@@ -640,8 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             if constexpr (MODE == MODE_COLLECT) {
                 __syncwarp();
-                if (q_tail > 0) drain(q_tail);
-                q_tail = 0;
+                if (q_tail > q_head) drain(q_tail - q_head);
+                q_head = q_tail = 0;
                 if (row_ok) p.cnt[row * kTBuf + tb] = qcnt[lane];
                 qcnt[lane] = 0;
                 __syncwarp();

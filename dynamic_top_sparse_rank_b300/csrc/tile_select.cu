@@ -29,15 +29,15 @@ namespace ssa {
 //
 // One block per 128-row half of a unit. Histograms live in shared memory as
 // [bin][row pair] words holding two 16-bit counters (a row has < 65536
-// groups). Thread t works on rows 4(t % 32) .. 4(t % 32) + 3 and reads the
-// four rows' maxima of one group in a 64-bit load (a warp reads 256
-// contiguous bytes per load), groups t / 32, t / 32 + 8, ...; eight loads in
-// flight per thread.
+// groups). Thread t works on rows 8(t % 16) .. 8(t % 16) + 7 and reads the
+// eight rows' maxima of one group in a 128-bit load (16 threads read one
+// group's 256 bytes), groups t / 16, t / 16 + 16, ...; eight loads in flight
+// per thread.
 constexpr int kSelThreads = 256;
 constexpr int kSelUnroll = 8;
 constexpr int kSelPairs = kTileM / 2;
-constexpr int kSelQuads = kTileM / 4;
-constexpr int kSelGStep = kSelThreads / kSelQuads;
+constexpr int kSelOcts = kTileM / 8;
+constexpr int kSelGStep = kSelThreads / kSelOcts;
 
 __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
     const uint16_t* __restrict__ gm, uint32_t* __restrict__ tau, int BH, int Tq, int Tk, int k,
@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
     const int units_per_head = (Tq + kUnitM - 1) / kUnitM;
     const int num_items = BH * units_per_head * 2;   // (unit, 128-row half)
     const int tid = threadIdx.x;
-    const int qd = tid % kSelQuads;                  // rows 4qd .. 4qd+3
+    const int qd = tid % kSelOcts;                   // rows 8qd .. 8qd+7
     for (int w = blockIdx.x; w < num_items; w += gridDim.x) {
         const int u = w >> 1, h = w & 1;
         const int bh = u / units_per_head;
@@ -69,8 +69,8 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
         }
         const int G_u = tile_groups_in_unit(n_hi, g);
         // row pair pr of this half: 32-bit words of the [group][256 rows] array
-        const uint64_t* gu = reinterpret_cast<const uint64_t*>(
-                                 gm + static_cast<int64_t>(u) * G_stride * kUnitM + h * kTileM) + qd;
+        const uint4* gu = reinterpret_cast<const uint4*>(
+                              gm + static_cast<int64_t>(u) * G_stride * kUnitM + h * kTileM) + qd;
         if (tid < kTileM) {
             const int nr = tid < rows ? tile_valid_count(i0 + tid, Tq, Tk, causal) : 0;
             n_row[tid] = nr;
@@ -78,25 +78,29 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
         }
         for (int x = tid; x < 256 * kSelPairs; x += kSelThreads) hist[x] = 0;
         __syncthreads();
-        int Gr[4];
+        int Gr[8];
+        int Gm = 0;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) Gr[r] = g_row[4 * qd + r];
-        const int Gm = max(max(Gr[0], Gr[1]), max(Gr[2], Gr[3]));
+        for (int r = 0; r < 8; ++r) {
+            Gr[r] = g_row[8 * qd + r];
+            Gm = max(Gm, Gr[r]);
+        }
         // pass 1: high byte of every group maximum of the rows
-        for (int g0 = tid / kSelQuads; g0 < Gm; g0 += kSelGStep * kSelUnroll) {
-            uint64_t v[kSelUnroll];
+        for (int g0 = tid / kSelOcts; g0 < Gm; g0 += kSelGStep * kSelUnroll) {
+            uint4 v[kSelUnroll];
 #pragma unroll
             for (int q = 0; q < kSelUnroll; ++q) {
                 const int grp = g0 + q * kSelGStep;
-                v[q] = grp < Gm ? gu[static_cast<int64_t>(grp) * (kUnitM / 4)] : 0ull;
+                v[q] = grp < Gm ? gu[static_cast<int64_t>(grp) * (kUnitM / 8)] : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int q = 0; q < kSelUnroll; ++q) {
                 const int grp = g0 + q * kSelGStep;
+                const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
+                for (int r = 0; r < 8; ++r)
                     if (grp < Gr[r])
-                        atomicAdd(&hist[((v[q] >> (16 * r + 8)) & 0xFFu) * kSelPairs + 2 * qd + (r >> 1)],
+                        atomicAdd(&hist[((w4[r >> 1] >> (16 * (r & 1) + 8)) & 0xFFu) * kSelPairs + 4 * qd + (r >> 1)],
                                   1u << (16 * (r & 1)));
             }
         }
@@ -123,24 +127,25 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
         __syncthreads();
         // pass 2: low byte of the group maxima in the selected high-byte bin
         {
-            uint32_t hsr[4];
+            uint32_t hsr[8];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) hsr[r] = sel_hi[4 * qd + r];
-            for (int g0 = tid / kSelQuads; g0 < Gm; g0 += kSelGStep * kSelUnroll) {
-                uint64_t v[kSelUnroll];
+            for (int r = 0; r < 8; ++r) hsr[r] = sel_hi[8 * qd + r];
+            for (int g0 = tid / kSelOcts; g0 < Gm; g0 += kSelGStep * kSelUnroll) {
+                uint4 v[kSelUnroll];
 #pragma unroll
                 for (int q = 0; q < kSelUnroll; ++q) {
                     const int grp = g0 + q * kSelGStep;
-                    v[q] = grp < Gm ? gu[static_cast<int64_t>(grp) * (kUnitM / 4)] : 0ull;
+                    v[q] = grp < Gm ? gu[static_cast<int64_t>(grp) * (kUnitM / 8)] : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
                 for (int q = 0; q < kSelUnroll; ++q) {
                     const int grp = g0 + q * kSelGStep;
+                    const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const uint32_t x = static_cast<uint32_t>(v[q] >> (16 * r)) & 0xFFFFu;
+                    for (int r = 0; r < 8; ++r) {
+                        const uint32_t x = (w4[r >> 1] >> (16 * (r & 1))) & 0xFFFFu;
                         if (grp < Gr[r] && (x >> 8) == hsr[r])
-                            atomicAdd(&hist[(x & 0xFFu) * kSelPairs + 2 * qd + (r >> 1)], 1u << (16 * (r & 1)));
+                            atomicAdd(&hist[(x & 0xFFu) * kSelPairs + 4 * qd + (r >> 1)], 1u << (16 * (r & 1)));
                     }
                 }
             }
