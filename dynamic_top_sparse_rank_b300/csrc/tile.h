@@ -24,10 +24,11 @@ __host__ __device__ __forceinline__ int tile_valid_count(int i, int Tq, int Tk, 
 }
 
 // Group size g of a unit whose rows have between n_lo and n_hi valid keys.
-// Every row with more than k valid keys must be split into at least 2k
-// groups (so that the k-th largest group maximum is a tight lower bound on
-// the k-th largest score), and g is a power of two. 0 when no row of the unit
-// has more than k valid keys (every valid key is then selected).
+// A row with n > k valid keys is split into at least min(n, 2k) groups (more
+// than k, which the exact bound needs; about 2k or more keeps the k-th largest
+// group maximum a tight lower bound on the k-th largest score), and g is a
+// power of two. 0 when no row of the unit has more than k valid keys (every
+// valid key is then selected).
 __host__ __device__ __forceinline__ int tile_group_size(int n_lo, int n_hi, int k) {
     if (n_hi <= k) return 0;
     const int n_ref = n_lo > k + 1 ? n_lo : k + 1;
