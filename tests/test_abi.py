@@ -99,3 +99,52 @@ def test_python_binding_refuses_cpu_tensors():
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(OSError):
         _native.load(str(tmp_path / "libssa.so"))
+
+
+def test_host_validation_of_the_later_calls():
+    """ssa_lowrank_project, ssa_sparse_attn_grouped, ssa_score_topk_smooth:
+    bad arguments are refused on the host before any launch."""
+    lib = ssa.load()
+    ok_ptr = V(4096)
+    bad_ptr = V(4100)
+    BF16, F32 = _native.SSA_BF16, _native.SSA_F32
+    # projection: d_model not a multiple of 64, P not 64/128, fp32, misaligned x, empty
+    assert lib.ssa_lowrank_project(ok_ptr, ok_ptr, BF16, 8, 100, 64, ok_ptr, None, None) == \
+        _native.SSA_ERR_UNSUPPORTED
+    assert lib.ssa_lowrank_project(ok_ptr, ok_ptr, BF16, 8, 128, 32, ok_ptr, None, None) == \
+        _native.SSA_ERR_UNSUPPORTED
+    assert lib.ssa_lowrank_project(ok_ptr, ok_ptr, F32, 8, 128, 64, ok_ptr, None, None) == \
+        _native.SSA_ERR_UNSUPPORTED
+    assert lib.ssa_lowrank_project(bad_ptr, ok_ptr, BF16, 8, 128, 64, ok_ptr, None, None) == \
+        _native.SSA_ERR_INVALID
+    assert lib.ssa_lowrank_project(ok_ptr, ok_ptr, BF16, -1, 128, 64, ok_ptr, None, None) == \
+        _native.SSA_ERR_INVALID
+    assert lib.ssa_lowrank_project(None, None, BF16, 0, 128, 64, None, None, None) == _native.SSA_OK
+    # grouped attention: H_kv or H_idx not dividing H, zero groups, unsupported D
+    args = lambda H, H_kv, H_idx, D: (ok_ptr, ok_ptr, ok_ptr, BF16, 1, H, H_kv, 8, 8, D,   # noqa: E731
+                                      ok_ptr, H_idx, 4, 0.0, ok_ptr, BF16, None, None)
+    assert lib.ssa_sparse_attn_grouped(*args(4, 3, 1, 64)) == _native.SSA_ERR_INVALID
+    assert lib.ssa_sparse_attn_grouped(*args(4, 2, 3, 64)) == _native.SSA_ERR_INVALID
+    assert lib.ssa_sparse_attn_grouped(*args(4, 0, 1, 64)) == _native.SSA_ERR_INVALID
+    assert lib.ssa_sparse_attn_grouped(*args(4, 2, 2, 96)) == _native.SSA_ERR_UNSUPPORTED
+    # smoothing: k + 1 beyond the largest k, k < 1, workspace too small
+    assert lib.ssa_score_topk_smooth(ok_ptr, ok_ptr, BF16, 1, 1, 8, 8, 64, 2048, 0, 0.0, 0.5,
+                                     ok_ptr, None, ok_ptr, 1 << 20, None, None) == \
+        _native.SSA_ERR_UNSUPPORTED
+    assert lib.ssa_score_topk_smooth(ok_ptr, ok_ptr, BF16, 1, 1, 8, 8, 64, 0, 0, 0.0, 0.5,
+                                     ok_ptr, None, ok_ptr, 1 << 20, None, None) == \
+        _native.SSA_ERR_INVALID
+    assert lib.ssa_score_topk_smooth(ok_ptr, ok_ptr, BF16, 1, 1, 8, 8, 64, 4, 0, 0.0, 0.5,
+                                     ok_ptr, None, ok_ptr, 16, None, None) == \
+        _native.SSA_ERR_WORKSPACE
+
+
+def test_smooth_workspace_covers_the_larger_selection():
+    """The smoothing call needs the workspace of a (k+1) selection plus room
+    for its scores; k + 1 beyond the largest supported k has no size."""
+    for (B, H, Tq, Tk, P, k) in [(1, 2, 1000, 1000, 64, 64), (1, 8, 4096, 4096, 64, 511),
+                                 (2, 3, 77, 400, 16, 40)]:
+        a = ssa.score_topk_workspace_size(B, H, Tq, Tk, P, k + 1, True)
+        s = ssa.score_topk_smooth_workspace_size(B, H, Tq, Tk, P, k, True)
+        assert s >= a + B * H * Tq * (k + 1) * 4
+    assert ssa.score_topk_smooth_workspace_size(1, 1, 8, 8, 64, 2048, True) == 0
