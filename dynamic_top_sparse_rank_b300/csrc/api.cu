@@ -47,10 +47,13 @@ int64_t rowwise_slots(int64_t rows) { return rows < kRowSlots ? rows : kRowSlots
 int64_t rowwise_stride(int Tk) { return round_up((int64_t)Tk, 64); }
 
 // The tensor-core path serves bf16 scorer inputs with d_proj 64 or 128 and
-// k <= 512 when there are enough query rows per head to fill 128-row tiles;
-// everything else (decode, fp32, other d_proj, larger k) runs row-wise.
-bool use_tile_path(int dtype, int P, int Tq, int Tk, int k) {
-    return dtype == SSA_BF16 && (P == 64 || P == 128) && k <= 512 && Tq >= 64 && Tk > 0;
+// k <= 512 when there are enough query rows per head to fill 128-row tiles,
+// and at most 2^31 - 1 rows of q_low and of k_low (its TMA coordinates,
+// head * T + row, are 32-bit); everything else (decode, fp32, other d_proj,
+// larger k) runs row-wise.
+bool use_tile_path(int dtype, int B, int H, int P, int Tq, int Tk, int k) {
+    return dtype == SSA_BF16 && (P == 64 || P == 128) && k <= 512 && Tq >= 64 && Tk > 0 &&
+           (int64_t)B * H * Tq <= INT32_MAX && (int64_t)B * H * Tk <= INT32_MAX;
 }
 
 }  // namespace
@@ -73,7 +76,7 @@ const char* ssa_status_string(int status) {
 static size_t path_workspace_bytes(int dtype, int B, int H, int Tq, int Tk, int P, int k) {
     const int64_t rows = (int64_t)B * H * Tq;
     if (rows == 0 || Tk == 0) return 256;
-    if (use_tile_path(dtype, P, Tq, Tk, k))
+    if (use_tile_path(dtype, B, H, P, Tq, Tk, k))
         return ssa::tile_workspace((int64_t)B * H, Tq, Tk, k).total;
     return (size_t)round_up(rowwise_slots(rows) * rowwise_stride(Tk) * 4, 256);
 }
@@ -103,7 +106,7 @@ ssa_status ssa_score_topk(const void* q_low, const void* k_low, int dtype, int B
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SSA_ERR_WORKSPACE;
     const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)P));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (!use_tile_path(dtype, P, Tq, Tk, k)) {
+    if (!use_tile_path(dtype, B, H, P, Tq, Tk, k)) {
         // Tk == 0: every row is empty; the row kernel writes the padding.
         cudaError_t e = ssa::topk_rows_dispatch(q_low, k_low, dtype == SSA_BF16, P, nullptr, rows,
                                                 nullptr, Tq, Tk, k, causal, sc, idx, score,
@@ -159,6 +162,7 @@ ssa_status ssa_lowrank_scores(const void* q_low, const void* k_low, int dtype, i
     if (dtype != SSA_BF16 || !(P == 64 || P == 128)) return SSA_ERR_UNSUPPORTED;
     const int64_t rows = (int64_t)B * H * Tq;
     if (rows == 0 || Tk == 0) return SSA_OK;
+    if (rows > INT32_MAX || (int64_t)B * H * Tk > INT32_MAX) return SSA_ERR_UNSUPPORTED;
     if (!S || !aligned(S, 4) || !q_low || !k_low || !aligned(q_low, 16) || !aligned(k_low, 16))
         return SSA_ERR_INVALID;
     if (dev_status && !aligned(dev_status, 4)) return SSA_ERR_INVALID;
@@ -212,6 +216,7 @@ ssa_status ssa_lowrank_project(const void* x, const void* W, int dtype, int64_t 
                                int P, void* out, int32_t* dev_status, void* stream) {
     if (rows < 0 || d_model <= 0 || !dtype_ok(dtype)) return SSA_ERR_INVALID;
     if (dtype != SSA_BF16 || !(P == 64 || P == 128) || d_model % 64 != 0) return SSA_ERR_UNSUPPORTED;
+    if (rows > INT32_MAX) return SSA_ERR_UNSUPPORTED;   // 32-bit TMA row coordinates
     if (rows == 0) return SSA_OK;
     if (!x || !W || !out || !aligned(x, 16) || !aligned(W, 16) || !aligned(out, 16))
         return SSA_ERR_INVALID;

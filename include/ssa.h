@@ -89,7 +89,7 @@ size_t ssa_score_topk_workspace_size(int B, int H, int Tq, int Tk, int P, int k,
  * the score of key j is s_j = fp32(sum_p q_low[b,h,i,p] * k_low[b,h,j,p]) *
  * scale, products and sums in fp32 (bf16 inputs are exact in fp32; integer
  * valued inputs give exact scores). For bf16 inputs with P in {64, 128},
- * k <= 512 and Tq >= 64 the sum runs on the tensor cores with fp32
+ * k <= 512, Tq >= 64 and B*H*Tq, B*H*Tk below 2^31 the sum runs on the tensor cores with fp32
  * accumulation in the hardware's order (the scores ssa_lowrank_scores
  * returns); otherwise as a sequential fp32 sum. The selection is exact for
  * the scores so computed. The call writes the k_eff = min(k,
@@ -194,7 +194,7 @@ ssa_status ssa_lowrank_scores(const void* q_low, const void* k_low, int dtype, i
  *            rows = B*H*T), 16-byte aligned
  *   W        device, bf16 [P, d_model] (a linear layer's weight), 16-byte aligned
  *   dtype    SSA_BF16 (SSA_F32 returns SSA_ERR_UNSUPPORTED)
- *   rows     >= 0
+ *   rows     0 <= rows <= 2^31 - 1 (larger: SSA_ERR_UNSUPPORTED)
  *   d_model  a positive multiple of 64
  *   P        64 or 128
  *   out      device, bf16 [rows, P], written, 16-byte aligned (feeds

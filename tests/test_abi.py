@@ -148,3 +148,17 @@ def test_smooth_workspace_covers_the_larger_selection():
         s = ssa.score_topk_smooth_workspace_size(B, H, Tq, Tk, P, k, True)
         assert s >= a + B * H * Tq * (k + 1) * 4
     assert ssa.score_topk_smooth_workspace_size(1, 1, 8, 8, 64, 2048, True) == 0
+
+
+def test_row_counts_beyond_32_bit_coordinates():
+    """The TMA paths address rows with 32-bit coordinates: a projection of
+    2^31 rows is refused, and a top-k with 2^31 scorer rows sizes (and would
+    run) the row-wise path instead of the tensor-core one."""
+    lib = ssa.load()
+    ok_ptr = V(4096)
+    assert lib.ssa_lowrank_project(ok_ptr, ok_ptr, _native.SSA_BF16, 1 << 31, 128, 64, ok_ptr,
+                                   None, None) == _native.SSA_ERR_UNSUPPORTED
+    big = ssa.score_topk_workspace_size(1, 32768, 65536, 64, 64, 64, True)   # 2^31 query rows
+    rowwise = 1024 * 64 * 4                                                    # 1024 slots of Tk keys
+    assert big == rowwise
+    assert ssa.score_topk_workspace_size(1, 32767, 65536, 64, 64, 64, True) > rowwise
