@@ -4,7 +4,10 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <float.h>
+#include <math.h>
 #include <stdint.h>
+#include <string.h>
 
 namespace ssa {
 
@@ -98,6 +101,55 @@ __host__ __device__ __forceinline__ int tile_cand_cap(int k) {
     int c = 32;
     while (c < k) c *= 2;
     return 2 * c;
+}
+
+// Bits of a float and the order-preserving map of the finite floats onto
+// uint32 used by the threshold search below (-0 and +0 get adjacent keys).
+__host__ __device__ __forceinline__ uint32_t tile_f32_bits(float f) {
+#ifdef __CUDA_ARCH__
+    return __float_as_uint(f);
+#else
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return u;
+#endif
+}
+
+__host__ __device__ __forceinline__ float tile_bits_f32(uint32_t u) {
+#ifdef __CUDA_ARCH__
+    return __uint_as_float(u);
+#else
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+#endif
+}
+
+// Threshold on the unscaled dot products: the smallest float x with
+// fl(x * scale) >= t (scale > 0). fl(x * scale) is non-decreasing in x, so
+// `raw >= x` decides `fl(raw * scale) >= t` exactly without a multiply per
+// score. t = -inf gives -FLT_MAX: every finite score qualifies, a masked
+// (-inf) one does not; +inf when no finite score reaches t. The answer is
+// found by bisection over the ordered finite floats (31 steps, once per row),
+// not by stepping from t / scale: when the products are subnormal many
+// consecutive x give the same product and the boundary can lie many ulps
+// below the quotient.
+__host__ __device__ __forceinline__ float tile_raw_threshold(float t, float scale) {
+    if (t == -INFINITY) return -FLT_MAX;
+    if (!(FLT_MAX * scale >= t)) return INFINITY;
+    if (-FLT_MAX * scale >= t) return -FLT_MAX;
+    // ordered keys: negative floats map to ~bits, non-negative ones to
+    // bits | 2^31; lo fails the test, hi passes it
+    uint32_t lo = ~tile_f32_bits(-FLT_MAX), hi = tile_f32_bits(FLT_MAX) | 0x80000000u;
+    while (hi - lo > 1) {
+        const uint32_t mid = lo + (hi - lo) / 2;
+        const float x = tile_bits_f32((mid & 0x80000000u) ? (mid & 0x7FFFFFFFu) : ~mid);
+        if (x * scale >= t)
+            hi = mid;
+        else
+            lo = mid;
+    }
+    return tile_bits_f32((hi & 0x80000000u) ? (hi & 0x7FFFFFFFu) : ~hi);
 }
 
 struct TileParams {

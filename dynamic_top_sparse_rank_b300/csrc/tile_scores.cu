@@ -203,18 +203,6 @@ SSA_DEVINL uint32_t ge_mask8(const float* v, float t) {
     return m;
 }
 
-// Smallest float x with fl(x * scale) >= t (scale > 0): fl(x * scale) is
-// non-decreasing in x, so `raw >= x` decides `fl(raw * scale) >= t` exactly
-// without a multiply per score.
-SSA_DEVINL float raw_threshold(float t, float scale) {
-    if (t == -INFINITY) return -FLT_MAX;   // every finite score qualifies, -inf (masked) does not
-    float x = t / scale;
-    for (int it = 0; it < 8 && x * scale < t; ++it) x = nextafterf(x, INFINITY);
-    for (int it = 0; it < 8 && nextafterf(x, -INFINITY) * scale >= t; ++it)
-        x = nextafterf(x, -INFINITY);
-    return x;
-}
-
 }  // namespace
 
 template <int P, int MODE>
@@ -500,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (MODE == MODE_COLLECT) {
                 if (row_ok) {
                     const uint32_t t32 = p.tau[row];
-                    t_raw = raw_threshold(t32 == 0 ? -INFINITY : order_key_f32(t32), p.scale);
+                    t_raw = tile_raw_threshold(t32 == 0 ? -INFINITY : order_key_f32(t32), p.scale);
                 }
             }
             row0 = row - lane;

@@ -7,8 +7,16 @@
 // index a unit writes to stay below the reserved stride. The key -> group map
 // is re-derived here from the score kernel's tile order (tile t of a unit goes
 // to TMEM buffer t % 2; chunk c of 32 keys; m = g / 32 consecutive tiles of a
-// buffer form a group), independently of tile_group_first_key.
+// buffer form a group), independently of tile_group_first_key. It also checks
+// the candidate threshold on the unscaled dot products (tile_raw_threshold):
+// for a bound t and scale s, a raw score x must pass `x >= threshold` exactly
+// when fl(x * s) >= t, or the candidate pass would drop a key of the top-k.
+// Host float arithmetic is IEEE single precision here, as the kernel's is
+// (no fast-math, no flush to zero).
+#include <cmath>
+#include <cstdint>
 #include <cstdio>
+#include <cstring>
 #include <vector>
 
 #include "tile.h"
@@ -105,6 +113,57 @@ int main() {
     }
     // 4. candidate capacity: each TMEM buffer's list holds at least k
     for (int k = 1; k <= 2048; ++k) CHECK(tile_cand_cap(k) / 2 >= k, "k %d cap %d", k, tile_cand_cap(k));
+    // 5. the raw threshold is the exact boundary of {x finite : fl(x * s) >= t}
+    {
+        auto passes = [](float x, float t, float s) { return x * s >= t; };
+        auto check_one = [&](float t, float s) {
+            const float x = tile_raw_threshold(t, s);
+            CHECK(x != -INFINITY && !std::isnan(x), "t %a s %a: threshold %a", t, s, x);
+            if (x == INFINITY) {   // no finite score reaches t
+                CHECK(!passes(FLT_MAX, t, s), "t %a s %a: +inf threshold but FLT_MAX passes", t, s);
+                return;
+            }
+            CHECK(passes(x, t, s), "t %a s %a: threshold %a fails", t, s, x);
+            if (x > -FLT_MAX) {
+                const float below = std::nextafter(x, -INFINITY);
+                CHECK(!passes(below, t, s), "t %a s %a: %a below the threshold %a passes", t, s,
+                      below, x);
+            }
+        };
+        auto from_bits = [](uint32_t u) {
+            float f;
+            std::memcpy(&f, &u, 4);
+            return f;
+        };
+        std::vector<float> scales = {0.25f, 1.0f / std::sqrt(32.0f), 0.125f, 1.0f / std::sqrt(128.0f),
+                                     1.0f, 1.25f, 10.0f, 0.01f, 3.0f, 1e-30f, 1e30f, FLT_MIN,
+                                     1e-40f, 0.1f * 0.125f, 1.0f / 0.1f * 0.125f};
+        uint64_t lcg = 0x9E3779B97F4A7C15ull;
+        auto next32 = [&]() {
+            lcg = lcg * 6364136223846793005ull + 1442695040888963407ull;
+            return static_cast<uint32_t>(lcg >> 32);
+        };
+        for (int i = 0; i < 200; ++i)   // log-uniform in [2^-100, 2^100)
+            scales.push_back(std::ldexp(1.0f + (next32() >> 9) * 0x1p-23f,
+                                        static_cast<int>(next32() % 200) - 100));
+        // every bound the selection can produce: an order key truncated to its
+        // high 16 bits, decoded back to a float (finite ones only)
+        for (uint32_t k16 = 1; k16 < 65536; ++k16) {
+            const uint32_t key = k16 << 16;
+            const uint32_t u = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
+            const float t = from_bits(u);
+            if (!std::isfinite(t)) continue;
+            for (float s : scales) check_one(t, s);
+        }
+        check_one(-INFINITY, 0.125f);
+        CHECK(tile_raw_threshold(-INFINITY, 0.125f) == -FLT_MAX, "t -inf must give -FLT_MAX");
+        // arbitrary finite bounds, subnormals included
+        for (int i = 0; i < 2000000; ++i) {
+            const float t = from_bits(next32());
+            if (!std::isfinite(t)) continue;
+            check_one(t, scales[next32() % scales.size()]);
+        }
+    }
     if (fails) {
         std::printf("FAILED %d\n", fails);
         return 1;
