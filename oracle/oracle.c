@@ -408,3 +408,187 @@ int oracle_project_rows(const double* x, const double* W, int64_t n, int64_t dm,
     for_rows(proj_row, &c, n, nthreads);
     return 0;
 }
+
+/* --------------------------------------------------------------- backward */
+
+/*
+ * Backward of the sparse attention under the straight-through estimator of
+ * mhpq.cn/news/1098205, section 2.3: the forward keeps its hard top-k; in the
+ * backward the selected (query, key) pairs pass their gradients exactly as the
+ * attention over those keys would, the keys a row did not select get nothing
+ * from it, and the scorer receives, for every selected pair, the gradient of
+ * that pair's attention logit (the route "through the attention weights of the
+ * selected positions"), zero for the pairs not selected.
+ *
+ * Row i with selected keys j_0 .. j_{m-1} (entries -1 skipped, repeated entries
+ * counted once per entry, as in the forward), logits l_t = scale * Q_i . K_{j_t},
+ * p = softmax(l), O_i = sum_t p_t V_{j_t}, and the incoming gradient dO_i:
+ *   dp_t  = dO_i . V_{j_t}
+ *   delta = sum_t p_t dp_t
+ *   dl_t  = p_t (dp_t - delta)              (softmax backward)
+ *   dQ_i  = scale * sum_t dl_t K_{j_t}
+ *   dK_j += scale * dl_t Q_i,   dV_j += p_t dO_i   for each (i, t) with j_t = j
+ *   dS[i][t] = dl_t  (0 in skipped slots)
+ */
+typedef struct {
+    const double* q_rows; /* [n, D] */
+    const double* K;      /* [Tk, D] */
+    const double* V;      /* [Tk, D] */
+    const double* dO;     /* [n, D] */
+    int64_t Tk;
+    int D, k;
+    const int32_t* idx;   /* [n, k] */
+    double scale;
+    double* dQ;           /* [n, D] */
+    double* dS;           /* [n, k] */
+    double* prob;         /* [n, k] softmax weights, 0 in skipped slots */
+    int64_t bad;
+    pthread_mutex_t mu;
+} bwd_ctx;
+
+/* Key of slot t of row r, or -1 when the slot is skipped (-1 or out of range). */
+static int64_t slot_key(const int32_t* idx, int k, int64_t Tk, int64_t r, int t) {
+    const int32_t j = idx[r * k + t];
+    return (j >= 0 && (int64_t)j < Tk) ? (int64_t)j : -1;
+}
+
+static double dot(const double* a, const double* b, int D) {
+    double acc = 0.0;
+    for (int d = 0; d < D; ++d) acc += a[d] * b[d];
+    return acc;
+}
+
+static void bwd_row(void* vctx, int64_t r) {
+    bwd_ctx* c = (bwd_ctx*)vctx;
+    const int k = c->k, D = c->D;
+    const double* q = c->q_rows + r * D;
+    const double* go = c->dO + r * D;
+    double* dq = c->dQ + r * D;
+    double* ds = c->dS + r * k;
+    double* p = c->prob + r * k;
+    int64_t bad = 0, m = 0;
+    double mx = -INFINITY;
+    for (int t = 0; t < k; ++t) {
+        ds[t] = 0.0;
+        p[t] = 0.0;
+        const int64_t j = slot_key(c->idx, k, c->Tk, r, t);
+        if (j < 0) {
+            if (c->idx[r * k + t] != -1) bad++;
+            continue;
+        }
+        p[t] = c->scale * dot(q, c->K + j * D, D); /* the logit, for now */
+        if (p[t] > mx) mx = p[t];
+        m++;
+    }
+    for (int d = 0; d < D; ++d) dq[d] = 0.0;
+    if (m > 0) {
+        double den = 0.0;
+        for (int t = 0; t < k; ++t) {
+            if (slot_key(c->idx, k, c->Tk, r, t) < 0) continue;
+            p[t] = exp(p[t] - mx);
+            den += p[t];
+        }
+        double delta = 0.0;
+        for (int t = 0; t < k; ++t) {
+            const int64_t j = slot_key(c->idx, k, c->Tk, r, t);
+            if (j < 0) continue;
+            p[t] /= den;
+            ds[t] = dot(go, c->V + j * D, D); /* dp_t, for now */
+            delta += p[t] * ds[t];
+        }
+        for (int t = 0; t < k; ++t) {
+            const int64_t j = slot_key(c->idx, k, c->Tk, r, t);
+            if (j < 0) continue;
+            ds[t] = p[t] * (ds[t] - delta);
+            for (int d = 0; d < D; ++d) dq[d] += c->scale * ds[t] * c->K[j * D + d];
+        }
+    }
+    if (bad) {
+        pthread_mutex_lock(&c->mu);
+        c->bad += bad;
+        pthread_mutex_unlock(&c->mu);
+    }
+}
+
+/*
+ * Gradients of n query rows of one head: dQ [n, D], dK and dV [Tk, D] (set
+ * here: zero, then the sum over every row and slot that selected the key), and
+ * dS [n, k], the gradient the straight-through estimator hands to each selected
+ * pair's score. scale <= 0 selects head_dim^-0.5. Returns the number of
+ * out-of-range entries (skipped), or -1 on bad arguments.
+ */
+int64_t oracle_attn_bwd_rows(const double* q_rows, int64_t n, const double* K, const double* V,
+                             int64_t Tk, int D, const int32_t* idx, int k, double scale,
+                             const double* dO, double* dQ, double* dK, double* dV, double* dS,
+                             int nthreads) {
+    if (!q_rows || !K || !V || !idx || !dO || !dQ || !dK || !dV || !dS || n < 0 || Tk < 0 ||
+        D < 1 || k < 1)
+        return -1;
+    bwd_ctx c;
+    c.q_rows = q_rows;
+    c.K = K;
+    c.V = V;
+    c.dO = dO;
+    c.Tk = Tk;
+    c.D = D;
+    c.k = k;
+    c.idx = idx;
+    c.scale = scale > 0.0 ? scale : 1.0 / sqrt((double)D);
+    c.dQ = dQ;
+    c.dS = dS;
+    c.prob = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * (size_t)k);
+    if (!c.prob) return -1;
+    c.bad = 0;
+    pthread_mutex_init(&c.mu, NULL);
+    for_rows(bwd_row, &c, n, nthreads);
+    pthread_mutex_destroy(&c.mu);
+    /* the key-side sums, one row and slot at a time */
+    for (int64_t e = 0; e < Tk * D; ++e) {
+        dK[e] = 0.0;
+        dV[e] = 0.0;
+    }
+    for (int64_t r = 0; r < n; ++r) {
+        for (int t = 0; t < k; ++t) {
+            const int64_t j = slot_key(idx, k, Tk, r, t);
+            if (j < 0) continue;
+            for (int d = 0; d < D; ++d) {
+                dK[j * D + d] += c.scale * dS[r * k + t] * q_rows[r * D + d];
+                dV[j * D + d] += c.prob[r * k + t] * dO[r * D + d];
+            }
+        }
+    }
+    free(c.prob);
+    return c.bad;
+}
+
+/*
+ * The scorer's gradients under the same estimator: the score of a selected
+ * pair, S = scale * q_low_i . k_low_j (mhpq.cn/news/1098205, section 2.2),
+ * receives dS[i][t], and a pair not selected receives nothing, so
+ *   dq_low_i  = scale * sum_t dS[i][t] k_low_{j_t}
+ *   dk_low_j += scale * dS[i][t] q_low_i   for each (i, t) with j_t = j.
+ * q_low [n, P], k_low [Tk, P], idx and dS [n, k]; dq_low [n, P] and dk_low
+ * [Tk, P] are set here. scale <= 0 selects d_proj^-0.5 rounded to fp32 (the
+ * factor the forward scores use). Returns 0, or 1 on bad arguments.
+ */
+int oracle_scorer_bwd_rows(const double* q_low, int64_t n, const double* k_low, int64_t Tk, int P,
+                           const int32_t* idx, int k, double scale, const double* dS,
+                           double* dq_low, double* dk_low) {
+    if (!q_low || !k_low || !idx || !dS || !dq_low || !dk_low || n < 0 || Tk < 0 || P < 1 || k < 1)
+        return 1;
+    const double s = scale > 0.0 ? scale : (double)(float)(1.0 / sqrt((double)P));
+    for (int64_t e = 0; e < n * P; ++e) dq_low[e] = 0.0;
+    for (int64_t e = 0; e < Tk * P; ++e) dk_low[e] = 0.0;
+    for (int64_t r = 0; r < n; ++r) {
+        for (int t = 0; t < k; ++t) {
+            const int64_t j = slot_key(idx, k, Tk, r, t);
+            if (j < 0) continue;
+            const double g = s * dS[r * k + t];
+            for (int p = 0; p < P; ++p) {
+                dq_low[r * P + p] += g * k_low[j * P + p];
+                dk_low[j * P + p] += g * q_low[r * P + p];
+            }
+        }
+    }
+    return 0;
+}

@@ -6,8 +6,8 @@ and converts tensors to float64 numpy arrays (exact for bf16 and fp32 inputs).
 Only the tests, the smoke check and the benchmark's CPU-baseline leg may import
 it; the CUDA library never does, and shares no code with it.
 
-Parity status: score_topk, sparse_attn, window_attn and lowrank_project are
-pinned by the
+Parity status: score_topk, sparse_attn, window_attn, lowrank_project and the
+backward (sparse_attn_bwd, scorer_bwd) are pinned by the
 ``-m "not gpu"`` tests (brute force, closed forms, special cases and an
 independent dense masked attention); none is pinned to printed values, because
 the pages print none for this path.
@@ -52,6 +52,11 @@ def _load():
         lib.oracle_scores_rows.argtypes = [P, P, i64, P, i64, i64, i32, i32, f32, P, i32]
         lib.oracle_project_rows.argtypes = [P, P, i64, i64, i32, P, i32]
         lib.oracle_scores_rows.restype = i32
+        lib.oracle_attn_bwd_rows.argtypes = [P, i64, P, P, i64, i32, P, i32, f64, P, P, P, P, P,
+                                             i32]
+        lib.oracle_attn_bwd_rows.restype = i64
+        lib.oracle_scorer_bwd_rows.argtypes = [P, i64, P, i64, i32, P, i32, f64, P, P, P]
+        lib.oracle_scorer_bwd_rows.restype = i32
         _lib = lib
     return _lib
 
@@ -177,6 +182,57 @@ def lowrank_project(x, W, nthreads: int | None = None):
     return out.reshape(lead + (P,))
 
 
+def attn_bwd_rows(q_rows, K, V, idx, dO, scale: float = 0.0, nthreads: int | None = None):
+    """Backward of one head's sparse attention under the straight-through
+    estimator (mhpq.cn/news/1098205, section 2.3; the formulas are in
+    oracle.c). q_rows and dO [n, D], K and V [Tk, D], idx [n, k].
+
+    Returns (dQ [n, D], dK [Tk, D], dV [Tk, D], dS [n, k], bad): float64, dS the
+    gradient each selected pair's score receives, bad the count of skipped
+    out-of-range entries."""
+    q = _f64(q_rows)
+    Kd = _f64(K)
+    Vd = _f64(V)
+    g = _f64(dO)
+    ix = np.ascontiguousarray(np.asarray(idx, dtype=np.int32))
+    n, D = q.shape
+    k = ix.shape[1]
+    Tk = Kd.shape[0]
+    assert g.shape == (n, D) and ix.shape[0] == n and Vd.shape == Kd.shape
+    dQ = np.empty((n, D), np.float64)
+    dK = np.empty((Tk, D), np.float64)
+    dV = np.empty((Tk, D), np.float64)
+    dS = np.empty((n, k), np.float64)
+    bad = _load().oracle_attn_bwd_rows(_ptr(q), n, _ptr(Kd), _ptr(Vd), Tk, D, _ptr(ix), k,
+                                       float(scale), _ptr(g), _ptr(dQ), _ptr(dK), _ptr(dV),
+                                       _ptr(dS), nthreads or default_threads())
+    if bad < 0:
+        raise ValueError("oracle_attn_bwd_rows: bad arguments")
+    return dQ, dK, dV, dS, int(bad)
+
+
+def scorer_bwd_rows(q_low_rows, k_low, idx, dS, scale: float = 0.0):
+    """The scorer's gradients of one head under the straight-through estimator:
+    the selected pairs' scores receive dS [n, k]. q_low_rows [n, P], k_low
+    [Tk, P]; scale <= 0 selects d_proj^-0.5 (as an fp32 factor, like the
+    forward). Returns float64 (dq_low [n, P], dk_low [Tk, P])."""
+    q = _f64(q_low_rows)
+    kl = _f64(k_low)
+    g = _f64(dS)
+    ix = np.ascontiguousarray(np.asarray(idx, dtype=np.int32))
+    n, P = q.shape
+    Tk = kl.shape[0]
+    k = ix.shape[1]
+    assert kl.shape[1] == P and ix.shape[0] == n and g.shape == (n, k)
+    dq = np.empty((n, P), np.float64)
+    dk = np.empty((Tk, P), np.float64)
+    rc = _load().oracle_scorer_bwd_rows(_ptr(q), n, _ptr(kl), Tk, P, _ptr(ix), k, float(scale),
+                                        _ptr(g), _ptr(dq), _ptr(dk))
+    if rc != 0:
+        raise ValueError("oracle_scorer_bwd_rows: bad arguments")
+    return dq, dk
+
+
 def round_bf16(v) -> np.ndarray:
     """float64 -> the nearest bf16 value (ties to even), returned as float64.
     bf16 keeps 8 significant bits: a value m * 2^e with m in [0.5, 1) becomes
@@ -292,3 +348,37 @@ def window_attn(Q, K, V, w_left: int, w_right: int, scale: float = 0.0, rows=Non
             for t, i in enumerate(qi):
                 O[where[(b * H + h) * T + int(i)]] = o_[t]
     return O
+
+
+def sparse_attn_bwd(Q, K, V, idx, dO, scale: float = 0.0, nthreads: int | None = None):
+    """Backward of sparse attention over [B,H,T,D] with idx [B,H,Tq,k] under the
+    straight-through estimator. Returns float64 (dQ, dK, dV, dS)."""
+    B, H, Tq, D = Q.shape
+    Tk = K.shape[2]
+    k = np.asarray(idx).shape[-1]
+    dQ = np.empty((B, H, Tq, D), np.float64)
+    dK = np.empty((B, H, Tk, D), np.float64)
+    dV = np.empty((B, H, Tk, D), np.float64)
+    dS = np.empty((B, H, Tq, k), np.float64)
+    idx = np.asarray(idx)
+    for b in range(B):
+        for h in range(H):
+            dQ[b, h], dK[b, h], dV[b, h], dS[b, h], _ = attn_bwd_rows(
+                Q[b, h], K[b, h], V[b, h], idx[b, h], dO[b, h], scale, nthreads)
+    return dQ, dK, dV, dS
+
+
+def scorer_bwd(q_low, k_low, idx, dS, scale: float = 0.0):
+    """The scorer's gradients over [B,H,T,P] with idx and dS [B,H,Tq,k]; float64
+    (dq_low, dk_low)."""
+    B, H, Tq, P = q_low.shape
+    Tk = k_low.shape[2]
+    dq = np.empty((B, H, Tq, P), np.float64)
+    dk = np.empty((B, H, Tk, P), np.float64)
+    idx = np.asarray(idx)
+    dS = np.asarray(dS)
+    for b in range(B):
+        for h in range(H):
+            dq[b, h], dk[b, h] = scorer_bwd_rows(q_low[b, h], k_low[b, h], idx[b, h], dS[b, h],
+                                                 scale)
+    return dq, dk
