@@ -40,6 +40,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 bool dtype_ok(int d) { return d == SSA_F32 || d == SSA_BF16; }
 bool p_ok(int P) { return P == 16 || P == 32 || P == 64 || P == 128; }
 bool d_ok(int D) { return D == 64 || D == 128; }
+// A scale is a finite factor (<= 0 selects the default); NaN and inf are rejected.
+bool scale_ok(float s) { return isfinite(s); }
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 // Row-wise path: one slot of Tk 32-bit keys per concurrently processed row.
@@ -94,7 +96,8 @@ ssa_status ssa_score_topk(const void* q_low, const void* k_low, int dtype, int B
                           int Tk, int P, int k, int causal, float scale, int32_t* idx,
                           float* score, void* workspace, size_t workspace_bytes,
                           int32_t* dev_status, void* stream) {
-    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || !dtype_ok(dtype) || k < 1) return SSA_ERR_INVALID;
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || !dtype_ok(dtype) || k < 1 || !scale_ok(scale))
+        return SSA_ERR_INVALID;
     if (!p_ok(P) || k > kMaxK) return SSA_ERR_UNSUPPORTED;
     const int64_t rows = (int64_t)B * H * Tq;
     if (rows == 0) return SSA_OK;
@@ -157,7 +160,8 @@ ssa_status ssa_score_topk(const void* q_low, const void* k_low, int dtype, int B
 ssa_status ssa_lowrank_scores(const void* q_low, const void* k_low, int dtype, int B, int H,
                               int Tq, int Tk, int P, int causal, float scale, float* S,
                               int32_t* dev_status, void* stream) {
-    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || !dtype_ok(dtype)) return SSA_ERR_INVALID;
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || !dtype_ok(dtype) || !scale_ok(scale))
+        return SSA_ERR_INVALID;
     if (!p_ok(P)) return SSA_ERR_UNSUPPORTED;
     if (dtype != SSA_BF16 || !(P == 64 || P == 128)) return SSA_ERR_UNSUPPORTED;
     const int64_t rows = (int64_t)B * H * Tq;
@@ -182,7 +186,7 @@ ssa_status ssa_lowrank_scores(const void* q_low, const void* k_low, int dtype, i
 
 size_t ssa_score_topk_smooth_workspace_size(int B, int H, int Tq, int Tk, int P, int k,
                                             int causal) {
-    if (k < 1 || k + 1 > kMaxK) return 0;
+    if (k < 1 || k >= kMaxK) return 0;   // the selection runs with k + 1 <= kMaxK
     const size_t a = ssa_score_topk_workspace_size(B, H, Tq, Tk, P, k + 1, causal);
     if (a == 0) return 0;
     const int64_t rows = (int64_t)B * H * Tq;
@@ -193,8 +197,10 @@ ssa_status ssa_score_topk_smooth(const void* q_low, const void* k_low, int dtype
                                  int Tq, int Tk, int P, int k, int causal, float scale,
                                  float delta, int32_t* idx, float* score, void* workspace,
                                  size_t workspace_bytes, int32_t* dev_status, void* stream) {
-    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || !dtype_ok(dtype) || k < 1) return SSA_ERR_INVALID;
-    if (!p_ok(P) || k + 1 > kMaxK) return SSA_ERR_UNSUPPORTED;
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || !dtype_ok(dtype) || k < 1 || !scale_ok(scale) ||
+        isnan(delta))
+        return SSA_ERR_INVALID;
+    if (!p_ok(P) || k >= kMaxK) return SSA_ERR_UNSUPPORTED;
     const int64_t rows = (int64_t)B * H * Tq;
     if (rows == 0) return SSA_OK;
     const size_t a = ssa_score_topk_workspace_size(B, H, Tq, Tk, P, k + 1, causal);
@@ -229,7 +235,8 @@ ssa_status ssa_lowrank_project(const void* x, const void* W, int dtype, int64_t 
 ssa_status ssa_sparse_attn(const void* Q, const void* K, const void* V, int dtype, int B, int H,
                            int Tq, int Tk, int D, const int32_t* idx, int k, float scale, void* O,
                            int out_dtype, int32_t* dev_status, void* stream) {
-    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || k < 1 || !dtype_ok(dtype) || !dtype_ok(out_dtype))
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || k < 1 || !dtype_ok(dtype) || !dtype_ok(out_dtype) ||
+        !scale_ok(scale))
         return SSA_ERR_INVALID;
     if (!d_ok(D)) return SSA_ERR_UNSUPPORTED;
     const int64_t rows = (int64_t)B * H * Tq;
@@ -251,7 +258,7 @@ ssa_status ssa_sparse_attn_grouped(const void* Q, const void* K, const void* V, 
                                    int H_idx, int k, float scale, void* O, int out_dtype,
                                    int32_t* dev_status, void* stream) {
     if (B < 0 || H < 1 || H_kv < 1 || H_idx < 1 || Tq < 0 || Tk < 0 || k < 1 || !dtype_ok(dtype) ||
-        !dtype_ok(out_dtype) || H % H_kv != 0 || H % H_idx != 0)
+        !dtype_ok(out_dtype) || H % H_kv != 0 || H % H_idx != 0 || !scale_ok(scale))
         return SSA_ERR_INVALID;
     if (!d_ok(D)) return SSA_ERR_UNSUPPORTED;
     const int64_t rows = (int64_t)B * H * Tq;
@@ -273,7 +280,7 @@ ssa_status ssa_window_attn(const void* Q, const void* K, const void* V, int dtyp
                            int T, int D, int w_left, int w_right, float scale, void* O,
                            int out_dtype, int32_t* dev_status, void* stream) {
     if (B < 0 || H < 0 || T < 0 || w_left < 0 || w_right < 0 || !dtype_ok(dtype) ||
-        !dtype_ok(out_dtype))
+        !dtype_ok(out_dtype) || !scale_ok(scale))
         return SSA_ERR_INVALID;
     if (!d_ok(D)) return SSA_ERR_UNSUPPORTED;
     const int64_t rows = (int64_t)B * H * T;

@@ -62,7 +62,8 @@ extern "C" ssa_status ssa_score_topk_noalloc(const void* q_low, const void* k_lo
                                              float scale, int32_t* idx, float* score,
                                              int32_t* dev_status, void* stream) {
     (void)dev_status;
-    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || k < 1 || (dtype != SSA_F32 && dtype != SSA_BF16))
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || k < 1 || (dtype != SSA_F32 && dtype != SSA_BF16) ||
+        !isfinite(scale))
         return SSA_ERR_INVALID;
     if (!(P == 16 || P == 32 || P == 64 || P == 128) || k > 2048) return SSA_ERR_UNSUPPORTED;
     const int64_t rows = (int64_t)B * H * Tq;

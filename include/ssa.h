@@ -24,8 +24,9 @@
  *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
  *    asynchronous on that stream and return after the launch.
  *  - Host-detectable errors (null pointers, unsupported sizes, misalignment,
- *    a workspace that is too small) return a status synchronously and launch
- *    nothing. A failed launch returns SSA_ERR_CUDA.
+ *    a workspace that is too small, a NaN or infinite `scale` or a NaN
+ *    `delta`) return a status synchronously and launch nothing. A failed
+ *    launch returns SSA_ERR_CUDA.
  *  - Errors found on the device (an index out of range, a bounded wait that
  *    ran out) never trap: the kernel ORs a bit into *dev_status (an int32 in
  *    device memory, may be NULL) and carries on or returns. The caller clears

@@ -162,3 +162,38 @@ def test_row_counts_beyond_32_bit_coordinates():
     rowwise = 1024 * 64 * 4                                                    # 1024 slots of Tk keys
     assert big == rowwise
     assert ssa.score_topk_workspace_size(1, 32767, 65536, 64, 64, 64, True) > rowwise
+
+
+@pytest.mark.parametrize("bad", [float("nan"), float("inf"), float("-inf")])
+def test_non_finite_scale_is_refused(bad):
+    """A NaN or infinite scale (or a NaN smoothing threshold) is an invalid
+    argument for every call that takes one; nothing is launched."""
+    lib = ssa.load()
+    ok = V(4096)
+    BF16, INV = _native.SSA_BF16, _native.SSA_ERR_INVALID
+    assert lib.ssa_score_topk(ok, ok, BF16, 1, 1, 8, 8, 64, 4, 0, bad, ok, None, ok, 1 << 20,
+                              None, None) == INV
+    assert lib.ssa_score_topk_noalloc(ok, ok, BF16, 1, 1, 8, 8, 64, 4, 0, bad, ok, None, None,
+                                      None) == INV
+    assert lib.ssa_lowrank_scores(ok, ok, BF16, 1, 1, 8, 8, 64, 0, bad, ok, None, None) == INV
+    assert lib.ssa_score_topk_smooth(ok, ok, BF16, 1, 1, 8, 8, 64, 4, 0, bad, 0.5, ok, None, ok,
+                                     1 << 20, None, None) == INV
+    assert lib.ssa_sparse_attn(ok, ok, ok, BF16, 1, 1, 8, 8, 64, ok, 4, bad, ok, BF16, None,
+                               None) == INV
+    assert lib.ssa_sparse_attn_grouped(ok, ok, ok, BF16, 1, 4, 2, 8, 8, 64, ok, 1, 4, bad, ok,
+                                       BF16, None, None) == INV
+    assert lib.ssa_window_attn(ok, ok, ok, BF16, 1, 1, 8, 64, 2, 2, bad, ok, BF16, None,
+                               None) == INV
+    if bad != bad:   # NaN threshold
+        assert lib.ssa_score_topk_smooth(ok, ok, BF16, 1, 1, 8, 8, 64, 4, 0, 0.0, bad, ok, None,
+                                         ok, 1 << 20, None, None) == INV
+
+
+def test_smoothing_k_at_the_int_limit_is_unsupported():
+    """k + 1 must not overflow: the largest int k is refused as too large."""
+    lib = ssa.load()
+    ok = V(4096)
+    assert lib.ssa_score_topk_smooth(ok, ok, _native.SSA_BF16, 1, 1, 8, 8, 64, 2 ** 31 - 1, 0,
+                                     0.0, 0.5, ok, None, ok, 1 << 20, None, None) == \
+        _native.SSA_ERR_UNSUPPORTED
+    assert ssa.score_topk_smooth_workspace_size(1, 1, 8, 8, 64, 2 ** 31 - 1, True) == 0
