@@ -71,3 +71,22 @@ def test_projection_workload_bytes():
     traffic = 2.0 * rows * DM + 2.0 * P * DM + 2.0 * rows * P
     assert abs(traffic - 2.181e9) / 2.181e9 < 1e-3
     assert DM % 64 == 0 and P in (64, 128)
+
+
+def test_clock_samples_summary():
+    """nvidia-smi CSV lines (noheader, nounits) -> median SM clock, max clock,
+    the throttle reasons seen active; malformed lines are skipped."""
+    lines = [
+        "0, 2032, 2032, 812.40, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n",
+        "0, 1980, 2032, 1099.1, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n",
+        "0, 2010, 2032, 1050.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n",
+        "garbage\n",
+        "0, [N/A], 2032, 1.0, 0x0, Not Active, Active, Not Active, Not Active\n",
+    ]
+    c = bench.parse_clock_samples(lines)
+    assert c["samples"] == 3 and c["sm_mhz"] == 2010.0 and c["sm_max_mhz"] == 2032.0
+    assert c["reasons"] == ["sw_power_cap"]
+    assert bench.parse_clock_samples(["x\n"]) is None
+    hot = lines[0].replace("Not Active, Not Active, Not Active, Not Active",
+                           "Active, Not Active, Active, Not Active")
+    assert bench.parse_clock_samples([hot])["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
