@@ -108,6 +108,29 @@ def test_topk_scale_and_order_invariants():
             assert np.all((S[rest] < S[last]) | ((S[rest] == S[last]) & (rest > last)))
 
 
+def test_topk_second_routine_on_the_fp32_workload():
+    """A second, independent selection on the whole fp32 workload
+    (B1 H2 T1024, d_proj 16, k 32, integer data): int64 dot products by a
+    library matmul, then a stable lexicographic sort on (-score, index). The
+    scale 16^-0.5 = 1/4 is exact, so ranking the integer dots is ranking the
+    scores; the oracle must agree bit for bit, scores included."""
+    w = WORKLOADS["topk_f32_t1024_k32"]
+    q, kl = make_scorer_inputs(w)
+    idx, sc = oracle.score_topk(q, kl, w.k, w.causal)
+    qi = q.numpy().astype(np.int64)
+    ki = kl.numpy().astype(np.int64)
+    assert np.array_equal(qi, q.numpy()) and np.array_equal(ki, kl.numpy())   # integer data
+    for b in range(w.B):
+        for h in range(w.H):
+            dots = qi[b, h] @ ki[b, h].T                     # [Tq, Tk], exact
+            j = np.arange(w.Tk)
+            for i in range(w.Tq):
+                order = np.lexsort((j, -dots[i]))            # last key is primary
+                top = order[:w.k]
+                np.testing.assert_array_equal(idx[b, h, i], top.astype(np.int32))
+                np.testing.assert_array_equal(sc[b, h, i], (dots[i, top] / 4.0).astype(np.float32))
+
+
 def test_topk_all_ties_lower_index_wins():
     Tq, Tk, k = 10, 50, 7
     q = np.zeros((Tq, 16))
