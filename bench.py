@@ -88,10 +88,14 @@ def algorithmic(w):
                 "scored_pairs": 0,
                 "window_bytes": float(esize * w.D * w.B * w.H * (w.Tq * 2 + w.Tk * 2))}
     pairs, sel = valid_pairs(w)
+    rows = w.B * w.H * w.Tq
     return {
         "score_flops": 2.0 * w.P * pairs,
         "attn_flops": 4.0 * w.D * sel,
         "gather_bytes": 2.0 * sel * w.D * esize,    # selected K and V rows
+        # the attention's other traffic: the index lists (int32), Q read and O
+        # written once (in the input dtype)
+        "gather_aux_bytes": float(rows * w.k * 4 + 2 * rows * w.D * esize),
         "selected_pairs": sel,
         "scored_pairs": pairs,
     }
@@ -432,6 +436,7 @@ def run_ours(args, rank, world, local_rank):
     if smooth:   # the gather runs over k + 1 slots per row
         alg_g = algorithmic(w.with_(k=w.k + 1))
         alg["gather_bytes"], alg["attn_flops"] = alg_g["gather_bytes"], alg_g["attn_flops"]
+        alg["gather_aux_bytes"] = alg_g["gather_aux_bytes"]
     if shared:   # one scorer for all heads
         alg["score_flops"] /= w.H
         alg["scored_pairs"] //= w.H
@@ -459,6 +464,7 @@ def run_ours(args, rank, world, local_rank):
         elif name == "sparse_attn":
             ph["gbs"] = alg["gather_bytes"] / (ms * 1e-3) / 1e9
             ph["frac_hbm"] = ph["gbs"] / pk["hbm_gbs"]
+            ph["aux_bytes"] = alg.get("gather_aux_bytes")   # idx, Q and O, beside the gather
         else:
             ph["gbs"] = alg["window_bytes"] / (ms * 1e-3) / 1e9
             ph["frac_hbm"] = ph["gbs"] / pk["hbm_gbs"]

@@ -90,3 +90,13 @@ def test_clock_samples_summary():
     hot = lines[0].replace("Not Active, Not Active, Not Active, Not Active",
                            "Active, Not Active, Active, Not Active")
     assert bench.parse_clock_samples([hot])["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+
+
+def test_gather_aux_bytes():
+    """Besides the selected K/V rows the attention reads the index lists
+    (int32) and Q and writes O: at 128K 2.15 GB + 2 x 268 MB."""
+    w = WORKLOADS["topk_causal_bf16_t128k_k512_planted"]
+    alg = bench.algorithmic(w)
+    rows = w.B * w.H * w.Tq
+    assert alg["gather_aux_bytes"] == rows * w.k * 4 + 2 * rows * w.D * 2
+    assert abs(alg["gather_aux_bytes"] - 2.684e9) / 2.684e9 < 1e-3
