@@ -25,7 +25,9 @@ SSA_DEV_BAD_INDEX, SSA_DEV_WAIT_LIMIT, SSA_DEV_OVERFLOW = 0x1, 0x2, 0x4
 EXPORTS = ("ssa_version", "ssa_status_string", "ssa_score_topk_workspace_size", "ssa_score_topk",
            "ssa_sparse_attn", "ssa_window_attn", "ssa_score_topk_noalloc", "ssa_lowrank_scores",
            "ssa_lowrank_project", "ssa_sparse_attn_grouped", "ssa_score_topk_smooth",
-           "ssa_score_topk_smooth_workspace_size", "ssa_trace_begin", "ssa_trace_end")
+           "ssa_score_topk_smooth_workspace_size", "ssa_trace_begin", "ssa_trace_end",
+           "ssa_sparse_attn_bwd_workspace_size", "ssa_sparse_attn_bwd",
+           "ssa_scorer_bwd_workspace_size", "ssa_scorer_bwd")
 
 # Fixed scratch of ssa_score_topk_noalloc and the largest Tk it accepts.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -80,6 +82,15 @@ def load(path: str | None = None):
     lib.ssa_score_topk_smooth.argtypes = [V, V, I, I, I, I, I, I, I, I, F, F, V, V, V, Z, V, V]
     lib.ssa_lowrank_project.restype = I
     lib.ssa_lowrank_project.argtypes = [V, V, I, ctypes.c_int64, I, I, V, V, V]
+    lib.ssa_sparse_attn_bwd_workspace_size.restype = Z
+    lib.ssa_sparse_attn_bwd_workspace_size.argtypes = [I, I, I, I, I]
+    lib.ssa_sparse_attn_bwd.restype = I
+    lib.ssa_sparse_attn_bwd.argtypes = [V, V, V, V, I, I, I, I, I, I, V, I, F, V, V, V, V, V, V, Z,
+                                        V, V]
+    lib.ssa_scorer_bwd_workspace_size.restype = Z
+    lib.ssa_scorer_bwd_workspace_size.argtypes = [I, I, I, I, I]
+    lib.ssa_scorer_bwd.restype = I
+    lib.ssa_scorer_bwd.argtypes = [V, V, I, I, I, I, I, I, V, I, V, F, V, V, V, Z, V, V]
     if path is None:
         _lib = lib
     return lib
@@ -355,6 +366,71 @@ def ssa_window_attn(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, w_left: i
 
 class _TraceRecord(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 56), ("ms", ctypes.c_float)]
+
+
+def ssa_sparse_attn_bwd(Q, K, V, idx, dO, scale: float = 0.0, workspace=None,
+                        dev_status=None, with_prob: bool = False):
+    """Gradients of ssa_sparse_attn under the straight-through estimator.
+
+    Returns fp32 (dQ [B,H,Tq,D], dK, dV [B,H,Tk,D], dS [B,H,Tq,k]) (+ prob)."""
+    lib = load()
+    dev = _dev(Q, K, V, idx, dO, workspace, dev_status)
+    if not (Q.dtype == K.dtype == V.dtype == dO.dtype):
+        raise TypeError("Q, K, V, dO must share a dtype")
+    if idx.dtype != torch.int32:
+        raise TypeError("idx must be int32")
+    B, H, Tq, D = Q.shape
+    Tk = K.shape[2]
+    if tuple(K.shape) != (B, H, Tk, D) or tuple(V.shape) != (B, H, Tk, D) or \
+            tuple(dO.shape) != (B, H, Tq, D):
+        raise ValueError("K/V/dO shapes do not match Q")
+    if idx.shape[:3] != (B, H, Tq):
+        raise ValueError("idx shape %s does not match Q" % (tuple(idx.shape),))
+    k = idx.shape[3]
+    f32 = dict(dtype=torch.float32, device=dev)
+    dQ = torch.empty((B, H, Tq, D), **f32)
+    dK = torch.empty((B, H, Tk, D), **f32)
+    dV = torch.empty((B, H, Tk, D), **f32)
+    dS = torch.empty((B, H, Tq, k), **f32)
+    prob = torch.empty((B, H, Tq, k), **f32) if with_prob else None
+    need = int(lib.ssa_sparse_attn_bwd_workspace_size(B, H, Tq, Tk, k))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = lib.ssa_sparse_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _dt(Q), B, H, Tq, Tk, D,
+                                 _ptr(idx), k, float(scale), _ptr(dQ), _ptr(dK), _ptr(dV),
+                                 _ptr(dS), _ptr(prob), _ptr(workspace), wbytes,
+                                 _ptr(dev_status), _stream(dev))
+    _check(rc, "ssa_sparse_attn_bwd")
+    return (dQ, dK, dV, dS, prob) if with_prob else (dQ, dK, dV, dS)
+
+
+def ssa_scorer_bwd(q_low, k_low, idx, dS, scale: float = 0.0, workspace=None, dev_status=None):
+    """The scorer's gradients under the straight-through estimator; fp32
+    (dq_low [B,H,Tq,P], dk_low [B,H,Tk,P])."""
+    lib = load()
+    dev = _dev(q_low, k_low, idx, dS, workspace, dev_status)
+    if q_low.dtype != k_low.dtype:
+        raise TypeError("q_low and k_low must share a dtype")
+    if idx.dtype != torch.int32 or dS.dtype != torch.float32:
+        raise TypeError("idx must be int32 and dS float32")
+    B, H, Tq, P = q_low.shape
+    Tk = k_low.shape[2]
+    k = idx.shape[3]
+    if tuple(dS.shape) != tuple(idx.shape) or idx.shape[:3] != (B, H, Tq):
+        raise ValueError("idx/dS shapes do not match q_low")
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq = torch.empty((B, H, Tq, P), **f32)
+    dk = torch.empty((B, H, Tk, P), **f32)
+    need = int(lib.ssa_scorer_bwd_workspace_size(B, H, Tq, Tk, k))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = lib.ssa_scorer_bwd(_ptr(q_low), _ptr(k_low), _dt(q_low), B, H, Tq, Tk, P, _ptr(idx), k,
+                            _ptr(dS), float(scale), _ptr(dq), _ptr(dk), _ptr(workspace), wbytes,
+                            _ptr(dev_status), _stream(dev))
+    _check(rc, "ssa_scorer_bwd")
+    return dq, dk
 
 
 def trace_begin():

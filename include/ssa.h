@@ -316,6 +316,66 @@ ssa_status ssa_score_topk_noalloc(const void* q_low, const void* k_low, int dtyp
                                   int32_t* idx, float* score, int32_t* dev_status, void* stream);
 
 /*
+ * ssa_sparse_attn_bwd — gradients of ssa_sparse_attn under the straight-through
+ * estimator.
+ *
+ * Source: mhpq.cn/news/1098205, section 2.3: the forward keeps a hard top-k;
+ * in the backward the selected positions pass their gradients normally and
+ * the others get none, and the scorer's gradient arrives through the attention
+ * weights of the selected positions. Read as: dQ, dK, dV are the exact
+ * gradients of the forward with the index lists held fixed, and the score of
+ * each selected pair receives the gradient of that pair's attention logit,
+ *   dS[b,h,i,t] = p_t (dO_i . V_{j_t} - sum_u p_u dO_i . V_{j_u}),
+ * with p the row's softmax weights; 0 in slots holding -1.
+ *
+ *   Q, dO      device, [B, H, Tq, D]; K, V device, [B, H, Tk, D]; all `dtype`
+ *   idx        device, int32 [B, H, Tq, k], as for ssa_sparse_attn (-1 skipped,
+ *              repeats counted per entry, other out-of-range entries skipped
+ *              and reported with SSA_DEV_BAD_INDEX)
+ *   scale      logit scale of the forward; <= 0 selects 1 / sqrt(D)
+ *   dQ         device, float [B, H, Tq, D], written
+ *   dK, dV     device, float [B, H, Tk, D], written (zero for keys no row chose)
+ *   dS         device, float [B, H, Tq, k], written
+ *   prob       device, float [B, H, Tq, k], written with p, or NULL
+ *   workspace  at least ssa_sparse_attn_bwd_workspace_size(B, H, Tq, Tk, k)
+ *              bytes, 256-byte aligned
+ *
+ * D in {64, 128}; Tq * k <= 2^31 - 1 (larger: SSA_ERR_UNSUPPORTED). Query-side
+ * pointers (Q, dO, idx, dQ, dS) may be NULL when B*H*Tq == 0 and key-side ones
+ * (K, V, dK, dV) when B*H*Tk == 0. Fp32 sums: dK, dV gather each key's pairs
+ * in an order that varies from run to run, so their last bits may too.
+ * Returns SSA_OK, SSA_ERR_INVALID, SSA_ERR_UNSUPPORTED, SSA_ERR_WORKSPACE or
+ * SSA_ERR_CUDA.
+ */
+size_t ssa_sparse_attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int k);
+ssa_status ssa_sparse_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                               int dtype, int B, int H, int Tq, int Tk, int D, const int32_t* idx,
+                               int k, float scale, float* dQ, float* dK, float* dV, float* dS,
+                               float* prob, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream);
+
+/*
+ * ssa_scorer_bwd — the scorer's gradients under the same estimator.
+ *
+ * Source: mhpq.cn/news/1098205, sections 2.2 (S = q_low . k_low^T * scale) and
+ * 2.3. With dS from ssa_sparse_attn_bwd:
+ *   dq_low[b,h,i] = scale * sum_t dS[b,h,i,t] k_low[b,h,j_t]
+ *   dk_low[b,h,j] = scale * sum over (i, t) with j_t = j of dS[b,h,i,t] q_low[b,h,i]
+ *
+ *   q_low [B,H,Tq,P], k_low [B,H,Tk,P] device, `dtype`; idx int32 and dS float
+ *   [B,H,Tq,k]; dq_low [B,H,Tq,P] and dk_low [B,H,Tk,P] float, written.
+ *   scale <= 0 selects fp32(1 / sqrt(P)). P in {16, 32, 64, 128};
+ *   Tq * k <= 2^31 - 1. workspace: ssa_scorer_bwd_workspace_size(...) bytes,
+ *   256-byte aligned. Same NULL, status and error rules as
+ *   ssa_sparse_attn_bwd.
+ */
+size_t ssa_scorer_bwd_workspace_size(int B, int H, int Tq, int Tk, int k);
+ssa_status ssa_scorer_bwd(const void* q_low, const void* k_low, int dtype, int B, int H, int Tq,
+                          int Tk, int P, const int32_t* idx, int k, const float* dS, float scale,
+                          float* dq_low, float* dk_low, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, void* stream);
+
+/*
  * Launch tracing. Between ssa_trace_begin() and ssa_trace_end(), every kernel
  * this library launches is bracketed by two CUDA events recorded on the
  * launching stream (the tracing itself launches nothing and allocates no

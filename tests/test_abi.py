@@ -197,3 +197,37 @@ def test_smoothing_k_at_the_int_limit_is_unsupported():
                                      0.0, 0.5, ok, None, ok, 1 << 20, None, None) == \
         _native.SSA_ERR_UNSUPPORTED
     assert ssa.score_topk_smooth_workspace_size(1, 1, 8, 8, 64, 2 ** 31 - 1, True) == 0
+
+
+def test_host_validation_of_the_backward_calls():
+    """ssa_sparse_attn_bwd / ssa_scorer_bwd refuse bad arguments on the host."""
+    lib = ssa.load()
+    ok, bad = V(4096), V(4100)
+    BF16 = _native.SSA_BF16
+    INV, UNS, WS = _native.SSA_ERR_INVALID, _native.SSA_ERR_UNSUPPORTED, _native.SSA_ERR_WORKSPACE
+    big = 1 << 30
+
+    def attn(D=64, Tq=8, k=4, scale=0.0, Q=ok, O=ok, wbytes=big, dt=BF16):
+        return lib.ssa_sparse_attn_bwd(Q, ok, ok, ok, dt, 1, 1, Tq, 16, D, ok, k, scale, O, ok, ok,
+                                       ok, None, ok, wbytes, None, None)
+
+    assert attn(D=96) == UNS
+    assert attn(Tq=1 << 20, k=4096) == UNS          # Tq * k beyond 32-bit pair ids
+    assert attn(scale=float("nan")) == INV
+    assert attn(Q=None) == INV                      # query rows but no Q
+    assert attn(O=bad) == INV                       # misaligned dQ
+    assert attn(dt=7) == INV
+    assert attn(wbytes=16) == WS
+    assert lib.ssa_sparse_attn_bwd(None, None, None, None, BF16, 0, 1, 8, 16, 64, None, 4, 0.0,
+                                   None, None, None, None, None, None, 0, None, None) == _native.SSA_OK
+    assert lib.ssa_sparse_attn_bwd_workspace_size(1, 1, 8, 16, 0) == 0
+
+    def scorer(P=64, scale=0.0, dS=ok, wbytes=big):
+        return lib.ssa_scorer_bwd(ok, ok, BF16, 1, 1, 8, 16, P, ok, 4, dS, scale, ok, ok, ok, wbytes,
+                                  None, None)
+
+    assert scorer(P=48) == UNS
+    assert scorer(scale=float("inf")) == INV
+    assert scorer(dS=None) == INV
+    assert scorer(wbytes=16) == WS
+    assert lib.ssa_scorer_bwd_workspace_size(1, 1, 8, 16, -1) == 0

@@ -4,8 +4,9 @@ The no-allocation entry point serves callers that may not allocate device
 memory where they run the op (an engine plugin confined to a pre-sized arena,
 a latency-critical loop that must never call cudaMalloc). It must give the
 same answer as the workspace entry point, bit for bit, call after call on the
-library's one shared scratch array. This file is collected last so that a run
-stopping at its first failure has already run every other test.
+library's one shared scratch array. This file is collected after the forward
+path's tests (only the backward's come later) so that a run stopping at its
+first failure has already run them.
 """
 import ctypes
 

@@ -1,0 +1,134 @@
+"""GPU parity of the backward under the straight-through estimator (B300).
+
+ssa_sparse_attn_bwd and ssa_scorer_bwd against the fp64 oracle
+(oracle.sparse_attn_bwd / scorer_bwd, pinned on the CPU). Inputs are exact in
+fp32 (bf16 or fp32 data) and every sum runs in fp32, so both dtypes share one
+tolerance: a relative bound per tensor, TOL x the tensor's largest magnitude.
+The sums have at most k terms (query side) or a key's pair count (key side),
+each of about that magnitude. 2e-5 covers the rounding of a few hundred such
+terms: k * 2^-24 is 3e-5 at k = 512, and the rounding errors rarely all add
+up. The same kernels run under host emulation in
+tests/test_backward_emulated.py. This file is collected last, after the
+no-allocation tests, so that a run stopping at its first failure has already
+run every other test.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dynamic_top_sparse_rank_b300 as ssa
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-5
+
+
+def _close(gpu, ref, what):
+    gpu = gpu.detach().cpu().double().numpy() if isinstance(gpu, torch.Tensor) else gpu
+    ref = np.asarray(ref, np.float64)
+    bound = TOL * max(1.0, float(np.abs(ref).max(initial=0.0)))
+    err = np.abs(gpu - ref)
+    assert err.max(initial=0.0) <= bound, "%s: max err %.3g > %.3g" % (what, err.max(), bound)
+
+
+def _inputs(B, H, Tq, Tk, D, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    mk = lambda T: torch.randn(B, H, T, D, generator=g).to(dtype)  # noqa: E731
+    return mk(Tq), mk(Tk), mk(Tk), mk(Tq)
+
+
+def _idx(B, H, Tq, Tk, k, seed):
+    g = np.random.default_rng(seed)
+    idx = g.integers(0, Tk, size=(B, H, Tq, k)).astype(np.int32)   # repeats allowed
+    if k > 1:
+        idx[..., -1] = -1                                           # a padded slot
+    idx[0, 0, 0, :] = -1                                            # an empty row
+    return idx
+
+
+CASES = [
+    # B, H, Tq, Tk, D, k, dtype
+    (1, 2, 100, 300, 128, 7, torch.bfloat16),
+    (2, 1, 129, 1000, 64, 33, torch.bfloat16),
+    (1, 1, 50, 2000, 128, 512, torch.bfloat16),
+    (1, 2, 77, 400, 64, 40, torch.float32),
+    (1, 1, 31, 700, 128, 96, torch.float32),
+    (1, 1, 40, 64, 64, 1, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("B,H,Tq,Tk,D,k,dtype", CASES)
+def test_sparse_attn_bwd_matches_oracle(cuda_dev, B, H, Tq, Tk, D, k, dtype):
+    Q, K, V, dO = _inputs(B, H, Tq, Tk, D, dtype, seed=300 + k)
+    idx = _idx(B, H, Tq, Tk, k, seed=k)
+    rQ, rK, rV, rS = oracle.sparse_attn_bwd(Q, K, V, idx, dO)
+    dev = [t.to(cuda_dev) for t in (Q, K, V, torch.from_numpy(idx), dO)]
+    dQ, dK, dV, dS, p = ssa.ssa_sparse_attn_bwd(*dev, with_prob=True)
+    _close(dQ, rQ, "dQ")
+    _close(dK, rK, "dK")
+    _close(dV, rV, "dV")
+    _close(dS, rS, "dS")
+    assert (dS[0, 0, 0] == 0).all() and (dQ[0, 0, 0] == 0).all()   # the empty row
+    pn = p.cpu().numpy()
+    live = idx >= 0
+    assert (pn[~live] == 0).all()
+    np.testing.assert_allclose(pn.sum(-1)[live.any(-1)], 1.0, atol=1e-5)
+
+
+@pytest.mark.parametrize("P,dtype", [(64, torch.bfloat16), (16, torch.float32),
+                                     (128, torch.bfloat16)])
+def test_scorer_bwd_matches_oracle(cuda_dev, P, dtype):
+    B, H, Tq, Tk, k = 1, 2, 90, 500, 24
+    g = torch.Generator().manual_seed(P)
+    ql = torch.randn(B, H, Tq, P, generator=g).to(dtype)
+    kl = torch.randn(B, H, Tk, P, generator=g).to(dtype)
+    idx = _idx(B, H, Tq, Tk, k, seed=P)
+    dS = torch.randn(B, H, Tq, k, generator=g)
+    rq, rk = oracle.scorer_bwd(ql, kl, idx, dS.numpy())
+    dq, dk = ssa.ssa_scorer_bwd(ql.to(cuda_dev), kl.to(cuda_dev),
+                                torch.from_numpy(idx).to(cuda_dev), dS.to(cuda_dev))
+    _close(dq, rq, "dq_low")
+    _close(dk, rk, "dk_low")
+
+
+def test_backward_of_the_exact_selection(cuda_dev):
+    """The path end to end: the GPU top-k feeds the backward; the oracle's
+    top-k (bit-identical on integer scorer data) feeds the oracle's."""
+    B, H, T, P, D, k = 1, 2, 300, 64, 128, 32
+    g = torch.Generator().manual_seed(7)
+    ql = torch.randint(-4, 5, (B, H, T, P), generator=g).to(torch.bfloat16)
+    kl = torch.randint(-4, 5, (B, H, T, P), generator=g).to(torch.bfloat16)
+    Q, K, V, dO = _inputs(B, H, T, T, D, torch.bfloat16, seed=8)
+    dv = [t.to(cuda_dev) for t in (ql, kl, Q, K, V, dO)]
+    idx = ssa.ssa_score_topk(dv[0], dv[1], k, True)
+    ref_idx, _ = oracle.score_topk(ql, kl, k, True)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    dQ, dK, dV, dS = ssa.ssa_sparse_attn_bwd(dv[2], dv[3], dv[4], idx, dv[5])
+    dq, dk = ssa.ssa_scorer_bwd(dv[0], dv[1], idx, dS)
+    rQ, rK, rV, rS = oracle.sparse_attn_bwd(Q, K, V, ref_idx, dO)
+    rq, rk = oracle.scorer_bwd(ql, kl, ref_idx, rS)
+    for a, b, n in ((dQ, rQ, "dQ"), (dK, rK, "dK"), (dV, rV, "dV"), (dS, rS, "dS"),
+                    (dq, rq, "dq_low"), (dk, rk, "dk_low")):
+        _close(a, b, n)
+
+
+def test_bwd_reports_bad_index(cuda_dev):
+    B, H, Tq, Tk, D, k = 1, 1, 8, 16, 64, 4
+    Q, K, V, dO = (t.to(cuda_dev) for t in _inputs(B, H, Tq, Tk, D, torch.bfloat16, seed=1))
+    idx = torch.zeros(B, H, Tq, k, dtype=torch.int32)
+    idx[0, 0, 3, 1] = Tk + 3
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    dQ, dK, dV, dS = ssa.ssa_sparse_attn_bwd(Q, K, V, idx.to(cuda_dev), dO, dev_status=st)
+    assert int(st.item()) & 0x1
+    assert float(dS[0, 0, 3, 1]) == 0.0
+
+
+def test_bwd_without_query_rows_zeroes_key_gradients(cuda_dev):
+    B, H, Tk, D, k = 1, 2, 40, 64, 4
+    Q = torch.zeros(B, H, 0, D, dtype=torch.bfloat16, device=cuda_dev)
+    K = torch.randn(B, H, Tk, D, device=cuda_dev).to(torch.bfloat16)
+    idx = torch.zeros(B, H, 0, k, dtype=torch.int32, device=cuda_dev)
+    dQ, dK, dV, dS = ssa.ssa_sparse_attn_bwd(Q, K, K.clone(), idx, Q.clone())
+    torch.cuda.synchronize()
+    assert (dK == 0).all() and (dV == 0).all()
