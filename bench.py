@@ -39,7 +39,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import WORKLOADS, fill, make_attn_inputs, make_scorer_inputs  # noqa: E402
+from workloads import (WORKLOADS, fill, make_attn_inputs, make_grad_output,  # noqa: E402
+                       make_scorer_inputs)
 
 DEFAULT_WORKLOAD = "topk_causal_bf16_t128k_k512_planted"
 METRIC = "queries/s and effective TFLOP/s at T=128K, k=512; % of phase roofline"
@@ -561,6 +562,28 @@ def run_reference(args):
     }
 
 
+def run_reference_backward(args):
+    """The reference arm of the backward workload: the oracle's backward on a
+    bounded sample per step (see cpu_baseline_backward)."""
+    vals, cores, sample, n = [], 1, "", 256
+    for s in range(args.warmup + args.steps):
+        v, cores, sample = cpu_baseline_backward(n, seed=s)
+        if s >= args.warmup:
+            vals.append(v)
+    value = float(np.mean(vals))
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * n / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": BACKWARD_WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "queries/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 # ------------------------------------------------------------ projection
 
 # The scorer's projections q_low = q_proj(query), k_low = k_proj(key) at the
@@ -674,6 +697,173 @@ def cpu_baseline_project(n_rows: int = 256):
     return n_rows / dt, cores, "%d rows of %s" % (n_rows, PROJECT_WORKLOAD)
 
 
+# ------------------------------------------------------------ backward
+
+# The backward of the 128K workload under the straight-through estimator
+# (mhpq.cn/news/1098205, section 2.3). The forward's index lists (the exact
+# top-k, computed once before timing) and an incoming gradient dO ~ N(0,1)
+# are given. One step = ssa_sparse_attn_bwd (dQ, dK, dV and the pair
+# gradients dS) + ssa_scorer_bwd (dq_low, dk_low).
+BACKWARD_WORKLOAD = "backward_topk_causal_bf16_t128k_k512"
+BACKWARD_BASE = "topk_causal_bf16_t128k_k512_planted"
+
+
+def backward_bytes(w, name):
+    """Algorithmic bytes of one launch of a backward kernel: its row gathers
+    per selected pair (K and V, or Q and dO: 2 D elements; k_low or q_low: P
+    elements), plus what it reads and writes per pair slot (dS, p, pair ids,
+    index lists)."""
+    esize = 4 if w.dtype == "f32" else 2
+    _, sel = valid_pairs(w)
+    slots = w.B * w.H * w.Tq * w.k
+    return {
+        "attn_bwd.query": sel * 2 * w.D * esize + slots * (4 + 8),   # idx in; dS, p out
+        "attn_bwd.key": sel * (2 * w.D * esize + 12),                # Q, dO; dS, p, pair id
+        "scorer_bwd.query": sel * w.P * esize + slots * 8,           # k_low; idx, dS
+        "scorer_bwd.key": sel * (w.P * esize + 8),                   # q_low; dS, pair id
+        "pair_lists.count": slots * 4,
+        "pair_lists.fill": slots * 4 + sel * 4,
+        "pair_lists.scan": w.B * w.H * w.Tk * 12,
+    }.get(name)
+
+
+def run_backward(args, rank, world, local_rank):
+    import dynamic_top_sparse_rank_b300 as ssa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = rank_workload(WORKLOADS[BACKWARD_BASE], rank)
+    q_low, k_low = make_scorer_inputs(w, dev)
+    Q, K, V = make_attn_inputs(w, dev)
+    dO = make_grad_output(w, dev)
+    idx = ssa.ssa_score_topk(q_low, k_low, w.k, w.causal)
+    ws_a = torch.empty(ssa.sparse_attn_bwd_workspace_size(w.B, w.H, w.Tq, w.Tk, w.k),
+                       dtype=torch.uint8, device=dev)
+    ws_s = torch.empty(ssa.scorer_bwd_workspace_size(w.B, w.H, w.Tq, w.Tk, w.k),
+                       dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(q_, k_, Q_, K_, V_, dO_, idx_):
+        dQ, dK, dV, dS = ssa.ssa_sparse_attn_bwd(Q_, K_, V_, idx_, dO_, workspace=ws_a)
+        dq, dk = ssa.ssa_scorer_bwd(q_, k_, idx_, dS, workspace=ws_s)
+        return dQ, dK, dV, dq, dk
+
+    args_dev = (q_low, k_low, Q, K, V, dO, idx)
+    for _ in range(args.warmup):
+        step(*args_dev)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for s_ in range(args.steps):
+        flush.fill_(s_ & 0xFF)
+        torch.cuda._sleep(HOST_COVER_CYCLES)
+        ev[s_][0].record(stream)
+        step(*args_dev)
+        ev[s_][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    ssa.trace_begin()
+    for s_ in range(args.steps):
+        flush.fill_(s_ & 0xFF)
+        step(*args_dev)
+    recs = ssa.trace_end()
+    torch.cuda.synchronize()
+    per_kernel = {}
+    for name, t in recs:
+        per_kernel.setdefault(name, []).append(t)
+    kernels = {n: {"launches_per_step": len(v) // args.steps, "ms": float(np.sum(v)) / args.steps}
+               for n, v in per_kernel.items()}
+    launches = len(recs) // args.steps
+    # end to end: every input from pinned host memory, every gradient back
+    hin = [t.cpu().pin_memory() for t in args_dev]
+    din = [torch.empty_like(t) for t in args_dev]
+    outs = step(*args_dev)
+    hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+
+    def e2e_step():
+        for d, h in zip(din, hin):
+            d.copy_(h, non_blocking=True)
+        for h, o in zip(hout, step(*din)):
+            h.copy_(o, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e], world, dev)
+    if rank != 0:
+        return None
+    pk, pk_kind = peaks()
+    for n, kinfo in kernels.items():
+        b = backward_bytes(w, n)
+        if b is not None and kinfo["ms"] > 0:
+            kinfo.update({"bound": "hbm", "unit": "GB/s",
+                          "achieved": b / (kinfo["ms"] * 1e-3) / 1e9})
+            kinfo["frac"] = kinfo["achieved"] / pk["hbm_gbs"]
+    dom = max(kernels, key=lambda n: kernels[n]["ms"])
+    dk_ = kernels[dom]
+    nq = w.n_queries * world
+    return {
+        "metric": METRIC, "value": nq / (ms * 1e-3), "unit": "queries/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64; integer q_low/k_low with planted keys, "
+                "Q/K/V/dO ~ N(0,1))",
+        "config": {"workload": BACKWARD_WORKLOAD, "B": w.B, "H": w.H, "Tq": w.Tq, "Tk": w.Tk,
+                   "D": w.D, "d_proj": w.P, "k": w.k, "causal": w.causal,
+                   "l2": "flushed between timed steps (512 MB write) and inputs > L2",
+                   "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
+        "kernels": kernels,
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": dk_.get("achieved"),
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": dk_.get("frac"),
+                     "traffic": None, "peak_kind": pk_kind + " HBM copy",
+                     "algorithmic": "row gathers and per-slot traffic of the kernel, %.4g bytes"
+                                    % (backward_bytes(w, dom) or 0.0)},
+        "e2e": {"value": nq / (ms_e2e * 1e-3), "unit": "queries/s", "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout)},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk,
+    }
+
+
+def cpu_baseline_backward(n_rows: int = 256, seed: int = 0):
+    """The oracle's backward (attention + scorer) on a bounded sample of query
+    rows of head 0 of the backward workload; rows per second. The sample's
+    index lists come from the oracle's top-k, outside the timed part."""
+    import oracle
+    w = WORKLOADS[BACKWARD_BASE].with_(B=1, H=1)
+    g = np.random.default_rng(seed)
+    qi = np.sort(g.choice(w.Tq, size=n_rows, replace=False)).astype(np.int64)
+    q_low, k_low = make_scorer_inputs(w)
+    Q, K, V = make_attn_inputs(w)
+    dO = make_grad_output(w)
+    cores = oracle.default_threads()
+    idx, _ = oracle.topk_rows(q_low[0, 0][qi], qi, k_low[0, 0], w.k, w.Tq, w.causal,
+                              nthreads=cores)
+    t0 = time.perf_counter()
+    _, _, _, dS, _ = oracle.attn_bwd_rows(Q[0, 0][qi], K[0, 0], V[0, 0], idx, dO[0, 0][qi],
+                                          nthreads=cores)
+    oracle.scorer_bwd_rows(q_low[0, 0][qi], k_low[0, 0], idx, dS)
+    dt = time.perf_counter() - t0
+    return n_rows / dt, cores, ("%d random query rows of head 0 of %s (attention and scorer "
+                                "backward)" % (n_rows, BACKWARD_WORKLOAD))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -682,7 +872,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(WORKLOADS) + [PROJECT_WORKLOAD, SHARED_WORKLOAD,
-                                                 SMOOTH_WORKLOAD])
+                                                 SMOOTH_WORKLOAD, BACKWARD_WORKLOAD])
     ap.add_argument("--cpu-rows", type=int, default=2048,
                     help="query rows the CPU oracle times (bounded sample)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -715,6 +905,24 @@ def main():
         if rank == 0:
             if not args.no_cpu_baseline:
                 v, cores, sample = cpu_baseline_project()
+                line["cpu_baseline"] = {"value": v, "unit": "queries/s", "cores": cores,
+                                        "kind": "oracle", "sample": sample}
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    if args.workload == BACKWARD_WORKLOAD:
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps(run_reference_backward(args)), flush=True)
+            return
+        if world > 1:
+            torch.distributed.init_process_group("nccl")
+        line = run_backward(args, rank, world, local_rank)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                v, cores, sample = cpu_baseline_backward()
                 line["cpu_baseline"] = {"value": v, "unit": "queries/s", "cores": cores,
                                         "kind": "oracle", "sample": sample}
             print(json.dumps(line), flush=True)

@@ -17,11 +17,13 @@ from ._native import (EXPORTS, SSA_BF16, SSA_DEV_BAD_INDEX, SSA_DEV_OVERFLOW, SS
                       ssa_lowrank_scores, ssa_score_topk, ssa_score_topk_smooth,
                       score_topk_smooth_workspace_size, trace_begin, trace_end,
                       ssa_score_topk_noalloc, ssa_scorer_bwd, ssa_sparse_attn, ssa_sparse_attn_bwd,
-                      ssa_sparse_attn_grouped, ssa_window_attn, status_string)
+                      ssa_sparse_attn_grouped, ssa_window_attn, status_string,
+                      sparse_attn_bwd_workspace_size, scorer_bwd_workspace_size)
 
 __all__ = ["EXPORTS", "SSA_BF16", "SSA_DEV_BAD_INDEX", "SSA_DEV_OVERFLOW", "SSA_DEV_WAIT_LIMIT",
            "SSA_F32", "SSAError", "load", "score_topk_workspace_size", "ssa_lowrank_project",
            "ssa_lowrank_scores", "ssa_score_topk_smooth", "score_topk_smooth_workspace_size",
            "ssa_score_topk", "trace_begin", "trace_end",
            "ssa_score_topk_noalloc", "ssa_scorer_bwd", "ssa_sparse_attn", "ssa_sparse_attn_bwd",
-           "ssa_sparse_attn_grouped", "ssa_window_attn", "status_string"]
+           "ssa_sparse_attn_grouped", "ssa_window_attn", "status_string",
+           "sparse_attn_bwd_workspace_size", "scorer_bwd_workspace_size"]

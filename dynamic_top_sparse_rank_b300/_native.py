@@ -368,6 +368,14 @@ class _TraceRecord(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 56), ("ms", ctypes.c_float)]
 
 
+def sparse_attn_bwd_workspace_size(B, H, Tq, Tk, k) -> int:
+    return int(load().ssa_sparse_attn_bwd_workspace_size(B, H, Tq, Tk, k))
+
+
+def scorer_bwd_workspace_size(B, H, Tq, Tk, k) -> int:
+    return int(load().ssa_scorer_bwd_workspace_size(B, H, Tq, Tk, k))
+
+
 def ssa_sparse_attn_bwd(Q, K, V, idx, dO, scale: float = 0.0, workspace=None,
                         dev_status=None, with_prob: bool = False):
     """Gradients of ssa_sparse_attn under the straight-through estimator.
@@ -393,7 +401,7 @@ def ssa_sparse_attn_bwd(Q, K, V, idx, dO, scale: float = 0.0, workspace=None,
     dV = torch.empty((B, H, Tk, D), **f32)
     dS = torch.empty((B, H, Tq, k), **f32)
     prob = torch.empty((B, H, Tq, k), **f32) if with_prob else None
-    need = int(lib.ssa_sparse_attn_bwd_workspace_size(B, H, Tq, Tk, k))
+    need = sparse_attn_bwd_workspace_size(B, H, Tq, Tk, k)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     wbytes = workspace.numel() * workspace.element_size()
@@ -422,7 +430,7 @@ def ssa_scorer_bwd(q_low, k_low, idx, dS, scale: float = 0.0, workspace=None, de
     f32 = dict(dtype=torch.float32, device=dev)
     dq = torch.empty((B, H, Tq, P), **f32)
     dk = torch.empty((B, H, Tk, P), **f32)
-    need = int(lib.ssa_scorer_bwd_workspace_size(B, H, Tq, Tk, k))
+    need = scorer_bwd_workspace_size(B, H, Tq, Tk, k)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     wbytes = workspace.numel() * workspace.element_size()

@@ -100,3 +100,17 @@ def test_gather_aux_bytes():
     rows = w.B * w.H * w.Tq
     assert alg["gather_aux_bytes"] == rows * w.k * 4 + 2 * rows * w.D * 2
     assert abs(alg["gather_aux_bytes"] - 2.684e9) / 2.684e9 < 1e-3
+
+
+def test_backward_kernel_bytes():
+    """Backward: each side gathers two rows of D elements per selected pair
+    (K and V, or Q and dO) plus its per-slot traffic; the scorer sides gather
+    one d_proj row per pair."""
+    w = WORKLOADS[bench.BACKWARD_BASE]
+    _, sel = bench.valid_pairs(w)
+    slots = w.B * w.H * w.Tq * w.k
+    assert bench.backward_bytes(w, "attn_bwd.query") == sel * 2 * w.D * 2 + slots * 12
+    assert bench.backward_bytes(w, "attn_bwd.key") == sel * (2 * w.D * 2 + 12)
+    assert bench.backward_bytes(w, "scorer_bwd.key") == sel * (w.P * 2 + 8)
+    assert abs(bench.backward_bytes(w, "attn_bwd.query") - 2.808e11) / 2.808e11 < 1e-3
+    assert bench.backward_bytes(w, "something else") is None

@@ -118,6 +118,7 @@ def fill(shape, kind: str, seed: int, tid: int, dtype, device) -> torch.Tensor:
 
 # Tensor ids inside one workload's seed.
 TID_QLOW, TID_KLOW, TID_Q, TID_K, TID_V, TID_PLANT_POS, TID_PLANT_GROUP = 1, 2, 3, 4, 5, 6, 7
+TID_DO = 8   # the incoming gradient of the attention output (backward workloads)
 
 
 @dataclass(frozen=True)
@@ -238,6 +239,12 @@ def make_attn_inputs(w: Workload, device="cpu"):
     K = fill((w.B, w.H, w.Tk, w.D), "normal", w.seed, TID_K, dt, device)
     V = fill((w.B, w.H, w.Tk, w.D), "normal", w.seed, TID_V, dt, device)
     return Q, K, V
+
+
+def make_grad_output(w: Workload, device="cpu"):
+    """dO ~ N(0,1) [B,H,Tq,D] in the workload dtype: the gradient reaching the
+    attention output in a backward step."""
+    return fill((w.B, w.H, w.Tq, w.D), "normal", w.seed, TID_DO, w.torch_dtype, device)
 
 
 def small(name: str, **kw) -> Workload:
