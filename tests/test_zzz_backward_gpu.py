@@ -18,16 +18,17 @@ import torch
 
 import dynamic_top_sparse_rank_b300 as ssa
 import oracle
+from workloads import WORKLOADS, make_attn_inputs, make_grad_output, make_scorer_inputs
 
 pytestmark = pytest.mark.gpu
 
 TOL = 2e-5
 
 
-def _close(gpu, ref, what):
+def _close(gpu, ref, what, tol=TOL):
     gpu = gpu.detach().cpu().double().numpy() if isinstance(gpu, torch.Tensor) else gpu
     ref = np.asarray(ref, np.float64)
-    bound = TOL * max(1.0, float(np.abs(ref).max(initial=0.0)))
+    bound = tol * max(1.0, float(np.abs(ref).max(initial=0.0)))
     err = np.abs(gpu - ref)
     assert err.max(initial=0.0) <= bound, "%s: max err %.3g > %.3g" % (what, err.max(), bound)
 
@@ -132,3 +133,56 @@ def test_bwd_without_query_rows_zeroes_key_gradients(cuda_dev):
     dQ, dK, dV, dS = ssa.ssa_sparse_attn_bwd(Q, K, K.clone(), idx, Q.clone())
     torch.cuda.synchronize()
     assert (dK == 0).all() and (dV == 0).all()
+
+
+# ------------------------------------------------- full-size sampled parity
+
+FULL_TOL = 1e-4   # keys chosen by thousands of rows sum that many fp32 terms
+
+
+def check_backward_sampled(w, dev, idx, n_rows=24, seed=0):
+    """The backward workload's launch at full size, checked on samples. Each
+    sampled row's dQ, dS and dq_low come from the oracle on that row alone.
+    Each sampled key's dK, dV and dk_low come from the oracle on exactly the
+    rows that chose it (their full index lists), so every term of the key's
+    sum is included. idx is the forward's index lists on `dev`."""
+    q_low, k_low = make_scorer_inputs(w, dev)
+    Q, K, V = make_attn_inputs(w, dev)
+    dO = make_grad_output(w, dev)
+    dQ, dK, dV, dS = ssa.ssa_sparse_attn_bwd(Q, K, V, idx, dO)
+    dq, dk = ssa.ssa_scorer_bwd(q_low, k_low, idx, dS)
+    g = np.random.default_rng(seed)
+    heads = sorted({0, w.B * w.H - 1})
+    for bh in heads:
+        b, h = divmod(bh, w.H)
+        ix = idx[b, h].cpu().numpy()
+        host = [t[b, h].cpu() for t in (Q, K, V, dO, q_low, k_low)]
+        Qh, Kh, Vh, dOh, qh, kh = host
+        rows = np.unique(np.concatenate([[0, w.Tq - 1], g.choice(w.Tq, n_rows, replace=False)]))
+        rQ, _, _, rS, _ = oracle.attn_bwd_rows(Qh[rows], Kh, Vh, ix[rows], dOh[rows])
+        rq, _ = oracle.scorer_bwd_rows(qh[rows], kh, ix[rows], rS)
+        sel = torch.from_numpy(rows).to(dev)
+        _close(dQ[b, h][sel], rQ, "dQ rows of head %d" % bh, FULL_TOL)
+        _close(dS[b, h][sel], rS, "dS rows of head %d" % bh, FULL_TOL)
+        _close(dq[b, h][sel], rq, "dq_low rows of head %d" % bh, FULL_TOL)
+        for j in sorted({0, w.Tk // 2, w.Tk - 1, int(g.integers(0, w.Tk))}):
+            who = np.unique(np.nonzero(ix == j)[0])
+            if len(who) == 0:
+                assert float(dK[b, h, j].abs().max()) == 0.0 and float(dV[b, h, j].abs().max()) == 0.0
+                continue
+            _, rK, rV, rSj, _ = oracle.attn_bwd_rows(Qh[who], Kh, Vh, ix[who], dOh[who])
+            _, rk = oracle.scorer_bwd_rows(qh[who], kh, ix[who], rSj)
+            _close(dK[b, h, j], rK[j], "dK key %d of head %d (%d rows)" % (j, bh, len(who)),
+                   FULL_TOL)
+            _close(dV[b, h, j], rV[j], "dV key %d of head %d" % (j, bh), FULL_TOL)
+            _close(dk[b, h, j], rk[j], "dk_low key %d of head %d" % (j, bh), FULL_TOL)
+
+
+def test_backward_full_size_sampled(cuda_dev):
+    """The 128K workload (B1 H8, k 512, D 128) in the bench's launch
+    configuration, on sampled rows and keys."""
+    w = WORKLOADS["topk_causal_bf16_t128k_k512_planted"]
+    q_low, k_low = make_scorer_inputs(w, cuda_dev)
+    idx = ssa.ssa_score_topk(q_low, k_low, w.k, w.causal)
+    del q_low, k_low
+    check_backward_sampled(w, cuda_dev, idx)
