@@ -382,3 +382,48 @@ def scorer_bwd(q_low, k_low, idx, dS, scale: float = 0.0):
             dq[b, h], dk[b, h] = scorer_bwd_rows(q_low[b, h], k_low[b, h], idx[b, h], dS[b, h],
                                                  scale)
     return dq, dk
+
+
+def sparse_attn_grouped_bwd(Q, K, V, idx, dO, scale: float = 0.0, nthreads: int | None = None):
+    """Backward of attention with shared key/value heads and shared index
+    lists (the grouped layouts of mhpq.cn/news/1098205, section 3.2, and of
+    grouped-query attention), under the straight-through estimator.
+
+    Q, dO [B,H,Tq,D]; K, V [B,H_kv,Tk,D]; idx [B,H_idx,Tq,k]. Query head h
+    reads key/value head h // (H // H_kv) and index head h // (H // H_idx).
+    Each query head's gradients are those of the plain routine on its own
+    operands; a shared key/value head's dK, dV sum over the query heads that
+    read it. Returns float64 (dQ [B,H,Tq,D], dK, dV [B,H_kv,Tk,D],
+    dS [B,H,Tq,k])."""
+    B, H, Tq, D = Q.shape
+    H_kv, Tk = K.shape[1], K.shape[2]
+    idx = np.asarray(idx)
+    H_idx, k = idx.shape[1], idx.shape[3]
+    gk, gi = H // H_kv, H // H_idx
+    assert gk * H_kv == H and gi * H_idx == H
+    dQ = np.empty((B, H, Tq, D), np.float64)
+    dK = np.zeros((B, H_kv, Tk, D), np.float64)
+    dV = np.zeros((B, H_kv, Tk, D), np.float64)
+    dS = np.empty((B, H, Tq, k), np.float64)
+    for b in range(B):
+        for h in range(H):
+            dQ[b, h], dKh, dVh, dS[b, h], _ = attn_bwd_rows(
+                Q[b, h], K[b, h // gk], V[b, h // gk], idx[b, h // gi], dO[b, h], scale, nthreads)
+            dK[b, h // gk] += dKh
+            dV[b, h // gk] += dVh
+    return dQ, dK, dV, dS
+
+
+def scorer_grouped_bwd(q_low, k_low, idx, dS, scale: float = 0.0):
+    """The scorer's gradients when H query heads share H_idx scorer heads
+    (q_low, k_low, idx with H_idx heads; dS [B,H,Tq,k] from the attention
+    backward): the score of a pair in index head hi feeds the logits of every
+    query head that reads hi, so its gradient is the sum of their dS. Returns
+    float64 (dq_low [B,H_idx,Tq,P], dk_low [B,H_idx,Tk,P])."""
+    dS = np.asarray(dS, np.float64)
+    B, H, Tq, k = dS.shape
+    H_idx = q_low.shape[1]
+    gi = H // H_idx
+    assert gi * H_idx == H
+    summed = dS.reshape(B, H_idx, gi, Tq, k).sum(axis=2)
+    return scorer_bwd(q_low, k_low, idx, summed, scale)

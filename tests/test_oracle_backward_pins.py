@@ -239,3 +239,76 @@ def test_whole_tensor_calls_match_per_head():
             s = oracle.scorer_bwd_rows(ql[b, h], kl[b, h], idx[b, h], dS[b, h])
             np.testing.assert_array_equal(dq[b, h], s[0])
             np.testing.assert_array_equal(dk[b, h], s[1])
+
+
+def _grouped_case(seed, B=1, H=4, H_kv=2, H_idx=1, Tq=5, Tk=7, D=3, k=3):
+    g = np.random.default_rng(seed)
+    Q = g.standard_normal((B, H, Tq, D))
+    dO = g.standard_normal((B, H, Tq, D))
+    K = g.standard_normal((B, H_kv, Tk, D))
+    V = g.standard_normal((B, H_kv, Tk, D))
+    idx = np.stack([[np.stack([g.choice(Tk, size=k, replace=False) for _ in range(Tq)])
+                     for _ in range(H_idx)] for _ in range(B)]).astype(np.int32)
+    idx[0, 0, 1, 2] = -1
+    return Q, K, V, dO, idx
+
+
+def _grouped_loss(Q, K, V, dO, idx, scale):
+    """sum over query heads of O_h . dO_h, each head through the forward
+    oracle with its shared key/value head and index list."""
+    B, H = Q.shape[:2]
+    gk, gi = H // K.shape[1], H // idx.shape[1]
+    tot = 0.0
+    for b in range(B):
+        for h in range(H):
+            O, _ = oracle.attn_rows(Q[b, h], K[b, h // gk], V[b, h // gk], idx[b, h // gi], scale,
+                                    nthreads=1)
+            tot += float(np.sum(O * dO[b, h]))
+    return tot
+
+
+@pytest.mark.parametrize("H,H_kv,H_idx", [(4, 2, 1), (4, 1, 2), (2, 2, 2)])
+def test_grouped_bwd_matches_finite_differences(H, H_kv, H_idx):
+    """A shared key/value head's gradient sums over the query heads reading it:
+    central differences of the forward oracle with shared K and V."""
+    Q, K, V, dO, idx = _grouped_case(30 + H_kv + 3 * H_idx, H=H, H_kv=H_kv, H_idx=H_idx)
+    c = 0.45
+    dQ, dK, dV, dS = oracle.sparse_attn_grouped_bwd(Q, K, V, idx, dO, c)
+    f = lambda: _grouped_loss(Q, K, V, dO, idx, c)  # noqa: E731
+    np.testing.assert_allclose(dQ, _fd(f, Q), atol=1e-7, rtol=1e-6)
+    np.testing.assert_allclose(dK, _fd(f, K), atol=1e-7, rtol=1e-6)
+    np.testing.assert_allclose(dV, _fd(f, V), atol=1e-7, rtol=1e-6)
+    if H_kv == H_idx == H:   # the plain layout is the plain routine
+        r = oracle.sparse_attn_bwd(Q, K, V, idx, dO, c)
+        for a, w in zip((dQ, dK, dV, dS), r):
+            np.testing.assert_array_equal(a, w)
+
+
+def test_shared_scorer_bwd_is_the_gradient_of_a_score_bias():
+    """One scorer head shared by all query heads (the layout of
+    mhpq.cn/news/1098205, section 3.2): a perturbation of the shared q_low or
+    k_low moves the selected logits of every head by sigma * dq . k_low (or
+    q_low . dk); the finite difference equals the grouped scorer gradient."""
+    B, H, H_kv, H_idx, Tq, Tk, D, P = 1, 3, 3, 1, 5, 7, 3, 2
+    Q, K, V, dO, idx = _grouped_case(41, B, H, H_kv, H_idx, Tq, Tk, D)
+    g = np.random.default_rng(42)
+    ql = g.standard_normal((B, H_idx, Tq, P))
+    kl = g.standard_normal((B, H_idx, Tk, P))
+    c, sigma = 0.5, 0.3
+    _, _, _, dS = oracle.sparse_attn_grouped_bwd(Q, K, V, idx, dO, c)
+    dq, dk = oracle.scorer_grouped_bwd(ql, kl, idx, dS, sigma)
+
+    def loss_with(qx, kx):
+        """Forward loss with Q' = [Q, (sigma / c) qx] and K' = [K, kx]: the
+        logits gain sigma * qx . kx (qx, kx of the one scorer head, shared by
+        every query head and every key/value head)."""
+        Qx = np.concatenate([Q, np.broadcast_to((sigma / c) * qx, (B, H, Tq, P))], axis=-1)
+        Kx = np.concatenate([K, np.broadcast_to(kx, (B, H_kv, Tk, P))], axis=-1)
+        Vx = np.concatenate([V, np.zeros((B, H_kv, Tk, P))], axis=-1)
+        dOx = np.concatenate([dO, np.zeros((B, H, Tq, P))], axis=-1)
+        return _grouped_loss(Qx, Kx, Vx, dOx, idx, c)
+
+    dqp = np.zeros((B, H_idx, Tq, P))   # perturbation of q_low around a bias-free forward
+    np.testing.assert_allclose(dq, _fd(lambda: loss_with(dqp, kl), dqp), atol=1e-7, rtol=1e-6)
+    dkp = np.zeros((B, H_idx, Tk, P))
+    np.testing.assert_allclose(dk, _fd(lambda: loss_with(ql, dkp), dkp), atol=1e-7, rtol=1e-6)
