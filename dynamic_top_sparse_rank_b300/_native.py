@@ -27,7 +27,9 @@ EXPORTS = ("ssa_version", "ssa_status_string", "ssa_score_topk_workspace_size", 
            "ssa_lowrank_project", "ssa_sparse_attn_grouped", "ssa_score_topk_smooth",
            "ssa_score_topk_smooth_workspace_size", "ssa_trace_begin", "ssa_trace_end",
            "ssa_sparse_attn_bwd_workspace_size", "ssa_sparse_attn_bwd",
-           "ssa_scorer_bwd_workspace_size", "ssa_scorer_bwd")
+           "ssa_scorer_bwd_workspace_size", "ssa_scorer_bwd",
+           "ssa_sparse_attn_grouped_bwd_workspace_size", "ssa_sparse_attn_grouped_bwd",
+           "ssa_scorer_grouped_bwd_workspace_size", "ssa_scorer_grouped_bwd")
 
 # Fixed scratch of ssa_score_topk_noalloc and the largest Tk it accepts.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -91,6 +93,15 @@ def load(path: str | None = None):
     lib.ssa_scorer_bwd_workspace_size.argtypes = [I, I, I, I, I]
     lib.ssa_scorer_bwd.restype = I
     lib.ssa_scorer_bwd.argtypes = [V, V, I, I, I, I, I, I, V, I, V, F, V, V, V, Z, V, V]
+    lib.ssa_sparse_attn_grouped_bwd_workspace_size.restype = Z
+    lib.ssa_sparse_attn_grouped_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
+    lib.ssa_sparse_attn_grouped_bwd.restype = I
+    lib.ssa_sparse_attn_grouped_bwd.argtypes = [V, V, V, V, I, I, I, I, I, I, I, V, I, I, F, V, V,
+                                                V, V, V, V, Z, V, V]
+    lib.ssa_scorer_grouped_bwd_workspace_size.restype = Z
+    lib.ssa_scorer_grouped_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
+    lib.ssa_scorer_grouped_bwd.restype = I
+    lib.ssa_scorer_grouped_bwd.argtypes = [V, V, I, I, I, I, I, I, I, V, I, V, F, V, V, V, Z, V, V]
     if path is None:
         _lib = lib
     return lib
@@ -438,6 +449,72 @@ def ssa_scorer_bwd(q_low, k_low, idx, dS, scale: float = 0.0, workspace=None, de
                             _ptr(dS), float(scale), _ptr(dq), _ptr(dk), _ptr(workspace), wbytes,
                             _ptr(dev_status), _stream(dev))
     _check(rc, "ssa_scorer_bwd")
+    return dq, dk
+
+
+def ssa_sparse_attn_grouped_bwd(Q, K, V, idx, dO, scale: float = 0.0, workspace=None,
+                                dev_status=None, with_prob: bool = False):
+    """ssa_sparse_attn_bwd for shared key/value heads and index lists: Q, dO
+    [B,H,Tq,D]; K, V [B,H_kv,Tk,D]; idx [B,H_idx,Tq,k]. Returns fp32 (dQ
+    [B,H,Tq,D], dK, dV [B,H_kv,Tk,D], dS [B,H,Tq,k]) (+ prob)."""
+    lib = load()
+    dev = _dev(Q, K, V, idx, dO, workspace, dev_status)
+    if not (Q.dtype == K.dtype == V.dtype == dO.dtype):
+        raise TypeError("Q, K, V, dO must share a dtype")
+    if idx.dtype != torch.int32:
+        raise TypeError("idx must be int32")
+    B, H, Tq, D = Q.shape
+    H_kv, Tk = K.shape[1], K.shape[2]
+    H_idx, k = idx.shape[1], idx.shape[3]
+    if tuple(K.shape) != (B, H_kv, Tk, D) or tuple(V.shape) != (B, H_kv, Tk, D) or \
+            tuple(dO.shape) != (B, H, Tq, D) or tuple(idx.shape[:3]) != (B, H_idx, Tq):
+        raise ValueError("shapes do not match: Q %s K %s V %s dO %s idx %s" % tuple(
+            tuple(t.shape) for t in (Q, K, V, dO, idx)))
+    f32 = dict(dtype=torch.float32, device=dev)
+    dQ = torch.empty((B, H, Tq, D), **f32)
+    dK = torch.empty((B, H_kv, Tk, D), **f32)
+    dV = torch.empty((B, H_kv, Tk, D), **f32)
+    dS = torch.empty((B, H, Tq, k), **f32)
+    prob = torch.empty((B, H, Tq, k), **f32) if with_prob else None
+    need = int(lib.ssa_sparse_attn_grouped_bwd_workspace_size(B, H, H_kv, Tq, Tk, k))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = lib.ssa_sparse_attn_grouped_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _dt(Q), B, H, H_kv,
+                                         Tq, Tk, D, _ptr(idx), H_idx, k, float(scale), _ptr(dQ),
+                                         _ptr(dK), _ptr(dV), _ptr(dS), _ptr(prob),
+                                         _ptr(workspace), wbytes, _ptr(dev_status), _stream(dev))
+    _check(rc, "ssa_sparse_attn_grouped_bwd")
+    return (dQ, dK, dV, dS, prob) if with_prob else (dQ, dK, dV, dS)
+
+
+def ssa_scorer_grouped_bwd(q_low, k_low, idx, dS, scale: float = 0.0, workspace=None,
+                           dev_status=None):
+    """The scorer's gradients for H_idx scorer heads shared by the H query
+    heads of dS [B,H,Tq,k]; q_low [B,H_idx,Tq,P], k_low [B,H_idx,Tk,P], idx
+    [B,H_idx,Tq,k]. Returns fp32 (dq_low, dk_low)."""
+    lib = load()
+    dev = _dev(q_low, k_low, idx, dS, workspace, dev_status)
+    if q_low.dtype != k_low.dtype:
+        raise TypeError("q_low and k_low must share a dtype")
+    if idx.dtype != torch.int32 or dS.dtype != torch.float32:
+        raise TypeError("idx must be int32 and dS float32")
+    B, H_idx, Tq, P = q_low.shape
+    Tk, k = k_low.shape[2], idx.shape[3]
+    H = dS.shape[1]
+    if tuple(idx.shape) != (B, H_idx, Tq, k) or tuple(dS.shape) != (B, H, Tq, k):
+        raise ValueError("idx/dS shapes do not match q_low")
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq = torch.empty((B, H_idx, Tq, P), **f32)
+    dk = torch.empty((B, H_idx, Tk, P), **f32)
+    need = int(lib.ssa_scorer_grouped_bwd_workspace_size(B, H, H_idx, Tq, Tk, k))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = lib.ssa_scorer_grouped_bwd(_ptr(q_low), _ptr(k_low), _dt(q_low), B, H, H_idx, Tq, Tk, P,
+                                    _ptr(idx), k, _ptr(dS), float(scale), _ptr(dq), _ptr(dk),
+                                    _ptr(workspace), wbytes, _ptr(dev_status), _stream(dev))
+    _check(rc, "ssa_scorer_grouped_bwd")
     return dq, dk
 
 

@@ -102,15 +102,24 @@ SSA_DEVINL void reduce_groups(float (&acc)[E]) {
 
 }  // namespace
 
+// Head grouping: H query heads; query head h reads key/value head h / gk and
+// index list head h / gi (gk = H / H_kv, gi = H / H_idx; both 1 in the plain
+// layout, where every head has its own).
+struct BwdHeads {
+    int H, gk, gi;
+};
+
 // ------------------------------------------------------------- query side
 
-// One warp per query row. dS and prob are [rows, k] fp32; on return slot t of
-// row i holds dS[i][t] and p_t (0 in padded or skipped slots).
+// One warp per query row (rows of [B, H, Tq]). dS and prob are [rows, k] fp32;
+// on return slot t of row i holds dS[i][t] and p_t (0 in padded or skipped
+// slots).
 template <bool BF16_IN, int D>
 __global__ void __launch_bounds__(256, 2) attn_bwd_query_kernel(
     const void* __restrict__ Q, const void* __restrict__ K, const void* __restrict__ V,
     const void* __restrict__ dO, const int32_t* __restrict__ idx, int64_t rows, int Tq, int Tk,
-    int k, float scale, float* __restrict__ dQ, float* dS, float* prob, int32_t* dev_status) {
+    int k, float scale, const BwdHeads hd, float* __restrict__ dQ, float* dS, float* prob,
+    int32_t* dev_status) {
     using Gm = BwdGeom<BF16_IN, D>;
     constexpr int L = Gm::L, G = Gm::G, E = Gm::E, R = Gm::R;
     const int lane = threadIdx.x & 31;
@@ -118,8 +127,13 @@ __global__ void __launch_bounds__(256, 2) attn_bwd_query_kernel(
     if (row >= rows) return;
     const int g = lane / L, s = lane % L;
     const int64_t bh = row / Tq;
-    const char* Kb = reinterpret_cast<const char*>(K) + bh * (int64_t)Tk * R + s * 16;
-    const char* Vb = reinterpret_cast<const char*>(V) + bh * (int64_t)Tk * R + s * 16;
+    const int i_row = (int)(row - bh * Tq);
+    const int64_t b = bh / hd.H;
+    const int h = (int)(bh - b * hd.H);
+    const int64_t bkv = b * (hd.H / hd.gk) + h / hd.gk;                       // key/value head
+    const int64_t irow_id = (b * (hd.H / hd.gi) + h / hd.gi) * Tq + i_row;    // index list row
+    const char* Kb = reinterpret_cast<const char*>(K) + bkv * (int64_t)Tk * R + s * 16;
+    const char* Vb = reinterpret_cast<const char*>(V) + bkv * (int64_t)Tk * R + s * 16;
     const float scale_log2 = scale * kLog2e;
 
     float q[E], go[E];
@@ -131,7 +145,7 @@ __global__ void __launch_bounds__(256, 2) attn_bwd_query_kernel(
     for (int e = 0; e < E; ++e) A[e] = Bk[e] = 0.f;
     float m = -INFINITY, lsum = 0.f, wsum = 0.f;   // m in log2 units
     const int n_entries = Tk > 0 ? k : 0;
-    const int32_t* irow = idx + row * (int64_t)k;
+    const int32_t* irow = idx + irow_id * (int64_t)k;
     float* dsr = dS + row * (int64_t)k;
     float* pr = prob + row * (int64_t)k;
 
@@ -247,32 +261,57 @@ __global__ void __launch_bounds__(256, 2) attn_bwd_query_kernel(
 
 // ------------------------------------------------------- key-major lists
 
-// cnt[bh*Tk + j] += number of slots of head bh's lists holding key j.
+// Slot e of the query rows [B, H, Tq, k]: the key it names (from its index
+// list row), its key/value head and its pair id within that head's lists,
+// ((h % gk) * Tq + i) * k + t.
+struct PairSlot {
+    int j;
+    int64_t bkv;
+    int32_t pid;
+};
+
+SSA_DEVINL PairSlot pair_slot(const int32_t* idx, int64_t e, int Tq, int k, const BwdHeads& hd) {
+    const int64_t row = e / k;
+    const int t = (int)(e - row * k);
+    const int64_t bh = row / Tq;
+    const int i = (int)(row - bh * Tq);
+    const int64_t b = bh / hd.H;
+    const int h = (int)(bh - b * hd.H);
+    PairSlot ps;
+    ps.j = __ldg(idx + ((b * (hd.H / hd.gi) + h / hd.gi) * Tq + i) * k + t);
+    ps.bkv = b * (hd.H / hd.gk) + h / hd.gk;
+    ps.pid = (int32_t)(((int64_t)(h % hd.gk) * Tq + i) * k + t);
+    return ps;
+}
+
+// cnt[bkv*Tk + j] += number of query-head slots of key/value head bkv that
+// name key j (entries = B*H*Tq*k slots).
 __global__ void pair_count_kernel(const int32_t* __restrict__ idx, int64_t entries, int Tq, int Tk,
-                                  int k, int32_t* __restrict__ cnt, int32_t* dev_status) {
-    const int64_t per_head = (int64_t)Tq * k;
+                                  int k, const BwdHeads hd, int32_t* __restrict__ cnt,
+                                  int32_t* dev_status) {
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < entries;
          e += (int64_t)gridDim.x * blockDim.x) {
-        const int j = __ldg(idx + e);
-        if (j == -1) continue;
-        if (j < -1 || j >= Tk) {
+        const PairSlot ps = pair_slot(idx, e, Tq, k, hd);
+        if (ps.j == -1) continue;
+        if (ps.j < -1 || ps.j >= Tk) {
             report(dev_status, SSA_DEV_BAD_INDEX);
             continue;
         }
-        atomicAdd(cnt + (e / per_head) * Tk + j, 1);
+        atomicAdd(cnt + ps.bkv * Tk + ps.j, 1);
     }
 }
 
-// Per head: off[bh*(Tk+1) + j] = sum of cnt over keys < j of the head (so
-// off[.. + Tk] is the head's pair count); cnt becomes the fill cursor (= off).
+// Per key/value head (one block each): off[bkv*(Tk+1) + j] = sum of cnt over
+// keys < j of the head (so off[.. + Tk] is the head's pair count); cnt
+// becomes the fill cursor (= off).
 constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(kScanThreads) pair_scan_kernel(int32_t* __restrict__ cnt,
                                                                  int32_t* __restrict__ off,
                                                                  int Tk) {
     __shared__ int32_t part[kScanThreads];
-    const int64_t bh = blockIdx.x;
-    int32_t* c = cnt + bh * Tk;
-    int32_t* o = off + bh * (int64_t)(Tk + 1);
+    const int64_t bkv = blockIdx.x;
+    int32_t* c = cnt + bkv * Tk;
+    int32_t* o = off + bkv * (int64_t)(Tk + 1);
     const int per = (Tk + kScanThreads - 1) / kScanThreads;
     const int lo = min(Tk, (int)threadIdx.x * per), hi = min(Tk, lo + per);
     int32_t local = 0;
@@ -296,32 +335,35 @@ __global__ void __launch_bounds__(kScanThreads) pair_scan_kernel(int32_t* __rest
     if (threadIdx.x == kScanThreads - 1) o[Tk] = part[kScanThreads - 1];
 }
 
-// list[bh*Tq*k + pos] = i*k + t for every usable slot (i, t) of head bh.
+// list[bkv*gk*Tq*k + pos] = the pair id of every usable slot of key/value
+// head bkv, grouped by key (pos from the key's cursor).
 __global__ void pair_fill_kernel(const int32_t* __restrict__ idx, int64_t entries, int Tq, int Tk,
-                                 int k, int32_t* __restrict__ cursor, int32_t* __restrict__ list) {
-    const int64_t per_head = (int64_t)Tq * k;
+                                 int k, const BwdHeads hd, int32_t* __restrict__ cursor,
+                                 int32_t* __restrict__ list) {
+    const int64_t per_kv = (int64_t)hd.gk * Tq * k;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < entries;
          e += (int64_t)gridDim.x * blockDim.x) {
-        const int j = __ldg(idx + e);
-        if (j < 0 || j >= Tk) continue;
-        const int64_t bh = e / per_head;
-        const int32_t pos = atomicAdd(cursor + bh * Tk + j, 1);
-        list[bh * per_head + pos] = static_cast<int32_t>(e - bh * per_head);
+        const PairSlot ps = pair_slot(idx, e, Tq, k, hd);
+        if (ps.j < 0 || ps.j >= Tk) continue;
+        const int32_t pos = atomicAdd(cursor + ps.bkv * Tk + ps.j, 1);
+        list[ps.bkv * per_kv + pos] = ps.pid;
     }
 }
 
 // ---------------------------------------------------------------- key side
 
-// One warp per key (bh, j): for every pair id pid = i*k + t of its list,
-// acc1 += w1[pid] * X1_i and acc2 += w2[pid] * X2_i, with X1/X2 rows of
-// [BH, Tq, D] (slot weights read from [BH, Tq, k] arrays at bh*Tq*k + pid).
-// out1 = f1 * acc1, out2 = acc2 (fp32 [BH, Tk, D]). TWO == false: only the
-// first sum (the scorer's dk_low).
+// One warp per key (bkv, j) of the key/value heads: for every pair id
+// pid = (h_g * Tq + i) * k + t of its list (query head h = hkv * gk + h_g of
+// the same batch), acc1 += w1[slot] * X1[qrow] and acc2 += w2[slot] *
+// X2[qrow], with qrow = (b * H + h) * Tq + i a row of the [B, H, Tq, D]
+// arrays X1/X2 and slot = qrow * k + t one of the [B, H, Tq, k] weights.
+// out1 = f1 * acc1, out2 = acc2 (fp32 [B, H / gk, Tk, D]). TWO == false: only
+// the first sum (the scorer's dk_low).
 template <bool BF16_IN, int D, bool TWO>
 __global__ void __launch_bounds__(256) pair_key_kernel(
     const void* __restrict__ X1, const void* __restrict__ X2, const float* __restrict__ w1,
     const float* __restrict__ w2, const int32_t* __restrict__ off, const int32_t* __restrict__ list,
-    int64_t keys, int Tq, int Tk, int k, float f1, float* __restrict__ out1,
+    int64_t keys, int Tq, int Tk, int k, const BwdHeads hd, float f1, float* __restrict__ out1,
     float* __restrict__ out2) {
     using Gm = BwdGeom<BF16_IN, D>;
     constexpr int L = Gm::L, G = Gm::G, E = Gm::E, R = Gm::R;
@@ -329,35 +371,38 @@ __global__ void __launch_bounds__(256) pair_key_kernel(
     const int64_t key = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (key >= keys) return;
     const int g = lane / L, s = lane % L;
-    const int64_t bh = key / Tk;
-    const int j = (int)(key - bh * Tk);
-    const int64_t per_head = (int64_t)Tq * k;
-    const int32_t* o = off + bh * (int64_t)(Tk + 1);
+    const int64_t bkv = key / Tk;
+    const int j = (int)(key - bkv * Tk);
+    const int Hkv = hd.H / hd.gk;
+    const int64_t b = bkv / Hkv;
+    const int hkv = (int)(bkv - b * Hkv);
+    const int64_t per_q = (int64_t)Tq * k;               // pair ids of one query head
+    const int32_t* o = off + bkv * (int64_t)(Tk + 1);
     const int32_t beg = o[j], end = o[j + 1];
-    const int32_t* lst = list + bh * per_head;
-    const float* w1h = w1 + bh * per_head;
-    const float* w2h = TWO ? w2 + bh * per_head : nullptr;
-    const char* X1b = reinterpret_cast<const char*>(X1) + bh * (int64_t)Tq * R + s * 16;
-    const char* X2b = TWO ? reinterpret_cast<const char*>(X2) + bh * (int64_t)Tq * R + s * 16
-                          : nullptr;
+    const int32_t* lst = list + bkv * (int64_t)hd.gk * per_q;
+    const int64_t row0 = (b * hd.H + (int64_t)hkv * hd.gk) * Tq;   // first query row of the group
+    const char* X1b = reinterpret_cast<const char*>(X1) + s * 16;
+    const char* X2b = TWO ? reinterpret_cast<const char*>(X2) + s * 16 : nullptr;
 
     float a1[E], a2[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) a1[e] = a2[e] = 0.f;
     for (int c0 = beg; c0 < end; c0 += 32) {
         const int n = min(32, end - c0);
-        int32_t pid = 0;
+        int64_t qrow = row0;   // this lane's pair: its query row (row0 for lanes past n)
         float x1 = 0.f, x2 = 0.f;
         if (lane < n) {
-            pid = __ldg(lst + c0 + lane);
-            x1 = __ldg(w1h + pid);
-            if constexpr (TWO) x2 = __ldg(w2h + pid);
+            const int32_t pid = __ldg(lst + c0 + lane);
+            const int64_t qi = pid / k;                   // h_g * Tq + i
+            qrow = row0 + qi;
+            const int64_t slot = qrow * k + (pid - qi * k);
+            x1 = __ldg(w1 + slot);
+            if constexpr (TWO) x2 = __ldg(w2 + slot);
         }
-        const int i_mine = pid / k;   // query row of this lane's pair (0 for lanes past n)
 #pragma unroll
         for (int r = 0; r < L; ++r) {
             const int sl = r * G + g;   // pair slot handled by this lane group in round r
-            const int ic = __shfl_sync(0xffffffffu, i_mine, sl);
+            const int64_t ic = __shfl_sync(0xffffffffu, qrow, sl);
             const float c1 = __shfl_sync(0xffffffffu, x1, sl);
             const float c2 = __shfl_sync(0xffffffffu, x2, sl);
             if (sl < n) {
@@ -460,38 +505,55 @@ unsigned stride_grid(int64_t n) {
     return (unsigned)(b < 148 * 16 ? (b > 0 ? b : 1) : 148 * 16);
 }
 
-// Key-major lists of every head's usable slots: off [BH, Tk+1] and list
-// [BH, Tq*k] (pair ids), with cnt [BH, Tk] as scratch.
-cudaError_t pair_lists_build(const int32_t* idx, int BH, int Tq, int Tk, int k, int32_t* cnt,
-                             int32_t* off, int32_t* list, int32_t* dev_status,
+// Key-major lists of the usable slots of every key/value head: off
+// [B*Hkv, Tk+1] and list [B*Hkv, gk*Tq*k] (pair ids), with cnt [B*Hkv, Tk] as
+// scratch (Hkv = H / gk key/value heads).
+cudaError_t pair_lists_build(const int32_t* idx, int B, int Tq, int Tk, int k, const BwdHeads& hd,
+                             int32_t* cnt, int32_t* off, int32_t* list, int32_t* dev_status,
                              cudaStream_t stream) {
-    const int64_t entries = (int64_t)BH * Tq * k;
-    cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * (size_t)BH * Tk, stream);
+    const int64_t entries = (int64_t)B * hd.H * Tq * k;
+    const int64_t key_heads = (int64_t)B * (hd.H / hd.gk);
+    cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int32_t) * (size_t)(key_heads * Tk), stream);
     if (e != cudaSuccess) return e;
     {
         TraceLaunch tr("pair_lists.count", stream);
         auto* kc = &pair_count_kernel;
-        SSA_LAUNCH(kc, stride_grid(entries), 256, stream, idx, entries, Tq, Tk, k, cnt, dev_status);
+        SSA_LAUNCH(kc, stride_grid(entries), 256, stream, idx, entries, Tq, Tk, k, hd, cnt,
+                   dev_status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     {
         TraceLaunch tr("pair_lists.scan", stream);
         auto* ks = &pair_scan_kernel;
-        SSA_LAUNCH(ks, (unsigned)BH, kScanThreads, stream, cnt, off, Tk);
+        SSA_LAUNCH(ks, (unsigned)key_heads, kScanThreads, stream, cnt, off, Tk);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     TraceLaunch tr("pair_lists.fill", stream);
     auto* kf = &pair_fill_kernel;
-    SSA_LAUNCH(kf, stride_grid(entries), 256, stream, idx, entries, Tq, Tk, k, cnt, list);
+    SSA_LAUNCH(kf, stride_grid(entries), 256, stream, idx, entries, Tq, Tk, k, hd, cnt, list);
     return cudaGetLastError();
+}
+
+// dS summed over the gi query heads that share each index head:
+// out[B, H/gi, Tq, k] from dS[B, H, Tq, k].
+__global__ void pair_grad_group_sum_kernel(const float* __restrict__ dS, int64_t n_out,
+                                           int64_t per_head, int gi, float* __restrict__ out) {
+    for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < n_out;
+         o += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t bhi = o / per_head, rem = o - bhi * per_head;
+        float acc = 0.f;
+        for (int gg = 0; gg < gi; ++gg) acc += __ldg(dS + (bhi * gi + gg) * per_head + rem);
+        out[o] = acc;
+    }
 }
 
 template <bool BF, int DD>
 cudaError_t attn_bwd_t(const void* Q, const void* K, const void* V, const void* dO,
-                       const int32_t* idx, int BH, int Tq, int Tk, int k, float scale, float* dQ,
-                       float* dK, float* dV, float* dS, float* prob, int32_t* cnt, int32_t* off,
-                       int32_t* list, int32_t* dev_status, cudaStream_t stream) {
-    const int64_t rows = (int64_t)BH * Tq, keys = (int64_t)BH * Tk;
+                       const int32_t* idx, int B, int Tq, int Tk, int k, const BwdHeads& hd,
+                       float scale, float* dQ, float* dK, float* dV, float* dS, float* prob,
+                       int32_t* cnt, int32_t* off, int32_t* list, int32_t* dev_status,
+                       cudaStream_t stream) {
+    const int64_t rows = (int64_t)B * hd.H * Tq, keys = (int64_t)B * (hd.H / hd.gk) * Tk;
     const int64_t qb = warp_blocks(rows), kb = warp_blocks(keys);
     if (qb < 0 || kb < 0) return cudaErrorInvalidConfiguration;
     cudaError_t e;
@@ -499,38 +561,52 @@ cudaError_t attn_bwd_t(const void* Q, const void* K, const void* V, const void* 
         TraceLaunch tr("attn_bwd.query", stream);
         auto* kq = &attn_bwd_query_kernel<BF, DD>;
         SSA_LAUNCH(kq, (unsigned)qb, kBwdWarps * 32, stream, Q, K, V, dO, idx, rows, Tq, Tk, k,
-                   scale, dQ, dS, prob, dev_status);
+                   scale, hd, dQ, dS, prob, dev_status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (kb == 0) return cudaSuccess;
-    if ((e = pair_lists_build(idx, BH, Tq, Tk, k, cnt, off, list, dev_status, stream)) !=
+    if ((e = pair_lists_build(idx, B, Tq, Tk, k, hd, cnt, off, list, dev_status, stream)) !=
         cudaSuccess)
         return e;
     TraceLaunch tr("attn_bwd.key", stream);
     auto* kk = &pair_key_kernel<BF, DD, true>;
     SSA_LAUNCH(kk, (unsigned)kb, kBwdWarps * 32, stream, Q, dO, dS, prob, off, list, keys, Tq, Tk,
-               k, scale, dK, dV);
+               k, hd, scale, dK, dV);
     return cudaGetLastError();
 }
 
+// The scorer's backward on H_idx scorer heads (idx, q_low, k_low) from the
+// pair gradients of H = gi * H_idx query heads: those are first summed over
+// each index head's query heads (into dS_sum), then every scorer head is a
+// plain head of its own.
 template <bool BF, int PP>
 cudaError_t scorer_bwd_t(const void* q_low, const void* k_low, const int32_t* idx,
-                         const float* dS, int BH, int Tq, int Tk, int k, float sigma,
-                         float* dq_low, float* dk_low, int32_t* cnt, int32_t* off, int32_t* list,
-                         int32_t* dev_status, cudaStream_t stream) {
-    const int64_t rows = (int64_t)BH * Tq, keys = (int64_t)BH * Tk;
+                         const float* dS, int B, int H_idx, int gi, int Tq, int Tk, int k,
+                         float sigma, float* dq_low, float* dk_low, float* dS_sum, int32_t* cnt,
+                         int32_t* off, int32_t* list, int32_t* dev_status, cudaStream_t stream) {
+    const int64_t rows = (int64_t)B * H_idx * Tq, keys = (int64_t)B * H_idx * Tk;
     const int64_t qb = warp_blocks(rows), kb = warp_blocks(keys);
     if (qb < 0 || kb < 0) return cudaErrorInvalidConfiguration;
     cudaError_t e;
+    const float* g = dS;
+    if (gi > 1 && rows > 0) {
+        TraceLaunch tr("scorer_bwd.group_sum", stream);
+        auto* ksum = &pair_grad_group_sum_kernel;
+        SSA_LAUNCH(ksum, stride_grid(rows * k), 256, stream, dS, rows * k, (int64_t)Tq * k, gi,
+                   dS_sum);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        g = dS_sum;
+    }
     if (qb > 0) {
         TraceLaunch tr("scorer_bwd.query", stream);
         auto* kq = &scorer_bwd_query_kernel<BF, PP>;
-        SSA_LAUNCH(kq, (unsigned)qb, kBwdWarps * 32, stream, k_low, idx, dS, rows, Tq, Tk, k,
+        SSA_LAUNCH(kq, (unsigned)qb, kBwdWarps * 32, stream, k_low, idx, g, rows, Tq, Tk, k,
                    sigma, dq_low, dev_status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (kb == 0) return cudaSuccess;
-    if ((e = pair_lists_build(idx, BH, Tq, Tk, k, cnt, off, list, dev_status, stream)) !=
+    const BwdHeads plain{H_idx, 1, 1};
+    if ((e = pair_lists_build(idx, B, Tq, Tk, k, plain, cnt, off, list, dev_status, stream)) !=
         cudaSuccess)
         return e;
     TraceLaunch tr("scorer_bwd.key", stream);
@@ -538,22 +614,23 @@ cudaError_t scorer_bwd_t(const void* q_low, const void* k_low, const int32_t* id
     const void* no_x = nullptr;
     const float* no_w = nullptr;
     float* no_out = nullptr;
-    SSA_LAUNCH(kk, (unsigned)kb, kBwdWarps * 32, stream, q_low, no_x, dS, no_w, off, list, keys,
-               Tq, Tk, k, sigma, dk_low, no_out);
+    SSA_LAUNCH(kk, (unsigned)kb, kBwdWarps * 32, stream, q_low, no_x, g, no_w, off, list, keys,
+               Tq, Tk, k, plain, sigma, dk_low, no_out);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t attn_bwd_launch(const void* Q, const void* K, const void* V, const void* dO,
-                            bool bf16, int D, const int32_t* idx, int BH, int Tq, int Tk, int k,
-                            float scale, float* dQ, float* dK, float* dV, float* dS, float* prob,
-                            int32_t* cnt, int32_t* off, int32_t* list, int32_t* dev_status,
-                            cudaStream_t stream) {
+                            bool bf16, int D, const int32_t* idx, int B, int H, int H_kv,
+                            int H_idx, int Tq, int Tk, int k, float scale, float* dQ, float* dK,
+                            float* dV, float* dS, float* prob, int32_t* cnt, int32_t* off,
+                            int32_t* list, int32_t* dev_status, cudaStream_t stream) {
+    const BwdHeads hd{H, H / H_kv, H / H_idx};
 #define SSA_BWD_CASE(BF, DD)                                                                  \
     if (bf16 == BF && D == DD)                                                                \
-        return attn_bwd_t<BF, DD>(Q, K, V, dO, idx, BH, Tq, Tk, k, scale, dQ, dK, dV, dS, prob, \
-                                  cnt, off, list, dev_status, stream);
+        return attn_bwd_t<BF, DD>(Q, K, V, dO, idx, B, Tq, Tk, k, hd, scale, dQ, dK, dV, dS,   \
+                                  prob, cnt, off, list, dev_status, stream);
     SSA_BWD_CASE(true, 64)
     SSA_BWD_CASE(true, 128)
     SSA_BWD_CASE(false, 64)
@@ -563,14 +640,15 @@ cudaError_t attn_bwd_launch(const void* Q, const void* K, const void* V, const v
 }
 
 cudaError_t scorer_bwd_launch(const void* q_low, const void* k_low, bool bf16, int P,
-                              const int32_t* idx, const float* dS, int BH, int Tq, int Tk, int k,
-                              float sigma, float* dq_low, float* dk_low, int32_t* cnt,
-                              int32_t* off, int32_t* list, int32_t* dev_status,
-                              cudaStream_t stream) {
+                              const int32_t* idx, const float* dS, int B, int H, int H_idx,
+                              int Tq, int Tk, int k, float sigma, float* dq_low, float* dk_low,
+                              float* dS_sum, int32_t* cnt, int32_t* off, int32_t* list,
+                              int32_t* dev_status, cudaStream_t stream) {
+    const int gi = H / H_idx;
 #define SSA_SBWD_CASE(BF, PP)                                                                 \
     if (bf16 == BF && P == PP)                                                                \
-        return scorer_bwd_t<BF, PP>(q_low, k_low, idx, dS, BH, Tq, Tk, k, sigma, dq_low, dk_low, \
-                                    cnt, off, list, dev_status, stream);
+        return scorer_bwd_t<BF, PP>(q_low, k_low, idx, dS, B, H_idx, gi, Tq, Tk, k, sigma,     \
+                                    dq_low, dk_low, dS_sum, cnt, off, list, dev_status, stream);
     SSA_SBWD_CASE(true, 16)
     SSA_SBWD_CASE(true, 32)
     SSA_SBWD_CASE(true, 64)
@@ -593,41 +671,100 @@ namespace {
 int64_t up256(int64_t x) { return (x + 255) / 256 * 256; }
 
 struct BwdWorkspace {
-    int64_t cnt, off, list, prob, total;
+    int64_t cnt, off, list, extra, total;
 };
 
-// cnt [BH*Tk] | off [BH*(Tk+1)] | list [BH*Tq*k] | prob [BH*Tq*k] (attention only)
-BwdWorkspace bwd_workspace(int64_t BH, int64_t Tq, int64_t Tk, int64_t k, bool with_prob) {
+// cnt [KH*Tk] | off [KH*(Tk+1)] | list [slots] | extra [extra_floats] fp32,
+// KH key heads and `slots` query-head slots (B*H*Tq*k).
+BwdWorkspace bwd_workspace(int64_t KH, int64_t Tk, int64_t slots, int64_t extra_floats) {
     BwdWorkspace w;
     int64_t o = 0;
     w.cnt = o;
-    o += up256(BH * Tk * 4);
+    o += up256(KH * Tk * 4);
     w.off = o;
-    o += up256(BH * (Tk + 1) * 4);
+    o += up256(KH * (Tk + 1) * 4);
     w.list = o;
-    o += up256(BH * Tq * k * 4);
-    w.prob = o;
-    if (with_prob) o += up256(BH * Tq * k * 4);
+    o += up256(slots * 4);
+    w.extra = o;
+    o += up256(extra_floats * 4);
     w.total = o > 0 ? o : 256;
     return w;
 }
 
 bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-}  // namespace
+bool heads_ok(int H, int Hs) { return H >= 1 && Hs >= 1 && H % Hs == 0; }
 
+}  // namespace
 }  // namespace ssa
 
 extern "C" {
 
+size_t ssa_sparse_attn_grouped_bwd_workspace_size(int B, int H, int H_kv, int Tq, int Tk, int k) {
+    if (B < 0 || Tq < 0 || Tk < 0 || k < 1 || !ssa::heads_ok(H, H_kv)) return 0;
+    const int64_t slots = (int64_t)B * H * Tq * k;
+    return (size_t)ssa::bwd_workspace((int64_t)B * H_kv, Tk, slots, slots).total;
+}
+
 size_t ssa_sparse_attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int k) {
-    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || k < 1) return 0;
-    return (size_t)ssa::bwd_workspace((int64_t)B * H, Tq, Tk, k, true).total;
+    if (H < 0) return 0;
+    return H == 0 ? ssa_sparse_attn_grouped_bwd_workspace_size(B, 1, 1, 0, Tk, k)
+                  : ssa_sparse_attn_grouped_bwd_workspace_size(B, H, H, Tq, Tk, k);
+}
+
+size_t ssa_scorer_grouped_bwd_workspace_size(int B, int H, int H_idx, int Tq, int Tk, int k) {
+    if (B < 0 || Tq < 0 || Tk < 0 || k < 1 || !ssa::heads_ok(H, H_idx)) return 0;
+    const int64_t slots = (int64_t)B * H_idx * Tq * k;
+    return (size_t)ssa::bwd_workspace((int64_t)B * H_idx, Tk, slots, H > H_idx ? slots : 0).total;
 }
 
 size_t ssa_scorer_bwd_workspace_size(int B, int H, int Tq, int Tk, int k) {
-    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || k < 1) return 0;
-    return (size_t)ssa::bwd_workspace((int64_t)B * H, Tq, Tk, k, false).total;
+    if (H < 0) return 0;
+    return H == 0 ? ssa_scorer_grouped_bwd_workspace_size(B, 1, 1, 0, Tk, k)
+                  : ssa_scorer_grouped_bwd_workspace_size(B, H, H, Tq, Tk, k);
+}
+
+ssa_status ssa_sparse_attn_grouped_bwd(const void* Q, const void* K, const void* V,
+                                       const void* dO, int dtype, int B, int H, int H_kv, int Tq,
+                                       int Tk, int D, const int32_t* idx, int H_idx, int k,
+                                       float scale, float* dQ, float* dK, float* dV, float* dS,
+                                       float* prob, void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_status, void* stream) {
+    if (B < 0 || Tq < 0 || Tk < 0 || k < 1 || (dtype != SSA_F32 && dtype != SSA_BF16) ||
+        !isfinite(scale) || !ssa::heads_ok(H, H_kv) || !ssa::heads_ok(H, H_idx))
+        return SSA_ERR_INVALID;
+    if (!(D == 64 || D == 128)) return SSA_ERR_UNSUPPORTED;
+    // pair ids are 32-bit per key/value head
+    if ((int64_t)(H / H_kv) * Tq * k > INT32_MAX) return SSA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)B * H * Tq, keys = (int64_t)B * H_kv * Tk;
+    if (rows == 0 && keys == 0) return SSA_OK;
+    if ((int64_t)B * H > INT32_MAX) return SSA_ERR_UNSUPPORTED;
+    // query-side buffers are needed when there are query rows, key-side ones
+    // when there are keys; every pointer given must be aligned
+    if (rows > 0 && (!Q || !dO || !idx || !dQ || !dS)) return SSA_ERR_INVALID;
+    if (keys > 0 && (!K || !V || !dK || !dV)) return SSA_ERR_INVALID;
+    if (!ssa::al(Q, 16) || !ssa::al(K, 16) || !ssa::al(V, 16) || !ssa::al(dO, 16) ||
+        !ssa::al(dQ, 16) || !ssa::al(dK, 16) || !ssa::al(dV, 16) || !ssa::al(dS, 4) ||
+        !ssa::al(idx, 4) || !ssa::al(prob, 4) || !ssa::al(dev_status, 4))
+        return SSA_ERR_INVALID;
+    const int64_t slots = rows * k;
+    const ssa::BwdWorkspace w = ssa::bwd_workspace((int64_t)B * H_kv, Tk, slots, slots);
+    if (!workspace || !ssa::al(workspace, 256) || workspace_bytes < (size_t)w.total)
+        return SSA_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    float* pr = prob ? prob : reinterpret_cast<float*>(ws + w.extra);
+    const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)D));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (rows == 0) {   // no query rows: every key's gradient is zero
+        cudaError_t e = cudaMemsetAsync(dK, 0, sizeof(float) * (size_t)(keys * D), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dV, 0, sizeof(float) * (size_t)(keys * D), s);
+        return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
+    }
+    const cudaError_t e = ssa::attn_bwd_launch(
+        Q, K, V, dO, dtype == SSA_BF16, D, idx, B, H, H_kv, H_idx, Tq, Tk, k, sc, dQ, dK, dV, dS,
+        pr, reinterpret_cast<int32_t*>(ws + w.cnt), reinterpret_cast<int32_t*>(ws + w.off),
+        reinterpret_cast<int32_t*>(ws + w.list), dev_status, s);
+    return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
 }
 
 ssa_status ssa_sparse_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
@@ -635,38 +772,53 @@ ssa_status ssa_sparse_attn_bwd(const void* Q, const void* K, const void* V, cons
                                int k, float scale, float* dQ, float* dK, float* dV, float* dS,
                                float* prob, void* workspace, size_t workspace_bytes,
                                int32_t* dev_status, void* stream) {
-    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || k < 1 || (dtype != SSA_F32 && dtype != SSA_BF16) ||
-        !isfinite(scale))
+    if (H < 0) return SSA_ERR_INVALID;
+    if (H == 0) {   // no heads: nothing to do once the other arguments are valid
+        if (B < 0 || Tq < 0 || Tk < 0 || k < 1 || (dtype != SSA_F32 && dtype != SSA_BF16) ||
+            !isfinite(scale))
+            return SSA_ERR_INVALID;
+        return (D == 64 || D == 128) ? SSA_OK : SSA_ERR_UNSUPPORTED;
+    }
+    return ssa_sparse_attn_grouped_bwd(Q, K, V, dO, dtype, B, H, H, Tq, Tk, D, idx, H, k, scale,
+                                       dQ, dK, dV, dS, prob, workspace, workspace_bytes,
+                                       dev_status, stream);
+}
+
+ssa_status ssa_scorer_grouped_bwd(const void* q_low, const void* k_low, int dtype, int B, int H,
+                                  int H_idx, int Tq, int Tk, int P, const int32_t* idx, int k,
+                                  const float* dS, float scale, float* dq_low, float* dk_low,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                  void* stream) {
+    if (B < 0 || Tq < 0 || Tk < 0 || k < 1 || (dtype != SSA_F32 && dtype != SSA_BF16) ||
+        !isfinite(scale) || !ssa::heads_ok(H, H_idx))
         return SSA_ERR_INVALID;
-    if (!(D == 64 || D == 128)) return SSA_ERR_UNSUPPORTED;
-    if ((int64_t)Tq * k > INT32_MAX) return SSA_ERR_UNSUPPORTED;   // pair ids are 32-bit per head
-    const int64_t BH = (int64_t)B * H;
-    if (BH * Tq == 0 && BH * Tk == 0) return SSA_OK;
-    if (BH > INT32_MAX) return SSA_ERR_UNSUPPORTED;
-    // query-side buffers are needed when there are query rows, key-side ones
-    // when there are keys; every pointer given must be aligned
-    if (BH * Tq > 0 && (!Q || !dO || !idx || !dQ || !dS)) return SSA_ERR_INVALID;
-    if (BH * Tk > 0 && (!K || !V || !dK || !dV)) return SSA_ERR_INVALID;
-    if (!ssa::al(Q, 16) || !ssa::al(K, 16) || !ssa::al(V, 16) || !ssa::al(dO, 16) ||
-        !ssa::al(dQ, 16) || !ssa::al(dK, 16) || !ssa::al(dV, 16) || !ssa::al(dS, 4) ||
-        !ssa::al(idx, 4) || !ssa::al(prob, 4) || !ssa::al(dev_status, 4))
+    if (!(P == 16 || P == 32 || P == 64 || P == 128)) return SSA_ERR_UNSUPPORTED;
+    if ((int64_t)Tq * k > INT32_MAX) return SSA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)B * H_idx * Tq, keys = (int64_t)B * H_idx * Tk;
+    if (rows == 0 && keys == 0) return SSA_OK;
+    if ((int64_t)B * H > INT32_MAX) return SSA_ERR_UNSUPPORTED;
+    if (rows > 0 && (!q_low || !idx || !dS || !dq_low)) return SSA_ERR_INVALID;
+    if (keys > 0 && (!k_low || !dk_low)) return SSA_ERR_INVALID;
+    if (!ssa::al(q_low, 16) || !ssa::al(k_low, 16) || !ssa::al(dq_low, 16) ||
+        !ssa::al(dk_low, 16) || !ssa::al(dS, 4) || !ssa::al(idx, 4) || !ssa::al(dev_status, 4))
         return SSA_ERR_INVALID;
-    const ssa::BwdWorkspace w = ssa::bwd_workspace(BH, Tq, Tk, k, true);
+    const int64_t slots = rows * k;
+    const ssa::BwdWorkspace w =
+        ssa::bwd_workspace((int64_t)B * H_idx, Tk, slots, H > H_idx ? slots : 0);
     if (!workspace || !ssa::al(workspace, 256) || workspace_bytes < (size_t)w.total)
         return SSA_ERR_WORKSPACE;
     char* ws = static_cast<char*>(workspace);
-    float* pr = prob ? prob : reinterpret_cast<float*>(ws + w.prob);
-    const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)D));
+    const float sg = scale > 0.f ? scale : (float)(1.0 / sqrt((double)P));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (BH * Tq == 0) {   // no query rows: every key's gradient is zero
-        cudaError_t e = cudaMemsetAsync(dK, 0, sizeof(float) * (size_t)(BH * Tk * D), s);
-        if (e == cudaSuccess) e = cudaMemsetAsync(dV, 0, sizeof(float) * (size_t)(BH * Tk * D), s);
+    if (rows == 0) {
+        const cudaError_t e = cudaMemsetAsync(dk_low, 0, sizeof(float) * (size_t)(keys * P), s);
         return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
     }
-    const cudaError_t e = ssa::attn_bwd_launch(
-        Q, K, V, dO, dtype == SSA_BF16, D, idx, (int)BH, Tq, Tk, k, sc, dQ, dK, dV, dS, pr,
-        reinterpret_cast<int32_t*>(ws + w.cnt), reinterpret_cast<int32_t*>(ws + w.off),
-        reinterpret_cast<int32_t*>(ws + w.list), dev_status, s);
+    const cudaError_t e = ssa::scorer_bwd_launch(
+        q_low, k_low, dtype == SSA_BF16, P, idx, dS, B, H, H_idx, Tq, Tk, k, sg, dq_low, dk_low,
+        reinterpret_cast<float*>(ws + w.extra), reinterpret_cast<int32_t*>(ws + w.cnt),
+        reinterpret_cast<int32_t*>(ws + w.off), reinterpret_cast<int32_t*>(ws + w.list),
+        dev_status, s);
     return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
 }
 
@@ -674,35 +826,15 @@ ssa_status ssa_scorer_bwd(const void* q_low, const void* k_low, int dtype, int B
                           int Tk, int P, const int32_t* idx, int k, const float* dS, float scale,
                           float* dq_low, float* dk_low, void* workspace, size_t workspace_bytes,
                           int32_t* dev_status, void* stream) {
-    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || k < 1 || (dtype != SSA_F32 && dtype != SSA_BF16) ||
-        !isfinite(scale))
-        return SSA_ERR_INVALID;
-    if (!(P == 16 || P == 32 || P == 64 || P == 128)) return SSA_ERR_UNSUPPORTED;
-    if ((int64_t)Tq * k > INT32_MAX) return SSA_ERR_UNSUPPORTED;
-    const int64_t BH = (int64_t)B * H;
-    if (BH * Tq == 0 && BH * Tk == 0) return SSA_OK;
-    if (BH > INT32_MAX) return SSA_ERR_UNSUPPORTED;
-    if (BH * Tq > 0 && (!q_low || !idx || !dS || !dq_low)) return SSA_ERR_INVALID;
-    if (BH * Tk > 0 && (!k_low || !dk_low)) return SSA_ERR_INVALID;
-    if (!ssa::al(q_low, 16) || !ssa::al(k_low, 16) || !ssa::al(dq_low, 16) ||
-        !ssa::al(dk_low, 16) || !ssa::al(dS, 4) || !ssa::al(idx, 4) || !ssa::al(dev_status, 4))
-        return SSA_ERR_INVALID;
-    const ssa::BwdWorkspace w = ssa::bwd_workspace(BH, Tq, Tk, k, false);
-    if (!workspace || !ssa::al(workspace, 256) || workspace_bytes < (size_t)w.total)
-        return SSA_ERR_WORKSPACE;
-    char* ws = static_cast<char*>(workspace);
-    const float sg = scale > 0.f ? scale : (float)(1.0 / sqrt((double)P));
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (BH * Tq == 0) {
-        const cudaError_t e = cudaMemsetAsync(dk_low, 0, sizeof(float) * (size_t)(BH * Tk * P), s);
-        return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
+    if (H < 0) return SSA_ERR_INVALID;
+    if (H == 0) {
+        if (B < 0 || Tq < 0 || Tk < 0 || k < 1 || (dtype != SSA_F32 && dtype != SSA_BF16) ||
+            !isfinite(scale))
+            return SSA_ERR_INVALID;
+        return (P == 16 || P == 32 || P == 64 || P == 128) ? SSA_OK : SSA_ERR_UNSUPPORTED;
     }
-    const cudaError_t e = ssa::scorer_bwd_launch(
-        q_low, k_low, dtype == SSA_BF16, P, idx, dS, (int)BH, Tq, Tk, k, sg, dq_low, dk_low,
-        reinterpret_cast<int32_t*>(ws + w.cnt), reinterpret_cast<int32_t*>(ws + w.off),
-        reinterpret_cast<int32_t*>(ws + w.list), dev_status, s);
-    return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
+    return ssa_scorer_grouped_bwd(q_low, k_low, dtype, B, H, H, Tq, Tk, P, idx, k, dS, scale,
+                                  dq_low, dk_low, workspace, workspace_bytes, dev_status, stream);
 }
 
 }  // extern "C"
-

@@ -355,6 +355,31 @@ ssa_status ssa_sparse_attn_bwd(const void* Q, const void* K, const void* V, cons
                                int32_t* dev_status, void* stream);
 
 /*
+ * ssa_sparse_attn_grouped_bwd — ssa_sparse_attn_bwd for the layouts of
+ * ssa_sparse_attn_grouped: query head h (of H) reads key/value head
+ * h / (H / H_kv) and index head h / (H / H_idx) (mhpq.cn/news/1098205,
+ * section 3.2, a scorer shared by all heads; "Attention机制优化：原理、挑战与
+ * 工程实践" (bjdmk.com.cn), sections 3.1-3.2, grouped-query attention).
+ * Each query head's gradients are those of ssa_sparse_attn_bwd on its own
+ * operands. A shared key/value head's dK and dV sum over the query heads
+ * that read it.
+ *
+ *   Q, dO, dQ [B, H, Tq, D]; K, V, dK, dV [B, H_kv, Tk, D]
+ *   idx [B, H_idx, Tq, k]; dS, prob [B, H, Tq, k] (per query head)
+ *   H_kv, H_idx >= 1, each dividing H; (H / H_kv) * Tq * k <= 2^31 - 1
+ *   workspace: ssa_sparse_attn_grouped_bwd_workspace_size(B, H, H_kv, Tq, Tk, k)
+ *
+ * Other rules as ssa_sparse_attn_bwd. H_kv = H_idx = H is ssa_sparse_attn_bwd.
+ */
+size_t ssa_sparse_attn_grouped_bwd_workspace_size(int B, int H, int H_kv, int Tq, int Tk, int k);
+ssa_status ssa_sparse_attn_grouped_bwd(const void* Q, const void* K, const void* V,
+                                       const void* dO, int dtype, int B, int H, int H_kv, int Tq,
+                                       int Tk, int D, const int32_t* idx, int H_idx, int k,
+                                       float scale, float* dQ, float* dK, float* dV, float* dS,
+                                       float* prob, void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_status, void* stream);
+
+/*
  * ssa_scorer_bwd — the scorer's gradients under the same estimator.
  *
  * Source: mhpq.cn/news/1098205, sections 2.2 (S = q_low . k_low^T * scale) and
@@ -374,6 +399,27 @@ ssa_status ssa_scorer_bwd(const void* q_low, const void* k_low, int dtype, int B
                           int Tk, int P, const int32_t* idx, int k, const float* dS, float scale,
                           float* dq_low, float* dk_low, void* workspace, size_t workspace_bytes,
                           int32_t* dev_status, void* stream);
+
+/*
+ * ssa_scorer_grouped_bwd — the scorer's gradients when H query heads share
+ * H_idx scorer heads (H_idx = 1: the shared scorer of mhpq.cn/news/1098205,
+ * section 3.2). The score of a pair in index head hi feeds the logits of
+ * every query head that reads hi. Its gradient is therefore the sum of their
+ * dS, and then the ssa_scorer_bwd formulas apply per scorer head.
+ *
+ *   q_low [B, H_idx, Tq, P], k_low [B, H_idx, Tk, P], idx [B, H_idx, Tq, k]
+ *   dS [B, H, Tq, k] (from ssa_sparse_attn_grouped_bwd); H_idx divides H
+ *   dq_low [B, H_idx, Tq, P], dk_low [B, H_idx, Tk, P] float, written
+ *   workspace: ssa_scorer_grouped_bwd_workspace_size(B, H, H_idx, Tq, Tk, k)
+ *
+ * Other rules as ssa_scorer_bwd. H_idx = H is ssa_scorer_bwd.
+ */
+size_t ssa_scorer_grouped_bwd_workspace_size(int B, int H, int H_idx, int Tq, int Tk, int k);
+ssa_status ssa_scorer_grouped_bwd(const void* q_low, const void* k_low, int dtype, int B, int H,
+                                  int H_idx, int Tq, int Tk, int P, const int32_t* idx, int k,
+                                  const float* dS, float scale, float* dq_low, float* dk_low,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                  void* stream);
 
 /*
  * Launch tracing. Between ssa_trace_begin() and ssa_trace_end(), every kernel

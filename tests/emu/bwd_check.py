@@ -53,6 +53,16 @@ class Emu:
         lib.ssa_sparse_attn_bwd.restype = I
         lib.ssa_scorer_bwd.argtypes = [P, P, I, I, I, I, I, I, P, I, P, F, P, P, P, Z, P, P]
         lib.ssa_scorer_bwd.restype = I
+        lib.ssa_sparse_attn_grouped_bwd_workspace_size.argtypes = [I] * 6
+        lib.ssa_sparse_attn_grouped_bwd_workspace_size.restype = Z
+        lib.ssa_sparse_attn_grouped_bwd.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, I, I, F, P,
+                                                    P, P, P, P, P, Z, P, P]
+        lib.ssa_sparse_attn_grouped_bwd.restype = I
+        lib.ssa_scorer_grouped_bwd_workspace_size.argtypes = [I] * 6
+        lib.ssa_scorer_grouped_bwd_workspace_size.restype = Z
+        lib.ssa_scorer_grouped_bwd.argtypes = [P, P, I, I, I, I, I, I, I, P, I, P, F, P, P, P, Z,
+                                               P, P]
+        lib.ssa_scorer_grouped_bwd.restype = I
         self.libc = libc = ctypes.CDLL(None)
         libc.aligned_alloc.argtypes = [Z, Z]
         libc.aligned_alloc.restype = P
@@ -99,6 +109,51 @@ class Emu:
                                      _p(st), None)
         self.libc.free(ws)
         return rc, dq, dk, int(st[0])
+
+
+def _grouped_attn_bwd(self, Q, K, V, dO, idx):
+    """Q, dO [B,H,Tq,D]; K, V [B,H_kv,Tk,D]; idx [B,H_idx,Tq,k]."""
+    B, H, Tq, D = Q.shape
+    H_kv, Tk = K.shape[1], K.shape[2]
+    H_idx, k = idx.shape[1], idx.shape[3]
+    bufs = [_raw(t) for t in (Q, K, V, dO)]
+    outs = dict(dQ=np.full((B, H, Tq, D), np.nan, np.float32),
+                dK=np.full((B, H_kv, Tk, D), np.nan, np.float32),
+                dV=np.full((B, H_kv, Tk, D), np.nan, np.float32),
+                dS=np.full((B, H, Tq, k), np.nan, np.float32))
+    st = np.zeros(1, np.int32)
+    ix = np.ascontiguousarray(idx, np.int32)
+    n = self.lib.ssa_sparse_attn_grouped_bwd_workspace_size(B, H, H_kv, Tq, Tk, k)
+    ws = self._ws(n)
+    rc = self.lib.ssa_sparse_attn_grouped_bwd(
+        *[_p(b) for b in bufs], int(Q.dtype == torch.bfloat16), B, H, H_kv, Tq, Tk, D, _p(ix),
+        H_idx, k, 0.0, *[_p(outs[n_]) for n_ in ("dQ", "dK", "dV", "dS")], None, ws, n, _p(st),
+        None)
+    self.libc.free(ws)
+    return rc, outs, int(st[0])
+
+
+def _grouped_scorer_bwd(self, ql, kl, idx, dS):
+    """ql, kl, idx with H_idx heads; dS [B,H,Tq,k] of the H query heads."""
+    B, H_idx, Tq, P = ql.shape
+    Tk, k = kl.shape[2], idx.shape[-1]
+    H = dS.shape[1]
+    dq = np.full((B, H_idx, Tq, P), np.nan, np.float32)
+    dk = np.full((B, H_idx, Tk, P), np.nan, np.float32)
+    st = np.zeros(1, np.int32)
+    ix = np.ascontiguousarray(idx, np.int32)
+    g = np.ascontiguousarray(dS, np.float32)
+    n = self.lib.ssa_scorer_grouped_bwd_workspace_size(B, H, H_idx, Tq, Tk, k)
+    ws = self._ws(n)
+    rc = self.lib.ssa_scorer_grouped_bwd(_p(_raw(ql)), _p(_raw(kl)), int(ql.dtype == torch.bfloat16),
+                                         B, H, H_idx, Tq, Tk, P, _p(ix), k, _p(g), 0.0, _p(dq),
+                                         _p(dk), ws, n, _p(st), None)
+    self.libc.free(ws)
+    return rc, dq, dk, int(st[0])
+
+
+Emu.grouped_attn_bwd = _grouped_attn_bwd
+Emu.grouped_scorer_bwd = _grouped_scorer_bwd
 
 
 def _raw(t):
@@ -189,6 +244,46 @@ def check_scorer(emu, case, fails):
     _close(dk, rk, tag + " dk_low", fails)
 
 
+GROUPED_CASES = [
+    # B, H, H_kv, H_idx, Tq, Tk, D, k, dtype
+    (2, 4, 2, 1, 15, 40, 64, 6, torch.bfloat16),     # grouped-query heads, one shared scorer
+    (1, 4, 1, 2, 11, 30, 128, 5, torch.float32),     # one key/value head, two index heads
+    (1, 6, 3, 3, 9, 50, 64, 7, torch.bfloat16),
+    (1, 3, 3, 1, 13, 20, 64, 4, torch.bfloat16),     # the pages' layout: shared scorer only
+]
+
+
+def check_grouped(emu, case, fails):
+    B, H, H_kv, H_idx, Tq, Tk, D, k, dtype = case
+    g = torch.Generator().manual_seed(H * 10 + H_kv)
+    Q = torch.randn(B, H, Tq, D, generator=g).to(dtype)
+    dO = torch.randn(B, H, Tq, D, generator=g).to(dtype)
+    K = torch.randn(B, H_kv, Tk, D, generator=g).to(dtype)
+    V = torch.randn(B, H_kv, Tk, D, generator=g).to(dtype)
+    rng = np.random.default_rng(H_idx + 7 * k)
+    idx = rng.integers(0, Tk, size=(B, H_idx, Tq, k)).astype(np.int32)
+    idx[..., -1] = -1
+    idx[0, 0, 0, :] = -1
+    tag = "grouped %s" % (case,)
+    rc, o, st = emu.grouped_attn_bwd(Q, K, V, dO, idx)
+    if rc != 0 or st != 0:
+        fails.append("%s: status %d, device status %d" % (tag, rc, st))
+        return
+    ref = oracle.sparse_attn_grouped_bwd(Q, K, V, idx, dO)
+    for n_, r in zip(("dQ", "dK", "dV", "dS"), ref):
+        _close(o[n_], r, "%s %s" % (tag, n_), fails)
+    P = 16
+    ql = torch.randn(B, H_idx, Tq, P, generator=g).to(dtype)
+    kl = torch.randn(B, H_idx, Tk, P, generator=g).to(dtype)
+    rc, dq, dk, st = emu.grouped_scorer_bwd(ql, kl, idx, o["dS"])
+    if rc != 0 or st != 0:
+        fails.append("%s scorer: status %d, device status %d" % (tag, rc, st))
+        return
+    rq, rk = oracle.scorer_grouped_bwd(ql, kl, idx, o["dS"])
+    _close(dq, rq, tag + " dq_low", fails)
+    _close(dk, rk, tag + " dk_low", fails)
+
+
 def check_edges(emu, fails):
     # an index outside [-1, Tk): reported, skipped
     Q, K, V, dO, idx = attn_inputs(1, 1, 8, 16, 64, 4, torch.bfloat16, 10)
@@ -245,14 +340,33 @@ def check_binding(emu, fails):
         rq, rk = oracle.scorer_bwd(ql, kl, idx, dS.numpy())
         _close(dq.numpy(), rq, "binding dq_low", fails)
         _close(dk.numpy(), rk, "binding dk_low", fails)
+        # the grouped calls: 4 query heads on 2 key/value heads and 1 scorer head
+        Qg = torch.cat([Q, Q.flip(1)], dim=1)
+        dOg = torch.cat([dO, dO.flip(1)], dim=1)
+        Kg, Vg = torch.cat([K[:, :1], K[:, 1:]], 1), torch.cat([V[:, :1], V[:, 1:]], 1)
+        ig = it[:, :1].contiguous()
+        n = emu.lib.ssa_sparse_attn_grouped_bwd_workspace_size(B, 2 * H, H, Tq, Tk, k)
+        gQ, gK, gV, gS = _native.ssa_sparse_attn_grouped_bwd(Qg, Kg, Vg, ig, dOg, workspace=ws(n))
+        ref = oracle.sparse_attn_grouped_bwd(Qg, Kg, Vg, ig.numpy(), dOg)
+        for n_, a, r in zip(("dQ", "dK", "dV", "dS"), (gQ, gK, gV, gS), ref):
+            _close(a.numpy(), r, "grouped binding " + n_, fails)
+        n = emu.lib.ssa_scorer_grouped_bwd_workspace_size(B, 2 * H, 1, Tq, Tk, k)
+        gq, gk = _native.ssa_scorer_grouped_bwd(ql[:, :1].contiguous(), kl[:, :1].contiguous(), ig,
+                                                gS, workspace=ws(n))
+        rq, rk = oracle.scorer_grouped_bwd(ql[:, :1], kl[:, :1], ig.numpy(), gS.numpy())
+        _close(gq.numpy(), rq, "grouped binding dq_low", fails)
+        _close(gk.numpy(), rk, "grouped binding dk_low", fails)
     finally:
         _native._lib, _native._dev, _native._stream = saved
 
 
-def check_all(path: str, attn_cases=ATTN_CASES, scorer_cases=SCORER_CASES, edges=True):
+def check_all(path: str, attn_cases=ATTN_CASES, scorer_cases=SCORER_CASES, edges=True,
+              grouped_cases=GROUPED_CASES):
     emu = Emu(path)
     fails = []
     check_binding(emu, fails)
+    for c in grouped_cases:
+        check_grouped(emu, c, fails)
     for c in attn_cases:
         check_attn(emu, c, fails)
     for c in scorer_cases:
@@ -266,6 +380,7 @@ if __name__ == "__main__":
     # python bwd_check.py LIB [small]: check (a small set of cases) and exit 1 on a mismatch
     small = len(sys.argv) > 2 and sys.argv[2] == "small"
     f = check_all(sys.argv[1], ATTN_CASES[:2] if small else ATTN_CASES,
-                  SCORER_CASES[:1] if small else SCORER_CASES)
+                  SCORER_CASES[:1] if small else SCORER_CASES,
+                  grouped_cases=GROUPED_CASES[:1] if small else GROUPED_CASES)
     print("\n".join(f) if f else "OK")
     sys.exit(1 if f else 0)

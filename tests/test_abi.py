@@ -231,3 +231,31 @@ def test_host_validation_of_the_backward_calls():
     assert scorer(dS=None) == INV
     assert scorer(wbytes=16) == WS
     assert lib.ssa_scorer_bwd_workspace_size(1, 1, 8, 16, -1) == 0
+
+
+def test_host_validation_of_the_grouped_backward_calls():
+    lib = ssa.load()
+    ok = V(4096)
+    BF16, INV, UNS = _native.SSA_BF16, _native.SSA_ERR_INVALID, _native.SSA_ERR_UNSUPPORTED
+
+    def attn(H=4, H_kv=2, H_idx=1, D=64, Tq=8, k=4):
+        return lib.ssa_sparse_attn_grouped_bwd(ok, ok, ok, ok, BF16, 1, H, H_kv, Tq, 16, D, ok, H_idx,
+                                               k, 0.0, ok, ok, ok, ok, None, ok, 1 << 30, None, None)
+
+    assert attn(H_kv=3) == INV            # does not divide H
+    assert attn(H_idx=0) == INV
+    assert attn(D=96) == UNS
+    assert attn(H=8, H_kv=1, Tq=1 << 20, k=512) == UNS   # 8 query heads' pair ids overflow 32 bits
+    assert lib.ssa_sparse_attn_grouped_bwd_workspace_size(1, 4, 3, 8, 16, 4) == 0
+    assert (lib.ssa_sparse_attn_grouped_bwd_workspace_size(1, 4, 4, 8, 16, 4) ==
+            lib.ssa_sparse_attn_bwd_workspace_size(1, 4, 8, 16, 4))
+
+    def scorer(H=4, H_idx=1, P=64):
+        return lib.ssa_scorer_grouped_bwd(ok, ok, BF16, 1, H, H_idx, 8, 16, P, ok, 4, ok, 0.0, ok,
+                                          ok, ok, 1 << 30, None, None)
+
+    assert scorer(H_idx=3) == INV
+    assert scorer(P=48) == UNS
+    # one scorer head shared by 4 query heads needs room for the summed pair gradients
+    assert (lib.ssa_scorer_grouped_bwd_workspace_size(1, 4, 1, 8, 16, 4) >
+            lib.ssa_scorer_grouped_bwd_workspace_size(1, 1, 1, 8, 16, 4))

@@ -135,6 +135,37 @@ def test_bwd_without_query_rows_zeroes_key_gradients(cuda_dev):
     assert (dK == 0).all() and (dV == 0).all()
 
 
+GROUPED_CASES = [
+    # B, H, H_kv, H_idx, Tq, Tk, D, k, dtype
+    (2, 4, 2, 1, 150, 400, 64, 24, torch.bfloat16),    # grouped-query heads, one shared scorer
+    (1, 4, 1, 2, 110, 300, 128, 40, torch.float32),    # one key/value head, two index heads
+    (1, 8, 8, 1, 130, 500, 128, 64, torch.bfloat16),   # the pages' layout: a shared scorer only
+]
+
+
+@pytest.mark.parametrize("B,H,H_kv,H_idx,Tq,Tk,D,k,dtype", GROUPED_CASES)
+def test_grouped_bwd_matches_oracle(cuda_dev, B, H, H_kv, H_idx, Tq, Tk, D, k, dtype):
+    g = torch.Generator().manual_seed(H * 10 + H_kv)
+    Q = torch.randn(B, H, Tq, D, generator=g).to(dtype)
+    dO = torch.randn(B, H, Tq, D, generator=g).to(dtype)
+    K = torch.randn(B, H_kv, Tk, D, generator=g).to(dtype)
+    V = torch.randn(B, H_kv, Tk, D, generator=g).to(dtype)
+    ql = torch.randn(B, H_idx, Tq, 64, generator=g).to(dtype)
+    kl = torch.randn(B, H_idx, Tk, 64, generator=g).to(dtype)
+    rng = np.random.default_rng(H_idx + 7 * k)
+    idx = rng.integers(0, Tk, size=(B, H_idx, Tq, k)).astype(np.int32)
+    idx[..., -1] = -1
+    idx[0, 0, 0, :] = -1
+    dv = [t.to(cuda_dev) for t in (Q, K, V, torch.from_numpy(idx), dO, ql, kl)]
+    dQ, dK, dV, dS = ssa.ssa_sparse_attn_grouped_bwd(*dv[:5])
+    dq, dk = ssa.ssa_scorer_grouped_bwd(dv[5], dv[6], dv[3], dS)
+    rQ, rK, rV, rS = oracle.sparse_attn_grouped_bwd(Q, K, V, idx, dO)
+    rq, rk = oracle.scorer_grouped_bwd(ql, kl, idx, rS)
+    for a, r, n in ((dQ, rQ, "dQ"), (dK, rK, "dK"), (dV, rV, "dV"), (dS, rS, "dS"),
+                    (dq, rq, "dq_low"), (dk, rk, "dk_low")):
+        _close(a, r, n)
+
+
 # ------------------------------------------------- full-size sampled parity
 
 FULL_TOL = 1e-4   # keys chosen by thousands of rows sum that many fp32 terms
