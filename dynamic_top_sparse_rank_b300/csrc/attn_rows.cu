@@ -22,8 +22,12 @@
 //      row to its accumulator; the G groups are summed at the end.
 // Padding entries (-1) and the tail of the last chunk are masked with a -inf
 // logit (their loads read row 0 of the head, which is always valid memory).
+#ifdef SSA_HOST_EMULATION
+#include "emu_device.h"   // the host stand-in of the CPU tests (tests/emu)
+#else
 #include "common.cuh"
 #include "trace.h"
+#endif
 
 namespace ssa {
 
@@ -69,6 +73,15 @@ SSA_DEVINL float warp_sum(float v) {
 // acc + sum of the products of the 8 bf16 pairs of two 16-byte slices, each
 // product and sum in fp32 (fma.rn.f32.bf16: the bf16 operands need no
 // conversion instruction).
+#ifdef SSA_HOST_EMULATION
+SSA_DEVINL float dot8_bf16(const uint4& a, const uint4& b, float acc) {
+    float fa[8], fb[8];   // bf16 -> fp32 is exact, so one fused multiply-add per pair
+    bf16x8_to_f32(a, fa);
+    bf16x8_to_f32(b, fb);
+    for (int e = 0; e < 8; ++e) acc = fmaf(fa[e], fb[e], acc);
+    return acc;
+}
+#else
 SSA_DEVINL float dot8_bf16(const uint4& a, const uint4& b, float acc) {
     asm("{\n\t.reg .b16 a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3, b4, b5, b6, b7;\n\t"
         "mov.b32 {a0, a1}, %1;\n\t mov.b32 {a2, a3}, %2;\n\t"
@@ -83,6 +96,7 @@ SSA_DEVINL float dot8_bf16(const uint4& a, const uint4& b, float acc) {
         : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w));
     return acc;
 }
+#endif
 
 template <bool BF16_OUT, int E>
 SSA_DEVINL void store_out(void* O, int64_t elem_off, const float* v) {
@@ -265,6 +279,7 @@ __global__ void __launch_bounds__(256, 3) attn_rows_kernel(
     }
 }
 
+#ifndef SSA_HOST_EMULATION   // the CPU tests launch the kernel themselves
 template <bool BF16_IN, int D, bool BF16_OUT, bool BAND>
 static cudaError_t launch_attn_rows(const void* Q, const void* K, const void* V, const int32_t* idx,
                                     void* O, int64_t rows, int Tq, int Tk, int k, int wl, int wr,
@@ -308,5 +323,6 @@ template cudaError_t attn_rows_dispatch<true>(const void*, const void*, const vo
                                               const int32_t*, void*, bool, int64_t, int, int, int,
                                               int, int, float, int32_t*, const HeadMap&,
                                               cudaStream_t);
+#endif  // SSA_HOST_EMULATION
 
 }  // namespace ssa

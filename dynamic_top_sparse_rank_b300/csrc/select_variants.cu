@@ -5,8 +5,12 @@
 // the boundary do not flip between runs; otherwise its slot becomes index -1
 // and score -inf. (The temperature of the same section is a positive factor
 // on the scores: the scale argument of the score calls.)
+#ifdef SSA_HOST_EMULATION
+#include "emu_device.h"   // the host stand-in of the CPU tests (tests/emu)
+#else
 #include "common.cuh"
 #include "trace.h"
+#endif
 
 namespace ssa {
 
@@ -23,6 +27,7 @@ __global__ void smooth_boundary_kernel(int32_t* __restrict__ idx, float* __restr
     }
 }
 
+#ifndef SSA_HOST_EMULATION   // the CPU tests launch the kernel themselves
 // idx / score: [rows, k + 1], sorted by score descending (the output of an
 // exact top-(k+1) selection); k >= 1.
 cudaError_t smooth_boundary_launch(int32_t* idx, float* score, int64_t rows, int k, float delta,
@@ -35,5 +40,6 @@ cudaError_t smooth_boundary_launch(int32_t* idx, float* score, int64_t rows, int
                                                                              delta);
     return cudaGetLastError();
 }
+#endif  // SSA_HOST_EMULATION
 
 }  // namespace ssa

@@ -14,8 +14,12 @@
 // path. The dot products use the same lane layout as the gather kernel: L
 // lanes share one 16-byte-sliced key row, a transpose-reduction leaves one
 // score per lane.
+#ifdef SSA_HOST_EMULATION
+#include "emu_device.h"   // the host stand-in of the CPU tests (tests/emu)
+#else
 #include "common.cuh"
 #include "trace.h"
+#endif
 
 namespace ssa {
 
@@ -295,6 +299,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_rows_kernel(
     }
 }
 
+#ifndef SSA_HOST_EMULATION   // the CPU tests launch the kernel themselves
 // rows_dev != NULL: the number of rows of row_list is read on the device
 // (at most `rows`), so a list built by an earlier kernel needs no host sync.
 cudaError_t topk_rows_dispatch(const void* q_low, const void* k_low, bool bf16, int P,
@@ -323,5 +328,6 @@ cudaError_t topk_rows_dispatch(const void* q_low, const void* k_low, bool bf16, 
 #undef SSA_TOPK_CASE
     return cudaErrorInvalidValue;
 }
+#endif  // SSA_HOST_EMULATION
 
 }  // namespace ssa
