@@ -3,7 +3,9 @@
 // parameters of the tile kernel and the workspace layout of the whole path.
 #pragma once
 
+#ifndef SSA_HOST_EMULATION
 #include <cuda_runtime.h>
+#endif
 #include <float.h>
 #include <math.h>
 #include <stdint.h>

@@ -18,10 +18,15 @@
 // A row with more candidates than its list holds, or with more than 256
 // candidates tied at its k-th score (heavy ties), is put on an overflow list
 // and redone by the row-wise kernel.
+#ifdef SSA_HOST_EMULATION
+#include "emu_device.h"   // the host stand-in of the CPU tests (tests/emu)
+#include "tile.h"
+#else
 #include "common.cuh"
 #include "tile.h"
 #include "tmap.h"
 #include "trace.h"
+#endif
 
 namespace ssa {
 
@@ -42,7 +47,11 @@ constexpr int kSelGStep = kSelThreads / kSelOcts;
 __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
     const uint16_t* __restrict__ gm, uint32_t* __restrict__ tau, int BH, int Tq, int Tk, int k,
     int causal, int G_stride) {
+#ifdef SSA_HOST_EMULATION
+    static uint32_t hist[256 * kSelPairs];
+#else
     extern __shared__ uint32_t hist[];   // 256 * kSelPairs words
+#endif
     __shared__ int n_row[kTileM], g_row[kTileM];   // valid keys, groups with a valid key
     __shared__ uint32_t sel_hi[kTileM], need[kTileM];
     const int units_per_head = (Tq + kUnitM - 1) / kUnitM;
@@ -475,6 +484,7 @@ __global__ void __launch_bounds__(kSortWarps * 32, 4) cand_sort_kernel(
     }
 }
 
+#ifndef SSA_HOST_EMULATION   // the CPU tests launch the kernels themselves
 cudaError_t tile_select_launch(const uint16_t* gm, uint32_t* tau, int BH, int Tq, int Tk, int k,
                                int causal, cudaStream_t stream) {
     const int items = 2 * BH * ((Tq + kUnitM - 1) / kUnitM);
@@ -513,5 +523,6 @@ cudaError_t tile_sort_launch(const uint64_t* cand, const int32_t* cnt, int64_t r
 #undef SSA_SORT_CASE
     return cudaErrorInvalidValue;
 }
+#endif  // SSA_HOST_EMULATION
 
 }  // namespace ssa
