@@ -18,11 +18,14 @@
 // Query side (one warp per query row, the lane layout of the forward gather
 // kernel): one pass over the index list gathers K_j and V_j once, keeps the
 // running max m and, rescaled like the forward's online softmax, the sums
-// s = sum e^(l-m), w = sum e^(l-m) dp, A = sum e^(l-m) dp K_j and
+// s = sum e^(l-m), w = sum e^(l-m) dp, A = sum e^(l-m) (dp - c) K_j and
 // B = sum e^(l-m) K_j; it parks l_t and dp_t in the row's dS and p slots.
-// Then delta = w / s and dQ_i = scale (A - delta B) / s without a second
-// gather, and a pass over the row's own slots turns (l_t, dp_t) into p_t and
-// dS[i][t].
+// Then delta = w / s and dQ_i = scale (A - (delta - c) B) / s without a
+// second gather, and a pass over the row's own slots turns (l_t, dp_t) into
+// p_t and dS[i][t]. The shift c is the dp of the row's first selected key, a
+// stand-in for delta within the spread of the dp: without it A and delta B
+// nearly cancel when the row's dp are close to one another (value rows
+// alike), and dQ would keep only the bits the cancellation leaves.
 //
 // Key side: the index lists are transposed per head into key-major lists of
 // pair ids i*k + t (a counting sort: count, per-head scan, fill), and one warp
@@ -144,6 +147,8 @@ __global__ void __launch_bounds__(256, 2) attn_bwd_query_kernel(
 #pragma unroll
     for (int e = 0; e < E; ++e) A[e] = Bk[e] = 0.f;
     float m = -INFINITY, lsum = 0.f, wsum = 0.f;   // m in log2 units
+    float cshift = 0.f;                             // see the header: set at the first selected key
+    bool have_c = false;
     const int n_entries = Tk > 0 ? k : 0;
     const int32_t* irow = idx + irow_id * (int64_t)k;
     float* dsr = dS + row * (int64_t)k;
@@ -205,6 +210,13 @@ __global__ void __launch_bounds__(256, 2) attn_bwd_query_kernel(
         lsum = lsum * alpha + ew;
         wsum = wsum * alpha + ew * dp;
         m = mn;
+        if (!have_c) {   // warp-uniform: the dp of the first slot with a key
+            const unsigned live = __ballot_sync(0xffffffffu, ok_mine);
+            if (live) {
+                cshift = __shfl_sync(0xffffffffu, dp, __ffs(live) - 1);
+                have_c = true;
+            }
+        }
         if (t0 + slot < n_entries) {   // park l (log2 units) and dp in the row's slots
             dsr[t0 + slot] = lg;
             pr[t0 + slot] = dp;
@@ -220,7 +232,7 @@ __global__ void __launch_bounds__(256, 2) attn_bwd_query_kernel(
         for (int r = 0; r < L; ++r) {
             // slot r*G + g sits in lane (g, r)
             const float er = __shfl_sync(0xffffffffu, ew, g * L + r);
-            const float edr = __shfl_sync(0xffffffffu, ew * dp, g * L + r);
+            const float edr = __shfl_sync(0xffffffffu, ew * (dp - cshift), g * L + r);
             const int jc = __shfl_sync(0xffffffffu, jj, r * G + g);
             float kf[E];
             Vec16<BF16_IN>::to_f32(ldg16(Kb + (int64_t)jc * R), kf);
@@ -240,7 +252,7 @@ __global__ void __launch_bounds__(256, 2) attn_bwd_query_kernel(
     if (g == 0) {
         float out[E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) out[e] = scale * (A[e] - delta * Bk[e]) * inv;
+        for (int e = 0; e < E; ++e) out[e] = scale * (A[e] - (delta - cshift) * Bk[e]) * inv;
         store_f32<E>(dQ + row * (int64_t)D + s * E, out);
     }
     __syncwarp();   // the parked values were written by other lanes

@@ -281,6 +281,28 @@ def check_grouped(emu, case, fails):
     _close(dk, rk, tag + " dk_low", fails)
 
 
+def check_near_equal_values(emu, fails):
+    """Value rows that differ by 1% of their size make the dp of a row nearly
+    equal, and dQ = sum_t p_t (dp_t - delta) K_t small next to its terms.
+    dQ must keep the accuracy that dS (the same differences) has: 5e-4 of its
+    largest entry. Accumulating dp K unshifted loses about 1e-3 here."""
+    B, H, Tq, Tk, D, k = 1, 1, 16, 600, 128, 512
+    g = torch.Generator().manual_seed(3)
+    Q = torch.randn(B, H, Tq, D, generator=g)
+    K = torch.randn(B, H, Tk, D, generator=g)
+    V = 3 * torch.randn(1, 1, 1, D, generator=g) + 1e-2 * torch.randn(B, H, Tk, D, generator=g)
+    dO = torch.randn(B, H, Tq, D, generator=g)
+    rng = np.random.default_rng(4)
+    idx = np.stack([rng.choice(Tk, k, replace=False) for _ in range(Tq)])[None, None]
+    rc, o, st = emu.attn_bwd(Q, K, V, dO, idx.astype(np.int32))
+    rQ, _, _, rS = oracle.sparse_attn_bwd(Q, K, V, idx, dO)
+    for n_, got, ref in (("dQ", o["dQ"], rQ), ("dS", o["dS"], rS)):
+        err = float(np.abs(got - ref).max())
+        if rc != 0 or not err <= 5e-4 * float(np.abs(ref).max()):
+            fails.append("near-equal value rows: %s error %.3g of max %.3g" % (
+                n_, err, float(np.abs(ref).max())))
+
+
 def check_edges(emu, fails):
     # an index outside [-1, Tk): reported, skipped
     Q, K, V, dO, idx = attn_inputs(1, 1, 8, 16, 64, 4, torch.bfloat16, 10)
@@ -370,6 +392,7 @@ def check_all(path: str, attn_cases=ATTN_CASES, scorer_cases=SCORER_CASES, edges
         check_scorer(emu, c, fails)
     if edges:
         check_edges(emu, fails)
+        check_near_equal_values(emu, fails)
     return fails
 
 
