@@ -47,3 +47,23 @@ def test_two_ranks_independent_batches_and_max_time():
     assert mx0 == mx1 == [2.0, 10.0, float(max(seed0, seed1))]
     assert seed0 != seed1          # each rank its own batch
     assert s0 != s1                # ... so different inputs
+
+
+def test_reference_arm_under_torchrun_prints_one_line():
+    """bench.py --impl reference launched the way the multi-GPU runs launch it
+    (torchrun, two ranks): rank 0 alone runs the oracle and prints one JSON
+    line, the other rank exits 0 without work."""
+    import json
+    import subprocess
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
+           "--warmup", "3", "--workload", "topk_f32_t1024_k32", "--cpu-rows", "128"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
