@@ -27,16 +27,20 @@
 // nearly cancel when the row's dp are close to one another (value rows
 // alike), and dQ would keep only the bits the cancellation leaves.
 //
-// Key side: the index lists are transposed per head into key-major lists of
-// pair ids i*k + t (a counting sort: count, per-head scan, fill), and one warp
-// per key sums over the rows that chose it, gathering Q_i and dO_i (q_low_i
-// for the scorer). No atomics on the gradients; the order of a key's list,
-// and so the fp32 rounding of its sums, depends on the fill's atomics.
+// Key side: the index lists are transposed per key/value head into key-major
+// lists of pair ids (h_g * Tq + i) * k + t, h_g the query head within the
+// group that shares the key/value head (a counting sort: count, scan per
+// key/value head, fill). One warp per key then sums over the rows that chose
+// it, gathering Q_i and dO_i (q_low_i for the scorer). No atomics on the
+// gradients; the order of a key's list, and so the fp32 rounding of its sums,
+// depends on the fill's atomics. With a scorer shared by several query heads,
+// their dS are summed per index head first.
 //
 // Compiled with SSA_HOST_EMULATION (and a host stand-in for common.cuh), the
 // same kernels and C entry points build as plain C++ whose launches run every
-// thread on the host: the CPU tests use that build to check the kernels'
-// indexing and lane layout against the oracle. libssa.so never contains it.
+// thread on the host. The CPU tests use that build to check the kernels'
+// indexing, lane layout and arithmetic against the oracle. libssa.so never
+// contains it.
 #ifdef SSA_HOST_EMULATION
 #include "emu_device.h"   // the host stand-in of the CPU tests (tests/emu)
 #else
