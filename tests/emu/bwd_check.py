@@ -379,6 +379,20 @@ def check_binding(emu, fails):
         _native._lib, _native._dev, _native._stream = saved
 
 
+def check_random_shapes(emu, n, seed, fails):
+    """n seeded random grouped shapes (plain when H_kv = H_idx = H): heads and
+    their sharing, ragged lengths, k from 1 past Tk, head size, dtype."""
+    g = np.random.default_rng(seed)
+    for _ in range(n):
+        H = int(g.choice([1, 2, 4]))
+        H_kv = int(g.choice([d for d in (1, 2, 4) if H % d == 0]))
+        H_idx = int(g.choice([d for d in (1, 2, 4) if H % d == 0]))
+        case = (int(g.integers(1, 3)), H, H_kv, H_idx, int(g.integers(1, 40)),
+                int(g.integers(1, 200)), int(g.choice([64, 128])), int(g.integers(1, 70)),
+                torch.bfloat16 if g.integers(0, 2) else torch.float32)
+        check_grouped(emu, case, fails)
+
+
 def check_all(path: str, attn_cases=ATTN_CASES, scorer_cases=SCORER_CASES, edges=True,
               grouped_cases=GROUPED_CASES):
     emu = Emu(path)
@@ -393,6 +407,8 @@ def check_all(path: str, attn_cases=ATTN_CASES, scorer_cases=SCORER_CASES, edges
     if edges:
         check_edges(emu, fails)
         check_near_equal_values(emu, fails)
+        check_random_shapes(emu, 4 if len(grouped_cases) < len(GROUPED_CASES) else 16, 7,
+                            fails)
     return fails
 
 

@@ -258,6 +258,23 @@ def check_smooth(emu, fails):
             fails.append("smoothing delta %g differs" % delta)
 
 
+def check_random_shapes(emu, n, seed, fails):
+    """n seeded random shapes: heads, sequence lengths (ragged, Tq above and
+    below Tk), k (1 up to past the valid count), d_proj, head size, dtypes,
+    causal or not."""
+    g = np.random.default_rng(seed)
+    for c in range(n):
+        BH = int(g.integers(1, 3))
+        Tq, Tk = int(g.integers(1, 90)), int(g.integers(1, 400))
+        P = int(g.choice([16, 32, 64, 128]))
+        k = int(g.integers(1, min(Tk + 20, 300)))
+        causal = bool(g.integers(0, 2))
+        dtype = torch.bfloat16 if g.integers(0, 2) else torch.float32
+        check_topk(emu, (BH, Tq, Tk, P, k, causal, dtype), fails)
+        D = int(g.choice([64, 128]))
+        check_attn(emu, (BH, Tq, max(Tk, 2), D, k, dtype, bool(g.integers(0, 2))), fails)
+
+
 def check_all(path, small=False):
     emu = Emu(path)
     fails = []
@@ -269,6 +286,7 @@ def check_all(path, small=False):
     check_window(emu, fails)
     check_grouped(emu, fails)
     check_smooth(emu, fails)
+    check_random_shapes(emu, 4 if small else 24, 2024, fails)
     return fails
 
 
