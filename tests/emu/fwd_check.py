@@ -131,6 +131,8 @@ TOPK_CASES = [
     (1, 9, 1000, 128, 100, True, torch.bfloat16),   # Tq < Tk, several digits of the radix select
     (2, 12, 77, 64, 77, False, torch.float32),      # k = Tk: every key
     (1, 6, 150, 64, 5, False, torch.bfloat16),
+    (1, 2, 6000, 64, 512, False, torch.bfloat16),   # the decode shape's k
+    (1, 1, 5000, 128, 2048, False, torch.float32),  # the largest k
 ]
 
 
