@@ -221,6 +221,7 @@ def check_sort(emu, BH, Tq, Tk, k, causal, seed, fails, margin=20, ties=False, o
 
 BOUND_CASES = [
     # BH, Tq, Tk, k, causal
+    (1, 20, 131072, 512, True),   # the headline shape's last rows: g = 64 (two tiles a group)
     (1, 300, 300, 16, True),      # g from 1 up; the first rows select everything
     (2, 260, 2000, 8, True),      # Tq < Tk: g >= 32 chunks across tiles
     (1, 100, 700, 40, False),
@@ -233,6 +234,7 @@ SORT_CASES = [
     (2, 40, 500, 33, False),
     (1, 30, 900, 100, True),
     (1, 20, 64, 64, False),       # k = Tk
+    (1, 8, 4000, 512, False),     # the headline k: 1024-entry capacity, 16 winners per lane
 ]
 
 
