@@ -29,7 +29,8 @@ EXPORTS = ("ssa_version", "ssa_status_string", "ssa_score_topk_workspace_size", 
            "ssa_sparse_attn_bwd_workspace_size", "ssa_sparse_attn_bwd",
            "ssa_scorer_bwd_workspace_size", "ssa_scorer_bwd",
            "ssa_sparse_attn_grouped_bwd_workspace_size", "ssa_sparse_attn_grouped_bwd",
-           "ssa_scorer_grouped_bwd_workspace_size", "ssa_scorer_grouped_bwd")
+           "ssa_scorer_grouped_bwd_workspace_size", "ssa_scorer_grouped_bwd",
+           "ssa_selftest_wait_limit")
 
 # Fixed scratch of ssa_score_topk_noalloc and the largest Tk it accepts.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -102,6 +103,8 @@ def load(path: str | None = None):
     lib.ssa_scorer_grouped_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
     lib.ssa_scorer_grouped_bwd.restype = I
     lib.ssa_scorer_grouped_bwd.argtypes = [V, V, I, I, I, I, I, I, I, V, I, V, F, V, V, V, Z, V, V]
+    lib.ssa_selftest_wait_limit.restype = I
+    lib.ssa_selftest_wait_limit.argtypes = [V, ctypes.c_uint64, V]
     if path is None:
         _lib = lib
     return lib
@@ -516,6 +519,18 @@ def ssa_scorer_grouped_bwd(q_low, k_low, idx, dS, scale: float = 0.0, workspace=
                                     _ptr(workspace), wbytes, _ptr(dev_status), _stream(dev))
     _check(rc, "ssa_scorer_grouped_bwd")
     return dq, dk
+
+
+def ssa_selftest_wait_limit(dev_status: torch.Tensor, limit_ns: int = 2_000_000):
+    """Launch the bounded-wait self-test on the current stream: one block waits
+    on an mbarrier nothing completes, gives up after limit_ns and ORs
+    SSA_DEV_WAIT_LIMIT into dev_status (a device int32 tensor)."""
+    lib = load()
+    dev = _dev(dev_status)
+    if dev_status.dtype != torch.int32:
+        raise TypeError("dev_status must be int32")
+    _check(lib.ssa_selftest_wait_limit(_ptr(dev_status), int(limit_ns), _stream(dev)),
+           "ssa_selftest_wait_limit")
 
 
 def trace_begin():

@@ -422,6 +422,23 @@ ssa_status ssa_scorer_grouped_bwd(const void* q_low, const void* k_low, int dtyp
                                   void* stream);
 
 /*
+ * ssa_selftest_wait_limit — exercises the bounded device waits.
+ *
+ * The tensor-core kernels wait on mbarriers for their TMA copies and MMAs.
+ * Each wait gives up after a time limit, sets SSA_DEV_WAIT_LIMIT in
+ * *dev_status and lets the kernel return, so that a copy or MMA that never
+ * completes leaves an error status and a usable context, not a hung GPU.
+ * This call launches one block that takes that path on purpose: it waits on
+ * an mbarrier that nothing completes until limit_ns has passed.
+ *
+ *   dev_status  device int32 (required); SSA_DEV_WAIT_LIMIT is ORed into it
+ *   limit_ns    1 .. 1e9 (one second)
+ *
+ * Returns SSA_OK (launched), SSA_ERR_INVALID or SSA_ERR_CUDA.
+ */
+ssa_status ssa_selftest_wait_limit(int32_t* dev_status, uint64_t limit_ns, void* stream);
+
+/*
  * Launch tracing. Between ssa_trace_begin() and ssa_trace_end(), every kernel
  * this library launches is bracketed by two CUDA events recorded on the
  * launching stream (the tracing itself launches nothing and allocates no

@@ -259,3 +259,12 @@ def test_host_validation_of_the_grouped_backward_calls():
     # one scorer head shared by 4 query heads needs room for the summed pair gradients
     assert (lib.ssa_scorer_grouped_bwd_workspace_size(1, 4, 1, 8, 16, 4) >
             lib.ssa_scorer_grouped_bwd_workspace_size(1, 1, 1, 8, 16, 4))
+
+
+def test_host_validation_of_the_wait_limit_selftest():
+    lib = ssa.load()
+    INV = _native.SSA_ERR_INVALID
+    assert lib.ssa_selftest_wait_limit(None, 1000, None) == INV        # no status word
+    assert lib.ssa_selftest_wait_limit(V(4098), 1000, None) == INV     # misaligned
+    assert lib.ssa_selftest_wait_limit(V(4096), 0, None) == INV        # no limit
+    assert lib.ssa_selftest_wait_limit(V(4096), 2 * 10 ** 9, None) == INV   # over a second
