@@ -103,10 +103,8 @@ def algorithmic(w):
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# ncu capture of these kernels on these workloads (the profile
-# traffic_tile_scores_topk_causal_bf16_t128k_k512.md); to be re-measured, or
+# ncu capture of these kernels on these workloads; to be re-measured, or
 # dropped, when the kernels change.
-# (The candidate pass changed after its capture, so it reports no traffic.)
 MEASURED_TRAFFIC = {
     ("topk_causal_bf16_t128k_k512_planted", "tile_scores.groupmax"): 3.580e9,
     ("topk_causal_bf16_t32k_k256", "tile_scores.groupmax"): 0.892e9,

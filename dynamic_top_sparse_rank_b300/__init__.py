@@ -20,7 +20,7 @@ from ._native import (EXPORTS, SSA_BF16, SSA_DEV_BAD_INDEX, SSA_DEV_OVERFLOW, SS
                       ssa_sparse_attn_grouped, ssa_window_attn, status_string,
                       sparse_attn_bwd_workspace_size, scorer_bwd_workspace_size,
                       ssa_sparse_attn_grouped_bwd, ssa_scorer_grouped_bwd,
-                      ssa_selftest_wait_limit)
+                      ssa_selftest_wait_limit, device_status, SSA_ERR_TIMEOUT)
 
 __all__ = ["EXPORTS", "SSA_BF16", "SSA_DEV_BAD_INDEX", "SSA_DEV_OVERFLOW", "SSA_DEV_WAIT_LIMIT",
            "SSA_F32", "SSAError", "load", "score_topk_workspace_size", "ssa_lowrank_project",
@@ -29,4 +29,5 @@ __all__ = ["EXPORTS", "SSA_BF16", "SSA_DEV_BAD_INDEX", "SSA_DEV_OVERFLOW", "SSA_
            "ssa_score_topk_noalloc", "ssa_scorer_bwd", "ssa_sparse_attn", "ssa_sparse_attn_bwd",
            "ssa_sparse_attn_grouped", "ssa_window_attn", "status_string",
            "sparse_attn_bwd_workspace_size", "scorer_bwd_workspace_size",
-           "ssa_sparse_attn_grouped_bwd", "ssa_scorer_grouped_bwd", "ssa_selftest_wait_limit"]
+           "ssa_sparse_attn_grouped_bwd", "ssa_scorer_grouped_bwd", "ssa_selftest_wait_limit",
+           "device_status", "SSA_ERR_TIMEOUT"]

@@ -18,7 +18,8 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libssa.so")
 
-SSA_OK, SSA_ERR_INVALID, SSA_ERR_UNSUPPORTED, SSA_ERR_CUDA, SSA_ERR_WORKSPACE = 0, 1, 2, 3, 4
+SSA_OK, SSA_ERR_INVALID, SSA_ERR_UNSUPPORTED, SSA_ERR_CUDA = 0, 1, 2, 3
+SSA_ERR_TIMEOUT, SSA_ERR_WORKSPACE = 4, 5
 SSA_F32, SSA_BF16 = 0, 1
 SSA_DEV_BAD_INDEX, SSA_DEV_WAIT_LIMIT, SSA_DEV_OVERFLOW = 0x1, 0x2, 0x4
 
@@ -30,7 +31,7 @@ EXPORTS = ("ssa_version", "ssa_status_string", "ssa_score_topk_workspace_size", 
            "ssa_scorer_bwd_workspace_size", "ssa_scorer_bwd",
            "ssa_sparse_attn_grouped_bwd_workspace_size", "ssa_sparse_attn_grouped_bwd",
            "ssa_scorer_grouped_bwd_workspace_size", "ssa_scorer_grouped_bwd",
-           "ssa_selftest_wait_limit")
+           "ssa_selftest_wait_limit", "ssa_device_status")
 
 # Fixed scratch of ssa_score_topk_noalloc and the largest Tk it accepts.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -103,6 +104,8 @@ def load(path: str | None = None):
     lib.ssa_scorer_grouped_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
     lib.ssa_scorer_grouped_bwd.restype = I
     lib.ssa_scorer_grouped_bwd.argtypes = [V, V, I, I, I, I, I, I, I, V, I, V, F, V, V, V, Z, V, V]
+    lib.ssa_device_status.restype = I
+    lib.ssa_device_status.argtypes = [V, V, V]
     lib.ssa_selftest_wait_limit.restype = I
     lib.ssa_selftest_wait_limit.argtypes = [V, ctypes.c_uint64, V]
     if path is None:
@@ -530,7 +533,22 @@ def ssa_selftest_wait_limit(dev_status: torch.Tensor, limit_ns: int = 2_000_000)
     if dev_status.dtype != torch.int32:
         raise TypeError("dev_status must be int32")
     _check(lib.ssa_selftest_wait_limit(_ptr(dev_status), int(limit_ns), _stream(dev)),
-           "ssa_selftest_wait_limit")
+           "ssa_selftest_wait_limit", "ssa_device_status")
+
+
+def device_status(dev_status: torch.Tensor):
+    """Wait for the current stream, read the device-side error bits and return
+    (status, bits): SSA_ERR_TIMEOUT when a bounded device wait ran out,
+    SSA_ERR_INVALID when an index entry was out of range, else SSA_OK."""
+    if dev_status.dtype != torch.int32 or dev_status.numel() < 1:
+        raise TypeError("dev_status must be an int32 tensor")
+    dev = _dev(dev_status)
+    bits = ctypes.c_int32(0)
+    rc = load().ssa_device_status(_ptr(dev_status), ctypes.cast(ctypes.byref(bits), ctypes.c_void_p),
+                                  _stream(dev))
+    if rc == SSA_ERR_CUDA:
+        raise SSAError(rc, "ssa_device_status")
+    return rc, int(bits.value)
 
 
 def trace_begin():

@@ -70,9 +70,23 @@ const char* ssa_status_string(int status) {
         case SSA_ERR_INVALID: return "invalid argument (null or misaligned pointer, bad size or dtype)";
         case SSA_ERR_UNSUPPORTED: return "unsupported size (P in {16,32,64,128}, D in {64,128}, k <= 2048)";
         case SSA_ERR_CUDA: return "CUDA launch or runtime error";
+        case SSA_ERR_TIMEOUT: return "a bounded device-side wait ran out";
         case SSA_ERR_WORKSPACE: return "workspace missing or too small";
         default: return "unknown status";
     }
+}
+
+ssa_status ssa_device_status(const int32_t* dev_status, int32_t* bits, void* stream) {
+    if (!dev_status || !aligned(dev_status, 4)) return SSA_ERR_INVALID;
+    int32_t h = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&h, dev_status, sizeof h, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return SSA_ERR_CUDA;
+    if (bits) *bits = h;
+    if (h & SSA_DEV_WAIT_LIMIT) return SSA_ERR_TIMEOUT;
+    if (h & SSA_DEV_BAD_INDEX) return SSA_ERR_INVALID;
+    return SSA_OK;
 }
 
 static size_t path_workspace_bytes(int dtype, int B, int H, int Tq, int Tk, int P, int k) {

@@ -30,7 +30,8 @@
  *  - Errors found on the device (an index out of range, a bounded wait that
  *    ran out) never trap: the kernel ORs a bit into *dev_status (an int32 in
  *    device memory, may be NULL) and carries on or returns. The caller clears
- *    *dev_status and reads it back when it wants to know.
+ *    *dev_status and reads it back when it wants to know, directly or through
+ *    ssa_device_status, which turns a wait that ran out into SSA_ERR_TIMEOUT.
  *  - Nothing is thrown across the ABI.
  */
 #ifndef SSA_H_
@@ -49,7 +50,8 @@ typedef enum {
     SSA_ERR_INVALID = 1,     /* null pointer, negative size, bad enum value, misaligned pointer */
     SSA_ERR_UNSUPPORTED = 2, /* a size outside the supported set (see each call) */
     SSA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
-    SSA_ERR_WORKSPACE = 4    /* workspace NULL or smaller than the size query returned */
+    SSA_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out (from ssa_device_status) */
+    SSA_ERR_WORKSPACE = 5    /* workspace NULL or smaller than the size query returned */
 } ssa_status;
 
 /* Element types of tensors at the ABI. */
@@ -62,6 +64,31 @@ typedef enum {
 #define SSA_DEV_BAD_INDEX 0x1   /* an index list entry outside [-1, Tk); the entry is skipped */
 #define SSA_DEV_WAIT_LIMIT 0x2  /* a bounded device-side wait ran out; the tile is abandoned */
 #define SSA_DEV_OVERFLOW 0x4    /* internal candidate buffer overflowed; the row was redone exactly */
+
+/*
+ * ssa_device_status — turns the device-side error bits into a status.
+ *
+ * Boundary plumbing, with no counterpart on the pages: the host end of the
+ * error rule above.
+ *
+ * Waits for the work queued on `stream` so far, reads *dev_status (the int32
+ * the calls above OR their device-side bits into) and returns:
+ *   SSA_ERR_TIMEOUT  if SSA_DEV_WAIT_LIMIT is set (a bounded wait of a
+ *                    tensor-core kernel ran out; that kernel's outputs are
+ *                    incomplete),
+ *   SSA_ERR_INVALID  else if SSA_DEV_BAD_INDEX is set (an index list held an
+ *                    entry outside [-1, Tk); it was skipped),
+ *   SSA_OK           otherwise (SSA_DEV_OVERFLOW alone is informational: the
+ *                    rows were redone exactly).
+ * The raw bits are written to *bits when bits is not NULL. *dev_status is
+ * not cleared. A failed CUDA call returns SSA_ERR_CUDA; a NULL or misaligned
+ * dev_status returns SSA_ERR_INVALID.
+ *
+ *   dev_status  device int32, 4-byte aligned
+ *   bits        host int32 or NULL
+ *   stream      cudaStream_t the calls ran on (synchronized)
+ */
+ssa_status ssa_device_status(const int32_t* dev_status, int32_t* bits, void* stream);
 
 /* Library version, (major << 16) | minor. */
 int ssa_version(void);
@@ -305,11 +332,16 @@ ssa_status ssa_window_attn(const void* Q, const void* K, const void* V, int dtyp
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture. All calls share the one array and it keeps the last call's
- * contents (the kernel overwrites every scratch word before reading it, so
- * nothing needs clearing); calls whose kernels overlap on the GPU (different
- * streams, no ordering between them) race on it and must be serialized by
- * the caller.
+ * capture. If the device's context is replaced (cudaDeviceReset), the next
+ * call looks the address up again in the new context. All calls share the
+ * one array and it keeps the last call's contents (the kernel overwrites
+ * every scratch word before reading it, so nothing needs clearing); calls
+ * whose kernels overlap on the GPU (different streams, no ordering between
+ * them) race on it and must be serialized by the caller.
+ *
+ * dev_status is checked (4-byte aligned or NULL) like every other call's, but
+ * the row-wise kernel has no device-side error condition, so this call never
+ * writes it.
  */
 ssa_status ssa_score_topk_noalloc(const void* q_low, const void* k_low, int dtype, int B, int H,
                                   int Tq, int Tk, int P, int k, int causal, float scale,

@@ -25,7 +25,7 @@
  *    the sequence ends; "Attention机制改进：稀疏注意力应用" (yongjin360.com),
  *    section 性能收益与硬件适配: the same band as a boolean mask.
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings where the pages are silent:
  *  - ties in the selection go to the lower key index; the output is ordered by
  *    (score descending, index ascending);
  *  - a row with fewer valid keys than k selects all of them and pads the rest

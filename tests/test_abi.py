@@ -34,8 +34,8 @@ def test_library_exports_every_declared_symbol():
 def test_version_and_status_strings():
     lib = ssa.load()
     assert lib.ssa_version() >= 1
-    for s in range(5):
-        assert lib.ssa_status_string(s)
+    for s in range(6):
+        assert b"unknown" not in lib.ssa_status_string(s)
     assert b"unknown" in lib.ssa_status_string(99)
 
 
@@ -268,3 +268,14 @@ def test_host_validation_of_the_wait_limit_selftest():
     assert lib.ssa_selftest_wait_limit(V(4098), 1000, None) == INV     # misaligned
     assert lib.ssa_selftest_wait_limit(V(4096), 0, None) == INV        # no limit
     assert lib.ssa_selftest_wait_limit(V(4096), 2 * 10 ** 9, None) == INV   # over a second
+
+
+def test_host_validation_of_the_device_status_reader():
+    lib = ssa.load()
+    INV = _native.SSA_ERR_INVALID
+    assert lib.ssa_device_status(None, None, None) == INV       # no status word
+    assert lib.ssa_device_status(V(4098), None, None) == INV    # misaligned
+    # the status codes keep the values the boundary defines
+    assert (_native.SSA_ERR_TIMEOUT, _native.SSA_ERR_WORKSPACE) == (4, 5)
+    assert b"wait" in lib.ssa_status_string(_native.SSA_ERR_TIMEOUT)
+    assert b"workspace" in lib.ssa_status_string(_native.SSA_ERR_WORKSPACE)

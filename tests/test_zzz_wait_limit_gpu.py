@@ -23,6 +23,10 @@ def test_wait_runs_out_reports_and_the_context_stays_usable(cuda_dev):
     waited = time.perf_counter() - t0
     assert int(st.item()) == ssa.SSA_DEV_WAIT_LIMIT
     assert 0.002 <= waited < 5.0
+    # the host end of the rule: the wait that ran out reads as SSA_ERR_TIMEOUT
+    assert ssa.device_status(st) == (ssa.SSA_ERR_TIMEOUT, ssa.SSA_DEV_WAIT_LIMIT)
+    st.zero_()
+    assert ssa.device_status(st) == (0, 0)
     # the context still runs the path: a small exact top-k against the oracle
     g = np.random.default_rng(0)
     q = torch.from_numpy(g.integers(-4, 5, size=(1, 2, 200, 64)).astype(np.float32)).to(torch.bfloat16)
