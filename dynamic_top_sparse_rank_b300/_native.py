@@ -533,7 +533,7 @@ def ssa_selftest_wait_limit(dev_status: torch.Tensor, limit_ns: int = 2_000_000)
     if dev_status.dtype != torch.int32:
         raise TypeError("dev_status must be int32")
     _check(lib.ssa_selftest_wait_limit(_ptr(dev_status), int(limit_ns), _stream(dev)),
-           "ssa_selftest_wait_limit", "ssa_device_status")
+           "ssa_selftest_wait_limit")
 
 
 def device_status(dev_status: torch.Tensor):

@@ -240,7 +240,26 @@ SSA_DEVINL void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane, as tmem_ld32,
+// and their maximum as an fp32 value, reduced on the way out of TMEM
+// (tcgen05.ld.red, sm_103a): the maximum costs no instruction of the warp.
+// Like the loaded registers, the maximum is valid after tmem_ld_wait().
+SSA_DEVINL float tmem_ldred_max16(uint32_t taddr, uint32_t (&r)[16]) {
+    float m;
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, %16, [%17];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=f"(m)
+        : "r"(taddr));
+    return m;
+}
+
 SSA_DEVINL void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Ties a value produced by an asynchronous TMEM load to the wait before it.
+SSA_DEVINL void reg_fence_f(float& x) { asm volatile("" : "+f"(x)); }
 
 // Ties the registers of a TMEM load to the tcgen05.wait::ld before this call:
 // the compiler may not move a use of them above it.

@@ -141,18 +141,6 @@ SSA_DEVINL float max16(const float* v) {
     return fmaxf(fmax3(a, b, c), fmax3(d, e, v[15]));
 }
 
-SSA_DEVINL float max32(const float (&v)[32]) {
-    float a[11];
-#pragma unroll
-    for (int t = 0; t < 10; ++t) a[t] = fmax3(v[3 * t], v[3 * t + 1], v[3 * t + 2]);
-    a[10] = fmaxf(v[30], v[31]);
-    const float b0 = fmax3(a[0], a[1], a[2]);
-    const float b1 = fmax3(a[3], a[4], a[5]);
-    const float b2 = fmax3(a[6], a[7], a[8]);
-    const float b3 = fmaxf(a[9], a[10]);
-    return fmaxf(fmax3(b0, b1, b2), b3);
-}
-
 // Maximum of the G consecutive scores at w (G a power of two <= 16).
 template <int G>
 SSA_DEVINL float max_of(const float* w) {
@@ -499,16 +487,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tpar ^= 1;
                 tc_fence_after();
-                // two 32-column loads in flight per wait: half the load round
-                // trips that hold the buffer
+                // four 16-column loads in flight per wait, each with the
+                // maximum of its 16 scores reduced on the way out of TMEM
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
-                  uint32_t raw2[2][32];
-                  tmem_ld32(t_lane + c2 * 64, raw2[0]);
-                  tmem_ld32(t_lane + c2 * 64 + 32, raw2[1]);
+                  uint32_t raw[4][16];
+                  float mx[4];
+#pragma unroll
+                  for (int h4 = 0; h4 < 4; ++h4)
+                      mx[h4] = tmem_ldred_max16(t_lane + c2 * 64 + 16 * h4, raw[h4]);
                   tmem_ld_wait();
-                  reg_fence(raw2[0]);
-                  reg_fence(raw2[1]);
+#pragma unroll
+                  for (int h4 = 0; h4 < 4; ++h4) {
+                      reg_fence(raw[h4]);
+                      reg_fence_f(mx[h4]);
+                  }
                   if (c2 == 1) {
                       tc_fence_before();
                       __syncwarp();
@@ -522,24 +515,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const int jp = t * kTileN + c2 * 64;   // first key of the pair
                       float v[64];
 #pragma unroll
-                      for (int e = 0; e < 32; ++e) {
-                          v[e] = __uint_as_float(raw2[0][e]);
-                          v[32 + e] = __uint_as_float(raw2[1][e]);
+                      for (int e = 0; e < 16; ++e) {
+#pragma unroll
+                          for (int h4 = 0; h4 < 4; ++h4) v[16 * h4 + e] = __uint_as_float(raw[h4][e]);
                       }
                       // mask the keys past the row's last one: only in the tile
-                      // where a row of this warp ends (a warp-uniform branch)
+                      // where a row of this warp ends (a warp-uniform branch);
+                      // there the maxima come from the masked registers
                       if (__any_sync(0xffffffffu, jp < n_i && jp + 64 > n_i)) {
+                          if (jp + 64 > n_i) {
 #pragma unroll
-                          for (int e = 0; e < 64; ++e)
-                              if (jp + e >= n_i) v[e] = -INFINITY;
+                              for (int e = 0; e < 64; ++e)
+                                  if (jp + e >= n_i) v[e] = -INFINITY;
+#pragma unroll
+                              for (int hs = 0; hs < 4; ++hs) mx[hs] = max16(v + 16 * hs);
+                          }
                       }
                       uint32_t B[4];
                       bool hot[4];
 #pragma unroll
-                      for (int hs = 0; hs < 4; ++hs) {
-                          const float* w = v + 16 * hs;
-                          hot[hs] = jp + 16 * hs < n_i && max16(w) >= t_raw;
-                      }
+                      for (int hs = 0; hs < 4; ++hs) hot[hs] = jp + 16 * hs < n_i && mx[hs] >= t_raw;
 #pragma unroll
                       for (int hs = 0; hs < 4; ++hs) B[hs] = __ballot_sync(0xffffffffu, hot[hs]);
 #pragma unroll
@@ -569,7 +564,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int j0 = t * kTileN + c * 32;
                     float v[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(raw2[c1][e]);
+                    for (int e = 0; e < 16; ++e) {
+                        v[e] = __uint_as_float(raw[2 * c1][e]);
+                        v[16 + e] = __uint_as_float(raw[2 * c1 + 1][e]);
+                    }
                     if constexpr (MODE == MODE_RAW) {
                         if (row_ok) {
                             float* out = p.S + row * static_cast<int64_t>(p.Tk);
@@ -581,14 +579,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     } else {
                         const bool live = j0 < n_i;   // this row has keys in the chunk
+                        // the 16-key maxima from TMEM hold for whole halves;
+                        // in the chunk where the row ends they come from the
+                        // masked registers
+                        float m0 = mx[2 * c1], m1 = mx[2 * c1 + 1];
                         if (live && j0 + 32 > n_i) {
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
                                 if (j0 + e >= n_i) v[e] = -INFINITY;
+                            m0 = max16(v);
+                            m1 = max16(v + 16);
                         }
                         if constexpr (MODE == MODE_GROUPMAX) {
                             if (live && g >= 32) {
-                                gacc[c] = fmaxf(gacc[c], max32(v));
+                                gacc[c] = fmax3(gacc[c], m0, m1);
                                 // last tile of the group, or the row has no key in this
                                 // chunk of this buffer's next tile
                                 const int lt = t / kTBuf;
@@ -599,13 +603,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         static_cast<uint16_t>(f32_order_key(gacc[c] * p.scale) >> 16);
                                     gacc[c] = -INFINITY;
                                 }
+                            } else if (live && g == 16) {
+                                gcol[static_cast<int64_t>(j0 / 16) * kUnitM] =
+                                    static_cast<uint16_t>(f32_order_key(m0 * p.scale) >> 16);
+                                if (j0 + 16 < n_i)
+                                    gcol[static_cast<int64_t>(j0 / 16 + 1) * kUnitM] =
+                                        static_cast<uint16_t>(f32_order_key(m1 * p.scale) >> 16);
+                            } else if (live && g == 8) {
+                                small_groups<8>(v, j0, n_i, gcol, p.scale);
                             } else if (live && g > 0) {
-                                if (g == 16)
-                                    small_groups<16>(v, j0, n_i, gcol, p.scale);
-                                else if (g == 8)
-                                    small_groups<8>(v, j0, n_i, gcol, p.scale);
-                                else
-                                    tiny_groups(v, j0, n_i, gcol, p.scale, g);
+                                tiny_groups(v, j0, n_i, gcol, p.scale, g);
                             }
                         }
                     }

@@ -289,43 +289,135 @@ def test_window_wide_band_uses_gather(cuda_dev):
     assert_out_close(O.cpu().numpy(), ref, TOL_BF16, False)
 
 
-# ------------------------------------------------- full-size sampled parity
+# ------------------------------------------------- full-size parity
 
-FULL = ["topk_causal_bf16_t32k_k256", "topk_causal_bf16_t128k_k512_planted",
-        "decode_bf16_b32_tk64k_k512"]
+UNIT_ROWS = 256   # query rows per work unit of the tensor-core top-k
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_workload_sampled(cuda_dev, name):
-    """Full-size inputs in the benchmark's launch configuration: every row is
-    checked for the invariants, sampled rows against the oracle (its own index
-    lists feed its attention)."""
-    w = WORKLOADS[name]
-    q, kl = make_scorer_inputs(w, cuda_dev)
-    Q, K, V = make_attn_inputs(w, cuda_dev)
-    ws = torch.empty(ssa.score_topk_workspace_size(w.B, w.H, w.Tq, w.Tk, w.P, w.k, w.causal),
-                     dtype=torch.uint8, device=cuda_dev)
-    idx, sc = ssa.ssa_score_topk(q, kl, w.k, w.causal, with_score=True, workspace=ws)
-    O = ssa.ssa_sparse_attn(Q, K, V, idx, out_dtype=torch.float32)
-    torch.cuda.synchronize()
-    check_topk_invariants(idx, sc, w.Tq, w.Tk, w.k, w.causal)
-    rows = sample_rows(w.B, w.H, w.Tq, 48, seed=w.cfg_id)
-    flat_idx = idx.view(-1, w.k)[torch.from_numpy(rows).to(cuda_dev)].cpu().numpy()
-    flat_sc = sc.view(-1, w.k)[torch.from_numpy(rows).to(cuda_dev)].cpu().numpy()
-    gpu_O = O.view(-1, w.D)[torch.from_numpy(rows).to(cuda_dev)].cpu().numpy()
-    # oracle, one head at a time (only the sampled heads are copied to the host)
-    by_head = {}
+def unit_rows(B, H, Tq, seed):
+    """Flat row ids: one row of every 256-row work unit of every head (its
+    first, its last or a random row, in turn), every row of one pair of units
+    that share a work item (unit qb of head 0 and unit units-1-qb), and the
+    sequence ends and tile edges of sample_rows."""
+    g = np.random.default_rng(seed)
+    units = (Tq + UNIT_ROWS - 1) // UNIT_ROWS
+    rows = set(int(r) for r in sample_rows(B, H, Tq, 0, seed=seed))
+    for bh in range(B * H):
+        for u in range(units):
+            n = min(UNIT_ROWS, Tq - UNIT_ROWS * u)
+            off = (0, n - 1, int(g.integers(0, n)))[(bh + u) % 3]
+            rows.add(bh * Tq + UNIT_ROWS * u + off)
+    qb = units // 3
+    for u in {qb, units - 1 - qb}:
+        for i in range(UNIT_ROWS * u, min(Tq, UNIT_ROWS * (u + 1))):
+            rows.add(i)
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def _by_head(rows, Tq):
+    out = {}
     for n, r in enumerate(rows):
-        bh, i = divmod(int(r), w.Tq)
-        by_head.setdefault(bh, []).append((n, i))
-    for bh, items in by_head.items():
+        bh, i = divmod(int(r), Tq)
+        out.setdefault(bh, []).append((n, i))
+    return out
+
+
+def _oracle_compare(w, q, kl, Q, K, V, rows, idx, sc, O32, O16, attn_heads=None):
+    """The oracle on the given flat rows, one head at a time (only those heads
+    are copied to the host): top-k bit for bit, attention (from the oracle's
+    own index lists) within the tolerance in fp32 and in bf16 output."""
+    dev = idx.device
+    rt = torch.from_numpy(rows).to(dev)
+    flat_idx = idx.view(-1, w.k)[rt].cpu().numpy()
+    flat_sc = sc.view(-1, w.k)[rt].cpu().numpy()
+    o32 = O32.view(-1, w.D)[rt].cpu().numpy()
+    o16 = O16.view(-1, w.D)[rt].float().cpu().numpy()
+    heads = _by_head(rows, w.Tq)
+    import concurrent.futures as cf
+
+    def one(bh):
+        items = heads[bh]
         b, h = divmod(bh, w.H)
         ns = [n for n, _ in items]
         qi = np.array([i for _, i in items], dtype=np.int64)
+        threads = 1 if len(qi) < 64 else None
         ref_idx, ref_sc = oracle.topk_rows(q[b, h].cpu()[qi], qi, kl[b, h].cpu(), w.k, w.Tq,
-                                           w.causal)
+                                           w.causal, nthreads=threads)
         np.testing.assert_array_equal(flat_idx[ns], ref_idx)
         np.testing.assert_array_equal(flat_sc[ns], ref_sc)
-        ref_O, bad = oracle.attn_rows(Q[b, h].cpu()[qi], K[b, h].cpu(), V[b, h].cpu(), ref_idx)
+        if attn_heads is not None and bh not in attn_heads:
+            return len(ns)
+        ref_O, bad = oracle.attn_rows(Q[b, h].cpu()[qi], K[b, h].cpu(), V[b, h].cpu(), ref_idx,
+                                      nthreads=threads)
         assert bad == 0
-        assert_out_close(gpu_O[ns], ref_O, TOL_BF16, False)
+        assert_out_close(o32[ns], ref_O, TOL_BF16, False)
+        assert_out_close(o16[ns], ref_O, TOL_BF16, True)
+        return len(ns)
+
+    workers = 16 if len(heads) > 64 else 1
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        checked = sum(ex.map(one, sorted(heads)))
+    assert checked == len(rows)
+
+
+def _run_full(w, dev):
+    q, kl = make_scorer_inputs(w, dev)
+    Q, K, V = make_attn_inputs(w, dev)
+    ws = torch.empty(ssa.score_topk_workspace_size(w.B, w.H, w.Tq, w.Tk, w.P, w.k, w.causal),
+                     dtype=torch.uint8, device=dev)
+    idx, sc = ssa.ssa_score_topk(q, kl, w.k, w.causal, with_score=True, workspace=ws)
+    O16 = ssa.ssa_sparse_attn(Q, K, V, idx)                           # as the bench runs it
+    O32 = ssa.ssa_sparse_attn(Q, K, V, idx, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    del ws
+    return q, kl, Q, K, V, idx, sc, O32, O16
+
+
+@pytest.mark.parametrize("name", ["topk_causal_bf16_t32k_k256",
+                                  "topk_causal_bf16_t128k_k512_planted"])
+def test_full_size_workload_every_unit(cuda_dev, name):
+    """Full-size inputs in the benchmark's launch configuration: every row is
+    checked for the invariants; one row of every 256-row work unit of every
+    head, and every row of one paired work item, against the oracle (top-k
+    bit for bit, attention in fp32 and bf16 output)."""
+    w = WORKLOADS[name]
+    q, kl, Q, K, V, idx, sc, O32, O16 = _run_full(w, cuda_dev)
+    check_topk_invariants(idx, sc, w.Tq, w.Tk, w.k, w.causal)
+    rows = unit_rows(w.B, w.H, w.Tq, seed=w.cfg_id)
+    assert len(rows) >= w.B * w.H * ((w.Tq + UNIT_ROWS - 1) // UNIT_ROWS)
+    _oracle_compare(w, q, kl, Q, K, V, rows, idx, sc, O32, O16)
+
+
+def test_full_size_decode_every_row(cuda_dev):
+    """The decode workload (B32 H32, one query against 65536 keys per head):
+    all 1024 rows' top-k against the oracle bit for bit; attention against
+    the oracle on 64 heads (their K and V are copied to the host)."""
+    w = WORKLOADS["decode_bf16_b32_tk64k_k512"]
+    q, kl, Q, K, V, idx, sc, O32, O16 = _run_full(w, cuda_dev)
+    check_topk_invariants(idx, sc, w.Tq, w.Tk, w.k, w.causal)
+    rows = np.arange(w.B * w.H * w.Tq, dtype=np.int64)
+    g = np.random.default_rng(w.cfg_id)
+    attn_heads = set(int(x) for x in g.choice(w.B * w.H, 64, replace=False)) | {0, w.B * w.H - 1}
+    _oracle_compare(w, q, kl, Q, K, V, rows, idx, sc, O32, O16, attn_heads=attn_heads)
+
+
+@pytest.mark.parametrize("name", ["topk_causal_bf16_t32k_k256",
+                                  "topk_causal_bf16_t128k_k512_planted"])
+def test_full_size_tile_path_matches_rowwise_every_row(cuda_dev, name):
+    """Every row of the full-size workload: the tensor-core top-k (bf16
+    inputs) against the row-wise kernel, which an fp32 input selects. The
+    inputs are integers, so both compute the same exact scores; the two
+    selections share no code beyond the output format, and the row-wise
+    kernel is itself checked against the oracle above."""
+    w = WORKLOADS[name]
+    q, kl = make_scorer_inputs(w, cuda_dev)
+    idx, sc = ssa.ssa_score_topk(q, kl, w.k, w.causal, with_score=True)
+    torch.cuda.synchronize()
+    q32, kl32 = q.float(), kl.float()
+    del q, kl
+    ssa.trace_begin()
+    idx_r, sc_r = ssa.ssa_score_topk(q32, kl32, w.k, w.causal, with_score=True)
+    torch.cuda.synchronize()
+    assert {n for n, _ in ssa.trace_end()} == {"topk_rows"}
+    assert torch.equal(idx, idx_r)
+    assert torch.equal(sc, sc_r)
