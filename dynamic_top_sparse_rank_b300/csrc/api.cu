@@ -11,6 +11,11 @@ cudaError_t topk_rows_dispatch(const void* q_low, const void* k_low, bool bf16, 
                                int Tq, int Tk, int k, int causal, float scale, int32_t* idx,
                                float* score, uint32_t* ws, int64_t ws_slots, int64_t ws_stride,
                                cudaStream_t stream);
+int topk_chunks_for(int Tk, int k);
+size_t topk_chunks_workspace(int64_t rows, int Tk, int k);
+cudaError_t topk_chunks_dispatch(const void* q_low, const void* k_low, bool bf16, int P,
+                                 int64_t rows, int Tq, int Tk, int k, int causal, float scale,
+                                 int32_t* idx, float* score, void* ws, cudaStream_t stream);
 cudaError_t tile_select_launch(const uint16_t* gm, uint32_t* tau, int BH, int Tq, int Tk, int k,
                                int causal, cudaStream_t stream);
 cudaError_t tile_sort_launch(const uint64_t* cand, const int32_t* cnt, int64_t rows, int Tq,
@@ -58,6 +63,14 @@ bool use_tile_path(int dtype, int B, int H, int P, int Tq, int Tk, int k) {
            (int64_t)B * H * Tq <= INT32_MAX && (int64_t)B * H * Tk <= INT32_MAX;
 }
 
+// Rows that the row-wise path takes split into key chunks (one CTA per row
+// and chunk): long rows (decode: one query per head against a long key
+// cache), when there are too few of them for one CTA per row to fill the GPU
+// and the chunks' selections fit a row's merge.
+bool use_chunked_rows(int64_t rows, int Tk, int k) {
+    return rows <= 4 * kRowSlots && ssa::topk_chunks_for(Tk, k) > 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -94,6 +107,7 @@ static size_t path_workspace_bytes(int dtype, int B, int H, int Tq, int Tk, int 
     if (rows == 0 || Tk == 0) return 256;
     if (use_tile_path(dtype, B, H, P, Tq, Tk, k))
         return ssa::tile_workspace((int64_t)B * H, Tq, Tk, k).total;
+    if (use_chunked_rows(rows, Tk, k)) return ssa::topk_chunks_workspace(rows, Tk, k);
     return (size_t)round_up(rowwise_slots(rows) * rowwise_stride(Tk) * 4, 256);
 }
 
@@ -124,6 +138,11 @@ ssa_status ssa_score_topk(const void* q_low, const void* k_low, int dtype, int B
     const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)P));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!use_tile_path(dtype, B, H, P, Tq, Tk, k)) {
+        if (use_chunked_rows(rows, Tk, k)) {
+            cudaError_t e = ssa::topk_chunks_dispatch(q_low, k_low, dtype == SSA_BF16, P, rows, Tq,
+                                                      Tk, k, causal, sc, idx, score, workspace, s);
+            return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
+        }
         // Tk == 0: every row is empty; the row kernel writes the padding.
         cudaError_t e = ssa::topk_rows_dispatch(q_low, k_low, dtype == SSA_BF16, P, nullptr, rows,
                                                 nullptr, Tq, Tk, k, causal, sc, idx, score,

@@ -59,6 +59,8 @@ class Emu:
         lib.emu_attn_rows.argtypes = [P, P, P, I, I, P, P, I, L, I, I, I, I, I, F, P, I, I, I, I,
                                       I, I]
         lib.emu_smooth.argtypes = [P, P, L, I, F]
+        lib.emu_topk_chunks.argtypes = [P, P, I, I, L, I, I, I, I, F, P, P, P, P]
+        lib.emu_topk_chunk_count.argtypes = [I, I]
 
     def topk(self, q, kl, k, causal, scale, row_list=None):
         """q [n_head_rows..] as [BH, Tq, P], kl [BH, Tk, P] torch; returns idx, score."""
@@ -73,6 +75,25 @@ class Emu:
         rc = self.lib.emu_topk_rows(_p(_raw(q)), _p(_raw(kl)), int(q.dtype == torch.bfloat16), P,
                                     _p(rl), rows, Tq, Tk, k, int(causal), scale, _p(idx), _p(sc),
                                     _p(ws), TOPK_SLOTS, stride)
+        assert rc == 0
+        return idx.reshape(BH, Tq, k), sc.reshape(BH, Tq, k)
+
+    def topk_chunks(self, q, kl, k, causal, scale):
+        """The long-row path (chunk selections, then the merge); garbage-filled
+        scratch of exactly the size the library's workspace gives it."""
+        BH, Tq, P = q.shape
+        Tk = kl.shape[1]
+        rows = BH * Tq
+        nchunks = self.lib.emu_topk_chunk_count(Tk, k)
+        assert nchunks > 0
+        kcap = min(k, 8192)
+        cand = np.full(rows * nchunks * kcap, 0xA5A5A5A5A5A5A5A5, np.uint64)
+        cnt = np.full(rows * nchunks, -9, np.int32)
+        idx = np.full((rows, k), -7, np.int32)
+        sc = np.full((rows, k), np.nan, np.float32)
+        rc = self.lib.emu_topk_chunks(_p(_raw(q)), _p(_raw(kl)), int(q.dtype == torch.bfloat16), P,
+                                      rows, Tq, Tk, k, int(causal), scale, _p(idx), _p(sc),
+                                      _p(cand), _p(cnt))
         assert rc == 0
         return idx.reshape(BH, Tq, k), sc.reshape(BH, Tq, k)
 
@@ -170,6 +191,33 @@ def check_topk_ties_and_list(emu, fails):
     untouched = np.setdiff1d(np.arange(60), rows)
     if not (flat[untouched] == -7).all():
         fails.append("topk row list: a row outside the list was written")
+
+
+CHUNK_CASES = [
+    # BH, Tq, Tk, P, k, causal, dtype: rows of 2 or 3 key chunks of 8192
+    (2, 1, 20000, 64, 64, False, torch.bfloat16),     # a ragged last chunk
+    (1, 3, 17000, 32, 512, True, torch.float32),      # causal, Tq < Tk: rows end in chunk 2
+    (1, 1, 16384, 64, 512, False, torch.bfloat16),    # two whole chunks, the decode k
+]
+
+
+def check_topk_chunks(emu, case, fails):
+    BH, Tq, Tk, P, k, causal, dtype = case
+    q = _ints((BH, Tq, P), 300 + Tq, dtype)
+    kl = _ints((BH, Tk, P), 400 + Tk, dtype)
+    scale = float(np.float32(P ** -0.5))
+    idx, sc = emu.topk_chunks(q, kl, k, causal, scale)
+    for h in range(BH):
+        ri, rs = oracle.topk_rows(q[h], np.arange(Tq), kl[h], k, Tq, causal)
+        if not (np.array_equal(idx[h], ri) and np.array_equal(sc[h], rs)):
+            bad = np.argwhere((idx[h] != ri).any(-1))[:3].ravel().tolist()
+            fails.append("topk chunks %s head %d: rows %s differ" % (case, h, bad))
+    # all scores equal: the lowest indices of the row, across chunks
+    q0 = torch.zeros(1, 1, 64, dtype=torch.bfloat16)
+    kl0 = _ints((1, 16500, 64), 9, torch.bfloat16)
+    idx0, _ = emu.topk_chunks(q0, kl0, 100, False, 0.125)
+    if not (idx0[0, 0] == np.arange(100)).all():
+        fails.append("topk chunks all ties: not the 100 lowest indices")
 
 
 ATTN_CASES = [
@@ -283,6 +331,8 @@ def check_all(path, small=False):
     for c in (TOPK_CASES[:2] if small else TOPK_CASES):
         check_topk(emu, c, fails)
     check_topk_ties_and_list(emu, fails)
+    for c in (CHUNK_CASES[:1] if small else CHUNK_CASES):
+        check_topk_chunks(emu, c, fails)
     for c in (ATTN_CASES[:2] if small else ATTN_CASES):
         check_attn(emu, c, fails)
     check_window(emu, fails)

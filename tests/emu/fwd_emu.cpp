@@ -1,4 +1,4 @@
-// The forward's CUDA-core kernels (row-wise top-k, gather and window
+// The forward's CUDA-core kernels (row-wise top-k and its long-row chunks, gather and window
 // attention, boundary smoothing) built for the host: see emu_device.h in this
 // directory. The launches mirror the library's: one 512-thread block per
 // row-wise top-k row (a grid of min(rows, slots) blocks), one warp per
@@ -26,6 +26,31 @@ extern "C" int emu_topk_rows(const void* q_low, const void* k_low, int bf16, int
 #undef C
     return 1;
 }
+
+// The long-row path: one 256-thread block per (row, key chunk), then one
+// 512-thread block per row for the merge, as the library launches them.
+extern "C" int emu_topk_chunks(const void* q_low, const void* k_low, int bf16, int P, int64_t rows,
+                               int Tq, int Tk, int k, int causal, float scale, int32_t* idx,
+                               float* score, uint64_t* cand, int32_t* cnt) {
+    const int nchunks = ssa::topk_chunk_count(Tk, k);
+    if (nchunks == 0) return 2;
+    const unsigned blocks = (unsigned)(rows * nchunks);
+#define C(BF, PP)                                                                             \
+    if (bf16 == BF && P == PP) {                                                              \
+        emu_launch(blocks, ssa::kChunkThreads, [&] {                                          \
+            ssa::topk_chunk_kernel<BF, PP>(q_low, k_low, nchunks, Tq, Tk, k, causal, scale,   \
+                                           cand, cnt);                                        \
+        });                                                                                   \
+    } else
+    C(1, 16) C(1, 32) C(1, 64) C(1, 128) C(0, 16) C(0, 32) C(0, 64) C(0, 128) return 1;
+#undef C
+    emu_launch((unsigned)rows, ssa::kMergeThreads, [&] {
+        ssa::topk_merge_kernel(cand, cnt, nchunks, Tq, Tk, k, causal, idx, score);
+    });
+    return 0;
+}
+
+extern "C" int emu_topk_chunk_count(int Tk, int k) { return ssa::topk_chunk_count(Tk, k); }
 
 extern "C" int emu_attn_rows(const void* Q, const void* K, const void* V, int bf16_in, int D,
                              const int32_t* idx, void* O, int bf16_out, int64_t rows, int Tq,
