@@ -308,9 +308,9 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_rows_kernel(
 //                      chunk's exact top-min(k, n) (same radix select and tie
 //                      rule as the row kernel), written unordered as
 //                      composite keys (score order key, ~index);
-//   topk_merge_kernel  gathers the chunks' selections of a row and sorts
-//                      them (bitonic, descending); the first k_eff are the
-//                      row's answer.
+//   topk_merge_kernel  gathers the chunks' selections of a row, finds the
+//                      k_eff largest by a radix select over the distinct
+//                      composite keys and sorts those (bitonic, descending).
 // A key of the row's top k has fewer than k keys ahead of it in the row,
 // hence fewer than k in its chunk: it is in its chunk's selection, so the
 // merge of the chunk selections holds the row's whole top k.
@@ -465,9 +465,14 @@ __global__ void __launch_bounds__(kChunkThreads, 4) topk_chunk_kernel(
 __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(
     const uint64_t* __restrict__ cand, const int32_t* __restrict__ cnt, int nchunks, int Tq,
     int Tk, int k, int causal, int32_t* __restrict__ idx_out, float* __restrict__ score_out) {
-    __shared__ uint64_t buf[kMergeMax];
+    constexpr int KPT = kMergeMax / kMergeThreads;   // candidates per thread
+    __shared__ uint64_t buf[kMergeMax];   // the candidates, then the winners
+    __shared__ uint32_t hist[256];
     __shared__ int off[65];
-    const int tid = threadIdx.x;
+    __shared__ uint64_t s_prefix;
+    __shared__ int s_need, s_done;
+    __shared__ uint32_t n_win;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int64_t row = blockIdx.x;
     const int i = static_cast<int>(row % Tq);
     int nv = Tk;
@@ -484,17 +489,96 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(
             o += cnt[row * nchunks + c];
         }
         off[nchunks] = o;
+        s_prefix = 0;
+        s_need = keff;
+        s_done = 0;
+        n_win = 0;
     }
     __syncthreads();
-    const int total = off[nchunks];   // <= nchunks * kcap <= kMergeMax
-    int n2 = 1;
-    while (n2 < total) n2 <<= 1;
+    const int total = off[nchunks];   // <= nchunks * kcap <= kMergeMax, >= keff
     for (int c = 0; c < nchunks; ++c) {
         const uint64_t* src = cand + (row * nchunks + c) * static_cast<int64_t>(kcap);
         const int m = off[c + 1] - off[c];
         for (int t = tid; t < m; t += kMergeThreads) buf[off[c] + t] = src[t];
     }
-    for (int t = total + tid; t < n2; t += kMergeThreads) buf[t] = 0ull;   // below every key
+    __syncthreads();
+    uint64_t mine[KPT];   // candidate t0*kMergeThreads + tid of the row, 0 past the last
+#pragma unroll
+    for (int r = 0; r < KPT; ++r) {
+        const int t = r * kMergeThreads + tid;
+        mine[r] = t < total ? buf[t] : 0ull;
+    }
+    __syncthreads();   // every thread holds its candidates before buf is reused
+    // The composite keys are distinct (they hold the index), so the keff-th
+    // largest is unique: a radix select over its 8-bit digits, most
+    // significant first, stops as soon as the remaining rank fills a bin;
+    // the winners are then every key at or above the prefix found.
+    if (keff < total) {
+        for (int sh = 56; sh >= 0; sh -= 8) {
+            if (tid < 256) hist[tid] = 0;
+            __syncthreads();
+            const uint64_t pre = s_prefix;
+#pragma unroll
+            for (int r = 0; r < KPT; ++r) {
+                const int t = r * kMergeThreads + tid;
+                const uint64_t key = mine[r];
+                const bool match = t < total && (sh == 56 || (key >> (sh + 8)) == (pre >> (sh + 8)));
+                hist_add(hist, static_cast<uint32_t>((key >> sh) & 0xFFu), match);
+            }
+            __syncthreads();
+            if (tid < 32) {   // the bin holding the need-th largest: lane l owns bins 255-8l ..
+                uint32_t c8[8], tot = 0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    c8[q] = hist[255 - 8 * lane - q];
+                    tot += c8[q];
+                }
+                uint32_t incl = tot;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const uint32_t need = static_cast<uint32_t>(s_need);
+                uint32_t above = incl - tot;
+                if (above < need && need <= incl) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        if (above + c8[q] >= need) {
+                            const uint32_t d = 255u - 8u * lane - q;
+                            s_prefix = pre | (static_cast<uint64_t>(d) << sh);
+                            s_need = static_cast<int>(need - above);
+                            s_done = c8[q] == need - above;   // the whole bin is taken
+                            break;
+                        }
+                        above += c8[q];
+                    }
+                }
+            }
+            __syncthreads();
+            if (s_done) break;
+        }
+    }
+    // winners: every key at or above the prefix (exactly keff of them),
+    // compacted to the front of buf (the candidates are in registers now)
+    const uint64_t thr = keff < total ? s_prefix : 0ull;
+    uint64_t* win = buf;
+#pragma unroll
+    for (int r = 0; r < KPT; ++r) {
+        const int t = r * kMergeThreads + tid;
+        const bool take = t < total && mine[r] >= thr;
+        const unsigned b = __ballot_sync(0xffffffffu, take);
+        uint32_t base = 0;
+        if (lane == 0 && b) base = atomicAdd(&n_win, static_cast<uint32_t>(__popc(b)));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const uint32_t slot = base + __popc(b & ((1u << lane) - 1));
+        if (take && slot < static_cast<uint32_t>(TOPK_KMAX)) win[slot] = mine[r];
+    }
+    __syncthreads();
+    // sort the winners descending (bitonic over the next power of two)
+    int n2 = 1;
+    while (n2 < keff) n2 <<= 1;
+    for (int t = keff + tid; t < n2; t += kMergeThreads) win[t] = 0ull;   // below every key
     __syncthreads();
     for (int size = 2; size <= n2; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -502,10 +586,10 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(
                 const int lo = 2 * t - (t & (stride - 1));
                 const int hi = lo + stride;
                 const bool desc = (lo & size) == 0;
-                const uint64_t a = buf[lo], b = buf[hi];
+                const uint64_t a = win[lo], b = win[hi];
                 if ((a < b) == desc) {
-                    buf[lo] = b;
-                    buf[hi] = a;
+                    win[lo] = b;
+                    win[hi] = a;
                 }
             }
             __syncthreads();
@@ -515,7 +599,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(
     float* so = score_out ? score_out + row * static_cast<int64_t>(k) : nullptr;
     for (int t = tid; t < k; t += kMergeThreads) {
         if (t < keff) {
-            const uint64_t key = buf[t];
+            const uint64_t key = win[t];
             io[t] = static_cast<int32_t>(sel_key_index(key));
             if (so) so[t] = order_key_f32(sel_key_okey(key));
         } else {
