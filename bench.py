@@ -102,13 +102,24 @@ def algorithmic(w):
     }
 
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# ncu capture of these kernels on these workloads; to be re-measured, or
-# dropped, when the kernels change.
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# score passes, from one-launch ncu captures on the 32K workload; to be
+# re-measured, or dropped, when the kernels change. Their traffic is the group
+# maxima and candidate lists they write, which grow with rows x k, so the
+# 128K figures are the 32K ones scaled by that ratio (4), not captured at 128K.
 MEASURED_TRAFFIC = {
-    ("topk_causal_bf16_t128k_k512_planted", "tile_scores.groupmax"): 3.580e9,
-    ("topk_causal_bf16_t32k_k256", "tile_scores.groupmax"): 0.892e9,
+    ("topk_causal_bf16_t32k_k256", "tile_scores.groupmax"): 0.897e9,
+    ("topk_causal_bf16_t32k_k256", "tile_scores.collect"): 1.836e9,
+    ("topk_causal_bf16_t128k_k512_planted", "tile_scores.groupmax"): 4 * 0.897e9,
+    ("topk_causal_bf16_t128k_k512_planted", "tile_scores.collect"): 4 * 1.836e9,
 }
+
+# Read throughput of the L2 slices (GB/s) that serve the gather: the kernel's
+# lts__t_sectors_srcunit_tex_op_read bytes divided by its duration and by the
+# fraction of peak ncu reports for that counter, on the 32K workload (66.2 GB
+# in 3.774 ms at 75.5% of peak). The gather's K/V rows come from L2 (97% hits),
+# so this, not the HBM copy rate, is the ceiling it runs against.
+L2_SLICE_READ_GBS = 23.2e3
 
 
 def roofline_for(name, ms, w, alg, pk, pk_kind):
@@ -142,13 +153,23 @@ def roofline_for(name, ms, w, alg, pk, pk_kind):
     elif name == "group_select":
         by = rows * 3 * w.k * 2 * 2
         what = "group maxima read twice (about 3k x 2 B per row)"
+    elif name == "topk_merge":
+        kcap = min(w.k, 8192)
+        nch = (w.Tk + 8191) // 8192
+        by = rows * nch * kcap * 8 + rows * w.k * 4
+        what = "the key chunks' selections read (8 B each) + index list written (k x 4 B) per row"
     else:   # the row-wise top-k: every valid key's k_low row, once per query row
         by = alg["scored_pairs"] * w.P * (4 if w.dtype == "f32" else 2)
         what = "k_low rows scored: d_proj * esize per valid (query, key) pair"
     achieved = by / sec / 1e9
-    return {"kernel": name, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+    line = {"kernel": name, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
             "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
             "peak_kind": pk_kind + " HBM copy", "algorithmic": "%s, %.4g B per launch" % (what, by)}
+    if name == "attn_rows.sparse":
+        line["l2"] = {"achieved": achieved, "peak": L2_SLICE_READ_GBS, "unit": "GB/s",
+                      "frac": achieved / L2_SLICE_READ_GBS,
+                      "peak_kind": "L2 slice read throughput derived from ncu (the gather is L2-served)"}
+    return line
 
 
 # ------------------------------------------------------------------ clocks
@@ -463,6 +484,7 @@ def run_ours(args, rank, world, local_rank):
         elif name == "sparse_attn":
             ph["gbs"] = alg["gather_bytes"] / (ms * 1e-3) / 1e9
             ph["frac_hbm"] = ph["gbs"] / pk["hbm_gbs"]
+            ph["frac_l2"] = ph["gbs"] / L2_SLICE_READ_GBS   # the ceiling of an L2-served gather
             ph["aux_bytes"] = alg.get("gather_aux_bytes")   # idx, Q and O, beside the gather
         else:
             ph["gbs"] = alg["window_bytes"] / (ms * 1e-3) / 1e9
