@@ -757,16 +757,16 @@ def run_backward(args, rank, world, local_rank):
     Q, K, V = make_attn_inputs(w, dev)
     dO = make_grad_output(w, dev)
     idx = ssa.ssa_score_topk(q_low, k_low, w.k, w.causal)
-    ws_a = torch.empty(ssa.sparse_attn_bwd_workspace_size(w.B, w.H, w.Tq, w.Tk, w.k),
-                       dtype=torch.uint8, device=dev)
-    ws_s = torch.empty(ssa.scorer_bwd_workspace_size(w.B, w.H, w.Tq, w.Tk, w.k),
-                       dtype=torch.uint8, device=dev)
+    ws = torch.empty(ssa.sparse_attn_scorer_bwd_workspace_size(w.B, w.H, w.Tq, w.Tk, w.k),
+                     dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(q_, k_, Q_, K_, V_, dO_, idx_):
-        dQ, dK, dV, dS = ssa.ssa_sparse_attn_bwd(Q_, K_, V_, idx_, dO_, workspace=ws_a)
-        dq, dk = ssa.ssa_scorer_bwd(q_, k_, idx_, dS, workspace=ws_s)
+        # the attention's and the scorer's gradients in one call: the
+        # key-major lists both key sides walk are built once
+        dQ, dK, dV, dS, dq, dk = ssa.ssa_sparse_attn_scorer_bwd(Q_, K_, V_, dO_, q_, k_, idx_,
+                                                               workspace=ws)
         return dQ, dK, dV, dq, dk
 
     args_dev = (q_low, k_low, Q, K, V, dO, idx)

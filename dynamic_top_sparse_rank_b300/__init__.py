@@ -20,7 +20,8 @@ from ._native import (EXPORTS, SSA_BF16, SSA_DEV_BAD_INDEX, SSA_DEV_OVERFLOW, SS
                       ssa_sparse_attn_grouped, ssa_window_attn, status_string,
                       sparse_attn_bwd_workspace_size, scorer_bwd_workspace_size,
                       ssa_sparse_attn_grouped_bwd, ssa_scorer_grouped_bwd,
-                      ssa_selftest_wait_limit, device_status, SSA_ERR_TIMEOUT)
+                      ssa_selftest_wait_limit, device_status, SSA_ERR_TIMEOUT,
+                      ssa_sparse_attn_scorer_bwd, sparse_attn_scorer_bwd_workspace_size)
 
 __all__ = ["EXPORTS", "SSA_BF16", "SSA_DEV_BAD_INDEX", "SSA_DEV_OVERFLOW", "SSA_DEV_WAIT_LIMIT",
            "SSA_F32", "SSAError", "load", "score_topk_workspace_size", "ssa_lowrank_project",
@@ -30,4 +31,5 @@ __all__ = ["EXPORTS", "SSA_BF16", "SSA_DEV_BAD_INDEX", "SSA_DEV_OVERFLOW", "SSA_
            "ssa_sparse_attn_grouped", "ssa_window_attn", "status_string",
            "sparse_attn_bwd_workspace_size", "scorer_bwd_workspace_size",
            "ssa_sparse_attn_grouped_bwd", "ssa_scorer_grouped_bwd", "ssa_selftest_wait_limit",
-           "device_status", "SSA_ERR_TIMEOUT"]
+           "device_status", "SSA_ERR_TIMEOUT", "ssa_sparse_attn_scorer_bwd",
+           "sparse_attn_scorer_bwd_workspace_size"]

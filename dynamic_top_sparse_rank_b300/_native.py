@@ -31,7 +31,8 @@ EXPORTS = ("ssa_version", "ssa_status_string", "ssa_score_topk_workspace_size", 
            "ssa_scorer_bwd_workspace_size", "ssa_scorer_bwd",
            "ssa_sparse_attn_grouped_bwd_workspace_size", "ssa_sparse_attn_grouped_bwd",
            "ssa_scorer_grouped_bwd_workspace_size", "ssa_scorer_grouped_bwd",
-           "ssa_selftest_wait_limit", "ssa_device_status")
+           "ssa_selftest_wait_limit", "ssa_device_status", "ssa_sparse_attn_scorer_bwd",
+           "ssa_sparse_attn_scorer_bwd_workspace_size")
 
 # Fixed scratch of ssa_score_topk_noalloc and the largest Tk it accepts.
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -104,6 +105,11 @@ def load(path: str | None = None):
     lib.ssa_scorer_grouped_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
     lib.ssa_scorer_grouped_bwd.restype = I
     lib.ssa_scorer_grouped_bwd.argtypes = [V, V, I, I, I, I, I, I, I, V, I, V, F, V, V, V, Z, V, V]
+    lib.ssa_sparse_attn_scorer_bwd_workspace_size.restype = Z
+    lib.ssa_sparse_attn_scorer_bwd_workspace_size.argtypes = [I, I, I, I, I]
+    lib.ssa_sparse_attn_scorer_bwd.restype = I
+    lib.ssa_sparse_attn_scorer_bwd.argtypes = [V, V, V, V, V, V, I, I, I, I, I, I, I, V, I, F, F,
+                                               V, V, V, V, V, V, V, V, Z, V, V]
     lib.ssa_device_status.restype = I
     lib.ssa_device_status.argtypes = [V, V, V]
     lib.ssa_selftest_wait_limit.restype = I
@@ -456,6 +462,48 @@ def ssa_scorer_bwd(q_low, k_low, idx, dS, scale: float = 0.0, workspace=None, de
                             _ptr(dev_status), _stream(dev))
     _check(rc, "ssa_scorer_bwd")
     return dq, dk
+
+
+def sparse_attn_scorer_bwd_workspace_size(B, H, Tq, Tk, k) -> int:
+    return int(load().ssa_sparse_attn_scorer_bwd_workspace_size(B, H, Tq, Tk, k))
+
+
+def ssa_sparse_attn_scorer_bwd(Q, K, V, dO, q_low, k_low, idx, scale: float = 0.0,
+                               scorer_scale: float = 0.0, workspace=None, dev_status=None,
+                               with_prob: bool = False):
+    """ssa_sparse_attn_bwd then ssa_scorer_bwd in one call (the key-major lists
+    built once). Returns fp32 (dQ, dK, dV, dS, dq_low, dk_low) (+ prob)."""
+    lib = load()
+    dev = _dev(Q, K, V, dO, q_low, k_low, idx, workspace, dev_status)
+    if not (Q.dtype == K.dtype == V.dtype == dO.dtype == q_low.dtype == k_low.dtype):
+        raise TypeError("Q, K, V, dO, q_low, k_low must share a dtype")
+    if idx.dtype != torch.int32:
+        raise TypeError("idx must be int32")
+    B, H, Tq, D = Q.shape
+    Tk, P, k = K.shape[2], q_low.shape[3], idx.shape[3]
+    if (tuple(K.shape) != (B, H, Tk, D) or tuple(V.shape) != (B, H, Tk, D) or
+            tuple(dO.shape) != (B, H, Tq, D) or tuple(q_low.shape) != (B, H, Tq, P) or
+            tuple(k_low.shape) != (B, H, Tk, P) or tuple(idx.shape[:3]) != (B, H, Tq)):
+        raise ValueError("shapes do not match")
+    f32 = dict(dtype=torch.float32, device=dev)
+    dQ = torch.empty((B, H, Tq, D), **f32)
+    dK = torch.empty((B, H, Tk, D), **f32)
+    dV = torch.empty((B, H, Tk, D), **f32)
+    dS = torch.empty((B, H, Tq, k), **f32)
+    dq = torch.empty((B, H, Tq, P), **f32)
+    dk = torch.empty((B, H, Tk, P), **f32)
+    prob = torch.empty((B, H, Tq, k), **f32) if with_prob else None
+    need = sparse_attn_scorer_bwd_workspace_size(B, H, Tq, Tk, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = lib.ssa_sparse_attn_scorer_bwd(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(q_low), _ptr(k_low), _dt(Q), B, H, Tq, Tk, D, P,
+        _ptr(idx), k, float(scale), float(scorer_scale), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dS),
+        _ptr(prob), _ptr(dq), _ptr(dk), _ptr(workspace), wbytes, _ptr(dev_status), _stream(dev))
+    _check(rc, "ssa_sparse_attn_scorer_bwd")
+    out = (dQ, dK, dV, dS, dq, dk)
+    return out + (prob,) if with_prob else out
 
 
 def ssa_sparse_attn_grouped_bwd(Q, K, V, idx, dO, scale: float = 0.0, workspace=None,

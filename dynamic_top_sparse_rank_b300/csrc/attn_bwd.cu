@@ -599,7 +599,8 @@ template <bool BF, int PP>
 cudaError_t scorer_bwd_t(const void* q_low, const void* k_low, const int32_t* idx,
                          const float* dS, int B, int H_idx, int gi, int Tq, int Tk, int k,
                          float sigma, float* dq_low, float* dk_low, float* dS_sum, int32_t* cnt,
-                         int32_t* off, int32_t* list, int32_t* dev_status, cudaStream_t stream) {
+                         int32_t* off, int32_t* list, bool lists_ready, int32_t* dev_status,
+                         cudaStream_t stream) {
     const int64_t rows = (int64_t)B * H_idx * Tq, keys = (int64_t)B * H_idx * Tk;
     const int64_t qb = warp_blocks(rows), kb = warp_blocks(keys);
     if (qb < 0 || kb < 0) return cudaErrorInvalidConfiguration;
@@ -622,8 +623,9 @@ cudaError_t scorer_bwd_t(const void* q_low, const void* k_low, const int32_t* id
     }
     if (kb == 0) return cudaSuccess;
     const BwdHeads plain{H_idx, 1, 1};
-    if ((e = pair_lists_build(idx, B, Tq, Tk, k, plain, cnt, off, list, dev_status, stream)) !=
-        cudaSuccess)
+    if (!lists_ready &&
+        (e = pair_lists_build(idx, B, Tq, Tk, k, plain, cnt, off, list, dev_status, stream)) !=
+            cudaSuccess)
         return e;
     TraceLaunch tr("scorer_bwd.key", stream);
     auto* kk = &pair_key_kernel<BF, PP, false>;
@@ -659,12 +661,13 @@ cudaError_t scorer_bwd_launch(const void* q_low, const void* k_low, bool bf16, i
                               const int32_t* idx, const float* dS, int B, int H, int H_idx,
                               int Tq, int Tk, int k, float sigma, float* dq_low, float* dk_low,
                               float* dS_sum, int32_t* cnt, int32_t* off, int32_t* list,
-                              int32_t* dev_status, cudaStream_t stream) {
+                              bool lists_ready, int32_t* dev_status, cudaStream_t stream) {
     const int gi = H / H_idx;
 #define SSA_SBWD_CASE(BF, PP)                                                                 \
     if (bf16 == BF && P == PP)                                                                \
         return scorer_bwd_t<BF, PP>(q_low, k_low, idx, dS, B, H_idx, gi, Tq, Tk, k, sigma,     \
-                                    dq_low, dk_low, dS_sum, cnt, off, list, dev_status, stream);
+                                    dq_low, dk_low, dS_sum, cnt, off, list, lists_ready,       \
+                                    dev_status, stream);
     SSA_SBWD_CASE(true, 16)
     SSA_SBWD_CASE(true, 32)
     SSA_SBWD_CASE(true, 64)
@@ -833,7 +836,7 @@ ssa_status ssa_scorer_grouped_bwd(const void* q_low, const void* k_low, int dtyp
     const cudaError_t e = ssa::scorer_bwd_launch(
         q_low, k_low, dtype == SSA_BF16, P, idx, dS, B, H, H_idx, Tq, Tk, k, sg, dq_low, dk_low,
         reinterpret_cast<float*>(ws + w.extra), reinterpret_cast<int32_t*>(ws + w.cnt),
-        reinterpret_cast<int32_t*>(ws + w.off), reinterpret_cast<int32_t*>(ws + w.list),
+        reinterpret_cast<int32_t*>(ws + w.off), reinterpret_cast<int32_t*>(ws + w.list), false,
         dev_status, s);
     return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
 }
@@ -851,6 +854,66 @@ ssa_status ssa_scorer_bwd(const void* q_low, const void* k_low, int dtype, int B
     }
     return ssa_scorer_grouped_bwd(q_low, k_low, dtype, B, H, H, Tq, Tk, P, idx, k, dS, scale,
                                   dq_low, dk_low, workspace, workspace_bytes, dev_status, stream);
+}
+
+size_t ssa_sparse_attn_scorer_bwd_workspace_size(int B, int H, int Tq, int Tk, int k) {
+    return ssa_sparse_attn_bwd_workspace_size(B, H, Tq, Tk, k);
+}
+
+// Both backward calls in one: the key-major lists of the index lists, which
+// the attention's key side and the scorer's key side both walk, are built
+// once.
+ssa_status ssa_sparse_attn_scorer_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                                      const void* q_low, const void* k_low, int dtype, int B,
+                                      int H, int Tq, int Tk, int D, int P, const int32_t* idx,
+                                      int k, float scale, float scorer_scale, float* dQ,
+                                      float* dK, float* dV, float* dS, float* prob,
+                                      float* dq_low, float* dk_low, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status,
+                                      void* stream) {
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || k < 1 || (dtype != SSA_F32 && dtype != SSA_BF16) ||
+        !isfinite(scale) || !isfinite(scorer_scale))
+        return SSA_ERR_INVALID;
+    if (!(D == 64 || D == 128) || !(P == 16 || P == 32 || P == 64 || P == 128))
+        return SSA_ERR_UNSUPPORTED;
+    if ((int64_t)Tq * k > INT32_MAX || (int64_t)B * H > INT32_MAX) return SSA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)B * H * Tq, keys = (int64_t)B * H * Tk;
+    if (rows == 0 && keys == 0) return SSA_OK;
+    if (rows > 0 && (!Q || !dO || !idx || !dQ || !dS || !q_low || !dq_low)) return SSA_ERR_INVALID;
+    if (keys > 0 && (!K || !V || !dK || !dV || !k_low || !dk_low)) return SSA_ERR_INVALID;
+    if (!ssa::al(Q, 16) || !ssa::al(K, 16) || !ssa::al(V, 16) || !ssa::al(dO, 16) ||
+        !ssa::al(q_low, 16) || !ssa::al(k_low, 16) || !ssa::al(dQ, 16) || !ssa::al(dK, 16) ||
+        !ssa::al(dV, 16) || !ssa::al(dq_low, 16) || !ssa::al(dk_low, 16) || !ssa::al(dS, 4) ||
+        !ssa::al(idx, 4) || !ssa::al(prob, 4) || !ssa::al(dev_status, 4))
+        return SSA_ERR_INVALID;
+    const int64_t slots = rows * k;
+    const ssa::BwdWorkspace w = ssa::bwd_workspace((int64_t)B * H, Tk, slots, slots);
+    if (!workspace || !ssa::al(workspace, 256) || workspace_bytes < (size_t)w.total)
+        return SSA_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    float* pr = prob ? prob : reinterpret_cast<float*>(ws + w.extra);
+    const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)D));
+    const float sg = scorer_scale > 0.f ? scorer_scale : (float)(1.0 / sqrt((double)P));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (rows == 0) {   // no query rows: every key's gradient is zero
+        cudaError_t e = cudaMemsetAsync(dK, 0, sizeof(float) * (size_t)(keys * D), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dV, 0, sizeof(float) * (size_t)(keys * D), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dk_low, 0, sizeof(float) * (size_t)(keys * P), s);
+        return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
+    }
+    int32_t* cnt = reinterpret_cast<int32_t*>(ws + w.cnt);
+    int32_t* off = reinterpret_cast<int32_t*>(ws + w.off);
+    int32_t* list = reinterpret_cast<int32_t*>(ws + w.list);
+    cudaError_t e = ssa::attn_bwd_launch(Q, K, V, dO, dtype == SSA_BF16, D, idx, B, H, H, H, Tq,
+                                         Tk, k, sc, dQ, dK, dV, dS, pr, cnt, off, list,
+                                         dev_status, s);
+    // the attention's key side built the lists (there are keys whenever there
+    // are query rows); the scorer's key side walks the same ones
+    if (e == cudaSuccess)
+        e = ssa::scorer_bwd_launch(q_low, k_low, dtype == SSA_BF16, P, idx, dS, B, H, H, Tq, Tk, k,
+                                   sg, dq_low, dk_low, nullptr, cnt, off, list, keys > 0,
+                                   dev_status, s);
+    return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -433,6 +433,36 @@ ssa_status ssa_scorer_bwd(const void* q_low, const void* k_low, int dtype, int B
                           int32_t* dev_status, void* stream);
 
 /*
+ * ssa_sparse_attn_scorer_bwd — ssa_sparse_attn_bwd and ssa_scorer_bwd in one
+ * call, for the plain layout (every head its own keys, values and scorer).
+ *
+ * Source: mhpq.cn/news/1098205, sections 2.2 and 2.3, as for the two calls.
+ * The gradients are exactly those of ssa_sparse_attn_bwd followed by
+ * ssa_scorer_bwd on the dS it produced (same arguments, same rules); the key
+ * sides of both walk the key-major lists of the index lists, which this call
+ * builds once instead of twice.
+ *
+ *   Q, dO, dQ [B, H, Tq, D]; K, V, dK, dV [B, H, Tk, D]; idx, dS, prob
+ *   [B, H, Tq, k]; q_low, dq_low [B, H, Tq, P]; k_low, dk_low [B, H, Tk, P]
+ *   scale         attention logit scale (<= 0: 1 / sqrt(D))
+ *   scorer_scale  scorer scale (<= 0: fp32(1 / sqrt(P)))
+ *   workspace     ssa_sparse_attn_scorer_bwd_workspace_size(B, H, Tq, Tk, k)
+ *                 bytes, 256-byte aligned
+ *
+ * D in {64, 128}, P in {16, 32, 64, 128}, Tq * k <= 2^31 - 1. Returns as
+ * ssa_sparse_attn_bwd.
+ */
+size_t ssa_sparse_attn_scorer_bwd_workspace_size(int B, int H, int Tq, int Tk, int k);
+ssa_status ssa_sparse_attn_scorer_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                                      const void* q_low, const void* k_low, int dtype, int B,
+                                      int H, int Tq, int Tk, int D, int P, const int32_t* idx,
+                                      int k, float scale, float scorer_scale, float* dQ,
+                                      float* dK, float* dV, float* dS, float* prob,
+                                      float* dq_low, float* dk_low, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status,
+                                      void* stream);
+
+/*
  * ssa_scorer_grouped_bwd — the scorer's gradients when H query heads share
  * H_idx scorer heads (H_idx = 1: the shared scorer of mhpq.cn/news/1098205,
  * section 3.2). The score of a pair in index head hi feeds the logits of

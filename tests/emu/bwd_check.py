@@ -63,6 +63,11 @@ class Emu:
         lib.ssa_scorer_grouped_bwd.argtypes = [P, P, I, I, I, I, I, I, I, P, I, P, F, P, P, P, Z,
                                                P, P]
         lib.ssa_scorer_grouped_bwd.restype = I
+        lib.ssa_sparse_attn_scorer_bwd_workspace_size.argtypes = [I] * 5
+        lib.ssa_sparse_attn_scorer_bwd_workspace_size.restype = Z
+        lib.ssa_sparse_attn_scorer_bwd.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, P, I, F,
+                                                   F, P, P, P, P, P, P, P, P, Z, P, P]
+        lib.ssa_sparse_attn_scorer_bwd.restype = I
         self.libc = libc = ctypes.CDLL(None)
         libc.aligned_alloc.argtypes = [Z, Z]
         libc.aligned_alloc.restype = P
@@ -109,6 +114,29 @@ class Emu:
                                      _p(st), None)
         self.libc.free(ws)
         return rc, dq, dk, int(st[0])
+
+    def fused_bwd(self, Q, K, V, dO, ql, kl, idx):
+        """ssa_sparse_attn_scorer_bwd: both backward calls with one list build."""
+        B, H, Tq, D = Q.shape
+        Tk, k, P = K.shape[2], idx.shape[-1], ql.shape[-1]
+        bufs = [_raw(t) for t in (Q, K, V, dO, ql, kl)]
+        outs = dict(dQ=np.full((B, H, Tq, D), np.nan, np.float32),
+                    dK=np.full((B, H, Tk, D), np.nan, np.float32),
+                    dV=np.full((B, H, Tk, D), np.nan, np.float32),
+                    dS=np.full((B, H, Tq, k), np.nan, np.float32),
+                    prob=np.full((B, H, Tq, k), np.nan, np.float32),
+                    dq=np.full((B, H, Tq, P), np.nan, np.float32),
+                    dk=np.full((B, H, Tk, P), np.nan, np.float32))
+        st = np.zeros(1, np.int32)
+        ix = np.ascontiguousarray(idx, np.int32)
+        n = self.lib.ssa_sparse_attn_scorer_bwd_workspace_size(B, H, Tq, Tk, k)
+        ws = self._ws(n)
+        rc = self.lib.ssa_sparse_attn_scorer_bwd(
+            *[_p(b) for b in bufs], int(Q.dtype == torch.bfloat16), B, H, Tq, Tk, D, P, _p(ix), k,
+            0.0, 0.0, *[_p(outs[n_]) for n_ in ("dQ", "dK", "dV", "dS", "prob", "dq", "dk")], ws,
+            n, _p(st), None)
+        self.libc.free(ws)
+        return rc, outs, int(st[0])
 
     def grouped_attn_bwd(self, Q, K, V, dO, idx):
         """Q, dO [B,H,Tq,D]; K, V [B,H_kv,Tk,D]; idx [B,H_idx,Tq,k]."""
@@ -239,6 +267,35 @@ def check_scorer(emu, case, fails):
     rq, rk = oracle.scorer_bwd(ql, kl, idx, dS)
     _close(dq, rq, tag + " dq_low", fails)
     _close(dk, rk, tag + " dk_low", fails)
+
+
+FUSED_CASES = [
+    # B, H, Tq, Tk, D, P, k, dtype, seed
+    (1, 2, 30, 80, 64, 64, 9, torch.bfloat16, 11),
+    (2, 1, 12, 40, 128, 16, 6, torch.float32, 12),
+]
+
+
+def check_fused(emu, case, fails):
+    """ssa_sparse_attn_scorer_bwd against the oracle: the attention's and the
+    scorer's gradients of one backward step, the lists built once."""
+    B, H, Tq, Tk, D, P, k, dtype, seed = case
+    Q, K, V, dO, idx = attn_inputs(B, H, Tq, Tk, D, k, dtype, seed)
+    g = torch.Generator().manual_seed(seed)
+    ql = torch.randn(B, H, Tq, P, generator=g).to(dtype)
+    kl = torch.randn(B, H, Tk, P, generator=g).to(dtype)
+    rc, o, st = emu.fused_bwd(Q, K, V, dO, ql, kl, idx)
+    tag = "fused %s" % (case[:8],)
+    if rc != 0 or st != 0:
+        fails.append("%s: status %d, device status %d" % (tag, rc, st))
+        return
+    rQ, rK, rV, rS = oracle.sparse_attn_bwd(Q, K, V, idx, dO)
+    for n_, r in (("dQ", rQ), ("dK", rK), ("dV", rV), ("dS", rS)):
+        _close(o[n_], r, "%s %s" % (tag, n_), fails)
+    # the scorer's gradients from the dS the call produced
+    rq, rk = oracle.scorer_bwd(ql, kl, idx, o["dS"])
+    _close(o["dq"], rq, tag + " dq_low", fails)
+    _close(o["dk"], rk, tag + " dk_low", fails)
 
 
 GROUPED_CASES = [
@@ -404,6 +461,8 @@ def check_all(path: str, attn_cases=ATTN_CASES, scorer_cases=SCORER_CASES, edges
         check_attn(emu, c, fails)
     for c in scorer_cases:
         check_scorer(emu, c, fails)
+    for c in (FUSED_CASES if edges else FUSED_CASES[:1]):
+        check_fused(emu, c, fails)
     if edges:
         check_edges(emu, fails)
         check_near_equal_values(emu, fails)

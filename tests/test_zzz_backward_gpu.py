@@ -93,6 +93,27 @@ def test_scorer_bwd_matches_oracle(cuda_dev, P, dtype):
     _close(dk, rk, "dk_low")
 
 
+@pytest.mark.parametrize("B,H,Tq,Tk,D,P,k,dtype", [
+    (1, 2, 100, 300, 128, 64, 7, torch.bfloat16),
+    (2, 1, 60, 900, 64, 16, 33, torch.float32),
+])
+def test_fused_attn_scorer_bwd_matches_oracle(cuda_dev, B, H, Tq, Tk, D, P, k, dtype):
+    """ssa_sparse_attn_scorer_bwd (one build of the key-major lists for both
+    key sides) against the oracle's attention and scorer gradients."""
+    Q, K, V, dO = _inputs(B, H, Tq, Tk, D, dtype, seed=500 + k)
+    g = torch.Generator().manual_seed(P + k)
+    ql = torch.randn(B, H, Tq, P, generator=g).to(dtype)
+    kl = torch.randn(B, H, Tk, P, generator=g).to(dtype)
+    idx = _idx(B, H, Tq, Tk, k, seed=k + 1)
+    rQ, rK, rV, rS = oracle.sparse_attn_bwd(Q, K, V, idx, dO)
+    rq, rk = oracle.scorer_bwd(ql, kl, idx, rS)
+    dv = [t.to(cuda_dev) for t in (Q, K, V, dO, ql, kl, torch.from_numpy(idx))]
+    dQ, dK, dV, dS, dq, dk = ssa.ssa_sparse_attn_scorer_bwd(*dv)
+    for a, r, n in ((dQ, rQ, "dQ"), (dK, rK, "dK"), (dV, rV, "dV"), (dS, rS, "dS"),
+                    (dq, rq, "dq_low"), (dk, rk, "dk_low")):
+        _close(a, r, n)
+
+
 def test_backward_of_the_exact_selection(cuda_dev):
     """The path end to end: the GPU top-k feeds the backward; the oracle's
     top-k (bit-identical on integer scorer data) feeds the oracle's."""
@@ -180,8 +201,8 @@ def check_backward_sampled(w, dev, idx, n_rows=24, seed=0):
     q_low, k_low = make_scorer_inputs(w, dev)
     Q, K, V = make_attn_inputs(w, dev)
     dO = make_grad_output(w, dev)
-    dQ, dK, dV, dS = ssa.ssa_sparse_attn_bwd(Q, K, V, idx, dO)
-    dq, dk = ssa.ssa_scorer_bwd(q_low, k_low, idx, dS)
+    # the bench's call: both backward passes, the key-major lists built once
+    dQ, dK, dV, dS, dq, dk = ssa.ssa_sparse_attn_scorer_bwd(Q, K, V, dO, q_low, k_low, idx)
     g = np.random.default_rng(seed)
     heads = sorted({0, w.B * w.H - 1})
     for bh in heads:
@@ -196,7 +217,9 @@ def check_backward_sampled(w, dev, idx, n_rows=24, seed=0):
         _close(dQ[b, h][sel], rQ, "dQ rows of head %d" % bh, FULL_TOL)
         _close(dS[b, h][sel], rS, "dS rows of head %d" % bh, FULL_TOL)
         _close(dq[b, h][sel], rq, "dq_low rows of head %d" % bh, FULL_TOL)
-        for j in sorted({0, w.Tk // 2, w.Tk - 1, int(g.integers(0, w.Tk))}):
+        # the head's most chosen key (a planted key: its sums are the longest)
+        top = int(np.bincount(ix[ix >= 0].ravel(), minlength=w.Tk).argmax())
+        for j in sorted({0, w.Tk // 2, w.Tk - 1, int(g.integers(0, w.Tk)), top}):
             who = np.unique(np.nonzero(ix == j)[0])
             if len(who) == 0:
                 assert float(dK[b, h, j].abs().max()) == 0.0 and float(dV[b, h, j].abs().max()) == 0.0
