@@ -50,7 +50,7 @@ L2_FLUSH_BYTES = 512 << 20
 # timed step: the GPU stays busy while Python enqueues the step, so the events
 # measure the step's device time and not the host's call overhead (which
 # matters only for sub-millisecond steps such as the window workload).
-HOST_COVER_CYCLES = 400_000
+HOST_COVER_CYCLES = 2_000_000
 
 
 def peaks():
