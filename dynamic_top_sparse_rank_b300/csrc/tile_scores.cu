@@ -72,7 +72,68 @@ constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 // conflicts).
 constexpr int kQueue = 64;                                   // entries, power of two
 constexpr int kSub = 16;                                     // keys per entry
-constexpr uint32_t kQueueWarpBytes = kQueue * kSub * 4 + kQueue * 4 + 32 * 4;
+constexpr uint32_t kQueueWarpBytes = kQueue * kSub * 4 + kQueue * 4 + 2 * 32 * 4;
+
+// The rare part of a candidate-queue drain (see the drain in
+// tile_scores_kernel), run after a drain in which some row's list reached its
+// capacity. Out of line: the drain is inlined at nine places, and keeping this
+// code out of them keeps the common path as fast as without it.
+//  - The drain's slots came from a shared-memory atomic, in no particular
+//    order. For each row whose list is now over its capacity, the lanes that
+//    hold its entries (not adjacent in general) add up their candidate counts
+//    in lane order through the drained entries' key words (free by now) and
+//    store the drain's candidates again, in ring order, into the same slots.
+//  - A candidate past the capacity that scores above the row's bound (order
+//    key > tau) flags the row; one exactly at the bound is dropped.
+//  - A row whose list is full moves its test to the first raw score whose
+//    scaled order key exceeds the bound (tau's low 16 bits are zero, so
+//    tau + 1 does not wrap; a row without a bound never fills past its keys).
+// Returns the lane's test; qmeta and bits are the lane's drained entry and
+// its candidates.
+__device__ __noinline__ float drain_fixup(uint32_t* qm, const float4* qv, const int* qcnt,
+                                          int* qovf, const uint32_t* tau, uint64_t* cand,
+                                          int64_t row0, int tb, int q_head, int lane, bool act,
+                                          int owner, uint32_t qmeta, uint32_t bits, int capc,
+                                          float t_hot, float scale) {
+    const int qi = (q_head + lane) & (kQueue - 1);
+    const int nb = __popc(bits);
+    const uint32_t peers = __match_any_sync(0xffffffffu, act ? owner : 32 + lane);
+    __syncwarp();   // every plain store and count is in, every key word read
+    if (act) qm[qi] = static_cast<uint32_t>(nb);
+    __syncwarp();
+    int before = 0, total = 0;
+    for (uint32_t m = peers; m; m &= m - 1) {
+        const int l = __ffs(m) - 1;
+        const int c = static_cast<int>(qm[(q_head + l) & (kQueue - 1)]);
+        total += c;
+        if (l < lane) before += c;
+    }
+    const int end = act ? qcnt[owner] : 0;
+    if (act && nb > 0 && end > capc) {
+        // the row's list is over its capacity: this drain's candidates again,
+        // in ring order, and a check of those past the capacity
+        int sl = end - total + before;
+        const uint32_t tau_own = tau[row0 + owner];
+        uint64_t* dst = cand + ((row0 + owner) * kTBuf + tb) * static_cast<int64_t>(capc);
+        const uint32_t jb = (qmeta >> 5) * kSub;
+        bool above = false;
+        for (uint32_t b = bits; b; b &= b - 1, ++sl) {
+            const int e = __ffs(b) - 1;
+            const float x = reinterpret_cast<const float*>(qv + (e >> 2) * kQueue + qi)[e & 3];
+            if (sl < capc)
+                dst[sl] = (static_cast<uint64_t>(__float_as_uint(x)) << 32) | (jb + static_cast<uint32_t>(e));
+            else if (f32_order_key(x * scale) > tau_own)
+                above = true;
+        }
+        if (above) qovf[owner] = 1;
+    }
+    __syncwarp();
+    if (qcnt[lane] >= capc) {
+        const uint32_t t32 = tau[row0 + lane];
+        t_hot = t32 == 0 ? -FLT_MAX : tile_raw_threshold(order_key_f32(t32 + 1u), scale);
+    }
+    return t_hot;
+}
 
 template <int P, int MODE>
 struct TileCfg {
@@ -406,26 +467,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         float4* qv = nullptr;                  // [kSub/4][kQueue] raw scores
         uint32_t* qm = nullptr;                // [kQueue] (first key / kSub) << 5 | owning lane
         int* qcnt = nullptr;                   // [32] candidates appended per row
+        int* qovf = nullptr;                   // [32] a key above the bound found no slot
         int q_head = 0, q_tail = 0;            // warp-uniform ring positions (unwrapped)
         int64_t row0 = 0;                      // global row of lane 0
-        float t_raw = -FLT_MAX;                // raw-score bound of this thread's row
+        float t_hot = -FLT_MAX;                // raw-score bound of this thread's row
+                                               // (above the bound once its list is full)
         if constexpr (MODE == MODE_COLLECT) {
             uint8_t* qb = smem + C::QUEUE_OFF + (warp - 2) * kQueueWarpBytes;
             qv = reinterpret_cast<float4*>(qb);
             qm = reinterpret_cast<uint32_t*>(qb + kQueue * kSub * 4);
             qcnt = reinterpret_cast<int*>(qb + kQueue * (kSub * 4 + 4));
+            qovf = qcnt + 32;
             qcnt[lane] = 0;
+            qovf[lane] = 0;
             __syncwarp();
         }
         // Drain the `n` (<= 32) ring entries from q_head on, entry l by lane l: its
         // candidates (scores >= the owning row's bound) are appended to that
         // row's list; a shared-memory count per row hands out the slots.
+        //
+        // A full list. Ring entries of a row sit in key order, and the list of
+        // (row, buffer) takes that buffer's tiles in ascending key order, so a
+        // list that keeps its first cap/2 candidates in key order holds
+        // cap/2 >= k keys that all score >= the bound and precede every later
+        // key. A later key that scores exactly at the bound is beaten by all
+        // of them (equal or higher score, lower index) and cannot be in the
+        // row's top k: it is dropped, and from then on the row's test moves
+        // to the first raw score above the bound, for queueing and draining
+        // alike. A later key above the bound that finds no slot flags the
+        // row, which the row-wise kernel then redoes. Slots from the
+        // shared-memory atomic come in no particular order within a drain;
+        // drain_fixup puts a drain that takes a list past its capacity back
+        // in ring order.
         auto drain = [&](int n) {
             const bool act = lane < n;
             const int qi = (q_head + lane) & (kQueue - 1);
             const uint32_t meta = act ? qm[qi] : 0u;
             const int owner = static_cast<int>(meta & 31u);
-            const float t_own = __shfl_sync(0xffffffffu, t_raw, owner);
+            const float t_own = __shfl_sync(0xffffffffu, t_hot, owner);
             uint32_t bits = 0;
             if (act) {
                 const float4 a = qv[qi], b = qv[kQueue + qi], c4 = qv[2 * kQueue + qi],
@@ -434,8 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float w1[8] = {c4.x, c4.y, c4.z, c4.w, d4.x, d4.y, d4.z, d4.w};
                 bits = ge_mask8(w0, t_own) | (ge_mask8(w1, t_own) << 8);
             }
+            const uint32_t bits0 = bits;
+            int slot = 0;
             if (bits) {
-                int slot = atomicAdd(qcnt + owner, __popc(bits));
+                slot = atomicAdd(qcnt + owner, __popc(bits));
                 uint64_t* dst = p.cand + ((row0 + owner) * kTBuf + tb) * static_cast<int64_t>(capc);
                 const uint32_t jb = (meta >> 5) * kSub;
                 while (bits) {
@@ -449,6 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++slot;
                 }
             }
+            if (__any_sync(0xffffffffu, bits0 != 0 && slot >= capc))   // a list filled
+                t_hot = drain_fixup(qm, qv, qcnt, qovf, p.tau, p.cand, row0, tb, q_head, lane,
+                                    act, owner, meta, bits0, capc, t_hot, p.scale);
             q_head += n;
             __syncwarp();
         };
@@ -464,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // mode state
             int g = 0, m_shift = 0, g_shift = 0;   // g and m = g/32 are powers of two
             float gacc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            t_raw = -FLT_MAX;
+            t_hot = -FLT_MAX;
             uint16_t* gcol = nullptr;
             if constexpr (MODE == MODE_GROUPMAX) {
                 g = tile_group_size(U.n_lo, U.n_hi, p.k);
@@ -476,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (MODE == MODE_COLLECT) {
                 if (row_ok) {
                     const uint32_t t32 = p.tau[row];
-                    t_raw = tile_raw_threshold(t32 == 0 ? -INFINITY : order_key_f32(t32), p.scale);
+                    t_hot = tile_raw_threshold(t32 == 0 ? -INFINITY : order_key_f32(t32), p.scale);
                 }
             }
             row0 = row - lane;
@@ -534,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       uint32_t B[4];
                       bool hot[4];
 #pragma unroll
-                      for (int hs = 0; hs < 4; ++hs) hot[hs] = jp + 16 * hs < n_i && mx[hs] >= t_raw;
+                      for (int hs = 0; hs < 4; ++hs) hot[hs] = jp + 16 * hs < n_i && mx[hs] >= t_hot;
 #pragma unroll
                       for (int hs = 0; hs < 4; ++hs) B[hs] = __ballot_sync(0xffffffffu, hot[hs]);
 #pragma unroll
@@ -625,8 +709,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (q_tail > q_head) drain(q_tail - q_head);
                 q_head = q_tail = 0;
-                if (row_ok) p.cnt[row * kTBuf + tb] = qcnt[lane];
+                // a flagged row reads as one over its capacity: redone row-wise
+                if (row_ok) p.cnt[row * kTBuf + tb] = qovf[lane] ? capc + 1 : min(qcnt[lane], capc);
                 qcnt[lane] = 0;
+                qovf[lane] = 0;
                 __syncwarp();
             }
             if constexpr (MODE == MODE_RAW) {

@@ -15,9 +15,11 @@
 //   cand_sort_kernel selects the k_eff largest candidates (radix select) and
 //   sorts them by (score desc, index asc).
 // With G between 2k and 4k, about k + k^2/(2G) <= 1.25k keys pass the bound.
-// A row with more candidates than its list holds, or with more than 256
-// candidates tied at its k-th score (heavy ties), is put on an overflow list
-// and redone by the row-wise kernel.
+// Once a list is full the candidate pass drops later keys that score exactly
+// at the bound (each is beaten by the cap/2 >= k earlier keys of that list),
+// so heavy ties at the bound do not overflow it; a row where a key above the
+// bound found no slot is put on an overflow list and redone by the row-wise
+// kernel.
 #ifdef SSA_HOST_EMULATION
 #include "emu_device.h"   // the host stand-in of the CPU tests (tests/emu)
 #include "tile.h"
@@ -195,8 +197,8 @@ __global__ void __launch_bounds__(kSelThreads) group_select_kernel(
 //     shared-memory list), are compacted into shared memory as composite keys
 //     (the index is read back from the candidate list) and sorted descending
 //     by a bitonic network in registers (strides below E inside a lane, the
-//     others across lanes by shuffles). A row with more ties at T than the
-//     list holds goes to the row-wise kernel.
+//     others across lanes by shuffles). With more ties at T than the list
+//     holds, a radix select over their indices picks the winners instead.
 // Keys live in registers batch-major: register b of lane l holds element
 // 32*b + l.
 constexpr int kSortWarps = 8;
@@ -412,11 +414,98 @@ __global__ void __launch_bounds__(kSortWarps * 32, 4) cand_sort_kernel(
         base += __popc(mu);
         nties += __popc(mt);
     }
-    if (partial) {
-        if (nties > kMaxTies) {   // too many equal scores at T for the list
-            if (lane == 0) ovf_list[atomicAdd(ovf_count, 1)] = row;
-            return;
+    if (partial && nties > kMaxTies) {
+        // More ties at T than the short list holds (heavy ties, e.g. equal
+        // scores): the `need` smallest indices among them by a radix select
+        // over the index bits, most significant digit first, digits that all
+        // ties share skipped; the winners are then the ties with an index <= J.
+        // (the candidates are read again rather than kept in registers, which
+        // keeps this rare path from costing the common one registers)
+        auto tie_index = [&](int e, uint32_t& j) -> bool {
+            if (e >= c) return false;
+            const uint64_t v = elem(e);
+            j = static_cast<uint32_t>(v);
+            return f32_order_key(__uint_as_float(static_cast<uint32_t>(v >> 32)) * scale) == thr;
+        };
+        uint32_t jor = 0, jand = ~0u;
+        for (int e = lane; e < c; e += 32) {
+            uint32_t j;
+            if (tie_index(e, j)) {
+                jor |= j;
+                jand &= j;
+            }
         }
+        jand = __reduce_and_sync(0xffffffffu, jand);
+        const uint32_t jvary = __reduce_or_sync(0xffffffffu, jor) ^ jand;
+        uint32_t jpre = 0, jmask = 0, rem = need;
+        for (int d = 3; d >= 0; --d) {
+            const int sh = 8 * d;
+            const uint32_t dm = 0xFFu << sh;
+            if ((jvary & dm) == 0) {
+                jpre |= jand & dm;
+                jmask |= dm;
+                continue;
+            }
+            for (int t = lane; t < 256; t += 32) bins[t] = 0;
+            __syncwarp();
+            for (int e = lane; e < c; e += 32) {
+                uint32_t j;
+                if (tie_index(e, j) && (j & jmask) == jpre) atomicAdd(&bins[(j >> sh) & 0xFFu], 1u);
+            }
+            __syncwarp();
+            // the smallest digit whose running count reaches rem: lane l owns
+            // bins 8l .. 8l+7
+            uint32_t cb[8], tot = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                cb[q] = bins[8 * lane + q];
+                tot += cb[q];
+            }
+            uint32_t incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const uint32_t excl = incl - tot;
+            uint32_t sel = 0, lower = 0, cnt_sel = 0;
+            const bool mine = excl < rem && rem <= incl;
+            if (mine) {
+                uint32_t a = excl;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (a + cb[q] >= rem) {
+                        sel = 8 * lane + q;
+                        lower = a;
+                        cnt_sel = cb[q];
+                        break;
+                    }
+                    a += cb[q];
+                }
+            }
+            const int src_lane = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+            sel = __shfl_sync(0xffffffffu, sel, src_lane);
+            lower = __shfl_sync(0xffffffffu, lower, src_lane);
+            cnt_sel = __shfl_sync(0xffffffffu, cnt_sel, src_lane);
+            __syncwarp();
+            jpre |= sel << sh;
+            jmask |= dm;
+            rem -= lower;
+            if (cnt_sel == rem) break;   // the whole bin wins: any lower digits
+        }
+        const uint32_t J = jpre | ~jmask;
+        for (int e0 = 0; e0 < c; e0 += 32) {
+            uint32_t j = 0;
+            const bool w = tie_index(e0 + lane, j) && j <= J;
+            const unsigned mw = __ballot_sync(0xffffffffu, w);
+            if (w) {
+                const int pos = base + __popc(mw & below);
+                const int pl = pos / E, pr = pos % E;
+                if (pos < W) win[pl * E + (pr ^ (pl % E))] = sel_key(thr, j);
+            }
+            base += __popc(mw);
+        }
+    } else if (partial) {
         __syncwarp();
         // a tie wins iff fewer than `need` ties have a smaller index
         for (int q0 = 0; q0 < nties; q0 += 32) {

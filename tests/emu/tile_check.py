@@ -13,9 +13,18 @@ kernels run on them:
   k keys).
 - cand_sort_kernel gets candidate lists as the candidate pass writes them:
   (raw score bits, key) pairs in two lists per row, in any order, with their
-  counts. Its output must equal the oracle's top-k bit for bit. A row whose
-  list holds more than its capacity, or with more than 256 candidates tied at
-  its k-th score, must go to the overflow list.
+  counts. Its output must equal the oracle's top-k bit for bit, however many
+  candidates tie at the k-th score. A row whose list count is over its
+  capacity must go to the overflow list.
+- The full-list rule of the candidate pass, end to end: lists are built the
+  way that pass fills them (keys of alternate 128-key tiles, in key order,
+  the first cap/2 kept; once a list is full a key scoring exactly at the
+  row's bound is dropped and a key above it marks the row as overflowing),
+  with the bound from the group maxima; the sort of those lists must give
+  the oracle's answer on every unmarked row. This checks the argument that
+  makes the drop exact (each dropped key is beaten by the cap/2 >= k earlier
+  keys of its list), including equal scores everywhere and ties above the
+  16-bit bound.
 
 Scores come from integer q_low, k_low, so every score is exact.
 """
@@ -89,12 +98,30 @@ def order_keys(s):
 
 
 def exact_scores(BH, Tq, Tk, P, causal, seed, ties=False):
-    """Integer q_low/k_low and their fp32 scores (raw dot products and scaled)."""
+    """Integer q_low/k_low and their fp32 scores (raw dot products and scaled).
+
+    ties: False; True (q_low = 0: every score equal); "few" (one-hot q_low,
+    k_low in {0, 1, 2}: three distinct scores, the top one held by about a
+    third of the keys); "wide" (a third of the keys score 1001, twelve score
+    1002, the rest below 1000: the two top scores share their 16-bit
+    truncated order key, so the bound sits below both, and the late 1002 keys
+    find the lists full)."""
     g = np.random.default_rng(seed)
     q = g.integers(-4, 5, size=(BH, Tq, P)).astype(np.float64)
     kl = g.integers(-4, 5, size=(BH, Tk, P)).astype(np.float64)
-    if ties:
+    if ties is True:
         q[:] = 0.0
+    elif ties == "few":
+        q[:] = 0.0
+        q[np.arange(BH)[:, None], np.arange(Tq)[None, :], g.integers(0, P, size=(BH, Tq))] = 1.0
+        kl = g.integers(0, 3, size=(BH, Tk, P)).astype(np.float64)
+    elif ties == "wide":
+        q[:] = 0.0
+        q[:, :, 0] = 1.0
+        kl[:] = 0.0
+        kl[:, :, 0] = np.where(g.random((BH, Tk)) < 0.3, 1001, g.integers(0, 1000, size=(BH, Tk)))
+        for bh in range(BH):   # a few keys scoring 1002, most of them late in the row
+            kl[bh, g.choice(np.arange(Tk // 4, Tk), size=12, replace=False), 0] = 1002
     raw = np.einsum("hip,hjp->hij", q, kl).astype(np.float32)   # exact integers
     return q, kl, raw
 
@@ -109,11 +136,9 @@ class Emu:
         lib.emu_tile_group_stride.argtypes = [I]
 
 
-def check_bound(emu, BH, Tq, Tk, k, causal, seed, fails):
-    P = 64
-    scale = np.float32(0.125)
-    _, _, raw = exact_scores(BH, Tq, Tk, P, causal, seed)
-    s = raw * scale
+def row_bounds(emu, s, BH, Tq, Tk, k, causal):
+    """The group maxima as the group-maximum pass writes them, and each row's
+    bound: the k-th largest truncated group maximum (0 for <= k keys)."""
     uph = (Tq + UNIT - 1) // UNIT
     stride = emu.lib.emu_tile_group_stride(k)
     gm = np.full((BH * uph, stride, UNIT), 0xA5A5, np.uint16)   # garbage where no group is
@@ -139,6 +164,15 @@ def check_bound(emu, BH, Tq, Tk, k, causal, seed, fails):
                 for gg, kk in gmax.items():
                     gm[u, gg, r] = kk
                 want[bh, i] = sorted(gmax.values(), reverse=True)[k - 1] << 16
+    return gm, want
+
+
+def check_bound(emu, BH, Tq, Tk, k, causal, seed, fails):
+    P = 64
+    scale = np.float32(0.125)
+    _, _, raw = exact_scores(BH, Tq, Tk, P, causal, seed)
+    s = raw * scale
+    gm, want = row_bounds(emu, s, BH, Tq, Tk, k, causal)
     tau = np.full((BH, Tq), 0xDEADBEEF, np.uint32)
     emu.lib.emu_group_select(_p(gm), _p(tau), BH, Tq, Tk, k, int(causal))
     if not np.array_equal(tau, want):
@@ -184,15 +218,12 @@ def check_sort(emu, BH, Tq, Tk, k, causal, seed, fails, margin=20, ties=False, o
             if row in overfill:
                 cnt[row, 0] = capc + 1
                 expect_ovf.add(row)
-            # more than 256 candidates tied at the k_eff-th score, only some of
-            # them selected: the tie list overflows
-            keff = min(k, n)
-            cs = np.sort(s[bh, i, js])[::-1]
-            if keff < len(cs):
-                T = cs[keff - 1]
-                above, inbin = int((cs > T).sum()), int((cs == T).sum())
-                if keff - above < inbin and inbin > 256:
-                    expect_ovf.add(row)
+    tag = "sort BH%d Tq%d Tk%d k%d causal %d%s" % (BH, Tq, Tk, k, causal, " ties" if ties else "")
+    sort_and_compare(emu, q, kl, cand, cnt, expect_ovf, BH, Tq, Tk, k, causal, scale, tag, fails)
+
+
+def sort_and_compare(emu, q, kl, cand, cnt, expect_ovf, BH, Tq, Tk, k, causal, scale, tag, fails):
+    rows = BH * Tq
     idx = np.full((rows, k), -7, np.int32)
     sc = np.full((rows, k), np.nan, np.float32)
     ovf = np.full(rows + 1, -1, np.int64)
@@ -200,7 +231,6 @@ def check_sort(emu, BH, Tq, Tk, k, causal, seed, fails, margin=20, ties=False, o
     emu.lib.emu_cand_sort(_p(cand), _p(cnt), rows, Tq, Tk, k, int(causal), float(scale), _p(idx),
                           _p(sc), _p(ovf), _p(ocount))
     got_ovf = set(ovf[:ocount[0]].tolist())
-    tag = "sort BH%d Tq%d Tk%d k%d causal %d%s" % (BH, Tq, Tk, k, causal, " ties" if ties else "")
     if got_ovf != expect_ovf:
         fails.append("%s: overflow rows %s, want %s" % (tag, sorted(got_ovf)[:5],
                                                          sorted(expect_ovf)[:5]))
@@ -238,6 +268,58 @@ SORT_CASES = [
 ]
 
 
+def check_full_lists(emu, BH, Tq, Tk, k, causal, seed, fails, ties, want_ovf=None):
+    """Lists built by the candidate pass's full-list rule (see the module
+    notes); want_ovf: whether some row must be marked (None: either)."""
+    P = 64
+    scale = np.float32(0.125)
+    q, kl, raw = exact_scores(BH, Tq, Tk, P, causal, seed, ties)
+    s = raw * scale
+    _, tau = row_bounds(emu, s, BH, Tq, Tk, k, causal)
+    capc = emu.lib.emu_tile_cand_cap(k) // 2
+    rows = BH * Tq
+    cand = np.zeros((rows, 2, capc), np.uint64)
+    cnt = np.zeros((rows, 2), np.int32)
+    marked = set()
+    dropped = 0
+    for bh in range(BH):
+        for i in range(Tq):
+            row = bh * Tq + i
+            n = valid_count(i, Tq, Tk, causal)
+            if n == 0:
+                continue
+            ok = order_keys(s[bh, i, :n]).astype(np.int64)
+            t = int(tau[bh, i])
+            js = np.arange(n) if t == 0 else np.nonzero(ok >= t)[0]   # ascending keys
+            for lst in (0, 1):
+                sel = js[(js // 128) % 2 == lst]
+                w = sel[:capc]
+                late = sel[capc:]
+                bits = raw[bh, i, w].view(np.uint32).astype(np.uint64)
+                cand[row, lst, :len(w)] = (bits << np.uint64(32)) | w.astype(np.uint64)
+                cnt[row, lst] = len(w)
+                if len(late):
+                    if (ok[late] > t).any():
+                        cnt[row, lst] = capc + 1
+                        marked.add(row)
+                    dropped += int((ok[late] == t).sum())
+    tag = "full lists BH%d Tq%d Tk%d k%d causal %d ties %s" % (BH, Tq, Tk, k, causal, ties)
+    if not want_ovf and dropped == 0:
+        fails.append("%s: no key was dropped, the case does not exercise the rule" % tag)
+    if want_ovf is not None and bool(marked) != want_ovf:
+        fails.append("%s: %d marked rows, want %s" % (tag, len(marked), "some" if want_ovf else "none"))
+    sort_and_compare(emu, q, kl, cand, cnt, marked, BH, Tq, Tk, k, causal, scale, tag, fails)
+
+
+FULL_CASES = [
+    # BH, Tq, Tk, k, causal, ties, some row marked
+    (1, 24, 3000, 150, False, True, False),    # every score equal: the first k keys
+    (1, 40, 1400, 50, True, True, False),      # causal, equal scores, rows of every length
+    (2, 16, 2500, 200, False, "few", False),   # three distinct scores
+    (1, 16, 2000, 40, False, "wide", True),    # ties above the truncated bound: marked rows
+]
+
+
 def check_all(path, small=False):
     emu = Emu(path)
     fails = []
@@ -251,6 +333,10 @@ def check_all(path, small=False):
     check_sort(emu, 1, 6, 300, 200, False, seed=6, fails=fails, ties=True, margin=400)
     # 200 tied candidates for k = 150: a partial tie list that fits
     check_sort(emu, 1, 6, 200, 150, False, seed=7, fails=fails, ties=True, margin=400)
+    # 900 tied candidates for k = 512: the index radix select
+    check_sort(emu, 1, 3, 900, 512, False, seed=8, fails=fails, ties=True, margin=2000)
+    for c in (FULL_CASES[:1] if small else FULL_CASES):
+        check_full_lists(emu, *c[:5], seed=sum(c[:5]), fails=fails, ties=c[5], want_ovf=c[6])
     return fails
 
 

@@ -401,6 +401,25 @@ def test_full_size_decode_every_row(cuda_dev):
     _oracle_compare(w, q, kl, Q, K, V, rows, idx, sc, O32, O16, attn_heads=attn_heads)
 
 
+def test_full_size_equal_scores_every_row(cuda_dev):
+    """The 128K workload with q_low = 0 (every score ties): every row of every
+    head must select its first k_eff valid keys with score 0, -1 / -inf past
+    them (the lower index wins ties)."""
+    w = WORKLOADS["topk_causal_bf16_t128k_k512_equal_scores"]
+    q, kl = make_scorer_inputs(w, cuda_dev)
+    assert not q.any()
+    idx, sc = ssa.ssa_score_topk(q, kl, w.k, w.causal, with_score=True)
+    torch.cuda.synchronize()
+    i = torch.arange(w.Tq, device=cuda_dev).view(-1, 1)
+    j = torch.arange(w.k, device=cuda_dev).view(1, -1)
+    valid = j <= i + (w.Tk - w.Tq)
+    want_idx = torch.where(valid, j, torch.full_like(j, -1)).to(torch.int32)
+    want_sc = torch.where(valid, torch.zeros((), device=cuda_dev),
+                          torch.full((), -float("inf"), device=cuda_dev))
+    assert torch.equal(idx, want_idx.expand_as(idx))
+    assert torch.equal(sc, want_sc.expand_as(sc))
+
+
 @pytest.mark.parametrize("name", ["topk_causal_bf16_t32k_k256",
                                   "topk_causal_bf16_t128k_k512_planted"])
 def test_full_size_tile_path_matches_rowwise_every_row(cuda_dev, name):

@@ -5,8 +5,9 @@ oracle's scores bit for bit on integer data. ssa_score_topk on bf16 inputs
 with d_proj 64 or 128, k <= 512 and at least 64 query rows runs the
 tensor-core selection (group maxima -> per-row bound -> candidates -> sort,
 rows that overflow their candidate list redone row-wise); these cases cover
-every group size, several 128-row tiles with ragged tails, Tq != Tk, and rows
-whose candidates overflow.
+every group size, several 128-row tiles with ragged tails, Tq != Tk, rows
+whose candidates overflow, and heavy ties (equal scores everywhere, few
+distinct scores, ties above the truncated bound).
 """
 import numpy as np
 import pytest
@@ -69,13 +70,86 @@ def test_tile_topk_matches_oracle(cuda_dev, B, H, Tq, Tk, P, k, causal):
 
 def test_tile_topk_heavy_ties_overflow(cuda_dev):
     """Values in {-1, 0, 1}: few distinct scores, so many rows hold more tied
-    candidates than their list and are redone row-wise; others are not."""
+    candidates than their lists; ties at the bound are dropped once a list is
+    full, and rows where a key above the bound finds no slot are redone
+    row-wise."""
     B, H, Tq, Tk, P, k = 1, 2, 700, 2500, 64, 64
     q, kl = _int_inputs(B, H, Tq, Tk, P, seed=77, lo=-1, hi=1)
     idx, sc = ssa.ssa_score_topk(q.to(cuda_dev), kl.to(cuda_dev), k, True, with_score=True)
     ref_idx, ref_sc = oracle.score_topk(q, kl, k, True)
     np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
     np.testing.assert_array_equal(sc.cpu().numpy(), ref_sc)
+
+
+ALL_TIES_CASES = [
+    # B, H, Tq, Tk, P, k, causal
+    (1, 2, 2048, 2048, 64, 512, True),    # the headline k: 1024-entry lists, 512 ties selected
+    (1, 1, 1000, 5000, 128, 100, False),  # d_proj 128, every row full
+    (2, 1, 700, 3000, 64, 64, True),      # Tq < Tk, small lists
+]
+
+
+@pytest.mark.parametrize("B,H,Tq,Tk,P,k,causal", ALL_TIES_CASES)
+def test_tile_topk_all_equal_scores(cuda_dev, B, H, Tq, Tk, P, k, causal):
+    """q_low = 0: every score is 0, so every row's answer is its first k_eff
+    valid keys. Each row's lists fill with ties at the bound, the later ties
+    are dropped, and the sort ranks more than 256 ties by index."""
+    q = torch.zeros((B, H, Tq, P), dtype=torch.bfloat16)
+    kl = fill((B, H, Tk, P), "int", 61 + k, 2, torch.bfloat16, "cpu")
+    idx, sc = ssa.ssa_score_topk(q.to(cuda_dev), kl.to(cuda_dev), k, causal, with_score=True)
+    idx, sc = idx.cpu().numpy(), sc.cpu().numpy()
+    i = np.arange(Tq)[:, None]
+    j = np.arange(k)[None, :]
+    n = np.clip(i + (Tk - Tq) + 1, 0, Tk) if causal else np.full_like(i, Tk)
+    want = np.where(j < n, j, -1).astype(np.int32)
+    np.testing.assert_array_equal(idx, np.broadcast_to(want, idx.shape))
+    np.testing.assert_array_equal(sc, np.broadcast_to(np.where(j < n, 0.0, -np.inf).astype(np.float32),
+                                                      sc.shape))
+    ref_idx, ref_sc = oracle.score_topk(q[:, :1], kl[:, :1], k, causal)
+    np.testing.assert_array_equal(idx[:, :1], ref_idx)
+    np.testing.assert_array_equal(sc[:, :1], ref_sc)
+
+
+def test_tile_topk_few_distinct_scores(cuda_dev):
+    """One-hot q_low, k_low in {0, 1, 2}: three distinct scores, the top one
+    held by about a third of the keys, so the lists fill with ties at the
+    bound (which is exact here)."""
+    B, H, Tq, Tk, P, k = 1, 2, 1024, 4096, 64, 256
+    g = np.random.default_rng(71)
+    q = np.zeros((B, H, Tq, P), np.float32)
+    q[0, np.arange(H)[:, None], np.arange(Tq)[None, :], g.integers(0, P, size=(H, Tq))] = 1.0
+    kl = g.integers(0, 3, size=(B, H, Tk, P)).astype(np.float32)
+    q, kl = torch.from_numpy(q).to(torch.bfloat16), torch.from_numpy(kl).to(torch.bfloat16)
+    idx, sc = ssa.ssa_score_topk(q.to(cuda_dev), kl.to(cuda_dev), k, True, with_score=True)
+    ref_idx, ref_sc = oracle.score_topk(q, kl, k, True)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    np.testing.assert_array_equal(sc.cpu().numpy(), ref_sc)
+
+
+def test_tile_topk_ties_above_the_bound(cuda_dev):
+    """Scores 128.25 (a third of the keys) and 128.5 (twelve late keys): after
+    scaling by 1/8 the two share their 16-bit truncated order key, so the
+    bound sits below both. The lists fill with 128.25 ties; the late 128.5
+    keys lie above the bound and find no slot, so their rows are redone
+    row-wise and must still match the oracle."""
+    B, H, Tq, Tk, P, k = 1, 1, 512, 3000, 64, 40
+    g = np.random.default_rng(72)
+    q = np.zeros((B, H, Tq, P), np.float32)
+    q[..., 0] = 1.0
+    q[..., 1] = 1.0
+    kl = np.zeros((B, H, Tk, P), np.float32)
+    top = g.random(Tk) < 0.3
+    kl[0, 0, :, 0] = np.where(top, 128.0, g.integers(0, 100, size=Tk))
+    kl[0, 0, :, 1] = np.where(top, 0.25, 0.0)
+    late = g.choice(np.arange(Tk // 4, Tk), size=12, replace=False)
+    kl[0, 0, late, 0] = 128.0
+    kl[0, 0, late, 1] = 0.5
+    q, kl = torch.from_numpy(q).to(torch.bfloat16), torch.from_numpy(kl).to(torch.bfloat16)
+    for causal in (False, True):
+        idx, sc = ssa.ssa_score_topk(q.to(cuda_dev), kl.to(cuda_dev), k, causal, with_score=True)
+        ref_idx, ref_sc = oracle.score_topk(q, kl, k, causal)
+        np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+        np.testing.assert_array_equal(sc.cpu().numpy(), ref_sc)
 
 
 def test_tile_topk_two_calls_one_workspace(cuda_dev):

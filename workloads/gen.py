@@ -137,6 +137,7 @@ class Workload:
     window: int = -1        # |i - j| <= window (window workload only)
     planted: int = 0        # planted keys per query group (0: none)
     plant_boost: int = 64   # exact dot-product boost of a planted key
+    equal_scores: bool = False   # q_low = 0: every score 0 (the all-ties case)
     seed_base: int = 1234
     cfg_id: int = 0
     notes: str = field(default="", compare=False)
@@ -174,6 +175,11 @@ WORKLOADS = {
         "topk_causal_bf16_t128k_k512_planted", B=1, H=8, Tq=131072, Tk=131072, D=128,
         dtype="bf16", P=64, k=512, causal=True, planted=16, cfg_id=3,
         notes="16 planted keys per query group, dot product boosted by exactly +64"),
+    "topk_causal_bf16_t128k_k512_equal_scores": Workload(
+        "topk_causal_bf16_t128k_k512_equal_scores", B=1, H=8, Tq=131072, Tk=131072, D=128,
+        dtype="bf16", P=64, k=512, causal=True, equal_scores=True, cfg_id=3,
+        notes="the 128K workload with q_low = 0: every score ties, each row selects its "
+              "first k_eff keys"),
     "decode_bf16_b32_tk64k_k512": Workload(
         "decode_bf16_b32_tk64k_k512", B=32, H=32, Tq=1, Tk=65536, D=128, dtype="bf16",
         P=64, k=512, causal=False, cfg_id=4, notes="one query per head against 65536 cached keys"),
@@ -215,7 +221,9 @@ def make_scorer_inputs(w: Workload, device="cpu"):
     dt = w.torch_dtype
     q = fill((w.B, w.H, w.Tq, w.P), "int", w.seed, TID_QLOW, dt, device)
     k = fill((w.B, w.H, w.Tk, w.P), "int", w.seed, TID_KLOW, dt, device)
-    if w.planted:
+    if w.equal_scores:
+        q.zero_()
+    elif w.planted:
         base = w.P - PLANT_GROUPS * PLANT_DIMS
         assert base > 0
         q[..., base:] = 0
