@@ -27,8 +27,8 @@ bool window_tc_supported(bool bf16_in, int D, int T, int wl, int wr);
 cudaError_t smooth_boundary_launch(int32_t* idx, float* score, int64_t rows, int k, float delta,
                                    cudaStream_t stream);
 cudaError_t window_tc_launch(const void* Q, const void* K, const void* V, void* O, bool bf16_out,
-                             int BH, int T, int wl, int wr, float scale, int32_t* dev_status,
-                             cudaStream_t stream);
+                             int BH, int T, int D, int wl, int wr, float scale,
+                             int32_t* dev_status, cudaStream_t stream);
 template <bool BAND>
 cudaError_t attn_rows_dispatch(const void* Q, const void* K, const void* V, bool bf16_in, int D,
                                const int32_t* idx, void* O, bool bf16_out, int64_t rows, int Tq,
@@ -329,8 +329,8 @@ ssa_status ssa_window_attn(const void* Q, const void* K, const void* V, int dtyp
     cudaError_t e;
     if (ssa::window_tc_supported(dtype == SSA_BF16, D, T, w_left, w_right)) {
         // dense band tiles on the tensor cores
-        e = ssa::window_tc_launch(Q, K, V, O, out_dtype == SSA_BF16, B * H, T, w_left, w_right, sc,
-                                  dev_status, reinterpret_cast<cudaStream_t>(stream));
+        e = ssa::window_tc_launch(Q, K, V, O, out_dtype == SSA_BF16, B * H, T, D, w_left, w_right,
+                                  sc, dev_status, reinterpret_cast<cudaStream_t>(stream));
     } else {
         e = ssa::attn_rows_dispatch<true>(Q, K, V, dtype == SSA_BF16, D, nullptr, O,
                                           out_dtype == SSA_BF16, rows, T, T, 1, w_left, w_right,

@@ -4,32 +4,38 @@
 // mask of the dense formulation; each row's softmax and weighted sum as in
 // mhpq.cn/news/1098205, section 3.2), computed as dense tiles of the band.
 //
-// One CTA per (head, 128-query tile). The tile's band spans at most three
-// 128-key tiles (the host sends wider bands, other head sizes and fp32 to the
-// gather kernel), so everything fits on chip at once and the softmax needs no
-// running rescale:
-//   warp 0  TMA: the query tile, the band's key tiles and value tiles (3-D
-//           maps [head][row][64], 128-byte swizzle; rows outside the sequence
-//           read as zeros);
+// Work item: one (head, 128-query tile). Its band spans at most three 128-key
+// tiles (the host sends wider bands and fp32 to the gather kernel), so the
+// whole band's scores fit in TMEM and the softmax needs no running rescale.
+// The kernel is persistent (one CTA per SM, items round-robin), so that the
+// loads of the next item overlap the softmax of this one:
+//   warp 0  TMA: per item the query tile, the band's key tiles and value
+//           tiles (3-D maps [head][row][64-column slice], 128-byte swizzle;
+//           rows outside the sequence read as zeros) into one of two
+//           shared-memory stages (D 64; one stage of twice the size for
+//           D 128);
 //   warp 1  allocates TMEM and issues the MMAs: S = Q K^T, one 128x128 fp32
-//           accumulator per key tile (columns 0..383), then O = P V (M=128,
-//           N=64, K=16 steps; V is read MN-major straight from its TMA
-//           layout) into columns 384..447, one key tile of P at a time;
-//   warps 2-5  one query row per thread: the band mask and the row maximum
-//           (first pass over S), then per key tile p = exp2((s - max) *
-//           scale * log2 e) in fp32, written to shared memory in the layout
-//           the second MMA reads (K-major, 128-byte swizzle) as two bf16
-//           parts, hi = bf16(p) and lo = bf16(p - hi), so that P V = hi V +
-//           lo V keeps p to about 2^-17 (one bf16 P would cost 2^-9, too much
-//           for rows with few keys); the row sum is taken in fp32; after the
-//           last MMA, O divided by the sum and stored in bf16 or fp32.
-// The weights of a key tile go through two 64 KB buffers in turn: the first
-// reuses the query and key tiles' space (free once S is in TMEM).
+//           accumulator per key tile (columns 0..383; two tiles per N=256
+//           MMA), then O = P V (M=128, N=D, K=16 steps) into columns 384..,
+//           with P read from TMEM (the A operand of tcgen05.mma may sit in
+//           TMEM) and V MN-major straight from its TMA layout;
+//   warps 2-9  one query row per thread, two warps per row splitting its key
+//           chunks and output columns: the band mask and the row maximum
+//           (first pass over S), then per key tile p = 2^((s - max) * scale *
+//           log2 e) in fp32, written back over that tile's S columns as two
+//           bf16 parts, hi = p truncated to bf16 and lo = bf16(p - hi), so
+//           that P V = hi V + lo V keeps p to about 2^-16 (one bf16 P would
+//           cost 2^-9, too much for rows with few keys); the row sum is taken
+//           in fp32; after the last MMA, O divided by the sum and stored in
+//           bf16 or fp32. A 32-key chunk outside the band of all 32 rows of a
+//           warp is neither loaded nor exponentiated (about a quarter of the
+//           chunks for a 128-key radius).
 // Every mbarrier wait is bounded; a wait that runs out reports
 // SSA_DEV_WAIT_LIMIT, stops the other roles and TMEM is freed.
 #include <float.h>
 
 #include "sm100.cuh"
+#include "tile.h"
 #include "tmap.h"
 #include "trace.h"
 
@@ -39,27 +45,40 @@ using namespace sm100;
 
 namespace {
 
-constexpr int kWM = 128;                     // query rows per CTA
+constexpr int kWM = 128;                     // query rows per item
 constexpr int kWN = 128;                     // keys per score tile
 constexpr int kWMaxTiles = 3;                // score tiles next to the output in TMEM
-constexpr int kWD = 64;                      // head size of this kernel
-constexpr int kWThreads = 192;
-constexpr uint32_t kTileBytes = kWN * kWD * 2;                 // 128 rows of 64 bf16
-constexpr uint32_t kQOff = 0;
-constexpr uint32_t kKOff = kQOff + kTileBytes;
-constexpr uint32_t kVOff = kKOff + kWMaxTiles * kTileBytes;
-// weight buffers: [hi | lo][2 blocks of 64 keys][128 rows][128 B] = 64 KB each
-constexpr uint32_t kPPart = kWM * kWN * 2;                      // one bf16 part of a key tile
-constexpr uint32_t kPBuf0 = kQOff;                              // over Q and K (64 KB)
-constexpr uint32_t kPBuf1 = kVOff + kWMaxTiles * kTileBytes;
-constexpr uint32_t kBarOff = kPBuf1 + 2 * kPPart;
-constexpr uint32_t kWSmem = kBarOff + 128 + 1024;               // + alignment slack
+constexpr int kWThreads = 320;            // TMA, MMA, 8 softmax warps
+constexpr uint32_t kSliceBytes = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle slice)
 constexpr uint32_t kWTmemCols = 512;
-constexpr uint32_t kOCol = kWMaxTiles * kWN;                   // output accumulator
+constexpr uint32_t kOCol = kWMaxTiles * kWN; // output accumulator
 constexpr uint64_t kWDefaultWaitNs = 1000000000ull;
+
+// Shared-memory layout of head size D: per stage the query tile (D/64 slices
+// of 16 KB), then the keys and then the values of the three key tiles, each
+// slice-major ([slice][384 rows][128 B]: the rows of consecutive key tiles are
+// contiguous, so one N=256 MMA spans two key tiles and one MN-major operand
+// of N=128 spans both value slices); stages, then the barriers.
+template <int D>
+struct WinCfg {
+    static constexpr int KA = D / 64;                          // 64-column slices
+    static constexpr int STAGES = D == 64 ? 2 : 1;
+    static constexpr uint32_t TILE = KA * kSliceBytes;         // one 128-row tile
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t SLICE3 = kWMaxTiles * kSliceBytes;   // one slice of the three tiles
+    static constexpr uint32_t K_OFF = TILE;
+    static constexpr uint32_t V_OFF = K_OFF + kWMaxTiles * TILE;
+    static constexpr uint32_t STAGE = V_OFF + kWMaxTiles * TILE;
+    static constexpr uint32_t BAR_OFF = STAGES * STAGE;
+    static constexpr uint32_t XCH_OFF = BAR_OFF + 128;        // [2 halves][128 rows] fp32 row sums
+    static constexpr uint32_t SMEM = XCH_OFF + 2 * 128 * 4 + 1024;   // + alignment slack
+    static_assert(kOCol + D <= kWTmemCols, "TMEM columns");
+    static_assert(SMEM <= 232448, "shared memory per block");
+};
 
 struct WindowParams {
     int BH, T, wl, wr;
+    int items;                   // BH * query tiles
     float scale_log2;
     void* O;
     int bf16_out;
@@ -77,45 +96,260 @@ __host__ __device__ inline void band_tiles(int qt, int T, int wl, int wr, int* k
     *kt1 = t1 > ntile - 1 ? ntile - 1 : static_cast<int>(t1);
 }
 
+struct WinItem {
+    int bh, i0, kt0, nkt;
+};
+
+__device__ inline WinItem win_item(const WindowParams& p, int item) {
+    const int ntq = (p.T + kWM - 1) / kWM;
+    WinItem w;
+    w.bh = item / ntq;
+    const int qt = item - w.bh * ntq;
+    w.i0 = qt * kWM;
+    int kt1;
+    band_tiles(qt, p.T, p.wl, p.wr, &w.kt0, &kt1);
+    w.nkt = kt1 - w.kt0 + 1;   // 1 .. kWMaxTiles (the host checks)
+    return w;
+}
+
+// 2^x on the special-function unit (ex2.approx, flush-to-zero: weights below
+// 2^-126 of the row maximum's are zero; -inf gives 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 }  // namespace
 
+// The softmax warps: eight, two per TMEM lane quarter (warp w reads lanes
+// 32 (w % 4) .. 32 (w % 4) + 31, one query row per thread); warp half g
+// (0 for warps 2-5, 1 for warps 6-9) takes the 32-key chunks 2g and 2g + 1 of
+// every key tile and the output columns of its half. Per item: the row
+// maximum over the band (both warps over all chunks: most chunks' maxima come
+// from tcgen05.ld.red; the eight warps meet before any overwrites a score),
+// then the weights of this warp's chunks written over
+// their own S columns (a chunk's 16 hi words, two keys per word with the
+// lower key in the low half, in its first 16 columns, its 16 lo words in the
+// next 16), then the two partial row sums exchanged through shared memory,
+// and the output.
+template <int D>
+__device__ __forceinline__ void softmax_rows(const WindowParams& p, uint32_t tmem_base, int warp,
+                                             int lane, uint64_t* s_full, uint64_t* o_full,
+                                             uint64_t* p_full, uint64_t* x_bar, float* xch,
+                                             volatile int* abort_flag, uint64_t lim) {
+    const int quarter = warp & 3;   // TMEM lane quarter of this warp
+    const int g = (warp - 2) >> 2;  // which half of the chunks and of the output
+    const int r = quarter * 32 + lane;
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    // x_bar: every thread of the eight warps arrives, twice per item. First
+    // once its pass-1 reads of the scores are done (the other warp of the pair
+    // overwrites half of them with weights in pass 2); then with its partial
+    // sum of row r posted, reading the other half's once all have posted.
+    // Sums are posted after the item's MMAs are done, so every warp has read
+    // the previous item's sums by then. Bounded waits.
+    uint32_t xpar = 0;
+    auto all_softmax_sync = [&]() -> bool {
+        tc_fence_before();
+        mbar_arrive(x_bar);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(x_bar, xpar, abort_flag, p.dev_status, lim));
+        xpar ^= 1;
+        tc_fence_after();
+        return ok;
+    };
+    auto exchange = [&](float v) -> float {
+        xch[g * 128 + r] = v;
+        return all_softmax_sync() ? xch[(g ^ 1) * 128 + r] : 0.f;
+    };
+    int n = 0;
+    for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++n) {
+        const WinItem w = win_item(p, item);
+        const int i = w.i0 + r;
+        const int jlo = i - p.wl > 0 ? i - p.wl : 0;
+        const int jhi = i + p.wr < p.T - 1 ? i + p.wr : p.T - 1;
+        // a 32-key chunk of the item, for the warp's 32 rows together: outside
+        // every row's band (skipped: zero weights, no load), inside every
+        // row's band (no per-key mask; its maximum from tcgen05.ld.red), or
+        // partial
+        const int iw = w.i0 + quarter * 32;
+        const int wlo = iw - p.wl > 0 ? iw - p.wl : 0;
+        const int whi = iw + 31 + p.wr < p.T - 1 ? iw + 31 + p.wr : p.T - 1;
+        const int flo = iw + 31 - p.wl > 0 ? iw + 31 - p.wl : 0;
+        const int fhi = iw + p.wr < p.T - 1 ? iw + p.wr : p.T - 1;
+        const int kbase = w.kt0 * kWN;
+        auto chunk_of = [&](int k) { return 4 * (k >> 1) + 2 * g + (k & 1); };   // this warp's k-th chunk
+        auto chunk_class = [&](int ch) {   // 0 outside, 1 inside, 2 partial
+            const int j0 = kbase + 32 * ch;
+            if (j0 + 31 < wlo || j0 > whi) return 0;
+            return (j0 >= flo && j0 + 31 <= fhi) ? 1 : 2;
+        };
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full, n & 1, abort_flag, p.dev_status, lim)))
+            return;
+        tc_fence_after();
+        const int nk = 2 * w.nkt;   // chunks of this warp
+        // pass 1: the row maximum over all chunks
+        float ma = -INFINITY, mb = -INFINITY;
+        for (int ch = 0; ch < 2 * nk; ++ch) {
+            const int cls = chunk_class(ch);
+            if (cls == 0) continue;   // warp-uniform
+            const uint32_t col = t_lane + 32 * ch;
+            uint32_t v[32];
+            if (cls == 1) {
+                float m0 = tmem_ldred_max16(col, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                float m1 = tmem_ldred_max16(col + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                tmem_ld_wait();
+                reg_fence_f(m0);
+                reg_fence_f(m1);
+                ma = fmax3(ma, m0, m1);
+            } else {
+                tmem_ld32(col, v);
+                tmem_ld_wait();
+                reg_fence(v);
+                const int j0 = kbase + 32 * ch;
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    if (j0 + e >= jlo && j0 + e <= jhi) ma = fmaxf(ma, __uint_as_float(v[e]));
+                    if (j0 + e + 1 >= jlo && j0 + e + 1 <= jhi) mb = fmaxf(mb, __uint_as_float(v[e + 1]));
+                }
+            }
+        }
+        float m = fmaxf(ma, mb);
+        // a padding row past the sequence has no key: zero weights
+        if (m == -INFINITY) m = 0.f;
+        if (!all_softmax_sync()) return;
+        // pass 2: the weights as hi + lo bf16 parts, the row sum in fp32; the
+        // next chunk's load is in flight while one is converted; each key tile
+        // is handed to the MMA warp once this warp's two chunks are written
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t v[32];
+        int cls = chunk_class(chunk_of(0));
+        if (cls) tmem_ld32(t_lane + 32 * chunk_of(0), v);
+        for (int k = 0; k < nk; ++k) {
+            const int ch = chunk_of(k);
+            tmem_ld_wait();
+            reg_fence(v);
+            uint32_t cur[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) cur[e] = v[e];
+            const int cur_cls = cls;
+            if (k + 1 < nk) {
+                cls = chunk_class(chunk_of(k + 1));
+                if (cls) tmem_ld32(t_lane + 32 * chunk_of(k + 1), v);
+            }
+            uint32_t whi[16], wlo[16];
+            if (cur_cls) {
+                const int j0 = kbase + 32 * ch;
+                const bool mask = cur_cls == 2;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    float pv[2];
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        const int j = j0 + 2 * q + b;
+                        // (s - max) first: exactly 0 at the maximum, whose weight is 1
+                        const float x = (__uint_as_float(cur[2 * q + b]) - m) * p.scale_log2;
+                        pv[b] = ex2_approx(!mask || (j >= jlo && j <= jhi) ? x : -INFINITY);
+                    }
+                    sum4[q & 3] += pv[0] + pv[1];
+                    const uint32_t b0 = __float_as_uint(pv[0]), b1 = __float_as_uint(pv[1]);
+                    whi[q] = __byte_perm(b0, b1, 0x7632);   // the high halves: bf16 truncation
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(
+                        pv[0] - __uint_as_float(b0 & 0xFFFF0000u), pv[1] - __uint_as_float(b1 & 0xFFFF0000u));
+                    wlo[q] = *reinterpret_cast<const uint32_t*>(&lo);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) whi[q] = wlo[q] = 0u;
+            }
+            tmem_st16(t_lane + 32 * ch, whi);
+            tmem_st16(t_lane + 32 * ch + 16, wlo);
+            if (k & 1) {   // this warp's two chunks of tile k / 2 are written
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full + (k >> 1));
+            }
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_full, n & 1, abort_flag, p.dev_status, lim)))
+            return;
+        tc_fence_after();
+        float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        sum += exchange(sum);
+        const float inv = sum > 0.f ? 1.f / sum : 0.f;
+        const int64_t off = (static_cast<int64_t>(w.bh) * p.T + i) * D;
+#pragma unroll
+        for (int c2 = 0; c2 < D / 64; ++c2) {
+            const int c = 2 * c2 + g;   // this warp's 32-column slices of O
+            uint32_t o[32];
+            tmem_ld32(t_lane + kOCol + 32 * c, o);
+            tmem_ld_wait();
+            reg_fence(o);
+            if (i >= p.T) continue;
+            if (p.bf16_out) {
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.O) + off + 32 * c);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int d = c8 * 8 + q * 2;
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[d]) * inv,
+                                                                        __uint_as_float(o[d + 1]) * inv);
+                        wv[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                    }
+                    dst[c8] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
+            } else {
+                float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.O) + off + 32 * c);
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4)
+                    dst[c4] = make_float4(__uint_as_float(o[4 * c4]) * inv, __uint_as_float(o[4 * c4 + 1]) * inv,
+                                          __uint_as_float(o[4 * c4 + 2]) * inv,
+                                          __uint_as_float(o[4 * c4 + 3]) * inv);
+            }
+        }
+        tc_fence_before();   // the O columns are read: the next item's MMAs may write them
+    }
+}
+
+template <int D>
 __global__ void __launch_bounds__(kWThreads, 1)
     window_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const WindowParams p) {
+    using C = WinCfg<D>;
+    constexpr int KA = C::KA;
     constexpr uint32_t IDESC_S = idesc_bf16_f32(kWM, kWN);
-    constexpr uint32_t IDESC_O = idesc_bf16_f32_bmn(kWM, kWD);
+    constexpr uint32_t IDESC_S2 = idesc_bf16_f32(kWM, 2 * kWN);
+    constexpr uint32_t IDESC_O = idesc_bf16_f32_bmn(kWM, D);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-    uint64_t* full_qk = bars;       // query and key tiles landed
-    uint64_t* full_v = bars + 1;    // value tiles landed
-    uint64_t* s_full = bars + 2;    // S in TMEM
-    uint64_t* o_full = bars + 3;    // O in TMEM
-    uint64_t* p_full = bars + 4;    // [2] weights of a key tile in buffer b (one arrive per softmax warp)
-    uint64_t* p_empty = bars + 6;   // [2] the MMAs reading buffer b are done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+    uint64_t* full_qk = bars;        // [stage] query and key tiles landed
+    uint64_t* full_v = bars + 2;     // [stage] value tiles landed
+    uint64_t* empty = bars + 4;      // [stage] the MMAs reading the stage are done
+    uint64_t* s_full = bars + 6;     // S of the item in TMEM
+    uint64_t* o_full = bars + 7;     // every MMA of the item done: O in TMEM
+    uint64_t* p_full = bars + 8;     // [3] weights of key tile t in TMEM (one arrive per softmax warp)
+    uint64_t* x_bar = bars + 11;     // the softmax warps' exchange of row sums
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+    float* xch = reinterpret_cast<float*>(smem + C::XCH_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ntq = (p.T + kWM - 1) / kWM;
-    const int bh = blockIdx.x / ntq, qt = blockIdx.x - (blockIdx.x / ntq) * ntq;
-    const int i0 = qt * kWM;
-    int kt0, kt1;
-    band_tiles(qt, p.T, p.wl, p.wr, &kt0, &kt1);
-    const int nkt = kt1 - kt0 + 1;   // 1 .. kWMaxTiles (the host checks)
     const uint64_t lim = p.wait_limit_ns ? p.wait_limit_ns : kWDefaultWaitNs;
 
     if (threadIdx.x == 0) {
-        mbar_init(full_qk, 1);
-        mbar_init(full_v, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(full_qk + s, 1);
+            mbar_init(full_v + s, 1);
+            mbar_init(empty + s, 1);
+        }
         mbar_init(s_full, 1);
         mbar_init(o_full, 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(p_full + b, 4);
-            mbar_init(p_empty + b, 1);
-        }
+        for (int t = 0; t < kWMaxTiles; ++t) mbar_init(p_full + t, 8);
+        mbar_init(x_bar, 256);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -133,194 +367,103 @@ __global__ void __launch_bounds__(kWThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA
         if (lane == 0) {
-            mbar_arrive_expect_tx(full_qk, kTileBytes * (1 + nkt));
-            tma_load_3d(smem + kQOff, &qmap, 0, i0, bh, full_qk);
-            for (int t = 0; t < nkt; ++t)
-                tma_load_3d(smem + kKOff + t * kTileBytes, &kmap, 0, (kt0 + t) * kWN, bh, full_qk);
-            mbar_arrive_expect_tx(full_v, kTileBytes * nkt);
-            for (int t = 0; t < nkt; ++t)
-                tma_load_3d(smem + kVOff + t * kTileBytes, &vmap, 0, (kt0 + t) * kWN, bh, full_v);
-            // the copies land before the block may exit
-            mbar_wait_bounded(full_qk, 0, nullptr, p.dev_status, lim);
-            mbar_wait_bounded(full_v, 0, nullptr, p.dev_status, lim);
+            int n = 0;
+            for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++n) {
+                const int s = n % C::STAGES;
+                const uint32_t use = static_cast<uint32_t>(n / C::STAGES);
+                if (use > 0 &&
+                    !mbar_wait_bounded(empty + s, (use - 1) & 1, abort_flag, p.dev_status, lim))
+                    break;
+                const WinItem w = win_item(p, item);
+                uint8_t* st = smem + s * C::STAGE;
+                mbar_arrive_expect_tx(full_qk + s, C::TILE * (1 + w.nkt));
+#pragma unroll
+                for (int a = 0; a < KA; ++a)
+                    tma_load_3d(st + C::Q_OFF + a * kSliceBytes, &qmap, 64 * a, w.i0, w.bh, full_qk + s);
+                for (int t = 0; t < w.nkt; ++t)
+#pragma unroll
+                    for (int a = 0; a < KA; ++a)
+                        tma_load_3d(st + C::K_OFF + a * C::SLICE3 + t * kSliceBytes, &kmap, 64 * a,
+                                    (w.kt0 + t) * kWN, w.bh, full_qk + s);
+                mbar_arrive_expect_tx(full_v + s, C::TILE * w.nkt);
+                for (int t = 0; t < w.nkt; ++t)
+#pragma unroll
+                    for (int a = 0; a < KA; ++a)
+                        tma_load_3d(st + C::V_OFF + a * C::SLICE3 + t * kSliceBytes, &vmap, 64 * a,
+                                    (w.kt0 + t) * kWN, w.bh, full_v + s);
+            }
+            // the copies land before the block may exit: the last use of each stage
+            for (int s = 0; s < C::STAGES && s < n; ++s) {
+                const uint32_t last = static_cast<uint32_t>((n - 1 - s) / C::STAGES);
+                mbar_wait_bounded(full_qk + s, last & 1, nullptr, p.dev_status, lim);
+                mbar_wait_bounded(full_v + s, last & 1, nullptr, p.dev_status, lim);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA
         if (lane == 0) {
-            bool s_issued = false, o_issued = false;
-            if (mbar_wait_bounded(full_qk, 0, abort_flag, p.dev_status, lim)) {
+            int n = 0, committed = 0;
+            uint32_t pt = 0;   // bit t: phase parity of p_full[t]
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++n) {
+                const int s = n % C::STAGES;
+                const uint32_t use = static_cast<uint32_t>(n / C::STAGES);
+                const WinItem w = win_item(p, item);
+                // this item's query and key tiles landed. Its S MMAs overwrite
+                // the previous item's weights; tcgen05.mma instructions of one
+                // thread execute in issue order, so they run after the previous
+                // item's P V MMAs that read those weights, with no wait here.
+                ok = mbar_wait_bounded(full_qk + s, use & 1, abort_flag, p.dev_status, lim);
+                if (!ok) break;
                 tc_fence_after();
-                const uint64_t adesc = smem_desc_k_sw128(smem_u32(smem + kQOff));
-                for (int t = 0; t < nkt; ++t) {
-                    const uint64_t bdesc = smem_desc_k_sw128(smem_u32(smem + kKOff + t * kTileBytes));
+                const uint8_t* st = smem + s * C::STAGE;
+                // S by key-tile pairs: N=256 over tiles 0-1, N=128 for a third
+                for (int t = 0; t < w.nkt; t += 2) {
+                    const uint32_t idesc = t + 1 < w.nkt ? IDESC_S2 : IDESC_S;
 #pragma unroll
-                    for (int kk = 0; kk < kWD / 16; ++kk)
-                        mma_bf16(tmem_base + t * kWN, adesc + ((kk * 32) >> 4), bdesc + ((kk * 32) >> 4),
-                                 IDESC_S, kk != 0);
+                    for (int a = 0; a < KA; ++a) {
+                        const uint64_t ad = smem_desc_k_sw128(smem_u32(st + C::Q_OFF + a * kSliceBytes));
+                        const uint64_t bd =
+                            smem_desc_k_sw128(smem_u32(st + C::K_OFF + a * C::SLICE3 + t * kSliceBytes));
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16(tmem_base + t * kWN, ad + ((kk * 32) >> 4), bd + ((kk * 32) >> 4),
+                                     idesc, (a | kk) != 0);
+                    }
                 }
                 mma_commit(s_full);
-                s_issued = true;
-                bool ok = mbar_wait_bounded(full_v, 0, abort_flag, p.dev_status, lim);
-                for (int t = 0; ok && t < nkt; ++t) {
-                    const int b = t & 1;
-                    if (!mbar_wait_bounded(p_full + b, (t >> 1) & 1, abort_flag, p.dev_status, lim)) {
+                ok = mbar_wait_bounded(full_v + s, use & 1, abort_flag, p.dev_status, lim);
+                for (int t = 0; ok && t < w.nkt; ++t) {
+                    if (!mbar_wait_bounded(p_full + t, (pt >> t) & 1, abort_flag, p.dev_status, lim)) {
                         ok = false;
                         break;
                     }
+                    pt ^= 1u << t;
                     tc_fence_after();
-                    const uint32_t buf = b ? kPBuf1 : kPBuf0;
 #pragma unroll
                     for (int s8 = 0; s8 < kWN / 16; ++s8) {
-                        const int k16 = s8 * 16;   // key offset within the tile
-                        const uint64_t bdesc_v = smem_desc_mn_sw128(
-                            smem_u32(smem + kVOff + t * kTileBytes + s8 * 16 * 128), 0);
-#pragma unroll
-                        for (int part = 0; part < 2; ++part) {   // hi, lo
-                            const uint64_t adesc_p =
-                                smem_desc_k_sw128(smem_u32(smem + buf + part * kPPart +
-                                                           (k16 / 64) * (kWM * 128))) +
-                                (((k16 % 64) * 2) >> 4);
-                            mma_bf16(tmem_base + kOCol, adesc_p, bdesc_v, IDESC_O,
-                                     (t | s8 | part) != 0);
-                        }
+                        // keys 16 s8 .. 16 s8 + 15 of the tile: their hi and lo
+                        // weights (see the softmax warps' layout)
+                        const uint32_t hi = t * kWN + 32 * (s8 / 2) + 8 * (s8 % 2);
+                        // all D columns of V in one operand: its 64-column
+                        // slices are SLICE3 bytes apart
+                        const uint64_t bd = smem_desc_mn_sw128(
+                            smem_u32(st + C::V_OFF + t * kSliceBytes + s8 * 16 * 128), C::SLICE3);
+                        mma_bf16_ta(tmem_base + kOCol, tmem_base + hi, bd, IDESC_O, (t | s8) != 0);
+                        mma_bf16_ta(tmem_base + kOCol, tmem_base + hi + 16, bd, IDESC_O, 1);
                     }
-                    mma_commit(p_empty + b);
                 }
-                // every MMA of this thread (also after a stop) is tracked by o_full
+                // every MMA of the item (also after a stop) is tracked by o_full
                 mma_commit(o_full);
-                o_issued = true;
+                mma_commit(empty + s);
+                ++committed;
             }
             // MMAs in flight finish before TMEM is freed
-            if (s_issued) mbar_wait_bounded(s_full, 0, nullptr, p.dev_status, lim);
-            if (o_issued) mbar_wait_bounded(o_full, 0, nullptr, p.dev_status, lim);
+            if (committed > 0)
+                mbar_wait_bounded(o_full, (committed - 1) & 1, nullptr, p.dev_status, lim);
         }
     } else {
-        // ------------------------------------------------ softmax and output
-        const int quarter = warp & 3;   // TMEM lane quarter of this warp
-        const int r = quarter * 32 + lane;
-        const int i = i0 + r;
-        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-        const int jlo = i - p.wl > 0 ? i - p.wl : 0;
-        const int jhi = i + p.wr < p.T - 1 ? i + p.wr : p.T - 1;
-        const int kbase = kt0 * kWN;
-        bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full, 0, abort_flag, p.dev_status, lim));
-        if (ok) {
-            tc_fence_after();
-            // pass 1: the row maximum over the band
-            float m = -INFINITY;
-            for (int t = 0; t < nkt; ++t) {
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    uint32_t raw2[2][32];
-                    tmem_ld32(t_lane + t * kWN + c2 * 64, raw2[0]);
-                    tmem_ld32(t_lane + t * kWN + c2 * 64 + 32, raw2[1]);
-                    tmem_ld_wait();
-                    reg_fence(raw2[0]);
-                    reg_fence(raw2[1]);
-                    const int j0 = kbase + t * kWN + c2 * 64;
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) {
-                        const int j = j0 + e;
-                        if (j >= jlo && j <= jhi) m = fmaxf(m, __uint_as_float(raw2[e >> 5][e & 31]));
-                    }
-                }
-            }
-            // pass 2, key tile by key tile: the weights as hi + lo bf16 parts
-            // into buffer t % 2 (once the MMAs of tile t - 2 have read it),
-            // the row sum in fp32
-            float sum = 0.f;
-            for (int t = 0; ok && t < nkt; ++t) {
-                const int b = t & 1;
-                if (t >= 2)
-                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(p_empty + b, ((t >> 1) - 1) & 1,
-                                                                  abort_flag, p.dev_status, lim));
-                if (!ok) break;
-                uint8_t* prow = smem + (b ? kPBuf1 : kPBuf0) + r * 128;
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    uint32_t raw2[2][32];
-                    tmem_ld32(t_lane + t * kWN + c2 * 64, raw2[0]);
-                    tmem_ld32(t_lane + t * kWN + c2 * 64 + 32, raw2[1]);
-                    tmem_ld_wait();
-                    reg_fence(raw2[0]);
-                    reg_fence(raw2[1]);
-                    const int j0 = kbase + t * kWN + c2 * 64;
-                    uint8_t* pblk = prow + c2 * (kWM * 128);   // 64-key block of the tile
-#pragma unroll
-                    for (int g8 = 0; g8 < 8; ++g8) {
-                        uint32_t whi[4], wlo[4];
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            float pv[2];
-#pragma unroll
-                            for (int q = 0; q < 2; ++q) {
-                                const int e = g8 * 8 + h * 2 + q;
-                                const int j = j0 + e;
-                                pv[q] = (j >= jlo && j <= jhi)
-                                            ? exp2f((__uint_as_float(raw2[e >> 5][e & 31]) - m) * p.scale_log2)
-                                            : 0.f;
-                            }
-                            sum += pv[0] + pv[1];
-                            const __nv_bfloat162 hi = __floats2bfloat162_rn(pv[0], pv[1]);
-                            const __nv_bfloat162 lo = __floats2bfloat162_rn(pv[0] - __low2float(hi),
-                                                                            pv[1] - __high2float(hi));
-                            whi[h] = *reinterpret_cast<const uint32_t*>(&hi);
-                            wlo[h] = *reinterpret_cast<const uint32_t*>(&lo);
-                        }
-                        // 16-byte chunk g8 of the row, swizzled by the row within its 8-row atom
-                        const int off = (g8 ^ (r & 7)) * 16;
-                        *reinterpret_cast<uint4*>(pblk + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
-                        *reinterpret_cast<uint4*>(pblk + kPPart + off) =
-                            make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
-                    }
-                }
-                fence_proxy_async_smem();   // the MMA reads the weights through the async proxy
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_full + b);
-            }
-            if (ok)
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_full, 0, abort_flag, p.dev_status, lim));
-            if (ok) {
-                tc_fence_after();
-                uint32_t o2[2][32];
-                tmem_ld32(t_lane + kOCol, o2[0]);
-                tmem_ld32(t_lane + kOCol + 32, o2[1]);
-                tmem_ld_wait();
-                reg_fence(o2[0]);
-                reg_fence(o2[1]);
-                if (i < p.T) {
-                    const float inv = sum > 0.f ? 1.f / sum : 0.f;
-                    const int64_t off = (static_cast<int64_t>(bh) * p.T + i) * kWD;
-                    if (p.bf16_out) {
-                        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.O) + off);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                const int d = c * 8 + h * 2;
-                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(
-                                    __uint_as_float(o2[d >> 5][d & 31]) * inv,
-                                    __uint_as_float(o2[(d + 1) >> 5][(d + 1) & 31]) * inv);
-                                w[h] = *reinterpret_cast<const uint32_t*>(&b2);
-                            }
-                            dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.O) + off);
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const int d = c * 4;
-                            dst[c] = make_float4(__uint_as_float(o2[d >> 5][d & 31]) * inv,
-                                                 __uint_as_float(o2[(d + 1) >> 5][(d + 1) & 31]) * inv,
-                                                 __uint_as_float(o2[(d + 2) >> 5][(d + 2) & 31]) * inv,
-                                                 __uint_as_float(o2[(d + 3) >> 5][(d + 3) & 31]) * inv);
-                        }
-                    }
-                }
-            }
-        }
+        softmax_rows<D>(p, tmem_base, warp, lane, s_full, o_full, p_full, x_bar, xch, abort_flag, lim);
     }
 
     tc_fence_before();
@@ -335,23 +478,37 @@ __global__ void __launch_bounds__(kWThreads, 1)
 
 namespace {
 
-// [BH][T][64] bf16, box 64 x 128 rows x 1 head, 128-byte swizzle; rows outside
-// [0, T) of a head read as zeros.
-bool make_map_3d(CUtensorMap* m, const void* base, int BH, int T) {
-    const uint64_t dims[3] = {static_cast<uint64_t>(kWD), static_cast<uint64_t>(T),
+// [BH][T][D] bf16, box 64 columns x 128 rows x 1 head, 128-byte swizzle (a
+// D = 128 tile is two boxes, at columns 0 and 64); rows outside [0, T) of a
+// head read as zeros.
+bool make_map_3d(CUtensorMap* m, const void* base, int BH, int T, int D) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(T),
                               static_cast<uint64_t>(BH)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(kWD) * 2,
-                                 static_cast<uint64_t>(kWD) * 2 * static_cast<uint64_t>(T)};
-    const uint32_t box[3] = {static_cast<uint32_t>(kWD), static_cast<uint32_t>(kWN), 1};
+    const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2,
+                                 static_cast<uint64_t>(D) * 2 * static_cast<uint64_t>(T)};
+    const uint32_t box[3] = {64u, static_cast<uint32_t>(kWN), 1};
     return tmap_bf16_sw128(m, base, 3, dims, strides, box);
+}
+
+template <int D>
+cudaError_t window_tc_run(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
+                          const WindowParams& p, cudaStream_t stream) {
+    const int sms = tile_sm_count();
+    const int grid = p.items < sms ? p.items : sms;
+    cudaError_t e = set_max_dyn_smem(reinterpret_cast<const void*>(window_tc_kernel<D>),
+                                     static_cast<int>(WinCfg<D>::SMEM));
+    if (e != cudaSuccess) return e;
+    TraceLaunch tr("window_tc", stream);
+    window_tc_kernel<D><<<grid, kWThreads, WinCfg<D>::SMEM, stream>>>(qm, km, vm, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-// True when the tensor-core kernel covers the call: bf16 inputs, head size 64,
-// and the band of every 128-query tile within three 128-key tiles.
+// True when the tensor-core kernel covers the call: bf16 inputs, head size 64
+// or 128, and the band of every 128-query tile within three 128-key tiles.
 bool window_tc_supported(bool bf16_in, int D, int T, int wl, int wr) {
-    if (!bf16_in || D != kWD || T <= 0) return false;
+    if (!bf16_in || (D != 64 && D != 128) || T <= 0) return false;
     const int ntq = (T + kWM - 1) / kWM;
     for (int qt = 0; qt < ntq; ++qt) {
         int kt0, kt1;
@@ -362,30 +519,29 @@ bool window_tc_supported(bool bf16_in, int D, int T, int wl, int wr) {
 }
 
 cudaError_t window_tc_launch(const void* Q, const void* K, const void* V, void* O, bool bf16_out,
-                             int BH, int T, int wl, int wr, float scale, int32_t* dev_status,
-                             cudaStream_t stream) {
+                             int BH, int T, int D, int wl, int wr, float scale,
+                             int32_t* dev_status, cudaStream_t stream) {
+    if (D != 64 && D != 128) return cudaErrorInvalidValue;
+    const int64_t items = static_cast<int64_t>(BH) * ((T + kWM - 1) / kWM);
+    if (items == 0) return cudaSuccess;
+    if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     CUtensorMap qm, km, vm;
-    if (!make_map_3d(&qm, Q, BH, T) || !make_map_3d(&km, K, BH, T) || !make_map_3d(&vm, V, BH, T))
+    if (!make_map_3d(&qm, Q, BH, T, D) || !make_map_3d(&km, K, BH, T, D) ||
+        !make_map_3d(&vm, V, BH, T, D))
         return cudaErrorInvalidValue;
     WindowParams p;
     p.BH = BH;
     p.T = T;
     p.wl = wl;
     p.wr = wr;
+    p.items = static_cast<int>(items);
     p.scale_log2 = scale * kLog2e;
     p.O = O;
     p.bf16_out = bf16_out ? 1 : 0;
     p.dev_status = dev_status;
     p.wait_limit_ns = 0;
-    const int64_t blocks = static_cast<int64_t>(BH) * ((T + kWM - 1) / kWM);
-    if (blocks == 0) return cudaSuccess;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    cudaError_t e = set_max_dyn_smem(reinterpret_cast<const void*>(window_tc_kernel),
-                                     static_cast<int>(kWSmem));
-    if (e != cudaSuccess) return e;
-    TraceLaunch tr("window_tc", stream);
-    window_tc_kernel<<<static_cast<unsigned>(blocks), kWThreads, kWSmem, stream>>>(qm, km, vm, p);
-    return cudaGetLastError();
+    return D == 64 ? window_tc_run<64>(qm, km, vm, p, stream)
+                   : window_tc_run<128>(qm, km, vm, p, stream);
 }
 
 }  // namespace ssa

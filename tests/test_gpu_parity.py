@@ -254,15 +254,16 @@ def test_window_edges(cuda_dev, T, D, wl, wr, dtype):
         assert torch.equal(O.cpu(), V.float())
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("T,wl,wr", [
     (1, 0, 0), (2, 1, 1), (128, 128, 0), (129, 64, 64), (300, 100, 20), (385, 0, 128),
     (1000, 128, 128), (2048, 3, 117),
 ])
-def test_window_tensor_core_tiles(cuda_dev, T, wl, wr):
-    """bf16, head size 64 and a band of at most three 128-key tiles per
+def test_window_tensor_core_tiles(cuda_dev, T, wl, wr, D):
+    """bf16, head size 64 or 128 and a band of at most three 128-key tiles per
     128-query tile run as dense tensor-core tiles (the launch is window_tc);
     every row is compared with the oracle."""
-    Q, K, V = _normal_inputs(2, 3, T, T, 64, torch.bfloat16, seed=7 * T + wl + 3 * wr)
+    Q, K, V = _normal_inputs(2, 3, T, T, D, torch.bfloat16, seed=7 * T + wl + 3 * wr + D)
     ref = oracle.window_attn(Q, K, V, wl, wr)
     dq, dk, dv = (t.to(cuda_dev) for t in (Q, K, V))
     ssa.trace_begin()
@@ -274,6 +275,27 @@ def test_window_tensor_core_tiles(cuda_dev, T, wl, wr):
     assert_out_close(Ob.float().cpu().numpy(), ref, TOL_BF16, True)
     if wl == 0 and wr == 0:
         assert torch.equal(O.cpu(), V.float())
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_window_tensor_core_many_items_per_cta(cuda_dev, D):
+    """More 128-query items than SMs (80 heads x 8 tiles): each persistent CTA
+    takes several items in turn, through both shared-memory stages (D 64) or
+    its one stage (D 128) and the TMEM hand-offs between items; every row
+    against the oracle, fp32 and bf16 output."""
+    T, wl, wr = 1024, 128, 128
+    Q, K, V = _normal_inputs(2, 40, T, T, D, torch.bfloat16, seed=500 + D)
+    ref = oracle.window_attn(Q, K, V, wl, wr)
+    dq, dk, dv = (t.to(cuda_dev) for t in (Q, K, V))
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    ssa.trace_begin()
+    O = ssa.ssa_window_attn(dq, dk, dv, wl, wr, out_dtype=torch.float32, dev_status=st)
+    torch.cuda.synchronize()
+    assert [n for n, _ in ssa.trace_end()] == ["window_tc"]
+    assert int(st.item()) == 0
+    assert_out_close(O.cpu().numpy(), ref, TOL_BF16, False)
+    Ob = ssa.ssa_window_attn(dq, dk, dv, wl, wr)
+    assert_out_close(Ob.float().cpu().numpy(), ref, TOL_BF16, True)
 
 
 def test_window_wide_band_uses_gather(cuda_dev):
