@@ -88,13 +88,23 @@ constexpr uint32_t kQueueWarpBytes = kQueue * kSub * 4 + kQueue * 4 + 2 * 32 * 4
 //  - A row whose list is full moves its test to the first raw score whose
 //    scaled order key exceeds the bound (tau's low 16 bits are zero, so
 //    tau + 1 does not wrap; a row without a bound never fills past its keys).
-// Returns the lane's test; qmeta and bits are the lane's drained entry and
-// its candidates.
-__device__ __noinline__ float drain_fixup(uint32_t* qm, const float4* qv, const int* qcnt,
-                                          int* qovf, const uint32_t* tau, uint64_t* cand,
-                                          int64_t row0, int tb, int q_head, int lane, bool act,
-                                          int owner, uint32_t qmeta, uint32_t bits, int capc,
+// Returns the lane's test. qb is the warp's queue (ring, key words, counts,
+// flags); packed holds the drain's ring position q_head mod 64 (bits 0..15),
+// its entry count n (16..23) and the TMEM buffer tb (24..31), few arguments
+// being what keeps the call site cheap; bits are this lane's candidates.
+__device__ __noinline__ float drain_fixup(uint8_t* qb, const uint32_t* tau, uint64_t* cand,
+                                          int64_t row0, uint32_t packed, uint32_t bits, int capc,
                                           float t_hot, float scale) {
+    const int q_head = static_cast<int>(packed & 0xFFFFu), n = static_cast<int>((packed >> 16) & 0xFFu);
+    const int tb = static_cast<int>(packed >> 24);
+    const int lane = threadIdx.x & 31;
+    const bool act = lane < n;
+    float4* qv = reinterpret_cast<float4*>(qb);
+    uint32_t* qm = reinterpret_cast<uint32_t*>(qb + kQueue * kSub * 4);
+    int* qcnt = reinterpret_cast<int*>(qb + kQueue * (kSub * 4 + 4));
+    int* qovf = qcnt + 32;
+    const uint32_t qmeta = act ? qm[(q_head + lane) & (kQueue - 1)] : 0u;
+    const int owner = static_cast<int>(qmeta & 31u);
     const int qi = (q_head + lane) & (kQueue - 1);
     const int nb = __popc(bits);
     const uint32_t peers = __match_any_sync(0xffffffffu, act ? owner : 32 + lane);
@@ -531,8 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (__any_sync(0xffffffffu, bits0 != 0 && slot >= capc))   // a list filled
-                t_hot = drain_fixup(qm, qv, qcnt, qovf, p.tau, p.cand, row0, tb, q_head, lane,
-                                    act, owner, meta, bits0, capc, t_hot, p.scale);
+                t_hot = drain_fixup(reinterpret_cast<uint8_t*>(qv), p.tau, p.cand, row0,
+                                    static_cast<uint32_t>(q_head & (kQueue - 1)) | (static_cast<uint32_t>(n) << 16) |
+                                        (static_cast<uint32_t>(tb) << 24),
+                                    bits0, capc, t_hot, p.scale);
             q_head += n;
             __syncwarp();
         };
