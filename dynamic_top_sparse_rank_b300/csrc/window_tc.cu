@@ -20,16 +20,15 @@
 //           with P read from TMEM (the A operand of tcgen05.mma may sit in
 //           TMEM) and V MN-major straight from its TMA layout;
 //   warps 2-9  one query row per thread, two warps per row splitting its key
-//           chunks and output columns: the band mask and the row maximum
-//           (first pass over S), then per key tile p = 2^((s - max) * scale *
-//           log2 e) in fp32, written back over that tile's S columns as two
-//           bf16 parts, hi = p truncated to bf16 and lo = bf16(p - hi), so
-//           that P V = hi V + lo V keeps p to about 2^-16 (one bf16 P would
-//           cost 2^-9, too much for rows with few keys); the row sum is taken
-//           in fp32; after the last MMA, O divided by the sum and stored in
-//           bf16 or fp32. A 32-key chunk outside the band of all 32 rows of a
-//           warp is neither loaded nor exponentiated (about a quarter of the
-//           chunks for a 128-key radius).
+//           chunks and output columns: one pass over the key tiles with a
+//           running shift per row (the online softmax; see softmax_rows):
+//           p = 2^((s - M) * scale * log2 e) in fp32, written back over that
+//           tile's S columns as two bf16 parts, hi = p truncated to bf16 and
+//           lo = bf16(p - hi), so that P V = hi V + lo V keeps p to about 2^-16
+//           (one bf16 P would cost 2^-9, too much for rows with few keys);
+//           each tile goes to the MMA warp once written, so its P V runs
+//           under the next tile's softmax; the row sum is taken in fp32; after
+//           the last MMA, O divided by the sum and stored in bf16 or fp32.
 // Every mbarrier wait is bounded; a wait that runs out reports
 // SSA_DEV_WAIT_LIMIT, stops the other roles and TMEM is freed.
 #include <float.h>
@@ -48,7 +47,9 @@ namespace {
 constexpr int kWM = 128;                     // query rows per item
 constexpr int kWN = 128;                     // keys per score tile
 constexpr int kWMaxTiles = 3;                // score tiles next to the output in TMEM
-constexpr int kWThreads = 320;            // TMA, MMA, 8 softmax warps
+constexpr int kNW = 4;                       // softmax warps per TMEM lane quarter
+constexpr int kCPW = 4 / kNW;                // 32-key chunks of a key tile per softmax warp
+constexpr int kWThreads = 64 + 128 * kNW;    // TMA warp, MMA warp, softmax warps
 constexpr uint32_t kSliceBytes = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle slice)
 constexpr uint32_t kWTmemCols = 512;
 constexpr uint32_t kOCol = kWMaxTiles * kWN; // output accumulator
@@ -63,6 +64,7 @@ template <int D>
 struct WinCfg {
     static constexpr int KA = D / 64;                          // 64-column slices
     static constexpr int STAGES = D == 64 ? 2 : 1;
+    static constexpr bool VT = D == 64;                        // V turned K-major in shared memory
     static constexpr uint32_t TILE = KA * kSliceBytes;         // one 128-row tile
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t SLICE3 = kWMaxTiles * kSliceBytes;   // one slice of the three tiles
@@ -70,8 +72,8 @@ struct WinCfg {
     static constexpr uint32_t V_OFF = K_OFF + kWMaxTiles * TILE;
     static constexpr uint32_t STAGE = V_OFF + kWMaxTiles * TILE;
     static constexpr uint32_t BAR_OFF = STAGES * STAGE;
-    static constexpr uint32_t XCH_OFF = BAR_OFF + 128;        // [2 halves][128 rows] fp32 row sums
-    static constexpr uint32_t SMEM = XCH_OFF + 2 * 128 * 4 + 1024;   // + alignment slack
+    static constexpr uint32_t XCH_OFF = BAR_OFF + 256;        // [3 slots][128 rows] 32-bit words
+    static constexpr uint32_t SMEM = XCH_OFF + 3 * 128 * 4 + 1024;   // + alignment slack
     static_assert(kOCol + D <= kWTmemCols, "TMEM columns");
     static_assert(SMEM <= 232448, "shared memory per block");
 };
@@ -122,44 +124,92 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 }  // namespace
 
+// Turns 64 keys x 64 columns of a value tile, as TMA wrote it (row = key,
+// 128 bytes of 64 bf16 columns, 128-byte swizzle: 16-byte chunk c of row r at
+// r * 128 + (c ^ (r & 7)) * 16), into the K-major operand of the same 8 KB
+// (row = column d, its 64 keys in 128 bytes, the same swizzle), in place. The
+// 8x8 blocks go through registers: ldmatrix .trans reads block (keys 8kb..,
+// columns 8db..) transposed, stmatrix writes it as block (columns 8db..,
+// keys 8kb..); the whole half is read before any of it is written. The P V
+// MMAs read V^T K-major at 73.5 cycles per M=128, K=16 instruction against
+// 125 for V MN-major (measured at N=64 and N=128).
+__device__ __forceinline__ void vt_transpose_half(uint32_t base, int lane) {
+    const int m = lane >> 3, i = lane & 7;   // the lane's matrix of an x4 group and its row
+    uint32_t r[16][4];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const int kb = q >> 1, db = (q & 1) * 4 + m;
+        const uint32_t src = base + (8 * kb + i) * 128 + ((db ^ i) << 4);
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r[q][0]), "=r"(r[q][1]), "=r"(r[q][2]), "=r"(r[q][3])
+                     : "r"(src)
+                     : "memory");
+    }
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const int kb = q >> 1, db = (q & 1) * 4 + m;
+        const uint32_t dst = base + (8 * db + i) * 128 + ((kb ^ i) << 4);
+        asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                     "r"(r[q][0]), "r"(r[q][1]), "r"(r[q][2]), "r"(r[q][3])
+                     : "memory");
+    }
+    __syncwarp();
+}
+
 // The softmax warps: eight, two per TMEM lane quarter (warp w reads lanes
 // 32 (w % 4) .. 32 (w % 4) + 31, one query row per thread); warp half g
 // (0 for warps 2-5, 1 for warps 6-9) takes the 32-key chunks 2g and 2g + 1 of
-// every key tile and the output columns of its half. Per item: the row
-// maximum over the band (both warps over all chunks: most chunks' maxima come
-// from tcgen05.ld.red; the eight warps meet before any overwrites a score),
-// then the weights of this warp's chunks written over
-// their own S columns (a chunk's 16 hi words, two keys per word with the
-// lower key in the low half, in its first 16 columns, its 16 lo words in the
-// next 16), then the two partial row sums exchanged through shared memory,
-// and the output.
+// every key tile and the output columns of its half.
+//
+// One pass, key tile by key tile, with a running shift M per row (the
+// online softmax): each warp takes the maximum of its two chunks (a chunk
+// inside every row's band of the warp from tcgen05.ld.red, a partial one
+// masked, one outside every band skipped), the pair combines the two through
+// shared memory (atomicMax on order keys) and meets at a bounded per-pair
+// barrier before either overwrites a score, so both warps hold the same tile
+// maximum and take the same decisions. M moves only when the tile maximum
+// exceeds it by more than 2^8 in weight: then the MMAs of the earlier tiles
+// are waited for and the row's O (this warp's columns) and partial sum are
+// scaled down, so weights stay below 2^8 and are exact at the maximum (the
+// first tile sets M to its maximum; w = 0 gives weight 1 and O = V exactly).
+// The weights are written over the warp's own S columns (a chunk's 16 hi
+// words, two keys per word with the lower key in the low half, in its first
+// 16 columns, its 16 lo words in the next 16) and each key tile is handed to
+// the MMA warp once both warps of every pair have written it. At the end the
+// two partial row sums meet the same way (atomicAdd), and each warp writes
+// its half of the output columns.
+//
+// Shared slots: three rotating 128-row words per pair use (step u uses slot
+// u mod 3); after the barrier of step u, warp 0 of the pair clears the slot
+// of step u - 1, which both have read before arriving, and which is next
+// used at step u + 2, after the partner has passed step u + 1's barrier.
 template <int D>
 __device__ __forceinline__ void softmax_rows(const WindowParams& p, uint32_t tmem_base, int warp,
                                              int lane, uint64_t* s_full, uint64_t* o_full,
-                                             uint64_t* p_full, uint64_t* x_bar, float* xch,
-                                             volatile int* abort_flag, uint64_t lim) {
+                                             uint64_t* p_full, uint64_t* pv_done, uint64_t* pair_bar,
+                                             uint32_t* slots, volatile int* abort_flag,
+                                             uint64_t lim) {
     const int quarter = warp & 3;   // TMEM lane quarter of this warp
-    const int g = (warp - 2) >> 2;  // which half of the chunks and of the output
+    const int g = (warp - 2) >> 2;  // which part of the chunks and of the output
     const int r = quarter * 32 + lane;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    // x_bar: every thread of the eight warps arrives, twice per item. First
-    // once its pass-1 reads of the scores are done (the other warp of the pair
-    // overwrites half of them with weights in pass 2); then with its partial
-    // sum of row r posted, reading the other half's once all have posted.
-    // Sums are posted after the item's MMAs are done, so every warp has read
-    // the previous item's sums by then. Bounded waits.
-    uint32_t xpar = 0;
-    auto all_softmax_sync = [&]() -> bool {
+    constexpr float kRescaleLog2 = 8.f;   // weights stay below 2^8
+    uint32_t u = 0;                        // pair steps taken
+    uint32_t pvpar = 0;                    // bit t: phase parity of pv_done[t]
+    // one step of the pair: combine (through slot u % 3, already updated by
+    // the caller), meet, clear the previous step's slot; false on a stop
+    auto pair_meet = [&]() -> bool {
         tc_fence_before();
-        mbar_arrive(x_bar);
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(x_bar, xpar, abort_flag, p.dev_status, lim));
-        xpar ^= 1;
+        mbar_arrive(pair_bar + quarter);
+        const bool ok =
+            __all_sync(0xffffffffu, mbar_wait_bounded(pair_bar + quarter, u & 1, abort_flag, p.dev_status, lim));
         tc_fence_after();
         return ok;
     };
-    auto exchange = [&](float v) -> float {
-        xch[g * 128 + r] = v;
-        return all_softmax_sync() ? xch[(g ^ 1) * 128 + r] : 0.f;
+    auto step_done = [&]() {
+        if (g == 0) slots[((u + 2) % 3) * 128 + r] = 0u;
+        ++u;
     };
     int n = 0;
     for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++n) {
@@ -168,16 +218,13 @@ __device__ __forceinline__ void softmax_rows(const WindowParams& p, uint32_t tme
         const int jlo = i - p.wl > 0 ? i - p.wl : 0;
         const int jhi = i + p.wr < p.T - 1 ? i + p.wr : p.T - 1;
         // a 32-key chunk of the item, for the warp's 32 rows together: outside
-        // every row's band (skipped: zero weights, no load), inside every
-        // row's band (no per-key mask; its maximum from tcgen05.ld.red), or
-        // partial
+        // every row's band, inside every row's band, or partial
         const int iw = w.i0 + quarter * 32;
         const int wlo = iw - p.wl > 0 ? iw - p.wl : 0;
         const int whi = iw + 31 + p.wr < p.T - 1 ? iw + 31 + p.wr : p.T - 1;
         const int flo = iw + 31 - p.wl > 0 ? iw + 31 - p.wl : 0;
         const int fhi = iw + p.wr < p.T - 1 ? iw + p.wr : p.T - 1;
         const int kbase = w.kt0 * kWN;
-        auto chunk_of = [&](int k) { return 4 * (k >> 1) + 2 * g + (k & 1); };   // this warp's k-th chunk
         auto chunk_class = [&](int ch) {   // 0 outside, 1 inside, 2 partial
             const int j0 = kbase + 32 * ch;
             if (j0 + 31 < wlo || j0 > whi) return 0;
@@ -186,109 +233,138 @@ __device__ __forceinline__ void softmax_rows(const WindowParams& p, uint32_t tme
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full, n & 1, abort_flag, p.dev_status, lim)))
             return;
         tc_fence_after();
-        const int nk = 2 * w.nkt;   // chunks of this warp
-        // pass 1: the row maximum over all chunks
-        float ma = -INFINITY, mb = -INFINITY;
-        for (int ch = 0; ch < 2 * nk; ++ch) {
-            const int cls = chunk_class(ch);
-            if (cls == 0) continue;   // warp-uniform
-            const uint32_t col = t_lane + 32 * ch;
-            uint32_t v[32];
-            if (cls == 1) {
-                float m0 = tmem_ldred_max16(col, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                float m1 = tmem_ldred_max16(col + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-                tmem_ld_wait();
-                reg_fence_f(m0);
-                reg_fence_f(m1);
-                ma = fmax3(ma, m0, m1);
-            } else {
-                tmem_ld32(col, v);
-                tmem_ld_wait();
-                reg_fence(v);
-                const int j0 = kbase + 32 * ch;
+        float M = -INFINITY;   // the row's shift
+        float l = 0.f;         // this warp's partial row sum
+        for (int t = 0; t < w.nkt; ++t) {
+            // this warp's two chunks of the tile and their maximum
+            uint32_t v[kCPW][32];
+            float mx[kCPW][2];
+            int cls[kCPW];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    if (j0 + e >= jlo && j0 + e <= jhi) ma = fmaxf(ma, __uint_as_float(v[e]));
-                    if (j0 + e + 1 >= jlo && j0 + e + 1 <= jhi) mb = fmaxf(mb, __uint_as_float(v[e + 1]));
+            for (int c = 0; c < kCPW; ++c) {
+                const int ch = 4 * t + kCPW * g + c;
+                cls[c] = chunk_class(ch);
+                const uint32_t col = t_lane + 32 * ch;
+                if (cls[c] == 1) {
+                    mx[c][0] = tmem_ldred_max16(col, *reinterpret_cast<uint32_t(*)[16]>(&v[c][0]));
+                    mx[c][1] = tmem_ldred_max16(col + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[c][16]));
+                } else if (cls[c] == 2) {
+                    tmem_ld32(col, v[c]);
                 }
             }
-        }
-        float m = fmaxf(ma, mb);
-        // a padding row past the sequence has no key: zero weights
-        if (m == -INFINITY) m = 0.f;
-        if (!all_softmax_sync()) return;
-        // pass 2: the weights as hi + lo bf16 parts, the row sum in fp32; the
-        // next chunk's load is in flight while one is converted; each key tile
-        // is handed to the MMA warp once this warp's two chunks are written
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t v[32];
-        int cls = chunk_class(chunk_of(0));
-        if (cls) tmem_ld32(t_lane + 32 * chunk_of(0), v);
-        for (int k = 0; k < nk; ++k) {
-            const int ch = chunk_of(k);
             tmem_ld_wait();
-            reg_fence(v);
-            uint32_t cur[32];
+            float m = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) cur[e] = v[e];
-            const int cur_cls = cls;
-            if (k + 1 < nk) {
-                cls = chunk_class(chunk_of(k + 1));
-                if (cls) tmem_ld32(t_lane + 32 * chunk_of(k + 1), v);
-            }
-            uint32_t whi[16], wlo[16];
-            if (cur_cls) {
-                const int j0 = kbase + 32 * ch;
-                const bool mask = cur_cls == 2;
+            for (int c = 0; c < kCPW; ++c) {
+                if (cls[c] == 0) continue;
+                reg_fence(v[c]);
+                if (cls[c] == 1) {
+                    reg_fence_f(mx[c][0]);
+                    reg_fence_f(mx[c][1]);
+                    m = fmax3(m, mx[c][0], mx[c][1]);
+                } else {
+                    const int j0 = kbase + 32 * (4 * t + kCPW * g + c);
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    float pv[2];
-#pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        const int j = j0 + 2 * q + b;
-                        // (s - max) first: exactly 0 at the maximum, whose weight is 1
-                        const float x = (__uint_as_float(cur[2 * q + b]) - m) * p.scale_log2;
-                        pv[b] = ex2_approx(!mask || (j >= jlo && j <= jhi) ? x : -INFINITY);
-                    }
-                    sum4[q & 3] += pv[0] + pv[1];
-                    const uint32_t b0 = __float_as_uint(pv[0]), b1 = __float_as_uint(pv[1]);
-                    whi[q] = __byte_perm(b0, b1, 0x7632);   // the high halves: bf16 truncation
-                    const __nv_bfloat162 lo = __floats2bfloat162_rn(
-                        pv[0] - __uint_as_float(b0 & 0xFFFF0000u), pv[1] - __uint_as_float(b1 & 0xFFFF0000u));
-                    wlo[q] = *reinterpret_cast<const uint32_t*>(&lo);
+                    for (int e = 0; e < 32; ++e)
+                        if (j0 + e >= jlo && j0 + e <= jhi) m = fmaxf(m, __uint_as_float(v[c][e]));
                 }
-            } else {
+            }
+            // the tile maximum of the row: both halves
+            uint32_t* slot = slots + (u % 3) * 128;
+            if (m > -INFINITY) atomicMax(slot + r, f32_order_key(m));
+            if (!pair_meet()) return;
+            const uint32_t mk = slot[r];
+            step_done();
+            const float mt = mk == 0u ? -INFINITY : order_key_f32(mk);
+            // the shift: set by the first tile with a key; moved when a
+            // weight would exceed 2^8
+            const bool move = mt > -INFINITY && (M == -INFINITY || (mt - M) * p.scale_log2 > kRescaleLog2);
+            if (__any_sync(0xffffffffu, move && M > -INFINITY)) {
+                // O holds earlier tiles' sums at the old shift: wait for their
+                // MMAs, then scale this warp's O columns of the moved rows
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(pv_done + (t - 1), (pvpar >> (t - 1)) & 1,
+                                                              abort_flag, p.dev_status, lim)))
+                    return;
+                tc_fence_after();
+                const float f = move && M > -INFINITY ? ex2_approx((M - mt) * p.scale_log2) : 1.f;
 #pragma unroll
-                for (int q = 0; q < 16; ++q) whi[q] = wlo[q] = 0u;
-            }
-            tmem_st16(t_lane + 32 * ch, whi);
-            tmem_st16(t_lane + 32 * ch + 16, wlo);
-            if (k & 1) {   // this warp's two chunks of tile k / 2 are written
+                for (int c16 = 0; c16 < D / kNW / 16; ++c16) {
+                    const uint32_t ocol = t_lane + kOCol + (D / kNW) * g + 16 * c16;
+                    uint32_t o[16];
+                    tmem_ldred_max16(ocol, o);
+                    tmem_ld_wait();
+                    reg_fence(o);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                    tmem_st16(ocol, o);
+                }
                 tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_full + (k >> 1));
+                l *= f;
             }
+            if (move) M = mt;
+            // the weights of the two chunks
+#pragma unroll
+            for (int c = 0; c < kCPW; ++c) {
+                const int ch = 4 * t + kCPW * g + c;
+                uint32_t whi[16], wlo[16];
+                if (cls[c]) {
+                    const int j0 = kbase + 32 * ch;
+                    const bool mask = cls[c] == 2;
+                    float s4[2] = {0.f, 0.f};
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        float pv[2];
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            const int j = j0 + 2 * q + b;
+                            // (s - M) first: exactly 0 at the maximum, whose weight is 1
+                            const float x = (__uint_as_float(v[c][2 * q + b]) - M) * p.scale_log2;
+                            pv[b] = ex2_approx(!mask || (j >= jlo && j <= jhi) ? x : -INFINITY);
+                        }
+                        s4[q & 1] += pv[0] + pv[1];
+                        const uint32_t b0 = __float_as_uint(pv[0]), b1 = __float_as_uint(pv[1]);
+                        whi[q] = __byte_perm(b0, b1, 0x7632);   // the high halves: bf16 truncation
+                        const __nv_bfloat162 lo = __floats2bfloat162_rn(
+                            pv[0] - __uint_as_float(b0 & 0xFFFF0000u), pv[1] - __uint_as_float(b1 & 0xFFFF0000u));
+                        wlo[q] = *reinterpret_cast<const uint32_t*>(&lo);
+                    }
+                    l += s4[0] + s4[1];
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) whi[q] = wlo[q] = 0u;
+                }
+                tmem_st16(t_lane + 32 * ch, whi);
+                tmem_st16(t_lane + 32 * ch + 16, wlo);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full + t);
         }
+        for (int t = 0; t < w.nkt; ++t) pvpar ^= 1u << t;   // one pv_done phase per tile of the item
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_full, n & 1, abort_flag, p.dev_status, lim)))
             return;
         tc_fence_after();
-        float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-        sum += exchange(sum);
+        // the row sum: both halves
+        uint32_t* slot = slots + (u % 3) * 128;
+        atomicAdd(reinterpret_cast<float*>(slot) + r, l);
+        if (!pair_meet()) return;
+        const float sum = __uint_as_float(slot[r]);
+        step_done();
         const float inv = sum > 0.f ? 1.f / sum : 0.f;
         const int64_t off = (static_cast<int64_t>(w.bh) * p.T + i) * D;
 #pragma unroll
-        for (int c2 = 0; c2 < D / 64; ++c2) {
-            const int c = 2 * c2 + g;   // this warp's 32-column slices of O
-            uint32_t o[32];
-            tmem_ld32(t_lane + kOCol + 32 * c, o);
+        for (int c16 = 0; c16 < D / kNW / 16; ++c16) {
+            const int col = (D / kNW) * g + 16 * c16;   // this warp's 16-column slices of O
+            uint32_t o[16];
+            tmem_ldred_max16(t_lane + kOCol + col, o);
             tmem_ld_wait();
             reg_fence(o);
             if (i >= p.T) continue;
             if (p.bf16_out) {
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.O) + off + 32 * c);
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.O) + off + col);
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
+                for (int c8 = 0; c8 < 2; ++c8) {
                     uint32_t wv[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -300,9 +376,9 @@ __device__ __forceinline__ void softmax_rows(const WindowParams& p, uint32_t tme
                     dst[c8] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
             } else {
-                float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.O) + off + 32 * c);
+                float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.O) + off + col);
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4)
+                for (int c4 = 0; c4 < 4; ++c4)
                     dst[c4] = make_float4(__uint_as_float(o[4 * c4]) * inv, __uint_as_float(o[4 * c4 + 1]) * inv,
                                           __uint_as_float(o[4 * c4 + 2]) * inv,
                                           __uint_as_float(o[4 * c4 + 3]) * inv);
@@ -321,7 +397,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
     constexpr int KA = C::KA;
     constexpr uint32_t IDESC_S = idesc_bf16_f32(kWM, kWN);
     constexpr uint32_t IDESC_S2 = idesc_bf16_f32(kWM, 2 * kWN);
-    constexpr uint32_t IDESC_O = idesc_bf16_f32_bmn(kWM, D);
+    // P V: V^T K-major (D 64, turned in shared memory) or V MN-major (D 128)
+    constexpr uint32_t IDESC_O = C::VT ? idesc_bf16_f32(kWM, D) : idesc_bf16_f32_bmn(kWM, D);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -332,9 +409,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
     uint64_t* s_full = bars + 6;     // S of the item in TMEM
     uint64_t* o_full = bars + 7;     // every MMA of the item done: O in TMEM
     uint64_t* p_full = bars + 8;     // [3] weights of key tile t in TMEM (one arrive per softmax warp)
-    uint64_t* x_bar = bars + 11;     // the softmax warps' exchange of row sums
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
-    float* xch = reinterpret_cast<float*>(smem + C::XCH_OFF);
+    uint64_t* pair_bar = bars + 11;  // [4] the two softmax warps of a lane quarter meet
+    uint64_t* pv_done = bars + 15;   // [3] the MMAs up to key tile t's P V are done
+    uint64_t* vt_full = bars + 18;   // [stage] value tiles turned K-major (D 64)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+    uint32_t* slots = reinterpret_cast<uint32_t*>(smem + C::XCH_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -345,11 +424,15 @@ __global__ void __launch_bounds__(kWThreads, 1)
             mbar_init(full_qk + s, 1);
             mbar_init(full_v + s, 1);
             mbar_init(empty + s, 1);
+            mbar_init(vt_full + s, 1);
         }
         mbar_init(s_full, 1);
         mbar_init(o_full, 1);
-        for (int t = 0; t < kWMaxTiles; ++t) mbar_init(p_full + t, 8);
-        mbar_init(x_bar, 256);
+        for (int t = 0; t < kWMaxTiles; ++t) {
+            mbar_init(p_full + t, 4 * kNW);
+            mbar_init(pv_done + t, 1);
+        }
+        for (int q = 0; q < 4; ++q) mbar_init(pair_bar + q, 32 * kNW);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -358,6 +441,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
     }
+    for (int x = threadIdx.x; x < 3 * 128; x += kWThreads) slots[x] = 0u;
     if (warp == 1) tmem_alloc(tmem_slot, kWTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -365,40 +449,61 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA
-        if (lane == 0) {
-            int n = 0;
-            for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++n) {
-                const int s = n % C::STAGES;
-                const uint32_t use = static_cast<uint32_t>(n / C::STAGES);
-                if (use > 0 &&
-                    !mbar_wait_bounded(empty + s, (use - 1) & 1, abort_flag, p.dev_status, lim))
-                    break;
-                const WinItem w = win_item(p, item);
-                uint8_t* st = smem + s * C::STAGE;
-                mbar_arrive_expect_tx(full_qk + s, C::TILE * (1 + w.nkt));
-#pragma unroll
-                for (int a = 0; a < KA; ++a)
-                    tma_load_3d(st + C::Q_OFF + a * kSliceBytes, &qmap, 64 * a, w.i0, w.bh, full_qk + s);
-                for (int t = 0; t < w.nkt; ++t)
+        // ------------------------------------------------ TMA (lane 0); for D 64 the
+        // whole warp then turns each landed value tile K-major (see vt_transpose_half)
+        int n = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++n) {
+            const int s = n % C::STAGES;
+            const uint32_t use = static_cast<uint32_t>(n / C::STAGES);
+            const WinItem w = win_item(p, item);
+            uint8_t* st = smem + s * C::STAGE;
+            if (lane == 0) {
+                if (use > 0) ok = mbar_wait_bounded(empty + s, (use - 1) & 1, abort_flag, p.dev_status, lim);
+                if (ok) {
+                    mbar_arrive_expect_tx(full_qk + s, C::TILE * (1 + w.nkt));
 #pragma unroll
                     for (int a = 0; a < KA; ++a)
-                        tma_load_3d(st + C::K_OFF + a * C::SLICE3 + t * kSliceBytes, &kmap, 64 * a,
-                                    (w.kt0 + t) * kWN, w.bh, full_qk + s);
-                mbar_arrive_expect_tx(full_v + s, C::TILE * w.nkt);
-                for (int t = 0; t < w.nkt; ++t)
+                        tma_load_3d(st + C::Q_OFF + a * kSliceBytes, &qmap, 64 * a, w.i0, w.bh, full_qk + s);
+                    for (int t = 0; t < w.nkt; ++t)
 #pragma unroll
-                    for (int a = 0; a < KA; ++a)
-                        tma_load_3d(st + C::V_OFF + a * C::SLICE3 + t * kSliceBytes, &vmap, 64 * a,
-                                    (w.kt0 + t) * kWN, w.bh, full_v + s);
+                        for (int a = 0; a < KA; ++a)
+                            tma_load_3d(st + C::K_OFF + a * C::SLICE3 + t * kSliceBytes, &kmap, 64 * a,
+                                        (w.kt0 + t) * kWN, w.bh, full_qk + s);
+                    mbar_arrive_expect_tx(full_v + s, C::TILE * w.nkt);
+                    for (int t = 0; t < w.nkt; ++t)
+#pragma unroll
+                        for (int a = 0; a < KA; ++a)
+                            tma_load_3d(st + C::V_OFF + a * C::SLICE3 + t * kSliceBytes, &vmap, 64 * a,
+                                        (w.kt0 + t) * kWN, w.bh, full_v + s);
+                }
             }
-            // the copies land before the block may exit: the last use of each stage
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                ok = false;
+                break;
+            }
+            if constexpr (C::VT) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(full_v + s, use & 1, abort_flag, p.dev_status, lim))) {
+                    ok = false;
+                    ++n;   // this item's copies were issued
+                    break;
+                }
+                for (int t = 0; t < w.nkt; ++t)
+                    for (int h = 0; h < 2; ++h)
+                        vt_transpose_half(smem_u32(st + C::V_OFF + t * kSliceBytes + h * (kSliceBytes / 2)), lane);
+                fence_proxy_async_smem();   // the MMAs read the tiles through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(vt_full + s);
+            }
+        }
+        // the copies land before the block may exit: the last use of each stage
+        if (lane == 0)
             for (int s = 0; s < C::STAGES && s < n; ++s) {
                 const uint32_t last = static_cast<uint32_t>((n - 1 - s) / C::STAGES);
                 mbar_wait_bounded(full_qk + s, last & 1, nullptr, p.dev_status, lim);
                 mbar_wait_bounded(full_v + s, last & 1, nullptr, p.dev_status, lim);
             }
-        }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA
         if (lane == 0) {
@@ -432,7 +537,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                     }
                 }
                 mma_commit(s_full);
-                ok = mbar_wait_bounded(full_v + s, use & 1, abort_flag, p.dev_status, lim);
+                ok = mbar_wait_bounded(C::VT ? vt_full + s : full_v + s, use & 1, abort_flag, p.dev_status, lim);
                 for (int t = 0; ok && t < w.nkt; ++t) {
                     if (!mbar_wait_bounded(p_full + t, (pt >> t) & 1, abort_flag, p.dev_status, lim)) {
                         ok = false;
@@ -445,13 +550,19 @@ __global__ void __launch_bounds__(kWThreads, 1)
                         // keys 16 s8 .. 16 s8 + 15 of the tile: their hi and lo
                         // weights (see the softmax warps' layout)
                         const uint32_t hi = t * kWN + 32 * (s8 / 2) + 8 * (s8 % 2);
-                        // all D columns of V in one operand: its 64-column
-                        // slices are SLICE3 bytes apart
-                        const uint64_t bd = smem_desc_mn_sw128(
-                            smem_u32(st + C::V_OFF + t * kSliceBytes + s8 * 16 * 128), C::SLICE3);
+                        // D 64: the 16 keys are a 32-byte K slice of V^T's
+                        // 64-key half s8 / 4. D 128: all columns of V in one
+                        // MN-major operand, its 64-column slices SLICE3 bytes apart
+                        const uint64_t bd =
+                            C::VT ? smem_desc_k_sw128(smem_u32(st + C::V_OFF + t * kSliceBytes +
+                                                               (s8 / 4) * (kSliceBytes / 2))) +
+                                        (((s8 % 4) * 32) >> 4)
+                                  : smem_desc_mn_sw128(smem_u32(st + C::V_OFF + t * kSliceBytes + s8 * 16 * 128),
+                                                       C::SLICE3);
                         mma_bf16_ta(tmem_base + kOCol, tmem_base + hi, bd, IDESC_O, (t | s8) != 0);
                         mma_bf16_ta(tmem_base + kOCol, tmem_base + hi + 16, bd, IDESC_O, 1);
                     }
+                    mma_commit(pv_done + t);   // for a softmax warp that rescales O
                 }
                 // every MMA of the item (also after a stop) is tracked by o_full
                 mma_commit(o_full);
@@ -463,7 +574,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 mbar_wait_bounded(o_full, (committed - 1) & 1, nullptr, p.dev_status, lim);
         }
     } else {
-        softmax_rows<D>(p, tmem_base, warp, lane, s_full, o_full, p_full, x_bar, xch, abort_flag, lim);
+        softmax_rows<D>(p, tmem_base, warp, lane, s_full, o_full, p_full, pv_done, pair_bar, slots,
+                        abort_flag, lim);
     }
 
     tc_fence_before();
