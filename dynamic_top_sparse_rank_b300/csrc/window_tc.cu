@@ -5,30 +5,30 @@
 // mhpq.cn/news/1098205, section 3.2), computed as dense tiles of the band.
 //
 // Work item: one (head, 128-query tile). Its band spans at most three 128-key
-// tiles (the host sends wider bands and fp32 to the gather kernel), so the
-// whole band's scores fit in TMEM and the softmax needs no running rescale.
-// The kernel is persistent (one CTA per SM, items round-robin), so that the
-// loads of the next item overlap the softmax of this one:
+// tiles (the host sends wider bands and fp32 to the gather kernel). Both
+// kernels are persistent, take items round-robin, keep the weights in TMEM
+// (the A operand of tcgen05.mma may sit in TMEM) and run one pass over the
+// key tiles with a running shift per row (the online softmax):
+// p = 2^((s - M) * scale * log2 e) in fp32, written over the tile's scores
+// as two bf16 parts, hi = p truncated to bf16 and lo = bf16(p - hi), so that
+// P V = hi V + lo V keeps p to about 2^-16 (one bf16 P would cost 2^-9, too
+// much for rows with few keys); the row sum in fp32; O divided by it at the
+// end and stored in bf16 or fp32.
+//
+// window_tc_kernel (head size 128): one CTA per SM, 576 threads.
 //   warp 0  TMA: per item the query tile, the band's key tiles and value
 //           tiles (3-D maps [head][row][64-column slice], 128-byte swizzle;
-//           rows outside the sequence read as zeros) into one of two
-//           shared-memory stages (D 64; one stage of twice the size for
-//           D 128);
+//           rows outside the sequence read as zeros) into one 224 KB stage;
 //   warp 1  allocates TMEM and issues the MMAs: S = Q K^T, one 128x128 fp32
 //           accumulator per key tile (columns 0..383; two tiles per N=256
-//           MMA), then O = P V (M=128, N=D, K=16 steps) into columns 384..,
-//           with P read from TMEM (the A operand of tcgen05.mma may sit in
-//           TMEM) and V MN-major straight from its TMA layout;
-//   warps 2-9  one query row per thread, two warps per row splitting its key
-//           chunks and output columns: one pass over the key tiles with a
-//           running shift per row (the online softmax; see softmax_rows):
-//           p = 2^((s - M) * scale * log2 e) in fp32, written back over that
-//           tile's S columns as two bf16 parts, hi = p truncated to bf16 and
-//           lo = bf16(p - hi), so that P V = hi V + lo V keeps p to about 2^-16
-//           (one bf16 P would cost 2^-9, too much for rows with few keys);
-//           each tile goes to the MMA warp once written, so its P V runs
-//           under the next tile's softmax; the row sum is taken in fp32; after
-//           the last MMA, O divided by the sum and stored in bf16 or fp32.
+//           MMA), then O = P V (M=128, N=128, K=16 steps) into columns
+//           384..511 with V MN-major straight from its TMA layout;
+//   warps 2-17  one query row per thread, four warps per row splitting its
+//           key chunks and output columns (softmax_rows); each key tile goes
+//           to the MMA warp once written, so its P V runs under the next
+//           tile's softmax.
+// window_tc64_kernel (head size 64): two CTAs per SM, each on 256 TMEM
+// columns and one key tile at a time (see the notes above it).
 // Every mbarrier wait is bounded; a wait that runs out reports
 // SSA_DEV_WAIT_LIMIT, stops the other roles and TMEM is freed.
 #include <float.h>
@@ -64,7 +64,6 @@ template <int D>
 struct WinCfg {
     static constexpr int KA = D / 64;                          // 64-column slices
     static constexpr int STAGES = D == 64 ? 2 : 1;
-    static constexpr bool VT = D == 64;                        // V turned K-major in shared memory
     static constexpr uint32_t TILE = KA * kSliceBytes;         // one 128-row tile
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t SLICE3 = kWMaxTiles * kSliceBytes;   // one slice of the three tiles
@@ -127,63 +126,84 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // Turns 64 keys x 64 columns of a value tile, as TMA wrote it (row = key,
 // 128 bytes of 64 bf16 columns, 128-byte swizzle: 16-byte chunk c of row r at
 // r * 128 + (c ^ (r & 7)) * 16), into the K-major operand of the same 8 KB
-// (row = column d, its 64 keys in 128 bytes, the same swizzle), in place. The
-// 8x8 blocks go through registers: ldmatrix .trans reads block (keys 8kb..,
-// columns 8db..) transposed, stmatrix writes it as block (columns 8db..,
-// keys 8kb..); the whole half is read before any of it is written. The P V
-// MMAs read V^T K-major at 73.5 cycles per M=128, K=16 instruction against
-// 125 for V MN-major (measured at N=64 and N=128).
+// (row = column d, its 64 keys in 128 bytes, the same swizzle), in place.
+// In 8x8 blocks: block (keys 8kb.., columns 8db..) transposed is block
+// (columns 8db.., keys 8kb..) of the result, which sits exactly where block
+// (db, kb) of the source was; so a block and its mirror are read together
+// (ldmatrix .trans) and written crosswise (stmatrix), four pairs at a time
+// (the eight diagonal blocks in one batch). The P V MMAs read V^T K-major at
+// 73.5 cycles per M=128, K=16 instruction against 125 for V MN-major
+// (measured at N=64 and N=128).
 __device__ __forceinline__ void vt_transpose_half(uint32_t base, int lane) {
     const int m = lane >> 3, i = lane & 7;   // the lane's matrix of an x4 group and its row
-    uint32_t r[16][4];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        const int kb = q >> 1, db = (q & 1) * 4 + m;
-        const uint32_t src = base + (8 * kb + i) * 128 + ((db ^ i) << 4);
+    auto src = [&](int kb, int db) { return base + (8 * kb + i) * 128 + ((db ^ i) << 4); };
+    auto ld4 = [&](uint32_t addr, uint32_t (&r)[4]) {
         asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(r[q][0]), "=r"(r[q][1]), "=r"(r[q][2]), "=r"(r[q][3])
-                     : "r"(src)
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "r"(addr)
                      : "memory");
+    };
+    auto st4 = [&](uint32_t addr, const uint32_t (&r)[4]) {
+        asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                     "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                     : "memory");
+    };
+    // the 28 blocks above the diagonal, four per batch (pair index q: the
+    // q-th (kb, db) with kb < db in row-major order)
+#pragma unroll 1
+    for (int bt = 0; bt < 7; ++bt) {
+        int q = 4 * bt + m, kb = 0;
+        while (q >= 7 - kb) {   // row kb holds 7 - kb blocks above the diagonal
+            q -= 7 - kb;
+            ++kb;
+        }
+        const int db = kb + 1 + q;
+        uint32_t a[4], b[4];
+        ld4(src(kb, db), a);   // lane group m: block (kb, db) of its pair
+        ld4(src(db, kb), b);   // and its mirror
+        __syncwarp();
+        st4(src(db, kb), a);   // (kb, db) transposed goes where (db, kb) was
+        st4(src(kb, db), b);
+        __syncwarp();
     }
-    __syncwarp();
+    // the diagonal blocks, in place
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        const int kb = q >> 1, db = (q & 1) * 4 + m;
-        const uint32_t dst = base + (8 * db + i) * 128 + ((kb ^ i) << 4);
-        asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                     "r"(r[q][0]), "r"(r[q][1]), "r"(r[q][2]), "r"(r[q][3])
-                     : "memory");
+    for (int h = 0; h < 2; ++h) {
+        const int kb = 4 * h + m;
+        uint32_t a[4];
+        ld4(src(kb, kb), a);
+        __syncwarp();
+        st4(src(kb, kb), a);
+        __syncwarp();
     }
-    __syncwarp();
 }
 
-// The softmax warps: eight, two per TMEM lane quarter (warp w reads lanes
-// 32 (w % 4) .. 32 (w % 4) + 31, one query row per thread); warp half g
-// (0 for warps 2-5, 1 for warps 6-9) takes the 32-key chunks 2g and 2g + 1 of
-// every key tile and the output columns of its half.
+// The softmax warps of window_tc_kernel: kNW per TMEM lane quarter (warp w
+// reads lanes 32 (w % 4) .. 32 (w % 4) + 31, one query row per thread); warp
+// g of a quarter (g = (w - 2) / 4) takes kCPW 32-key chunks of every key tile
+// (chunks kCPW g ..) and D / kNW output columns.
 //
 // One pass, key tile by key tile, with a running shift M per row (the
-// online softmax): each warp takes the maximum of its two chunks (a chunk
-// inside every row's band of the warp from tcgen05.ld.red, a partial one
-// masked, one outside every band skipped), the pair combines the two through
-// shared memory (atomicMax on order keys) and meets at a bounded per-pair
-// barrier before either overwrites a score, so both warps hold the same tile
-// maximum and take the same decisions. M moves only when the tile maximum
-// exceeds it by more than 2^8 in weight: then the MMAs of the earlier tiles
-// are waited for and the row's O (this warp's columns) and partial sum are
-// scaled down, so weights stay below 2^8 and are exact at the maximum (the
-// first tile sets M to its maximum; w = 0 gives weight 1 and O = V exactly).
-// The weights are written over the warp's own S columns (a chunk's 16 hi
-// words, two keys per word with the lower key in the low half, in its first
-// 16 columns, its 16 lo words in the next 16) and each key tile is handed to
-// the MMA warp once both warps of every pair have written it. At the end the
-// two partial row sums meet the same way (atomicAdd), and each warp writes
-// its half of the output columns.
+// online softmax): each warp takes the maximum of its chunks (a chunk inside
+// every row's band of the warp from tcgen05.ld.red, a partial one masked,
+// one outside every band skipped), the quarter's warps combine them through
+// shared memory (atomicMax on order keys) and meet at a bounded per-quarter
+// barrier before any overwrites a score, so all hold the same tile maximum
+// and take the same decisions. M moves only when the tile maximum exceeds it
+// by more than 2^8 in weight: then the MMAs of the earlier tiles are waited
+// for and the row's O (this warp's columns) and partial sum are scaled down,
+// so weights stay below 2^8 and are exact at the maximum (the first tile sets
+// M to its maximum; w = 0 gives weight 1 and O = V exactly). The weights are
+// written over the warp's own S columns (a chunk's 16 hi words, two keys per
+// word with the lower key in the low half, in its first 16 columns, its 16
+// lo words in the next 16) and each key tile is handed to the MMA warp once
+// every warp has written it. At the end the partial row sums meet the same
+// way (atomicAdd), and each warp writes its output columns.
 //
-// Shared slots: three rotating 128-row words per pair use (step u uses slot
-// u mod 3); after the barrier of step u, warp 0 of the pair clears the slot
-// of step u - 1, which both have read before arriving, and which is next
-// used at step u + 2, after the partner has passed step u + 1's barrier.
+// Shared slots: three rotating 128-row words per quarter step (step u uses
+// slot u mod 3); after the barrier of step u, warp 0 of the quarter clears
+// the slot of step u - 1, which all have read before arriving, and which is
+// next used at step u + 2, after the others have passed step u + 1's barrier.
 template <int D>
 __device__ __forceinline__ void softmax_rows(const WindowParams& p, uint32_t tmem_base, int warp,
                                              int lane, uint64_t* s_full, uint64_t* o_full,
@@ -397,8 +417,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     constexpr int KA = C::KA;
     constexpr uint32_t IDESC_S = idesc_bf16_f32(kWM, kWN);
     constexpr uint32_t IDESC_S2 = idesc_bf16_f32(kWM, 2 * kWN);
-    // P V: V^T K-major (D 64, turned in shared memory) or V MN-major (D 128)
-    constexpr uint32_t IDESC_O = C::VT ? idesc_bf16_f32(kWM, D) : idesc_bf16_f32_bmn(kWM, D);
+    constexpr uint32_t IDESC_O = idesc_bf16_f32_bmn(kWM, D);   // V MN-major
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -411,7 +430,6 @@ __global__ void __launch_bounds__(kWThreads, 1)
     uint64_t* p_full = bars + 8;     // [3] weights of key tile t in TMEM (one arrive per softmax warp)
     uint64_t* pair_bar = bars + 11;  // [4] the two softmax warps of a lane quarter meet
     uint64_t* pv_done = bars + 15;   // [3] the MMAs up to key tile t's P V are done
-    uint64_t* vt_full = bars + 18;   // [stage] value tiles turned K-major (D 64)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
     uint32_t* slots = reinterpret_cast<uint32_t*>(smem + C::XCH_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -424,7 +442,6 @@ __global__ void __launch_bounds__(kWThreads, 1)
             mbar_init(full_qk + s, 1);
             mbar_init(full_v + s, 1);
             mbar_init(empty + s, 1);
-            mbar_init(vt_full + s, 1);
         }
         mbar_init(s_full, 1);
         mbar_init(o_full, 1);
@@ -482,19 +499,6 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 ok = false;
                 break;
             }
-            if constexpr (C::VT) {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(full_v + s, use & 1, abort_flag, p.dev_status, lim))) {
-                    ok = false;
-                    ++n;   // this item's copies were issued
-                    break;
-                }
-                for (int t = 0; t < w.nkt; ++t)
-                    for (int h = 0; h < 2; ++h)
-                        vt_transpose_half(smem_u32(st + C::V_OFF + t * kSliceBytes + h * (kSliceBytes / 2)), lane);
-                fence_proxy_async_smem();   // the MMAs read the tiles through the async proxy
-                __syncwarp();
-                if (lane == 0) mbar_arrive(vt_full + s);
-            }
         }
         // the copies land before the block may exit: the last use of each stage
         if (lane == 0)
@@ -537,7 +541,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                     }
                 }
                 mma_commit(s_full);
-                ok = mbar_wait_bounded(C::VT ? vt_full + s : full_v + s, use & 1, abort_flag, p.dev_status, lim);
+                ok = mbar_wait_bounded(full_v + s, use & 1, abort_flag, p.dev_status, lim);
                 for (int t = 0; ok && t < w.nkt; ++t) {
                     if (!mbar_wait_bounded(p_full + t, (pt >> t) & 1, abort_flag, p.dev_status, lim)) {
                         ok = false;
@@ -550,15 +554,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
                         // keys 16 s8 .. 16 s8 + 15 of the tile: their hi and lo
                         // weights (see the softmax warps' layout)
                         const uint32_t hi = t * kWN + 32 * (s8 / 2) + 8 * (s8 % 2);
-                        // D 64: the 16 keys are a 32-byte K slice of V^T's
-                        // 64-key half s8 / 4. D 128: all columns of V in one
-                        // MN-major operand, its 64-column slices SLICE3 bytes apart
-                        const uint64_t bd =
-                            C::VT ? smem_desc_k_sw128(smem_u32(st + C::V_OFF + t * kSliceBytes +
-                                                               (s8 / 4) * (kSliceBytes / 2))) +
-                                        (((s8 % 4) * 32) >> 4)
-                                  : smem_desc_mn_sw128(smem_u32(st + C::V_OFF + t * kSliceBytes + s8 * 16 * 128),
-                                                       C::SLICE3);
+                        // all D columns of V in one MN-major operand, its
+                        // 64-column slices SLICE3 bytes apart
+                        const uint64_t bd = smem_desc_mn_sw128(
+                            smem_u32(st + C::V_OFF + t * kSliceBytes + s8 * 16 * 128), C::SLICE3);
                         mma_bf16_ta(tmem_base + kOCol, tmem_base + hi, bd, IDESC_O, (t | s8) != 0);
                         mma_bf16_ta(tmem_base + kOCol, tmem_base + hi + 16, bd, IDESC_O, 1);
                     }
@@ -586,6 +585,395 @@ __global__ void __launch_bounds__(kWThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------- D 64: two CTAs per SM
+//
+// For head size 64 the item's chain of dependent steps (scores, softmax, P V
+// per key tile), not any one unit, sets the pace of window_tc_kernel, and one
+// item's scores fill 384 of the 512 TMEM columns. window_tc64_kernel runs two
+// CTAs per SM instead, each on 256 TMEM columns and about 83 KB of shared
+// memory, so that one CTA's softmax runs while the other's MMAs and loads do:
+//   - one key tile at a time: S(t) = Q K(t)^T into columns 0..127, the
+//     weights over them, P(t) V(t) into O (columns 128..191); S(t+1) is
+//     issued behind P(t) V(t), which reads those columns, and tcgen05.mma
+//     instructions of one thread run in issue order;
+//   - the TMA warp streams the query tile and key and value tiles through
+//     rings of two slots each, turning each value tile K-major;
+//   - the softmax warps (eight, two per lane quarter) take the running-shift
+//     softmax of softmax_rows tile by tile; a rescale of O needs no extra
+//     wait, as the tile's S commit follows the previous tile's P V.
+namespace w64 {
+constexpr int kThreads = 320;                   // TMA warp, MMA warp, 8 softmax warps
+constexpr int kWarps = 2;                       // softmax warps per lane quarter
+constexpr uint32_t kTile = kSliceBytes;         // one 128-row x 64-column bf16 tile
+constexpr uint32_t Q_OFF = 0;
+constexpr uint32_t K_OFF = Q_OFF + kTile;       // [2] key tile ring
+constexpr uint32_t V_OFF = K_OFF + 2 * kTile;   // [2] value tile ring (turned K-major)
+constexpr uint32_t BAR_OFF = V_OFF + 2 * kTile;
+constexpr uint32_t XCH_OFF = BAR_OFF + 256;     // [3 slots][128 rows] 32-bit words
+constexpr uint32_t SMEM = XCH_OFF + 3 * 128 * 4 + 1024;   // + alignment slack
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kOut = 128;                  // first TMEM column of O
+static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
+}  // namespace w64
+
+__device__ __forceinline__ void softmax_rows64(const WindowParams& p, uint32_t tmem_base, int warp,
+                                               int lane, uint64_t* s_full, uint64_t* o_full,
+                                               uint64_t* p_full, uint64_t* pair_bar,
+                                               uint32_t* slots, volatile int* abort_flag,
+                                               uint64_t lim) {
+    using namespace w64;
+    const int quarter = warp & 3;   // TMEM lane quarter of this warp
+    const int g = (warp - 2) >> 2;  // which half of each tile's chunks and of the output
+    const int r = quarter * 32 + lane;
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    constexpr float kRescaleLog2 = 8.f;   // weights stay below 2^8
+    uint32_t u = 0;                        // quarter steps taken (see softmax_rows)
+    uint32_t sc = 0;                       // S tiles consumed (s_full phases)
+    auto quarter_meet = [&]() -> bool {
+        tc_fence_before();
+        mbar_arrive(pair_bar + quarter);
+        const bool ok =
+            __all_sync(0xffffffffu, mbar_wait_bounded(pair_bar + quarter, u & 1, abort_flag, p.dev_status, lim));
+        tc_fence_after();
+        return ok;
+    };
+    auto step_done = [&]() {
+        if (g == 0) slots[((u + 2) % 3) * 128 + r] = 0u;
+        ++u;
+    };
+    int n = 0;
+    for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++n) {
+        const WinItem w = win_item(p, item);
+        const int i = w.i0 + r;
+        const int jlo = i - p.wl > 0 ? i - p.wl : 0;
+        const int jhi = i + p.wr < p.T - 1 ? i + p.wr : p.T - 1;
+        const int iw = w.i0 + quarter * 32;
+        const int wlo = iw - p.wl > 0 ? iw - p.wl : 0;
+        const int whi = iw + 31 + p.wr < p.T - 1 ? iw + 31 + p.wr : p.T - 1;
+        const int flo = iw + 31 - p.wl > 0 ? iw + 31 - p.wl : 0;
+        const int fhi = iw + p.wr < p.T - 1 ? iw + p.wr : p.T - 1;
+        const int kbase = w.kt0 * kWN;
+        auto chunk_class = [&](int ch) {   // 0 outside, 1 inside, 2 partial (as softmax_rows)
+            const int j0 = kbase + 32 * ch;
+            if (j0 + 31 < wlo || j0 > whi) return 0;
+            return (j0 >= flo && j0 + 31 <= fhi) ? 1 : 2;
+        };
+        float M = -INFINITY;   // the row's shift
+        float l = 0.f;         // this warp's partial row sum
+        for (int t = 0; t < w.nkt; ++t) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full, sc & 1, abort_flag, p.dev_status, lim)))
+                return;
+            ++sc;
+            tc_fence_after();
+            // the maximum of this warp's two chunks, one chunk per load (the
+            // scores are loaded again for the weights: a TMEM load and its
+            // wait take about 28 ns, registers are short at two CTAs per SM)
+            int cls[2];
+            float m = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int cc = 2 * g + c;   // chunk of the tile
+                cls[c] = chunk_class(4 * t + cc);
+                const uint32_t col = t_lane + 32 * cc;
+                uint32_t v[32];
+                if (cls[c] == 1) {
+                    float m0 = tmem_ldred_max16(col, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    float m1 = tmem_ldred_max16(col + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    tmem_ld_wait();
+                    reg_fence_f(m0);
+                    reg_fence_f(m1);
+                    m = fmax3(m, m0, m1);
+                } else if (cls[c] == 2) {
+                    tmem_ld32(col, v);
+                    tmem_ld_wait();
+                    reg_fence(v);
+                    const int j0 = kbase + 32 * (4 * t + cc);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (j0 + e >= jlo && j0 + e <= jhi) m = fmaxf(m, __uint_as_float(v[e]));
+                }
+            }
+            uint32_t* slot = slots + (u % 3) * 128;
+            if (m > -INFINITY) atomicMax(slot + r, f32_order_key(m));
+            if (!quarter_meet()) return;
+            const uint32_t mk = slot[r];
+            step_done();
+            const float mt = mk == 0u ? -INFINITY : order_key_f32(mk);
+            const bool move = mt > -INFINITY && (M == -INFINITY || (mt - M) * p.scale_log2 > kRescaleLog2);
+            if (__any_sync(0xffffffffu, move && M > -INFINITY)) {
+                // this tile's S landed after the previous tile's P V: O holds
+                // the earlier tiles' sums at the old shift; scale this warp's
+                // columns of the moved rows
+                const float f = move && M > -INFINITY ? ex2_approx((M - mt) * p.scale_log2) : 1.f;
+                const uint32_t ocol = t_lane + w64::kOut + 32 * g;
+                uint32_t o[32];
+                tmem_ld32(ocol, o);
+                tmem_ld_wait();
+                reg_fence(o);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                tmem_st32(ocol, o);
+                tmem_st_wait();
+                l *= f;
+            }
+            if (move) M = mt;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int cc = 2 * g + c;
+                uint32_t whi[16], wlo[16];
+                if (cls[c]) {
+                    uint32_t v[32];
+                    tmem_ld32(t_lane + 32 * cc, v);
+                    tmem_ld_wait();
+                    reg_fence(v);
+                    const int j0 = kbase + 32 * (4 * t + cc);
+                    const bool mask = cls[c] == 2;
+                    float s2[2] = {0.f, 0.f};
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        float pv[2];
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            const int j = j0 + 2 * q + b;
+                            const float x = (__uint_as_float(v[2 * q + b]) - M) * p.scale_log2;
+                            pv[b] = ex2_approx(!mask || (j >= jlo && j <= jhi) ? x : -INFINITY);
+                        }
+                        s2[q & 1] += pv[0] + pv[1];
+                        const uint32_t b0 = __float_as_uint(pv[0]), b1 = __float_as_uint(pv[1]);
+                        whi[q] = __byte_perm(b0, b1, 0x7632);
+                        const __nv_bfloat162 lo = __floats2bfloat162_rn(
+                            pv[0] - __uint_as_float(b0 & 0xFFFF0000u), pv[1] - __uint_as_float(b1 & 0xFFFF0000u));
+                        wlo[q] = *reinterpret_cast<const uint32_t*>(&lo);
+                    }
+                    l += s2[0] + s2[1];
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) whi[q] = wlo[q] = 0u;
+                }
+                tmem_st16(t_lane + 32 * cc, whi);
+                tmem_st16(t_lane + 32 * cc + 16, wlo);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_full, n & 1, abort_flag, p.dev_status, lim)))
+            return;
+        tc_fence_after();
+        uint32_t* slot = slots + (u % 3) * 128;
+        atomicAdd(reinterpret_cast<float*>(slot) + r, l);
+        if (!quarter_meet()) return;
+        const float sum = __uint_as_float(slot[r]);
+        step_done();
+        const float inv = sum > 0.f ? 1.f / sum : 0.f;
+        uint32_t o[32];
+        tmem_ld32(t_lane + w64::kOut + 32 * g, o);
+        tmem_ld_wait();
+        reg_fence(o);
+        tc_fence_before();   // the O columns are read: the next item's MMAs may write them
+        if (i < p.T) {
+            const int64_t off = (static_cast<int64_t>(w.bh) * p.T + i) * 64 + 32 * g;
+            if (p.bf16_out) {
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.O) + off);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int d = c8 * 8 + q * 2;
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[d]) * inv,
+                                                                        __uint_as_float(o[d + 1]) * inv);
+                        wv[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                    }
+                    dst[c8] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
+            } else {
+                float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.O) + off);
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4)
+                    dst[c4] = make_float4(__uint_as_float(o[4 * c4]) * inv, __uint_as_float(o[4 * c4 + 1]) * inv,
+                                          __uint_as_float(o[4 * c4 + 2]) * inv,
+                                          __uint_as_float(o[4 * c4 + 3]) * inv);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(w64::kThreads, 2)
+    window_tc64_kernel(const __grid_constant__ CUtensorMap qmap,
+                       const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap, const WindowParams p) {
+    using namespace w64;
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(kWM, kWN);
+    constexpr uint32_t IDESC_O = idesc_bf16_f32(kWM, 64);   // V^T K-major
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+    uint64_t* q_full = bars;         // the query tile landed
+    uint64_t* q_empty = bars + 1;    // the item's S MMAs are done
+    uint64_t* k_full = bars + 2;     // [2] key tile landed
+    uint64_t* k_empty = bars + 4;    // [2] its S MMA is done
+    uint64_t* v_full = bars + 6;     // [2] value tile landed
+    uint64_t* vt_full = bars + 8;    // [2] value tile turned K-major
+    uint64_t* v_empty = bars + 10;   // [2] its P V MMAs are done
+    uint64_t* s_full = bars + 12;    // S of the current key tile in TMEM
+    uint64_t* p_full = bars + 13;    // its weights in TMEM (one arrive per softmax warp)
+    uint64_t* o_full = bars + 14;    // every MMA of the item done
+    uint64_t* pair_bar = bars + 15;  // [4] the two softmax warps of a lane quarter meet
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint32_t* slots = reinterpret_cast<uint32_t*>(smem + XCH_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t lim = p.wait_limit_ns ? p.wait_limit_ns : kWDefaultWaitNs;
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(k_full + s, 1);
+            mbar_init(k_empty + s, 1);
+            mbar_init(v_full + s, 1);
+            mbar_init(vt_full + s, 1);
+            mbar_init(v_empty + s, 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 4 * w64::kWarps);
+        mbar_init(o_full, 1);
+        for (int q = 0; q < 4; ++q) mbar_init(pair_bar + q, 32 * w64::kWarps);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&qmap);
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    for (int x = threadIdx.x; x < 3 * 128; x += kThreads) slots[x] = 0u;
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA (lane 0) and the
+        // turning of each landed value tile K-major (whole warp)
+        int n = 0;
+        uint32_t kc = 0, vc = 0;   // key and value tiles issued
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++n) {
+            const WinItem w = win_item(p, item);
+            if (lane == 0) {
+                if (n > 0) ok = mbar_wait_bounded(q_empty, (n - 1) & 1, abort_flag, p.dev_status, lim);
+                if (ok) {
+                    mbar_arrive_expect_tx(q_full, kTile);
+                    tma_load_3d(smem + Q_OFF, &qmap, 0, w.i0, w.bh, q_full);
+                }
+            }
+            for (int t = 0; ok && t < w.nkt; ++t) {
+                const uint32_t ks = kc & 1, vs = vc & 1;
+                if (lane == 0) {
+                    if (kc >= 2) ok = mbar_wait_bounded(k_empty + ks, ((kc >> 1) - 1) & 1, abort_flag, p.dev_status, lim);
+                    if (ok) {
+                        mbar_arrive_expect_tx(k_full + ks, kTile);
+                        tma_load_3d(smem + K_OFF + ks * kTile, &kmap, 0, (w.kt0 + t) * kWN, w.bh, k_full + ks);
+                    }
+                    if (ok && vc >= 2)
+                        ok = mbar_wait_bounded(v_empty + vs, ((vc >> 1) - 1) & 1, abort_flag, p.dev_status, lim);
+                    if (ok) {
+                        mbar_arrive_expect_tx(v_full + vs, kTile);
+                        tma_load_3d(smem + V_OFF + vs * kTile, &vmap, 0, (w.kt0 + t) * kWN, w.bh, v_full + vs);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                ++kc;
+                ++vc;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(v_full + vs, ((vc - 1) >> 1) & 1, abort_flag,
+                                                              p.dev_status, lim))) {
+                    ok = false;
+                    break;
+                }
+                for (int h = 0; h < 2; ++h)
+                    vt_transpose_half(smem_u32(smem + V_OFF + vs * kTile + h * (kTile / 2)), lane);
+                fence_proxy_async_smem();   // the MMAs read the tile through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(vt_full + vs);
+            }
+        }
+        // the copies land before the block may exit
+        if (lane == 0) {
+            if (n > 0) mbar_wait_bounded(q_full, (n - 1) & 1, nullptr, p.dev_status, lim);
+            for (uint32_t s = 0; s < 2; ++s)
+                if (kc > s) {
+                    mbar_wait_bounded(k_full + s, ((kc - 1 - s) >> 1) & 1, nullptr, p.dev_status, lim);
+                    mbar_wait_bounded(v_full + s, ((vc - 1 - s) >> 1) & 1, nullptr, p.dev_status, lim);
+                }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA
+        if (lane == 0) {
+            int n = 0;
+            uint32_t kc = 0, vc = 0, pc = 0, committed = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++n) {
+                const WinItem w = win_item(p, item);
+                if (!mbar_wait_bounded(q_full, n & 1, abort_flag, p.dev_status, lim)) break;
+                const uint64_t qd = smem_desc_k_sw128(smem_u32(smem + Q_OFF));
+                for (int t = 0; ok && t < w.nkt; ++t) {
+                    const uint32_t ks = kc & 1, vs = vc & 1;
+                    ok = mbar_wait_bounded(k_full + ks, (kc >> 1) & 1, abort_flag, p.dev_status, lim);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // S(t) over the previous tile's weights: issued behind its P V
+                    const uint64_t kd = smem_desc_k_sw128(smem_u32(smem + K_OFF + ks * kTile));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem_base, qd + ((kk * 32) >> 4), kd + ((kk * 32) >> 4), IDESC_S, kk != 0);
+                    mma_commit(k_empty + ks);
+                    if (t == w.nkt - 1) mma_commit(q_empty);
+                    mma_commit(s_full);
+                    ++kc;
+                    ok = mbar_wait_bounded(p_full, pc & 1, abort_flag, p.dev_status, lim) &&
+                         mbar_wait_bounded(vt_full + vs, (vc >> 1) & 1, abort_flag, p.dev_status, lim);
+                    ++pc;
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int s8 = 0; s8 < kWN / 16; ++s8) {
+                        // keys 16 s8 .. 16 s8 + 15: their hi and lo weights, and a
+                        // 32-byte K slice of V^T's 64-key half s8 / 4
+                        const uint32_t hi = 32 * (s8 / 2) + 8 * (s8 % 2);
+                        const uint64_t bd =
+                            smem_desc_k_sw128(smem_u32(smem + V_OFF + vs * kTile + (s8 / 4) * (kTile / 2))) +
+                            (((s8 % 4) * 32) >> 4);
+                        mma_bf16_ta(tmem_base + w64::kOut, tmem_base + hi, bd, IDESC_O, (t | s8) != 0);
+                        mma_bf16_ta(tmem_base + w64::kOut, tmem_base + hi + 16, bd, IDESC_O, 1);
+                    }
+                    mma_commit(v_empty + vs);
+                    ++vc;
+                }
+                // every MMA of the item (also after a stop) is tracked by o_full
+                mma_commit(o_full);
+                ++committed;
+            }
+            if (committed > 0) mbar_wait_bounded(o_full, (committed - 1) & 1, nullptr, p.dev_status, lim);
+        }
+    } else {
+        softmax_rows64(p, tmem_base, warp, lane, s_full, o_full, p_full, pair_bar, slots, abort_flag, lim);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 namespace {
@@ -605,6 +993,7 @@ bool make_map_3d(CUtensorMap* m, const void* base, int BH, int T, int D) {
 template <int D>
 cudaError_t window_tc_run(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
                           const WindowParams& p, cudaStream_t stream) {
+    static_assert(D == 128, "head size 64 runs window_tc64_kernel");
     const int sms = tile_sm_count();
     const int grid = p.items < sms ? p.items : sms;
     cudaError_t e = set_max_dyn_smem(reinterpret_cast<const void*>(window_tc_kernel<D>),
@@ -652,8 +1041,15 @@ cudaError_t window_tc_launch(const void* Q, const void* K, const void* V, void* 
     p.bf16_out = bf16_out ? 1 : 0;
     p.dev_status = dev_status;
     p.wait_limit_ns = 0;
-    return D == 64 ? window_tc_run<64>(qm, km, vm, p, stream)
-                   : window_tc_run<128>(qm, km, vm, p, stream);
+    if (D == 128) return window_tc_run<128>(qm, km, vm, p, stream);
+    // D 64: two CTAs per SM, each on its own items
+    const int64_t grid = std::min<int64_t>(items, 2 * static_cast<int64_t>(tile_sm_count()));
+    cudaError_t e = set_max_dyn_smem(reinterpret_cast<const void*>(window_tc64_kernel),
+                                     static_cast<int>(w64::SMEM));
+    if (e != cudaSuccess) return e;
+    TraceLaunch tr("window_tc", stream);
+    window_tc64_kernel<<<static_cast<unsigned>(grid), w64::kThreads, w64::SMEM, stream>>>(qm, km, vm, p);
+    return cudaGetLastError();
 }
 
 }  // namespace ssa
