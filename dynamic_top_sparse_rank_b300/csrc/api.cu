@@ -20,7 +20,8 @@ cudaError_t tile_select_launch(const uint16_t* gm, uint32_t* tau, int BH, int Tq
                                int causal, cudaStream_t stream);
 cudaError_t tile_sort_launch(const uint64_t* cand, const int32_t* cnt, int64_t rows, int Tq,
                              int Tk, int k, int causal, float scale, int32_t* idx, float* score,
-                             int64_t* ovf_list, int32_t* ovf_count, cudaStream_t stream);
+                             int64_t* ovf_list, int32_t* ovf_count, int32_t* dev_status,
+                             cudaStream_t stream);
 cudaError_t lowrank_project_launch(const void* x, const void* W, int64_t rows, int d_model, int P,
                                    void* out, int32_t* dev_status, cudaStream_t stream);
 bool window_tc_supported(bool bf16_in, int D, int T, int wl, int wr);
@@ -181,7 +182,7 @@ ssa_status ssa_score_topk(const void* q_low, const void* k_low, int dtype, int B
     if (e == cudaSuccess) e = ssa::tile_scores_launch(q_low, k_low, P, ssa::MODE_COLLECT, p, s);
     if (e == cudaSuccess)
         e = ssa::tile_sort_launch(cand, cnt, rows, Tq, Tk, k, p.causal, sc, idx, score,
-                                  ovf_list, ovf_count, s);
+                                  ovf_list, ovf_count, dev_status, s);
     if (e == cudaSuccess)
         e = ssa::topk_rows_dispatch(q_low, k_low, true, P, ovf_list, rows, ovf_count, Tq, Tk, k,
                                     p.causal, sc, idx, score,

@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kSortWarps * 32, 4) cand_sort_kernel(
     const uint64_t* __restrict__ cand, const int32_t* __restrict__ cnt, int64_t rows, int Tq,
     int Tk, int k, int causal, float scale, int32_t* __restrict__ idx_out,
     float* __restrict__ score_out, int64_t* __restrict__ ovf_list,
-    int32_t* __restrict__ ovf_count) {
+    int32_t* __restrict__ ovf_count, int32_t* dev_status) {
     constexpr int CAP = 32 * NB;      // two lists of CAP/2
     constexpr int CAPC = CAP / 2;
     constexpr int W = 32 * E;         // sorted winners
@@ -294,8 +294,11 @@ __global__ void __launch_bounds__(kSortWarps * 32, 4) cand_sort_kernel(
     const int n = tile_valid_count(i, Tq, Tk, causal);
     const int keff = min(k, n);
     const int c0 = n > 0 ? cnt[row * 2] : 0, c1 = n > 0 ? cnt[row * 2 + 1] : 0;
-    if (c0 > CAPC || c1 > CAPC) {
-        if (lane == 0) ovf_list[atomicAdd(ovf_count, 1)] = row;
+    if (c0 > CAPC || c1 > CAPC) {   // redone by the row-wise kernel (informational status)
+        if (lane == 0) {
+            ovf_list[atomicAdd(ovf_count, 1)] = row;
+            report(dev_status, SSA_DEV_OVERFLOW);
+        }
         return;
     }
     const int c = c0 + c1;
@@ -591,7 +594,8 @@ cudaError_t tile_select_launch(const uint16_t* gm, uint32_t* tau, int BH, int Tq
 
 cudaError_t tile_sort_launch(const uint64_t* cand, const int32_t* cnt, int64_t rows, int Tq,
                              int Tk, int k, int causal, float scale, int32_t* idx, float* score,
-                             int64_t* ovf_list, int32_t* ovf_count, cudaStream_t stream) {
+                             int64_t* ovf_list, int32_t* ovf_count, int32_t* dev_status,
+                             cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
     const int64_t blocks = (rows + kSortWarps - 1) / kSortWarps;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -601,7 +605,7 @@ cudaError_t tile_sort_launch(const uint64_t* cand, const int32_t* cnt, int64_t r
     if (cap == 32 * NB) {                                                                      \
         cand_sort_kernel<NB, NB / 2><<<static_cast<unsigned>(blocks), kSortWarps * 32, 0,      \
                                        stream>>>(cand, cnt, rows, Tq, Tk, k, causal, scale,    \
-                                                 idx, score, ovf_list, ovf_count);             \
+                                                 idx, score, ovf_list, ovf_count, dev_status); \
         return cudaGetLastError();                                                             \
     }
     SSA_SORT_CASE(2)

@@ -63,7 +63,8 @@ typedef enum {
 /* Bits ORed into *dev_status by kernels. */
 #define SSA_DEV_BAD_INDEX 0x1   /* an index list entry outside [-1, Tk); the entry is skipped */
 #define SSA_DEV_WAIT_LIMIT 0x2  /* a bounded device-side wait ran out; the tile is abandoned */
-#define SSA_DEV_OVERFLOW 0x4    /* internal candidate buffer overflowed; the row was redone exactly */
+#define SSA_DEV_OVERFLOW 0x4    /* a row's candidate list overflowed (a key above the bound found it
+                                   full); the row was redone exactly by the row-wise kernel */
 
 /*
  * ssa_device_status — turns the device-side error bits into a status.

@@ -131,7 +131,7 @@ class Emu:
         self.lib = lib = ctypes.CDLL(path)
         P, I, F, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int64
         lib.emu_group_select.argtypes = [P, P, I, I, I, I, I]
-        lib.emu_cand_sort.argtypes = [P, P, L, I, I, I, I, F, P, P, P, P]
+        lib.emu_cand_sort.argtypes = [P, P, L, I, I, I, I, F, P, P, P, P, P]
         lib.emu_tile_cand_cap.argtypes = [I]
         lib.emu_tile_group_stride.argtypes = [I]
 
@@ -228,9 +228,13 @@ def sort_and_compare(emu, q, kl, cand, cnt, expect_ovf, BH, Tq, Tk, k, causal, s
     sc = np.full((rows, k), np.nan, np.float32)
     ovf = np.full(rows + 1, -1, np.int64)
     ocount = np.zeros(1, np.int32)
+    status = np.zeros(1, np.int32)
     emu.lib.emu_cand_sort(_p(cand), _p(cnt), rows, Tq, Tk, k, int(causal), float(scale), _p(idx),
-                          _p(sc), _p(ovf), _p(ocount))
+                          _p(sc), _p(ovf), _p(ocount), _p(status))
     got_ovf = set(ovf[:ocount[0]].tolist())
+    if bool(status[0] & 0x4) != bool(got_ovf) or status[0] & ~0x4:
+        fails.append("%s: status %#x with %d overflow rows (SSA_DEV_OVERFLOW iff some)" % (
+            tag, status[0], len(got_ovf)))
     if got_ovf != expect_ovf:
         fails.append("%s: overflow rows %s, want %s" % (tag, sorted(got_ovf)[:5],
                                                          sorted(expect_ovf)[:5]))

@@ -20,14 +20,14 @@ extern "C" int emu_group_select(const uint16_t* gm, uint32_t* tau, int BH, int T
 
 extern "C" int emu_cand_sort(const uint64_t* cand, const int32_t* cnt, int64_t rows, int Tq,
                              int Tk, int k, int causal, float scale, int32_t* idx, float* score,
-                             int64_t* ovf_list, int32_t* ovf_count) {
+                             int64_t* ovf_list, int32_t* ovf_count, int32_t* dev_status) {
     const unsigned blocks = (unsigned)((rows + ssa::kSortWarps - 1) / ssa::kSortWarps);
     const int cap = ssa::tile_cand_cap(k);
 #define C(NB)                                                                                   \
     if (cap == 32 * NB) {                                                                       \
         emu_launch(blocks, ssa::kSortWarps * 32, [&] {                                          \
             ssa::cand_sort_kernel<NB, NB / 2>(cand, cnt, rows, Tq, Tk, k, causal, scale, idx,   \
-                                              score, ovf_list, ovf_count);                      \
+                                              score, ovf_list, ovf_count, dev_status);          \
         });                                                                                     \
         return 0;                                                                               \
     }
