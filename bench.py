@@ -13,8 +13,9 @@ second over the whole job) with inputs resident in HBM; ``e2e`` is the same
 metric through the public calls with pinned host buffers, the host<->device
 copies inside the timed region (the copies of Q, K and V, which only the
 attention call reads, run on a second stream while the scorer computes; with
-B = 1 the step runs in two halves of the heads so that copies of one half
-overlap the other half's kernels). Under torchrun (N > 1) every rank runs its own
+B = 1 the step runs in groups of heads (four, or two) so that copies of one
+group overlap the other groups' kernels, and a step's input copies overlap the
+previous step's last output copy). Under torchrun (N > 1) every rank runs its own
 independent batch (weak scaling, no collective on the data path); the timed
 region is bracketed by barriers and the slowest rank's time is used.
 
@@ -376,32 +377,44 @@ def run_ours(args, rank, world, local_rank):
 
     copy_stream = torch.cuda.Stream(dev)
     d2h_stream = torch.cuda.Stream(dev)
-    # one batch of heads split in two halves (contiguous head slices): the
-    # second half's inputs arrive while the first half computes, and the first
-    # half's output returns while the second half's attention runs
+    # one batch of heads split in groups of contiguous heads (four when each
+    # keeps at least four heads, else two: a scorer call over fewer heads
+    # loses more to its tail than the finer overlap gains): a group's inputs
+    # arrive while the groups before it compute and its output returns while
+    # the groups after it run.
+    # Consecutive steps overlap too: a step's input copies start once the
+    # previous step's last attention is done (the buffers are free), while
+    # that step's last output copy is still running; a group's attention waits
+    # only for the previous step's read of the same output slice.
     split = not window and not shared and not smooth and w.B == 1 and w.H >= 2
-    halves = [(0, w.H // 2), (w.H // 2, w.H)]
+    ngroups = 4 if w.H % 4 == 0 and w.H // 4 >= 4 else 2
+    groups = [(g * w.H // ngroups, (g + 1) * w.H // ngroups) for g in range(ngroups)]
+    prev = {"done": None, "read": [None] * ngroups}   # events of the previous step
 
     def e2e_step_split():
-        copy_stream.wait_stream(stream)   # the previous step is done with the buffers
+        if prev["done"] is None:
+            copy_stream.wait_stream(stream)
+        else:
+            copy_stream.wait_event(prev["done"])   # its compute is done with the buffers
         ev_in = []
         with torch.cuda.stream(copy_stream):
-            for h0, h1 in halves:           # q_low, k_low of each half, then Q, K, V of each
+            for h0, h1 in groups:           # q_low, k_low of each group, then Q, K, V of each
                 for d, h in zip(dev_in[:2], host_in[:2]):
                     d[:, h0:h1].copy_(h[:, h0:h1], non_blocking=True)
                 ev_in.append(torch.cuda.Event())
                 ev_in[-1].record(copy_stream)
-            for h0, h1 in halves:
+            for h0, h1 in groups:
                 for d, h in zip(dev_in[2:], host_in[2:]):
                     d[:, h0:h1].copy_(h[:, h0:h1], non_blocking=True)
                 ev_in.append(torch.cuda.Event())
                 ev_in[-1].record(copy_stream)
-        for n, (h0, h1) in enumerate(halves):
+        for n, (h0, h1) in enumerate(groups):
             stream.wait_event(ev_in[n])
             topk(dev_in[0][:, h0:h1], dev_in[1][:, h0:h1], idx[:, h0:h1])
-        d2h_stream.wait_stream(stream)
-        for n, (h0, h1) in enumerate(halves):
-            stream.wait_event(ev_in[2 + n])
+        for n, (h0, h1) in enumerate(groups):
+            stream.wait_event(ev_in[ngroups + n])
+            if prev["read"][n] is not None:
+                stream.wait_event(prev["read"][n])   # the previous step has read this slice
             attn(dev_in[2][:, h0:h1], dev_in[3][:, h0:h1], dev_in[4][:, h0:h1], idx[:, h0:h1],
                  out=O[:, h0:h1])
             ev_o = torch.cuda.Event()
@@ -409,7 +422,10 @@ def run_ours(args, rank, world, local_rank):
             d2h_stream.wait_event(ev_o)
             with torch.cuda.stream(d2h_stream):
                 host_out[:, h0:h1].copy_(O[:, h0:h1], non_blocking=True)
-        stream.wait_stream(d2h_stream)
+                prev["read"][n] = torch.cuda.Event()
+                prev["read"][n].record(d2h_stream)
+        prev["done"] = torch.cuda.Event()
+        prev["done"].record(stream)
 
     def e2e_step():
         if split:
@@ -439,9 +455,12 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    stream.wait_stream(d2h_stream)
     e0.record(stream)
+    prev["done"] = e0   # the first timed step's copies start after the start event
     for _ in range(args.steps):
         e2e_step()
+    stream.wait_stream(d2h_stream)   # the last step's result is read back
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1) / args.steps
@@ -667,9 +686,12 @@ def run_project(args, rank, world, local_rank):
     e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream.wait_stream(d2h_stream)
     e0.record(stream)
+    prev["done"] = e0   # the first timed step's copies start after the start event
     for _ in range(args.steps):
         e2e_step()
+    stream.wait_stream(d2h_stream)   # the last step's result is read back
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1) / args.steps
@@ -818,9 +840,12 @@ def run_backward(args, rank, world, local_rank):
     e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream.wait_stream(d2h_stream)
     e0.record(stream)
+    prev["done"] = e0   # the first timed step's copies start after the start event
     for _ in range(args.steps):
         e2e_step()
+    stream.wait_stream(d2h_stream)   # the last step's result is read back
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1) / args.steps
