@@ -14,7 +14,8 @@ metric through the public calls with pinned host buffers, the host<->device
 copies inside the timed region (the copies of Q, K and V, which only the
 attention call reads, run on a second stream while the scorer computes; with
 B = 1 the step runs in groups of heads (four, or two) so that copies of one
-group overlap the other groups' kernels, and a step's input copies overlap the
+group overlap the other groups' kernels; the scorer's inputs are copied a step
+ahead into a second buffer set, and a step's other input copies overlap the
 previous step's last output copy). Under torchrun (N > 1) every rank runs its own
 independent batch (weak scaling, no collective on the data path); the timed
 region is bracketed by barriers and the slowest rank's time is used.
@@ -389,32 +390,50 @@ def run_ours(args, rank, world, local_rank):
     split = not window and not shared and not smooth and w.B == 1 and w.H >= 2
     ngroups = 4 if w.H % 4 == 0 and w.H // 4 >= 4 else 2
     groups = [(g * w.H // ngroups, (g + 1) * w.H // ngroups) for g in range(ngroups)]
-    prev = {"done": None, "read": [None] * ngroups}   # events of the previous step
+    # q_low and k_low in two buffer sets: a step prefetches the next step's
+    # into the other set while it computes (the last timed step does not, so
+    # every copy in the timed region is a timed step's)
+    qk_sets = [dev_in[:2], [torch.empty_like(t) for t in dev_in[:2]]] if split else None
+    prev = {"done": None, "read": [None] * ngroups, "topk_done": None, "qk_ready": None, "n": 0}
 
-    def e2e_step_split():
-        if prev["done"] is None:
-            copy_stream.wait_stream(stream)
-        else:
-            copy_stream.wait_event(prev["done"])   # its compute is done with the buffers
+    def copy_qk(n, after):
+        """q_low, k_low of step n into buffer set n % 2, group by group."""
+        evs = []
+        with torch.cuda.stream(copy_stream):
+            if after is not None:
+                copy_stream.wait_event(after)
+            for h0, h1 in groups:
+                for d, h in zip(qk_sets[n % 2], host_in[:2]):
+                    d[:, h0:h1].copy_(h[:, h0:h1], non_blocking=True)
+                evs.append(torch.cuda.Event())
+                evs[-1].record(copy_stream)
+        return evs
+
+    def e2e_step_split(prefetch_next):
+        n = prev["n"]
+        ev_qk = prev["qk_ready"] or copy_qk(n, prev["done"])
         ev_in = []
         with torch.cuda.stream(copy_stream):
-            for h0, h1 in groups:           # q_low, k_low of each group, then Q, K, V of each
-                for d, h in zip(dev_in[:2], host_in[:2]):
-                    d[:, h0:h1].copy_(h[:, h0:h1], non_blocking=True)
-                ev_in.append(torch.cuda.Event())
-                ev_in[-1].record(copy_stream)
+            if prev["done"] is not None:
+                copy_stream.wait_event(prev["done"])   # its compute is done with Q, K, V
             for h0, h1 in groups:
                 for d, h in zip(dev_in[2:], host_in[2:]):
                     d[:, h0:h1].copy_(h[:, h0:h1], non_blocking=True)
                 ev_in.append(torch.cuda.Event())
                 ev_in[-1].record(copy_stream)
-        for n, (h0, h1) in enumerate(groups):
-            stream.wait_event(ev_in[n])
-            topk(dev_in[0][:, h0:h1], dev_in[1][:, h0:h1], idx[:, h0:h1])
-        for n, (h0, h1) in enumerate(groups):
-            stream.wait_event(ev_in[ngroups + n])
-            if prev["read"][n] is not None:
-                stream.wait_event(prev["read"][n])   # the previous step has read this slice
+        qk = qk_sets[n % 2]
+        for g, (h0, h1) in enumerate(groups):
+            stream.wait_event(ev_qk[g])
+            topk(qk[0][:, h0:h1], qk[1][:, h0:h1], idx[:, h0:h1])
+        topk_done = torch.cuda.Event()
+        topk_done.record(stream)
+        # the next step's q_low, k_low into the set the previous step's scorer read
+        prev["qk_ready"] = copy_qk(n + 1, prev["topk_done"]) if prefetch_next else None
+        prev["topk_done"] = topk_done
+        for g, (h0, h1) in enumerate(groups):
+            stream.wait_event(ev_in[g])
+            if prev["read"][g] is not None:
+                stream.wait_event(prev["read"][g])   # the previous step has read this slice
             attn(dev_in[2][:, h0:h1], dev_in[3][:, h0:h1], dev_in[4][:, h0:h1], idx[:, h0:h1],
                  out=O[:, h0:h1])
             ev_o = torch.cuda.Event()
@@ -422,14 +441,15 @@ def run_ours(args, rank, world, local_rank):
             d2h_stream.wait_event(ev_o)
             with torch.cuda.stream(d2h_stream):
                 host_out[:, h0:h1].copy_(O[:, h0:h1], non_blocking=True)
-                prev["read"][n] = torch.cuda.Event()
-                prev["read"][n].record(d2h_stream)
+                prev["read"][g] = torch.cuda.Event()
+                prev["read"][g].record(d2h_stream)
         prev["done"] = torch.cuda.Event()
         prev["done"].record(stream)
+        prev["n"] = n + 1
 
-    def e2e_step():
+    def e2e_step(prefetch_next=False):
         if split:
-            e2e_step_split()
+            e2e_step_split(prefetch_next)
             return
         if window:
             for d, h in zip(dev_in, host_in):
@@ -458,8 +478,8 @@ def run_ours(args, rank, world, local_rank):
     stream.wait_stream(d2h_stream)
     e0.record(stream)
     prev["done"] = e0   # the first timed step's copies start after the start event
-    for _ in range(args.steps):
-        e2e_step()
+    for st in range(args.steps):
+        e2e_step(prefetch_next=st + 1 < args.steps)
     stream.wait_stream(d2h_stream)   # the last step's result is read back
     e1.record(stream)
     torch.cuda.synchronize()
@@ -686,12 +706,9 @@ def run_project(args, rank, world, local_rank):
     e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    stream.wait_stream(d2h_stream)
     e0.record(stream)
-    prev["done"] = e0   # the first timed step's copies start after the start event
     for _ in range(args.steps):
         e2e_step()
-    stream.wait_stream(d2h_stream)   # the last step's result is read back
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1) / args.steps
@@ -840,12 +857,9 @@ def run_backward(args, rank, world, local_rank):
     e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    stream.wait_stream(d2h_stream)
     e0.record(stream)
-    prev["done"] = e0   # the first timed step's copies start after the start event
     for _ in range(args.steps):
         e2e_step()
-    stream.wait_stream(d2h_stream)   # the last step's result is read back
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1) / args.steps
