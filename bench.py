@@ -842,24 +842,66 @@ def run_backward(args, rank, world, local_rank):
     kernels = {n: {"launches_per_step": len(v) // args.steps, "ms": float(np.sum(v)) / args.steps}
                for n, v in per_kernel.items()}
     launches = len(recs) // args.steps
-    # end to end: every input from pinned host memory, every gradient back
+    # end to end: every input from pinned host memory, every gradient back.
+    # The heads run in two groups, each group's gradients read back while the
+    # next computes; the inputs sit in two buffer sets, each step copying the
+    # next step's into the other set while it computes (the last timed step
+    # copies nothing ahead, so every copy in the timed region is a timed
+    # step's).
     hin = [t.cpu().pin_memory() for t in args_dev]
-    din = [torch.empty_like(t) for t in args_dev]
+    dsets = [[torch.empty_like(t) for t in args_dev] for _ in range(2)]
     outs = step(*args_dev)
     hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    copy_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    halves = [(0, w.H // 2), (w.H // 2, w.H)] if w.H >= 2 else [(0, w.H)]
+    prev = {"n": 0, "ready": None, "done": [None, None], "read": [None] * len(halves)}
 
-    def e2e_step():
-        for d, h in zip(din, hin):
-            d.copy_(h, non_blocking=True)
-        for h, o in zip(hout, step(*din)):
-            h.copy_(o, non_blocking=True)
+    def copy_in(n, after):
+        evs = []
+        with torch.cuda.stream(copy_stream):
+            if after is not None:
+                copy_stream.wait_event(after)
+            for h0, h1 in halves:
+                for d, h in zip(dsets[n % 2], hin):
+                    d[:, h0:h1].copy_(h[:, h0:h1], non_blocking=True)
+                evs.append(torch.cuda.Event())
+                evs[-1].record(copy_stream)
+        return evs
+
+    def e2e_step(prefetch_next=False):
+        n = prev["n"]
+        ev_in = prev["ready"] or copy_in(n, prev["done"][(n + 1) % 2])
+        din = dsets[n % 2]
+        for g, (h0, h1) in enumerate(halves):
+            stream.wait_event(ev_in[g])
+            if prev["read"][g] is not None:
+                stream.wait_event(prev["read"][g])
+            res = step(*[t[:, h0:h1] for t in din])
+            ev_o = torch.cuda.Event()
+            ev_o.record(stream)
+            d2h_stream.wait_event(ev_o)
+            with torch.cuda.stream(d2h_stream):
+                for h, o in zip(hout, res):
+                    o.record_stream(d2h_stream)   # freed only after the copy has read it
+                    h[:, h0:h1].copy_(o, non_blocking=True)
+                prev["read"][g] = torch.cuda.Event()
+                prev["read"][g].record(d2h_stream)
+        done = torch.cuda.Event()
+        done.record(stream)
+        # the next step's inputs into the set the previous step read
+        prev["ready"] = copy_in(n + 1, prev["done"][(n + 1) % 2]) if prefetch_next else None
+        prev["done"][n % 2] = done
+        prev["n"] = n + 1
 
     e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream.wait_stream(d2h_stream)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    prev["done"] = [e0, e0]   # the first timed step's copies start after the start event
+    for st in range(args.steps):
+        e2e_step(prefetch_next=st + 1 < args.steps)
+    stream.wait_stream(d2h_stream)   # the last step's gradients are read back
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1) / args.steps
