@@ -387,7 +387,7 @@ def run_ours(args, rank, world, local_rank):
     # previous step's last attention is done (the buffers are free), while
     # that step's last output copy is still running; a group's attention waits
     # only for the previous step's read of the same output slice.
-    split = not window and not shared and not smooth and w.B == 1 and w.H >= 2
+    split = not window and not shared and w.B == 1 and w.H >= 2
     ngroups = 4 if w.H % 4 == 0 and w.H // 4 >= 4 else 2
     groups = [(g * w.H // ngroups, (g + 1) * w.H // ngroups) for g in range(ngroups)]
     # q_low and k_low in two buffer sets: a step prefetches the next step's
