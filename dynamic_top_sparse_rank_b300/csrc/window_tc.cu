@@ -131,7 +131,7 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // (columns 8db.., keys 8kb..) of the result, which sits exactly where block
 // (db, kb) of the source was; so a block and its mirror are read together
 // (ldmatrix .trans) and written crosswise (stmatrix), four pairs at a time
-// (the eight diagonal blocks in one batch). The P V MMAs read V^T K-major at
+// (the eight diagonal blocks in two batches). The P V MMAs read V^T K-major at
 // 73.5 cycles per M=128, K=16 instruction against 125 for V MN-major
 // (measured at N=64 and N=128).
 __device__ __forceinline__ void vt_transpose_half(uint32_t base, int lane) {
@@ -149,33 +149,55 @@ __device__ __forceinline__ void vt_transpose_half(uint32_t base, int lane) {
                      : "memory");
     };
     // the 28 blocks above the diagonal, four per batch (pair index q: the
-    // q-th (kb, db) with kb < db in row-major order)
-#pragma unroll 1
-    for (int bt = 0; bt < 7; ++bt) {
-        int q = 4 * bt + m, kb = 0;
-        while (q >= 7 - kb) {   // row kb holds 7 - kb blocks above the diagonal
-            q -= 7 - kb;
-            ++kb;
-        }
-        const int db = kb + 1 + q;
-        uint32_t a[4], b[4];
-        ld4(src(kb, db), a);   // lane group m: block (kb, db) of its pair
-        ld4(src(db, kb), b);   // and its mirror
-        __syncwarp();
-        st4(src(db, kb), a);   // (kb, db) transposed goes where (db, kb) was
-        st4(src(kb, db), b);
-        __syncwarp();
-    }
-    // the diagonal blocks, in place
+    // q-th (kb, db) with kb < db in row-major order; row kb starts at pair
+    // 7 kb - kb (kb - 1) / 2), then the eight diagonal blocks; two rounds
+    // (batches 0-3, then 4-6 and the diagonal), each reading every block of
+    // its batches before writing any, so the loads' latencies overlap
+    auto pair_block = [](int q, int& kb, int& db) {
+        kb = (q >= 7) + (q >= 13) + (q >= 18) + (q >= 22) + (q >= 25) + (q >= 27);
+        db = kb + 1 + q - (7 * kb - kb * (kb - 1) / 2);
+    };
+    {
+        uint32_t a[4][4], b[4][4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int kb = 4 * h + m;
-        uint32_t a[4];
-        ld4(src(kb, kb), a);
+        for (int bt = 0; bt < 4; ++bt) {
+            int kb, db;
+            pair_block(4 * bt + m, kb, db);
+            ld4(src(kb, db), a[bt]);   // lane group m: block (kb, db) of its pair
+            ld4(src(db, kb), b[bt]);   // and its mirror
+        }
         __syncwarp();
-        st4(src(kb, kb), a);
-        __syncwarp();
+#pragma unroll
+        for (int bt = 0; bt < 4; ++bt) {
+            int kb, db;
+            pair_block(4 * bt + m, kb, db);
+            st4(src(db, kb), a[bt]);   // (kb, db) transposed goes where (db, kb) was
+            st4(src(kb, db), b[bt]);
+        }
     }
+    {
+        uint32_t a[3][4], b[3][4], d[2][4];
+#pragma unroll
+        for (int bt = 0; bt < 3; ++bt) {
+            int kb, db;
+            pair_block(4 * (bt + 4) + m, kb, db);
+            ld4(src(kb, db), a[bt]);
+            ld4(src(db, kb), b[bt]);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) ld4(src(4 * h + m, 4 * h + m), d[h]);
+        __syncwarp();
+#pragma unroll
+        for (int bt = 0; bt < 3; ++bt) {
+            int kb, db;
+            pair_block(4 * (bt + 4) + m, kb, db);
+            st4(src(db, kb), a[bt]);
+            st4(src(kb, db), b[bt]);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) st4(src(4 * h + m, 4 * h + m), d[h]);
+    }
+    __syncwarp();
 }
 
 // The softmax warps of window_tc_kernel: kNW per TMEM lane quarter (warp w
@@ -597,7 +619,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
 //     issued behind P(t) V(t), which reads those columns, and tcgen05.mma
 //     instructions of one thread run in issue order;
 //   - the TMA warp streams the query tile and key and value tiles through
-//     rings of two slots each, turning each value tile K-major;
+//     a two-slot key ring and a three-slot value ring, two tiles ahead of
+//     the one it turns K-major (a tile's copy latency is then off the chain);
 //   - the softmax warps (eight, two per lane quarter) take the running-shift
 //     softmax of softmax_rows tile by tile; a rescale of O needs no extra
 //     wait, as the tile's S commit follows the previous tile's P V.
@@ -606,29 +629,32 @@ constexpr int kThreads = 320;                   // TMA warp, MMA warp, 8 softmax
 constexpr int kWarps = 2;                       // softmax warps per lane quarter
 constexpr uint32_t kTile = kSliceBytes;         // one 128-row x 64-column bf16 tile
 constexpr uint32_t Q_OFF = 0;
-constexpr uint32_t K_OFF = Q_OFF + kTile;       // [2] key tile ring
-constexpr uint32_t V_OFF = K_OFF + 2 * kTile;   // [2] value tile ring (turned K-major)
-constexpr uint32_t BAR_OFF = V_OFF + 2 * kTile;
+constexpr uint32_t kKS = 2, kVS = 3;            // key and value ring slots
+constexpr uint32_t K_OFF = Q_OFF + kTile;       // [kKS] key tile ring
+constexpr uint32_t V_OFF = K_OFF + kKS * kTile; // [kVS] value tile ring (turned K-major)
+constexpr uint32_t BAR_OFF = V_OFF + kVS * kTile;
 constexpr uint32_t XCH_OFF = BAR_OFF + 256;     // [3 slots][128 rows] 32-bit words
 constexpr uint32_t SMEM = XCH_OFF + 3 * 128 * 4 + 1024;   // + alignment slack
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kOut = 128;                  // first TMEM column of O
+constexpr uint32_t kSSlots = 3;                 // score slots of 64 keys (64 columns each)
+// TMEM columns of score slot j: 0..63, 64..127 and, beside O, 192..255
+__device__ __forceinline__ uint32_t slot_col(uint32_t j) { return j == 2 ? 192u : 64u * j; }
 static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
 }  // namespace w64
 
 __device__ __forceinline__ void softmax_rows64(const WindowParams& p, uint32_t tmem_base, int warp,
                                                int lane, uint64_t* s_full, uint64_t* o_full,
-                                               uint64_t* p_full, uint64_t* pair_bar,
-                                               uint32_t* slots, volatile int* abort_flag,
-                                               uint64_t lim) {
+                                               uint64_t* p_full, uint64_t* pv_done, uint64_t* pair_bar,
+                                               uint32_t* slots, volatile int* abort_flag, uint64_t lim) {
     using namespace w64;
     const int quarter = warp & 3;   // TMEM lane quarter of this warp
-    const int g = (warp - 2) >> 2;  // which half of each tile's chunks and of the output
+    const int g = (warp - 2) >> 2;  // which 32-key chunk of each 64-key step, and half of the output
     const int r = quarter * 32 + lane;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     constexpr float kRescaleLog2 = 8.f;   // weights stay below 2^8
     uint32_t u = 0;                        // quarter steps taken (see softmax_rows)
-    uint32_t sc = 0;                       // S tiles consumed (s_full phases)
+    uint32_t sc = 0;                       // 64-key steps consumed (score slot ring, P V count)
     auto quarter_meet = [&]() -> bool {
         tc_fence_before();
         mbar_arrive(pair_bar + quarter);
@@ -653,41 +679,35 @@ __device__ __forceinline__ void softmax_rows64(const WindowParams& p, uint32_t t
         const int flo = iw + 31 - p.wl > 0 ? iw + 31 - p.wl : 0;
         const int fhi = iw + p.wr < p.T - 1 ? iw + p.wr : p.T - 1;
         const int kbase = w.kt0 * kWN;
-        auto chunk_class = [&](int ch) {   // 0 outside, 1 inside, 2 partial (as softmax_rows)
-            const int j0 = kbase + 32 * ch;
-            if (j0 + 31 < wlo || j0 > whi) return 0;
-            return (j0 >= flo && j0 + 31 <= fhi) ? 1 : 2;
-        };
         float M = -INFINITY;   // the row's shift
         float l = 0.f;         // this warp's partial row sum
-        for (int t = 0; t < w.nkt; ++t) {
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full, sc & 1, abort_flag, p.dev_status, lim)))
+        for (int h = 0; h < 2 * w.nkt; ++h) {
+            // step h: keys kbase + 64 h .. + 63 in score slot sc % 3; this warp
+            // takes their 32-key chunk g (chunk 2 h + g of the item)
+            const uint32_t ss = sc % kSSlots;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full + ss, (sc / kSSlots) & 1, abort_flag,
+                                                          p.dev_status, lim)))
                 return;
             ++sc;
             tc_fence_after();
-            // the maximum of this warp's two chunks, one chunk per load (the
-            // scores are loaded again for the weights: a TMEM load and its
-            // wait take about 28 ns, registers are short at two CTAs per SM)
-            int cls[2];
+            const uint32_t col = t_lane + slot_col(ss) + 32 * g;
+            const int j0 = kbase + 32 * (2 * h + g);
+            // 0 outside every band of the warp, 1 inside all of them, 2 partial
+            const int cls = (j0 + 31 < wlo || j0 > whi) ? 0 : (j0 >= flo && j0 + 31 <= fhi) ? 1 : 2;
             float m = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int cc = 2 * g + c;   // chunk of the tile
-                cls[c] = chunk_class(4 * t + cc);
-                const uint32_t col = t_lane + 32 * cc;
+            {
                 uint32_t v[32];
-                if (cls[c] == 1) {
+                if (cls == 1) {
                     float m0 = tmem_ldred_max16(col, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
                     float m1 = tmem_ldred_max16(col + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
                     tmem_ld_wait();
                     reg_fence_f(m0);
                     reg_fence_f(m1);
-                    m = fmax3(m, m0, m1);
-                } else if (cls[c] == 2) {
+                    m = fmaxf(m0, m1);
+                } else if (cls == 2) {
                     tmem_ld32(col, v);
                     tmem_ld_wait();
                     reg_fence(v);
-                    const int j0 = kbase + 32 * (4 * t + cc);
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         if (j0 + e >= jlo && j0 + e <= jhi) m = fmaxf(m, __uint_as_float(v[e]));
@@ -701,9 +721,14 @@ __device__ __forceinline__ void softmax_rows64(const WindowParams& p, uint32_t t
             const float mt = mk == 0u ? -INFINITY : order_key_f32(mk);
             const bool move = mt > -INFINITY && (M == -INFINITY || (mt - M) * p.scale_log2 > kRescaleLog2);
             if (__any_sync(0xffffffffu, move && M > -INFINITY)) {
-                // this tile's S landed after the previous tile's P V: O holds
-                // the earlier tiles' sums at the old shift; scale this warp's
-                // columns of the moved rows
+                // O holds the earlier steps' sums at the old shift: once the
+                // previous step's P V is done (the one before it finished
+                // ahead of this step's scores), scale this warp's columns of
+                // the moved rows
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(pv_done, (sc - 2) & 1, abort_flag,
+                                                              p.dev_status, lim)))
+                    return;
+                tc_fence_after();
                 const float f = move && M > -INFINITY ? ex2_approx((M - mt) * p.scale_log2) : 1.f;
                 const uint32_t ocol = t_lane + w64::kOut + 32 * g;
                 uint32_t o[32];
@@ -717,46 +742,41 @@ __device__ __forceinline__ void softmax_rows64(const WindowParams& p, uint32_t t
                 l *= f;
             }
             if (move) M = mt;
+            uint32_t whi[16], wlo[16];
+            if (cls) {
+                uint32_t v[32];
+                tmem_ld32(col, v);
+                tmem_ld_wait();
+                reg_fence(v);
+                const bool mask = cls == 2;
+                float s2[2] = {0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int cc = 2 * g + c;
-                uint32_t whi[16], wlo[16];
-                if (cls[c]) {
-                    uint32_t v[32];
-                    tmem_ld32(t_lane + 32 * cc, v);
-                    tmem_ld_wait();
-                    reg_fence(v);
-                    const int j0 = kbase + 32 * (4 * t + cc);
-                    const bool mask = cls[c] == 2;
-                    float s2[2] = {0.f, 0.f};
+                for (int q = 0; q < 16; ++q) {
+                    float pv[2];
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        float pv[2];
-#pragma unroll
-                        for (int b = 0; b < 2; ++b) {
-                            const int j = j0 + 2 * q + b;
-                            const float x = (__uint_as_float(v[2 * q + b]) - M) * p.scale_log2;
-                            pv[b] = ex2_approx(!mask || (j >= jlo && j <= jhi) ? x : -INFINITY);
-                        }
-                        s2[q & 1] += pv[0] + pv[1];
-                        const uint32_t b0 = __float_as_uint(pv[0]), b1 = __float_as_uint(pv[1]);
-                        whi[q] = __byte_perm(b0, b1, 0x7632);
-                        const __nv_bfloat162 lo = __floats2bfloat162_rn(
-                            pv[0] - __uint_as_float(b0 & 0xFFFF0000u), pv[1] - __uint_as_float(b1 & 0xFFFF0000u));
-                        wlo[q] = *reinterpret_cast<const uint32_t*>(&lo);
+                    for (int b = 0; b < 2; ++b) {
+                        const int j = j0 + 2 * q + b;
+                        const float x = (__uint_as_float(v[2 * q + b]) - M) * p.scale_log2;
+                        pv[b] = ex2_approx(!mask || (j >= jlo && j <= jhi) ? x : -INFINITY);
                     }
-                    l += s2[0] + s2[1];
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) whi[q] = wlo[q] = 0u;
+                    s2[q & 1] += pv[0] + pv[1];
+                    const uint32_t b0 = __float_as_uint(pv[0]), b1 = __float_as_uint(pv[1]);
+                    whi[q] = __byte_perm(b0, b1, 0x7632);
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(
+                        pv[0] - __uint_as_float(b0 & 0xFFFF0000u), pv[1] - __uint_as_float(b1 & 0xFFFF0000u));
+                    wlo[q] = *reinterpret_cast<const uint32_t*>(&lo);
                 }
-                tmem_st16(t_lane + 32 * cc, whi);
-                tmem_st16(t_lane + 32 * cc + 16, wlo);
+                l += s2[0] + s2[1];
+            } else {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) whi[q] = wlo[q] = 0u;
             }
+            tmem_st16(col, whi);
+            tmem_st16(col + 16, wlo);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(p_full + ss);
         }
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_full, n & 1, abort_flag, p.dev_status, lim)))
             return;
@@ -805,7 +825,7 @@ __global__ void __launch_bounds__(w64::kThreads, 2)
                        const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const WindowParams p) {
     using namespace w64;
-    constexpr uint32_t IDESC_S = idesc_bf16_f32(kWM, kWN);
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(kWM, 64);    // one 64-key step
     constexpr uint32_t IDESC_O = idesc_bf16_f32(kWM, 64);   // V^T K-major
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -813,16 +833,17 @@ __global__ void __launch_bounds__(w64::kThreads, 2)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
     uint64_t* q_full = bars;         // the query tile landed
     uint64_t* q_empty = bars + 1;    // the item's S MMAs are done
-    uint64_t* k_full = bars + 2;     // [2] key tile landed
-    uint64_t* k_empty = bars + 4;    // [2] its S MMA is done
-    uint64_t* v_full = bars + 6;     // [2] value tile landed
-    uint64_t* vt_full = bars + 8;    // [2] value tile turned K-major
-    uint64_t* v_empty = bars + 10;   // [2] its P V MMAs are done
-    uint64_t* s_full = bars + 12;    // S of the current key tile in TMEM
-    uint64_t* p_full = bars + 13;    // its weights in TMEM (one arrive per softmax warp)
-    uint64_t* o_full = bars + 14;    // every MMA of the item done
-    uint64_t* pair_bar = bars + 15;  // [4] the two softmax warps of a lane quarter meet
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+    uint64_t* k_full = bars + 2;          // [kKS] key tile landed
+    uint64_t* k_empty = k_full + kKS;     // [kKS] its S MMA is done
+    uint64_t* v_full = k_empty + kKS;     // [kVS] value tile landed
+    uint64_t* vt_full = v_full + kVS;     // [kVS] value tile turned K-major
+    uint64_t* v_empty = vt_full + kVS;    // [kVS] its P V MMAs are done
+    uint64_t* s_full = v_empty + kVS;     // [kSSlots] a 64-key step's scores in its slot
+    uint64_t* p_full = s_full + kSSlots;  // [kSSlots] its weights (one arrive per softmax warp)
+    uint64_t* pv_done = p_full + kSSlots; // a step's P V MMAs are done
+    uint64_t* o_full = pv_done + 1;       // every MMA of the item done
+    uint64_t* pair_bar = o_full + 1;      // [4] the two softmax warps of a lane quarter meet
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pair_bar + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     uint32_t* slots = reinterpret_cast<uint32_t*>(smem + XCH_OFF);
 
@@ -831,15 +852,20 @@ __global__ void __launch_bounds__(w64::kThreads, 2)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (uint32_t s = 0; s < kKS; ++s) {
             mbar_init(k_full + s, 1);
             mbar_init(k_empty + s, 1);
+        }
+        for (uint32_t s = 0; s < kVS; ++s) {
             mbar_init(v_full + s, 1);
             mbar_init(vt_full + s, 1);
             mbar_init(v_empty + s, 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 4 * w64::kWarps);
+        for (uint32_t s = 0; s < kSSlots; ++s) {
+            mbar_init(s_full + s, 1);
+            mbar_init(p_full + s, 4 * w64::kWarps);
+        }
+        mbar_init(pv_done, 1);
         mbar_init(o_full, 1);
         for (int q = 0; q < 4; ++q) mbar_init(pair_bar + q, 32 * w64::kWarps);
         *abort_flag = 0;
@@ -859,39 +885,53 @@ __global__ void __launch_bounds__(w64::kThreads, 2)
 
     if (warp == 0) {
         // ------------------------------------------------ TMA (lane 0) and the
-        // turning of each landed value tile K-major (whole warp)
-        int n = 0;
-        uint32_t kc = 0, vc = 0;   // key and value tiles issued
-        bool ok = true;
-        for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++n) {
-            const WinItem w = win_item(p, item);
-            if (lane == 0) {
-                if (n > 0) ok = mbar_wait_bounded(q_empty, (n - 1) & 1, abort_flag, p.dev_status, lim);
-                if (ok) {
-                    mbar_arrive_expect_tx(q_full, kTile);
-                    tma_load_3d(smem + Q_OFF, &qmap, 0, w.i0, w.bh, q_full);
-                }
+        // turning of each landed value tile K-major (whole warp). The block's
+        // key tiles are numbered c = 0, 1, ... over its items in order; lane 0
+        // has the copies of tiles c + 1 and c + 2 in flight while the warp
+        // turns tile c, so no tile waits for its copy to be issued.
+        int ld_item = blockIdx.x, ld_t = 0;   // the next tile to copy: its item and key tile
+        WinItem ld_w{};
+        if (ld_item < p.items) ld_w = win_item(p, ld_item);
+        uint32_t nq = 0, nl = 0;              // query tiles, key and value tile pairs issued
+        // lane 0: the next tile's key and value copies, after its item's query
+        // tile if it is the item's first; false when a wait ran out or the
+        // block stopped (what was issued is counted)
+        auto issue_next = [&]() -> bool {
+            if (ld_item >= p.items) return true;
+            if (ld_t == 0) {
+                if (nq > 0 && !mbar_wait_bounded(q_empty, (nq - 1) & 1, abort_flag, p.dev_status, lim))
+                    return false;
+                mbar_arrive_expect_tx(q_full, kTile);
+                tma_load_3d(smem + Q_OFF, &qmap, 0, ld_w.i0, ld_w.bh, q_full);
+                ++nq;
             }
-            for (int t = 0; ok && t < w.nkt; ++t) {
-                const uint32_t ks = kc & 1, vs = vc & 1;
-                if (lane == 0) {
-                    if (kc >= 2) ok = mbar_wait_bounded(k_empty + ks, ((kc >> 1) - 1) & 1, abort_flag, p.dev_status, lim);
-                    if (ok) {
-                        mbar_arrive_expect_tx(k_full + ks, kTile);
-                        tma_load_3d(smem + K_OFF + ks * kTile, &kmap, 0, (w.kt0 + t) * kWN, w.bh, k_full + ks);
-                    }
-                    if (ok && vc >= 2)
-                        ok = mbar_wait_bounded(v_empty + vs, ((vc >> 1) - 1) & 1, abort_flag, p.dev_status, lim);
-                    if (ok) {
-                        mbar_arrive_expect_tx(v_full + vs, kTile);
-                        tma_load_3d(smem + V_OFF + vs * kTile, &vmap, 0, (w.kt0 + t) * kWN, w.bh, v_full + vs);
-                    }
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                ++kc;
-                ++vc;
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(v_full + vs, ((vc - 1) >> 1) & 1, abort_flag,
+            const uint32_t ks = nl % kKS, vs = nl % kVS;
+            if (nl >= kKS && !mbar_wait_bounded(k_empty + ks, (nl / kKS - 1) & 1, abort_flag, p.dev_status, lim))
+                return false;
+            if (nl >= kVS && !mbar_wait_bounded(v_empty + vs, (nl / kVS - 1) & 1, abort_flag, p.dev_status, lim))
+                return false;
+            const int key0 = (ld_w.kt0 + ld_t) * kWN;
+            mbar_arrive_expect_tx(k_full + ks, kTile);
+            tma_load_3d(smem + K_OFF + ks * kTile, &kmap, 0, key0, ld_w.bh, k_full + ks);
+            mbar_arrive_expect_tx(v_full + vs, kTile);
+            tma_load_3d(smem + V_OFF + vs * kTile, &vmap, 0, key0, ld_w.bh, v_full + vs);
+            ++nl;
+            if (++ld_t == ld_w.nkt) {
+                ld_t = 0;
+                ld_item += gridDim.x;
+                if (ld_item < p.items) ld_w = win_item(p, ld_item);
+            }
+            return true;
+        };
+        bool ok = true;
+        if (lane == 0) ok = issue_next() && issue_next();
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        uint32_t vc = 0;   // value tiles turned
+        for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x) {
+            const int nkt = win_item(p, item).nkt;
+            for (int t = 0; t < nkt; ++t) {
+                const uint32_t vs = vc % kVS;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(v_full + vs, (vc / kVS) & 1, abort_flag,
                                                               p.dev_status, lim))) {
                     ok = false;
                     break;
@@ -901,60 +941,90 @@ __global__ void __launch_bounds__(w64::kThreads, 2)
                 fence_proxy_async_smem();   // the MMAs read the tile through the async proxy
                 __syncwarp();
                 if (lane == 0) mbar_arrive(vt_full + vs);
+                ++vc;
+                if (lane == 0) ok = issue_next();
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
             }
         }
-        // the copies land before the block may exit
+        // the copies land before the block may exit (slot s last held tile
+        // s + kS * floor((n - 1 - s) / kS) of the n issued)
         if (lane == 0) {
-            if (n > 0) mbar_wait_bounded(q_full, (n - 1) & 1, nullptr, p.dev_status, lim);
-            for (uint32_t s = 0; s < 2; ++s)
-                if (kc > s) {
-                    mbar_wait_bounded(k_full + s, ((kc - 1 - s) >> 1) & 1, nullptr, p.dev_status, lim);
-                    mbar_wait_bounded(v_full + s, ((vc - 1 - s) >> 1) & 1, nullptr, p.dev_status, lim);
-                }
+            if (nq > 0) mbar_wait_bounded(q_full, (nq - 1) & 1, nullptr, p.dev_status, lim);
+            for (uint32_t s = 0; s < kKS; ++s)
+                if (nl > s) mbar_wait_bounded(k_full + s, ((nl - 1 - s) / kKS) & 1, nullptr, p.dev_status, lim);
+            for (uint32_t s = 0; s < kVS; ++s)
+                if (nl > s) mbar_wait_bounded(v_full + s, ((nl - 1 - s) / kVS) & 1, nullptr, p.dev_status, lim);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA
+        // Per item, 64-key steps h = 0 .. 2 nkt - 1 (key tile h / 2, its half
+        // h % 2): S(h) into score slot h % 3 (counted over the block's steps),
+        // then, once its weights are written, P(h) V(h) into O. S(h + 2) is
+        // issued right behind P(h) V(h), so the softmax warps work on step
+        // h + 1 while the tensor pipe runs P(h) V(h): S(h + 2) takes the slot
+        // of step h - 1, whose P V ran before it (tcgen05.mma instructions of
+        // one thread run in issue order).
         if (lane == 0) {
             int n = 0;
-            uint32_t kc = 0, vc = 0, pc = 0, committed = 0;
+            uint32_t kc = 0, vc = 0, sc = 0, pc = 0, committed = 0;
             bool ok = true;
             for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++n) {
                 const WinItem w = win_item(p, item);
                 if (!mbar_wait_bounded(q_full, n & 1, abort_flag, p.dev_status, lim)) break;
                 const uint64_t qd = smem_desc_k_sw128(smem_u32(smem + Q_OFF));
-                for (int t = 0; ok && t < w.nkt; ++t) {
-                    const uint32_t ks = kc & 1, vs = vc & 1;
-                    ok = mbar_wait_bounded(k_full + ks, (kc >> 1) & 1, abort_flag, p.dev_status, lim);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // S(t) over the previous tile's weights: issued behind its P V
-                    const uint64_t kd = smem_desc_k_sw128(smem_u32(smem + K_OFF + ks * kTile));
+                const int H = 2 * w.nkt;
+                auto issue_s = [&](int h) -> bool {
+                    const uint32_t ks = kc % kKS;
+                    if ((h & 1) == 0) {   // a new key tile
+                        if (!mbar_wait_bounded(k_full + ks, (kc / kKS) & 1, abort_flag, p.dev_status, lim))
+                            return false;
+                        tc_fence_after();
+                    }
+                    const uint64_t kd = smem_desc_k_sw128(smem_u32(smem + K_OFF + ks * kTile + (h & 1) * (kTile / 2)));
+                    const uint32_t d = tmem_base + slot_col(sc % kSSlots);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tmem_base, qd + ((kk * 32) >> 4), kd + ((kk * 32) >> 4), IDESC_S, kk != 0);
-                    mma_commit(k_empty + ks);
-                    if (t == w.nkt - 1) mma_commit(q_empty);
-                    mma_commit(s_full);
-                    ++kc;
-                    ok = mbar_wait_bounded(p_full, pc & 1, abort_flag, p.dev_status, lim) &&
-                         mbar_wait_bounded(vt_full + vs, (vc >> 1) & 1, abort_flag, p.dev_status, lim);
-                    ++pc;
+                        mma_bf16(d, qd + ((kk * 32) >> 4), kd + ((kk * 32) >> 4), IDESC_S, kk != 0);
+                    if (h & 1) {
+                        mma_commit(k_empty + ks);
+                        ++kc;
+                    }
+                    if (h == H - 1) mma_commit(q_empty);
+                    mma_commit(s_full + sc % kSSlots);
+                    ++sc;
+                    return true;
+                };
+                ok = issue_s(0) && issue_s(1);
+                for (int h = 0; ok && h < H; ++h) {
+                    const uint32_t ps = pc % kSSlots, vs = vc % kVS;
+                    ok = mbar_wait_bounded(p_full + ps, (pc / kSSlots) & 1, abort_flag, p.dev_status, lim);
+                    if (ok && (h & 1) == 0)
+                        ok = mbar_wait_bounded(vt_full + vs, (vc / kVS) & 1, abort_flag, p.dev_status, lim);
                     if (!ok) break;
                     tc_fence_after();
+                    const uint32_t pcol = slot_col(ps);
 #pragma unroll
-                    for (int s8 = 0; s8 < kWN / 16; ++s8) {
-                        // keys 16 s8 .. 16 s8 + 15: their hi and lo weights, and a
-                        // 32-byte K slice of V^T's 64-key half s8 / 4
-                        const uint32_t hi = 32 * (s8 / 2) + 8 * (s8 % 2);
+                    for (int s4 = 0; s4 < 4; ++s4) {
+                        // keys 16 s4 .. 16 s4 + 15 of the step: their hi and lo
+                        // weights (chunk s4 / 2: hi words in its first 16
+                        // columns, lo in the next 16) and a 32-byte K slice of
+                        // V^T's 64-key half h % 2
+                        const uint32_t hi = pcol + 32 * (s4 / 2) + 8 * (s4 % 2);
                         const uint64_t bd =
-                            smem_desc_k_sw128(smem_u32(smem + V_OFF + vs * kTile + (s8 / 4) * (kTile / 2))) +
-                            (((s8 % 4) * 32) >> 4);
-                        mma_bf16_ta(tmem_base + w64::kOut, tmem_base + hi, bd, IDESC_O, (t | s8) != 0);
+                            smem_desc_k_sw128(smem_u32(smem + V_OFF + vs * kTile + (h & 1) * (kTile / 2))) +
+                            ((s4 * 32) >> 4);
+                        mma_bf16_ta(tmem_base + w64::kOut, tmem_base + hi, bd, IDESC_O, (h | s4) != 0);
                         mma_bf16_ta(tmem_base + w64::kOut, tmem_base + hi + 16, bd, IDESC_O, 1);
                     }
-                    mma_commit(v_empty + vs);
-                    ++vc;
+                    mma_commit(pv_done);
+                    if (h & 1) {
+                        mma_commit(v_empty + vs);
+                        ++vc;
+                    }
+                    ++pc;
+                    if (h + 2 < H) ok = issue_s(h + 2);
                 }
                 // every MMA of the item (also after a stop) is tracked by o_full
                 mma_commit(o_full);
@@ -963,7 +1033,8 @@ __global__ void __launch_bounds__(w64::kThreads, 2)
             if (committed > 0) mbar_wait_bounded(o_full, (committed - 1) & 1, nullptr, p.dev_status, lim);
         }
     } else {
-        softmax_rows64(p, tmem_base, warp, lane, s_full, o_full, p_full, pair_bar, slots, abort_flag, lim);
+        softmax_rows64(p, tmem_base, warp, lane, s_full, o_full, p_full, pv_done, pair_bar, slots, abort_flag,
+                       lim);
     }
 
     tc_fence_before();
