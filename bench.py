@@ -114,6 +114,7 @@ MEASURED_TRAFFIC = {
     ("topk_causal_bf16_t32k_k256", "tile_scores.collect"): 1.862e9,
     ("topk_causal_bf16_t128k_k512_planted", "tile_scores.groupmax"): 4 * 0.897e9,
     ("topk_causal_bf16_t128k_k512_planted", "tile_scores.collect"): 4 * 1.862e9,
+    ("window_bf16_t4096_w128", "window_tc"): 25.22e6,   # Q, K, V read once; O stays in L2
 }
 
 # Read throughput of the L2 slices (GB/s) that serve the gather: the kernel's
