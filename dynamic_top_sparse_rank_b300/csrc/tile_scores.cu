@@ -633,12 +633,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                       for (int hs = 0; hs < 4; ++hs) hot[hs] = jp + 16 * hs < n_i && mx[hs] >= t_hot;
 #pragma unroll
                       for (int hs = 0; hs < 4; ++hs) B[hs] = __ballot_sync(0xffffffffu, hot[hs]);
+                      const uint32_t below = (1u << lane) - 1;
+                      const int tot = __popc(B[0]) + __popc(B[1]) + __popc(B[2]) + __popc(B[3]);
+                      if (q_tail - q_head + tot <= kQueue) {
+                          // the usual case: every entry of the four half-chunks
+                          // fits the ring, so they go in without a drain between
+                          // (a row's entries still sit in key order); then the
+                          // ring drains down to fewer than 32
+                          int qb = q_tail;
 #pragma unroll
-                      for (int hs = 0; hs < 4; ++hs) {
-                          if (B[hs]) {
+                          for (int hs = 0; hs < 4; ++hs) {
                               const float* w = v + 16 * hs;
                               if (hot[hs]) {
-                                  const int q = (q_tail + __popc(B[hs] & ((1u << lane) - 1))) & (kQueue - 1);
+                                  const int q = (qb + __popc(B[hs] & below)) & (kQueue - 1);
                                   qv[q] = make_float4(w[0], w[1], w[2], w[3]);
                                   qv[kQueue + q] = make_float4(w[4], w[5], w[6], w[7]);
                                   qv[2 * kQueue + q] = make_float4(w[8], w[9], w[10], w[11]);
@@ -646,10 +653,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   qm[q] = (static_cast<uint32_t>((jp + 16 * hs) / kSub) << 5) |
                                           static_cast<uint32_t>(lane);
                               }
-                              q_tail += __popc(B[hs]);
-                              if (q_tail - q_head >= 32) {
-                                  __syncwarp();   // the queued entries are visible to every lane
-                                  drain(32);
+                              qb += __popc(B[hs]);
+                          }
+                          q_tail = qb;
+                          if (q_tail - q_head >= 32) {
+                              __syncwarp();   // the queued entries are visible to every lane
+                              drain(32);
+                              if (q_tail - q_head >= 32) drain(32);
+                          }
+                      } else {
+#pragma unroll
+                          for (int hs = 0; hs < 4; ++hs) {
+                              if (B[hs]) {
+                                  if (hot[hs]) {
+                                      const float* w = v + 16 * hs;
+                                      const int q = (q_tail + __popc(B[hs] & below)) & (kQueue - 1);
+                                      qv[q] = make_float4(w[0], w[1], w[2], w[3]);
+                                      qv[kQueue + q] = make_float4(w[4], w[5], w[6], w[7]);
+                                      qv[2 * kQueue + q] = make_float4(w[8], w[9], w[10], w[11]);
+                                      qv[3 * kQueue + q] = make_float4(w[12], w[13], w[14], w[15]);
+                                      qm[q] = (static_cast<uint32_t>((jp + 16 * hs) / kSub) << 5) |
+                                              static_cast<uint32_t>(lane);
+                                  }
+                                  q_tail += __popc(B[hs]);
+                                  if (q_tail - q_head >= 32) {
+                                      __syncwarp();
+                                      drain(32);
+                                  }
                               }
                           }
                       }
