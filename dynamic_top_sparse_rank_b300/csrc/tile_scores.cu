@@ -615,10 +615,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                           for (int h4 = 0; h4 < 4; ++h4) v[16 * h4 + e] = __uint_as_float(raw[h4][e]);
                       }
-                      // mask the keys past the row's last one: only in the tile
-                      // where a row of this warp ends (a warp-uniform branch);
-                      // there the maxima come from the masked registers
-                      if (__any_sync(0xffffffffu, jp < n_i && jp + 64 > n_i)) {
+                      // mask the keys past the row's last one: only in the chunks
+                      // where a row of this warp ends or has ended (a warp-uniform
+                      // branch); there the maxima come from the masked registers
+                      if (__any_sync(0xffffffffu, jp + 64 > n_i)) {
                           if (jp + 64 > n_i) {
 #pragma unroll
                               for (int e = 0; e < 64; ++e)
@@ -630,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       uint32_t B[4];
                       bool hot[4];
 #pragma unroll
-                      for (int hs = 0; hs < 4; ++hs) hot[hs] = jp + 16 * hs < n_i && mx[hs] >= t_hot;
+                      for (int hs = 0; hs < 4; ++hs) hot[hs] = mx[hs] >= t_hot;   // masked keys are -inf
 #pragma unroll
                       for (int hs = 0; hs < 4; ++hs) B[hs] = __ballot_sync(0xffffffffu, hot[hs]);
                       const uint32_t below = (1u << lane) - 1;
