@@ -166,7 +166,7 @@ def roofline_for(name, ms, w, alg, pk, pk_kind):
         what = "k_low rows scored: d_proj * esize per valid (query, key) pair"
     achieved = by / sec / 1e9
     line = {"kernel": name, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
-            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": MEASURED_TRAFFIC.get((w.name, name)),
             "peak_kind": pk_kind + " HBM copy", "algorithmic": "%s, %.4g B per launch" % (what, by)}
     if name == "attn_rows.sparse":
         line["l2"] = {"achieved": achieved, "peak": L2_SLICE_READ_GBS, "unit": "GB/s",
