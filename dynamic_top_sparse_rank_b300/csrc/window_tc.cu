@@ -28,7 +28,8 @@
 //           to the MMA warp once written, so its P V runs under the next
 //           tile's softmax.
 // window_tc64_kernel (head size 64): two CTAs per SM, each on 256 TMEM
-// columns and one key tile at a time (see the notes above it).
+// columns, in 64-key steps through a ring of three score slots (see the
+// notes above it).
 // Every mbarrier wait is bounded; a wait that runs out reports
 // SSA_DEV_WAIT_LIMIT, stops the other roles and TMEM is freed.
 #include <float.h>
@@ -63,7 +64,7 @@ constexpr uint64_t kWDefaultWaitNs = 1000000000ull;
 template <int D>
 struct WinCfg {
     static constexpr int KA = D / 64;                          // 64-column slices
-    static constexpr int STAGES = D == 64 ? 2 : 1;
+    static constexpr int STAGES = 1;
     static constexpr uint32_t TILE = KA * kSliceBytes;         // one 128-row tile
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t SLICE3 = kWMaxTiles * kSliceBytes;   // one slice of the three tiles
@@ -488,8 +489,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA (lane 0); for D 64 the
-        // whole warp then turns each landed value tile K-major (see vt_transpose_half)
+        // ------------------------------------------------ TMA (lane 0)
         int n = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++n) {
