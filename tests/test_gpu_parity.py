@@ -298,6 +298,35 @@ def test_window_tensor_core_many_items_per_cta(cuda_dev, D):
     assert_out_close(Ob.float().cpu().numpy(), ref, TOL_BF16, True)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_window_tensor_core_rescales(cuda_dev, D):
+    """Scores that grow along the key axis (q . k_j = c j, c such that the
+    weights grow by about 2^10 per 64 keys), so a row's maximum moves by more
+    than 2^8 in weight from one 64-key step of the band to the next: the running shift moves at almost every step and O, summed
+    at the old shift, is scaled each time (after the previous step's P V has
+    finished). A scale applied to a partial O, or not at all, would be off by
+    about the step's weight ratio; every row against the oracle."""
+    B, H, T, wl, wr = 1, 4, 600, 128, 128
+    g = torch.Generator().manual_seed(900 + D)
+    sign = torch.randint(0, 2, (D,), generator=g).float() * 2 - 1          # v0: entries +-1
+    j = torch.arange(T, dtype=torch.float32)
+    Q = sign.expand(B, H, T, D).clone()
+    c = 10.0 * D ** 0.5 / (64 * 1.4427)                                     # log2 weight +10 per 64 keys
+    K = (c * j / D)[None, None, :, None] * sign                              # q . k_j = c j
+    K = K + 0.01 * torch.randn(B, H, T, D, generator=g)
+    V = torch.randn(B, H, T, D, generator=g)
+    Q, K, V = (t.to(torch.bfloat16) for t in (Q, K.expand(B, H, T, D), V))
+    ref = oracle.window_attn(Q, K, V, wl, wr)
+    dq, dk, dv = (t.to(cuda_dev) for t in (Q, K, V))
+    ssa.trace_begin()
+    O = ssa.ssa_window_attn(dq, dk, dv, wl, wr, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert [n for n, _ in ssa.trace_end()] == ["window_tc"]
+    assert_out_close(O.cpu().numpy(), ref, TOL_BF16, False)
+    Ob = ssa.ssa_window_attn(dq, dk, dv, wl, wr)
+    assert_out_close(Ob.float().cpu().numpy(), ref, TOL_BF16, True)
+
+
 def test_window_wide_band_uses_gather(cuda_dev):
     """A band wider than three key tiles per query tile goes to the gather kernel."""
     T, wl, wr = 1000, 300, 300
