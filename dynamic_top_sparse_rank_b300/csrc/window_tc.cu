@@ -612,18 +612,22 @@ __global__ void __launch_bounds__(kWThreads, 1)
 // For head size 64 the item's chain of dependent steps (scores, softmax, P V
 // per key tile), not any one unit, sets the pace of window_tc_kernel, and one
 // item's scores fill 384 of the 512 TMEM columns. window_tc64_kernel runs two
-// CTAs per SM instead, each on 256 TMEM columns and about 83 KB of shared
-// memory, so that one CTA's softmax runs while the other's MMAs and loads do:
-//   - one key tile at a time: S(t) = Q K(t)^T into columns 0..127, the
-//     weights over them, P(t) V(t) into O (columns 128..191); S(t+1) is
-//     issued behind P(t) V(t), which reads those columns, and tcgen05.mma
-//     instructions of one thread run in issue order;
+// CTAs per SM instead, each on 256 TMEM columns and about 100 KB of shared
+// memory, so that one CTA's softmax runs while the other's MMAs and loads do,
+// and within a CTA the softmax of one 64-key step runs while the tensor pipe
+// works on the previous one:
+//   - 64-key steps h (key tile h / 2, its half h % 2): S(h) = Q K(h)^T (N=64)
+//     into score slot h % 3 (columns 0..63, 64..127, 192..255), the weights
+//     over it, P(h) V(h) into O (columns 128..191); S(h + 2) is issued behind
+//     P(h) V(h) and takes the slot of step h - 1, whose P V ran before it
+//     (tcgen05.mma instructions of one thread run in issue order);
 //   - the TMA warp streams the query tile and key and value tiles through
 //     a two-slot key ring and a three-slot value ring, two tiles ahead of
 //     the one it turns K-major (a tile's copy latency is then off the chain);
-//   - the softmax warps (eight, two per lane quarter) take the running-shift
-//     softmax of softmax_rows tile by tile; a rescale of O needs no extra
-//     wait, as the tile's S commit follows the previous tile's P V.
+//   - the softmax warps (eight, two per lane quarter, each one 32-key chunk
+//     of every step) take the running-shift softmax step by step; a rescale
+//     of O first waits for the previous step's P V (the one before it had
+//     finished ahead of this step's scores).
 namespace w64 {
 constexpr int kThreads = 320;                   // TMA warp, MMA warp, 8 softmax warps
 constexpr int kWarps = 2;                       // softmax warps per lane quarter
